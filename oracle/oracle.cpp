@@ -1,0 +1,615 @@
+// Oracle for the error-compensated 1-bit compressed optimizer step
+// (1-bit Adam / 1-bit LAMB) and the block-wise INT8 stochastic-rounding
+// quantizer.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, single-threaded
+// restatement of the method, written to be checked by eye against the
+// pages it follows.  Only tests/, __graft_entry__.smoke() and bench.py's
+// CPU-baseline leg may load it.  It shares no code, header, table or helper
+// with the CUDA library in momentum_compression_gb300/csrc/.
+//
+// Sources (cited by page title and section):
+//   [BLOG]  lqnn.cn, "1bit Adam" practitioner write-up:
+//           §2.1 error compensation (m/v recurrences; g' = g + e, q = sign(g'),
+//           e = g' - q), §6 tuning config (warmup without quantization).
+//   [TUT]   FreeGuideOnline, "梯度量化：将梯度从 FP32 压到 INT8 甚至 1-bit":
+//           "FP32 → INT8 量化" (scale = max|g|/127, block-wise scales,
+//           stochastic rounding), "1-bit 梯度量化" (scaled sign
+//           mean(|g|)*sign(g), error feedback), and the GradientQuantizeINT8
+//           example (floor + Bernoulli(frac), clamp to ±127).
+//   [LAMB]  "1-bit LAMB (Error-Compensated LAMB-Preconditioned Large-Batch
+//           Compressed Optimization)": ¶1 reconstructed g_t, fresh v_t, the
+//           clipped infinity-norm ratio r_t and the frozen denominator;
+//           ¶2 the fixed per-layer momentum scale and the fused 1-D buffer;
+//           ¶3 step-ratio-scaled error feedback and the global-momentum
+//           identity with the server error delta~; ¶4 the 3-phase
+//           worker -> server -> worker compressed exchange.
+//
+// Arithmetic: IEEE binary32, every operation rounded on its own.  Build with
+// -O2 -ffp-contract=off and without -ffast-math, so that no multiply-add is
+// contracted and no subnormal is flushed.  Readings where the pages leave a
+// step open are listed at each function.
+//
+// Layout (shared by every function; the pages fix none of it):
+//   n real elements, W workers, alignment A, chunk C.
+//   P = roundup(ceil(n/W), A); n_pad = W*P; server j owns [jP, (j+1)P).
+//   Each partition is cut into chunks of C elements (the last may be short);
+//   chunk g (global id) = partition g / cpp, chunk g % cpp within it,
+//   cpp = ceil(P/C).  Elements k >= n are padding: they count nowhere,
+//   their bit is 0 and their error is 0.
+//   Bit rule: bit k%32 of word k/32 (LSB first) is 1 iff x[k] >= 0.0f, so
+//   sign(+0) = sign(-0) = +1 and a NaN packs as -1.
+//
+// Parity pins: every function here is checked by tests/test_oracle_*.py
+// against hand-computed values, closed forms, invariants, brute force or
+// an independent library (curand's host Philox generator).
+
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Layout
+// ---------------------------------------------------------------------------
+
+struct orc_layout {
+  uint64_t n, W, A, C;
+  uint64_t P, n_pad, cpp, nc;
+};
+
+// Fills the derived sizes.  Returns 0, or -1 if the configuration is empty.
+int orc_make_layout(uint64_t n, uint64_t W, uint64_t A, uint64_t C,
+                    orc_layout* out) {
+  if (W == 0 || A == 0 || C == 0 || out == nullptr) return -1;
+  uint64_t per = (n + W - 1) / W;
+  uint64_t P = (per + A - 1) / A * A;
+  if (P == 0) P = A;  // n == 0 still has one aligned partition per worker
+  uint64_t c = C < P ? C : P;
+  out->n = n;
+  out->W = W;
+  out->A = A;
+  out->C = c;
+  out->P = P;
+  out->n_pad = W * P;
+  out->cpp = (P + c - 1) / c;
+  out->nc = W * out->cpp;
+  return 0;
+}
+
+static void chunk_range(const orc_layout* L, uint64_t g, uint64_t* start,
+                        uint64_t* len, uint64_t* real) {
+  uint64_t j = g / L->cpp, kc = g % L->cpp;
+  uint64_t s = j * L->P + kc * L->C;
+  uint64_t l = L->P - kc * L->C;
+  if (l > L->C) l = L->C;
+  uint64_t r = 0;
+  if (L->n > s) r = (L->n - s < l) ? (L->n - s) : l;
+  *start = s;
+  *len = l;
+  *real = r;
+}
+
+// ---------------------------------------------------------------------------
+// Canonical reduction CR
+// ---------------------------------------------------------------------------
+// The order of every floating-point sum that decides a scale or a norm is
+// fixed here, so that any implementation that follows it gets the same bits:
+//   1. the segment is cut into tiles of 4096 elements from its own start;
+//   2. inside a tile, lane p in [0,256) starts from 0 and adds, for i = 0..3
+//      and then c = 0..3, element 1024*i + 4*p + c when present;
+//   3. the 256 lanes are reduced in warps of 32 by a butterfly
+//      (v[l] = v[l] + v[l ^ o], o = 16, 8, 4, 2, 1), and the 8 warp sums
+//      pairwise: ((w0+w1)+(w2+w3)) + ((w4+w5)+(w6+w7));
+//   4. the segment total is the sum of the tile totals, in tile order,
+//      starting from 0.
+// The pages only say "mean(abs(g))" (TUT, "1-bit 梯度量化") and "norm"; they
+// fix no summation order.  `a` holds `count` present values; the segment
+// may be longer, but absent elements (padding) are skipped, which is the
+// same as ending it at `count`.
+
+static float cr_tile(const float* a, uint64_t len) {
+  float lane[256];
+  for (int p = 0; p < 256; ++p) {
+    float acc = 0.0f;
+    for (int i = 0; i < 4; ++i)
+      for (int c = 0; c < 4; ++c) {
+        uint64_t idx = (uint64_t)(1024 * i + 4 * p + c);
+        if (idx < len) acc = acc + a[idx];
+      }
+    lane[p] = acc;
+  }
+  float warp[8];
+  for (int w = 0; w < 8; ++w) {
+    float v[32];
+    for (int l = 0; l < 32; ++l) v[l] = lane[32 * w + l];
+    for (int o = 16; o >= 1; o >>= 1) {
+      float nv[32];
+      for (int l = 0; l < 32; ++l) nv[l] = v[l] + v[l ^ o];
+      for (int l = 0; l < 32; ++l) v[l] = nv[l];
+    }
+    warp[w] = v[0];
+  }
+  float s01 = warp[0] + warp[1], s23 = warp[2] + warp[3];
+  float s45 = warp[4] + warp[5], s67 = warp[6] + warp[7];
+  float s0123 = s01 + s23, s4567 = s45 + s67;
+  return s0123 + s4567;
+}
+
+float orc_cr_sum(const float* a, uint64_t count) {
+  float total = 0.0f;
+  for (uint64_t t = 0; t * 4096 < count; ++t) {
+    uint64_t len = count - t * 4096;
+    if (len > 4096) len = 4096;
+    total = total + cr_tile(a + t * 4096, len);
+  }
+  return total;
+}
+
+// ---------------------------------------------------------------------------
+// Per-layer lookups
+// ---------------------------------------------------------------------------
+// Layers are contiguous ranges of the fused 1-D buffer ([LAMB] ¶2):
+// offsets[0] = 0 < offsets[1] < ... < offsets[nl] = n.  nl == 0 means one
+// layer covering [0, n).
+
+static uint64_t layer_of(const uint64_t* off, uint64_t nl, uint64_t k) {
+  if (nl == 0) return 0;
+  uint64_t lo = 0, hi = nl;  // invariant: off[lo] <= k < off[hi]
+  while (hi - lo > 1) {
+    uint64_t mid = (lo + hi) / 2;
+    if (off[mid] <= k) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+static float sgn_of_bit(const uint32_t* words, uint64_t k) {
+  return ((words[k >> 5] >> (k & 31)) & 1u) ? 1.0f : -1.0f;
+}
+
+// ---------------------------------------------------------------------------
+// Compressor C[x]: scaled sign with error feedback
+// ---------------------------------------------------------------------------
+// [TUT] "1-bit 梯度量化": q = mean(|x|) * sign(x); the error x - q is kept and
+// added before the next compression ([BLOG] §2.1, e = g' - q; [TUT] error
+// feedback).  The mean is taken per chunk (the fused buffer of [LAMB] ¶2 is
+// cut into chunks); an all-padding chunk gets scale 0 (reading: the pages
+// never divide by zero, and the value is never used for a real element).
+//
+// Worker side, for worker w (one call per worker):
+//   m_w = b1*m + (1-b1)*g_w                        [BLOG] §2.1, momentum
+//   x   = sigma_l*m_w + rho_l*e_w                  [LAMB] ¶2 (scale sigma_l
+//         before compression) and ¶3 (step-ratio error feedback rho_l =
+//         c_{t-2}/c_{t-1}); both are 1 for 1-bit Adam
+//   scale(chunk) = CR(|x| over chunk) / realcount(chunk)
+//   bit = x >= 0;  e_w' = x - scale*sign(x)
+// `sigma`/`rho` are per-layer arrays or NULL (= 1).  e is updated in place.
+// `x_out`, if not NULL, receives x (used by tests).
+void orc_compress_worker(const orc_layout* L, const uint64_t* layer_off,
+                         uint64_t nl, const float* sigma, const float* rho,
+                         float b1, const float* g, const float* m, float* e,
+                         uint32_t* bits, float* scales, float* x_out) {
+  const float ob1 = 1.0f - b1;
+  std::vector<float> x(L->n_pad, 0.0f);
+  for (uint64_t k = 0; k < L->n; ++k) {
+    uint64_t l = layer_of(layer_off, nl, k);
+    float s = sigma ? sigma[l] : 1.0f;
+    float r = rho ? rho[l] : 1.0f;
+    float mw = (b1 * m[k]) + (ob1 * g[k]);
+    x[k] = (s * mw) + (r * e[k]);
+  }
+  for (uint64_t wd = 0; wd < L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0); ++wd)
+    bits[wd] = 0u;
+  std::vector<float> ax;
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    ax.assign(real, 0.0f);
+    for (uint64_t q = 0; q < real; ++q) ax[q] = std::fabs(x[start + q]);
+    float sum = orc_cr_sum(ax.data(), real);
+    float scale = real ? sum / (float)real : 0.0f;
+    scales[g_id] = scale;
+    for (uint64_t q = 0; q < len; ++q) {
+      uint64_t k = start + q;
+      if (q < real) {
+        float xv = x[k];
+        bool b = (xv >= 0.0f);
+        if (b) bits[k >> 5] |= (1u << (k & 31));
+        float sg = b ? 1.0f : -1.0f;
+        e[k] = xv - (scale * sg);
+      } else {
+        e[k] = 0.0f;
+      }
+    }
+  }
+  if (x_out)
+    for (uint64_t k = 0; k < L->n_pad; ++k) x_out[k] = x[k];
+}
+
+// Server side, all partitions ([LAMB] ¶3-¶4: worker chunks travel to the
+// server owning them, which averages, adds its own error delta~ and
+// compresses again):
+//   z_k = (sum over w = 0..W-1, in order, from 0, of scale_w(chunk)*sign_w(k)) / W
+//   y   = rho_l*e_s + z
+//   sscale(chunk) = CR(|y|) / realcount;  sbit = y >= 0;  e_s' = y - sscale*sign(y)
+// bits: [W][n_pad/32] words; scales: [W][nc] (each worker's scale for every
+// chunk of its full buffer).  Reading: the server uses the same chunking as
+// the workers, and divides by W after the sum.
+void orc_server_reduce(const orc_layout* L, const uint64_t* layer_off,
+                       uint64_t nl, const float* rho, const uint32_t* bits,
+                       const float* scales, float* e_s, uint32_t* sbits,
+                       float* sscales, float* y_out) {
+  const uint64_t words = L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0);
+  const float fW = (float)L->W;
+  std::vector<float> y(L->n_pad, 0.0f);
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    for (uint64_t q = 0; q < real; ++q) {
+      uint64_t k = start + q;
+      float z = 0.0f;
+      for (uint64_t w = 0; w < L->W; ++w)
+        z = z + scales[w * L->nc + g_id] * sgn_of_bit(bits + w * words, k);
+      z = z / fW;
+      uint64_t l = layer_of(layer_off, nl, k);
+      float r = rho ? rho[l] : 1.0f;
+      y[k] = (r * e_s[k]) + z;
+    }
+  }
+  for (uint64_t wd = 0; wd < words; ++wd) sbits[wd] = 0u;
+  std::vector<float> ay;
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    ay.assign(real, 0.0f);
+    for (uint64_t q = 0; q < real; ++q) ay[q] = std::fabs(y[start + q]);
+    float sum = orc_cr_sum(ay.data(), real);
+    float sscale = real ? sum / (float)real : 0.0f;
+    sscales[g_id] = sscale;
+    for (uint64_t q = 0; q < len; ++q) {
+      uint64_t k = start + q;
+      if (q < real) {
+        bool b = (y[k] >= 0.0f);
+        if (b) sbits[k >> 5] |= (1u << (k & 31));
+        e_s[k] = y[k] - (sscale * (b ? 1.0f : -1.0f));
+      } else {
+        e_s[k] = 0.0f;
+      }
+    }
+  }
+  if (y_out)
+    for (uint64_t k = 0; k < L->n_pad; ++k) y_out[k] = y[k];
+}
+
+// Decompression of the server result ([LAMB] ¶2: the global compressed
+// momentum is divided by the same fixed coefficient afterwards):
+//   out_k = sscale(chunk(k)) * sign(sbit_k) / sigma_l   (sigma = 1 if NULL)
+// Padding entries are 0.  With sigma == NULL no division is done.
+void orc_decompress(const orc_layout* L, const uint64_t* layer_off,
+                    uint64_t nl, const float* sigma, const uint32_t* sbits,
+                    const float* sscales, float* out) {
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    for (uint64_t q = 0; q < len; ++q) {
+      uint64_t k = start + q;
+      if (q < real) {
+        float M = sscales[g_id] * sgn_of_bit(sbits, k);
+        if (sigma) M = M / sigma[layer_of(layer_off, nl, k)];
+        out[k] = M;
+      } else {
+        out[k] = 0.0f;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Update with the frozen variance (1-bit Adam)
+// ---------------------------------------------------------------------------
+// [LAMB] ¶1: after warmup the denominator sqrt(v_{T_w}) is frozen; [BLOG]
+// §2.1 gives the Adam step.  No bias correction and no weight decay (the
+// pages show none).  m = sscale*sign(sbit), then
+//   p = p - lr * (m / (sqrt(v) + eps))
+void orc_adam_update(const orc_layout* L, const uint32_t* sbits,
+                     const float* sscales, const float* v, float eps, float lr,
+                     float* m, float* p) {
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    for (uint64_t q = 0; q < len; ++q) {
+      uint64_t k = start + q;
+      if (q >= real) {
+        m[k] = 0.0f;
+        continue;
+      }
+      float mk = sscales[g_id] * sgn_of_bit(sbits, k);
+      float d = std::sqrt(v[k]);
+      d = d + eps;
+      float u = mk / d;
+      float t = lr * u;
+      m[k] = mk;
+      p[k] = p[k] - t;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1-bit LAMB after warmup
+// ---------------------------------------------------------------------------
+// Pass A ([LAMB] ¶1 and ¶2), per real element k of layer l:
+//   M   = sscale*sign(sbit);  m_t = M / sigma_l
+//   g_t = (m_t - b1*m_{t-1}) / (1 - b1)
+//   v_t = b2*v_{t-1} + (1 - b2)*g_t^2          (fresh variance)
+//   R_l = max(R_l, v_Tw / v_t)                  (infinity norm of the ratio;
+//         a NaN ratio (0/0) is skipped, +Inf is kept)
+// m and v_t are updated in place; R must hold 0 on entry.
+void orc_lamb_pass_a(const orc_layout* L, const uint64_t* layer_off,
+                     uint64_t nl, const float* sigma, const uint32_t* sbits,
+                     const float* sscales, const float* v_frozen, float b1,
+                     float b2, float* m, float* v_fresh, float* R) {
+  const float ob1 = 1.0f - b1, ob2 = 1.0f - b2;
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    for (uint64_t q = 0; q < len; ++q) {
+      uint64_t k = start + q;
+      if (q >= real) {
+        m[k] = 0.0f;
+        continue;
+      }
+      uint64_t l = layer_of(layer_off, nl, k);
+      float M = sscales[g_id] * sgn_of_bit(sbits, k);
+      float mt = M / sigma[l];
+      float gt = (mt - (b1 * m[k])) / ob1;
+      float vt = (b2 * v_fresh[k]) + (ob2 * (gt * gt));
+      m[k] = mt;
+      v_fresh[k] = vt;
+      float ratio = v_frozen[k] / vt;
+      if (!std::isnan(ratio) && ratio > R[l]) R[l] = ratio;
+    }
+  }
+}
+
+static float fmax_plain(float a, float b) { return a > b ? a : b; }
+static float fmin_plain(float a, float b) { return a < b ? a : b; }
+
+// Per-layer ratio and coefficient ([LAMB] ¶1 and ¶3):
+//   r_t = clip(clip(R_l, (1-r_thr) r_{t-1}, (1+r_thr) r_{t-1}), r_min, r_max)
+//   c_t = clip(c_avg * r_t, c_min, c_max)       (gamma_t in [gamma_min, gamma_max])
+//   c_{t-2} <- c_{t-1}; c_{t-1} <- c_t; r_{t-1} <- r_t
+// With `frozen` != 0 the ratio is held at 1 and c_t = c_avg ("LAMB + basic
+// 1-bit" of ¶1).  c_out receives c_t.
+void orc_lamb_ratio(uint64_t nl, const float* R, float r_thr, float r_min,
+                    float r_max, float c_min, float c_max, int frozen,
+                    const float* c_avg, float* r_prev, float* c_prev,
+                    float* c_prev2, float* c_out) {
+  for (uint64_t l = 0; l < nl; ++l) {
+    float r;
+    if (frozen) {
+      r = 1.0f;
+    } else {
+      float lo = (1.0f - r_thr) * r_prev[l];
+      float hi = (1.0f + r_thr) * r_prev[l];
+      r = fmin_plain(fmax_plain(R[l], lo), hi);
+      r = fmin_plain(fmax_plain(r, r_min), r_max);
+    }
+    float c = c_avg[l] * r;
+    c = fmin_plain(fmax_plain(c, c_min), c_max);
+    c_prev2[l] = c_prev[l];
+    c_prev[l] = c;
+    r_prev[l] = r;
+    c_out[l] = c;
+  }
+}
+
+// Step-ratio factor of the error feedback ([LAMB] ¶3: the error carried
+// into step t is scaled by c_{t-2}/c_{t-1}); one fp32 division per layer.
+void orc_lamb_rho(uint64_t nl, const float* c_prev2, const float* c_prev,
+                  float* rho) {
+  for (uint64_t l = 0; l < nl; ++l) rho[l] = c_prev2[l] / c_prev[l];
+}
+
+// Pass B ([LAMB] ¶1, frozen denominator sqrt(v_Tw)):
+//   p = p - (lr*c_l) * (m_t / (sqrt(v_Tw) + eps))
+void orc_lamb_pass_b(const orc_layout* L, const uint64_t* layer_off,
+                     uint64_t nl, const float* c, const float* m,
+                     const float* v_frozen, float eps, float lr, float* p) {
+  for (uint64_t k = 0; k < L->n; ++k) {
+    uint64_t l = layer_of(layer_off, nl, k);
+    float t1 = lr * c[l];
+    float d = std::sqrt(v_frozen[k]) + eps;
+    float u = m[k] / d;
+    p[k] = p[k] - (t1 * u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warmup: uncompressed steps ([BLOG] §6 and [TUT] "预热训练": the first steps
+// run at full precision; [LAMB] ¶1: v is frozen at the end of warmup and
+// c_avg is the warmup average of LAMB's coefficient)
+// ---------------------------------------------------------------------------
+// g_bar = (sum over w in order, from 0, of g_w) / W
+// m = b1*m + (1-b1)*g_bar;  v = b2*v + (1-b2)*g_bar^2
+// Adam (mode 0): p = p - lr*(m/(sqrt(v)+eps))
+// LAMB (mode 1): u = m/(sqrt(v)+eps); per layer
+//     c = clip(||p_l|| / ||u_l||, c_min, c_max)   (c = 1 if either norm is 0)
+//     p = p - (lr*c)*u;  c_sum[l] += c
+// Norms are sqrt(CR(x^2)) over the layer, tiles counted from the layer's
+// start.  Reading: LAMB's coefficient is the standard trust ratio, clipped;
+// the pages name it only as "LAMB's scaling coefficient".
+// grads: W pointers, each to n_pad floats.
+void orc_warmup_step(const orc_layout* L, const uint64_t* layer_off,
+                     uint64_t nl, const float* const* grads, int mode,
+                     float b1, float b2, float eps, float lr, float c_min,
+                     float c_max, float* m, float* v, float* p, float* c_sum,
+                     float* c_out) {
+  const float ob1 = 1.0f - b1, ob2 = 1.0f - b2;
+  const float fW = (float)L->W;
+  std::vector<float> u(L->n, 0.0f);
+  for (uint64_t k = 0; k < L->n; ++k) {
+    float gb = 0.0f;
+    for (uint64_t w = 0; w < L->W; ++w) gb = gb + grads[w][k];
+    gb = gb / fW;
+    m[k] = (b1 * m[k]) + (ob1 * gb);
+    v[k] = (b2 * v[k]) + (ob2 * (gb * gb));
+    float d = std::sqrt(v[k]) + eps;
+    u[k] = m[k] / d;
+    if (mode == 0) p[k] = p[k] - (lr * u[k]);
+  }
+  for (uint64_t k = L->n; k < L->n_pad; ++k) m[k] = 0.0f;
+  if (mode == 0) return;
+  uint64_t L_count = nl ? nl : 1;
+  std::vector<float> sq;
+  for (uint64_t l = 0; l < L_count; ++l) {
+    uint64_t a = nl ? layer_off[l] : 0, b = nl ? layer_off[l + 1] : L->n;
+    sq.assign(b - a, 0.0f);
+    for (uint64_t k = a; k < b; ++k) sq[k - a] = p[k] * p[k];
+    float np_ = std::sqrt(orc_cr_sum(sq.data(), b - a));
+    for (uint64_t k = a; k < b; ++k) sq[k - a] = u[k] * u[k];
+    float nu_ = std::sqrt(orc_cr_sum(sq.data(), b - a));
+    float c;
+    if (np_ == 0.0f || nu_ == 0.0f) {
+      c = 1.0f;
+    } else {
+      c = np_ / nu_;
+      c = fmin_plain(fmax_plain(c, c_min), c_max);
+    }
+    float t1 = lr * c;
+    for (uint64_t k = a; k < b; ++k) p[k] = p[k] - (t1 * u[k]);
+    c_sum[l] = c_sum[l] + c;
+    if (c_out) c_out[l] = c;
+  }
+}
+
+// End of warmup for 1-bit LAMB ([LAMB] ¶1, ¶2):
+//   rms_l = sqrt(CR(m^2 over layer)) / sqrt(n_l)
+//   s_l   = mean_l(rms_l) / rms_l   (s_l = 1 if rms_l == 0); the mean is the
+//           in-order sum from 0 divided by the layer count
+//   c_avg = c_sum / T_w;  r_prev = 1;  c_prev = c_prev2 = c_avg
+// Reading: "a fixed per-layer momentum scale coefficient from the average
+// momentum norm" is taken as the factor that brings every layer's momentum
+// RMS to the mean RMS over layers; it is not clipped.
+void orc_lamb_begin(const orc_layout* L, const uint64_t* layer_off,
+                    uint64_t nl, const float* m, const float* c_sum,
+                    uint64_t warmup_steps, float* s, float* c_avg,
+                    float* r_prev, float* c_prev, float* c_prev2) {
+  uint64_t L_count = nl ? nl : 1;
+  std::vector<float> rms(L_count, 0.0f), sq;
+  for (uint64_t l = 0; l < L_count; ++l) {
+    uint64_t a = nl ? layer_off[l] : 0, b = nl ? layer_off[l + 1] : L->n;
+    sq.assign(b - a, 0.0f);
+    for (uint64_t k = a; k < b; ++k) sq[k - a] = m[k] * m[k];
+    float nrm = std::sqrt(orc_cr_sum(sq.data(), b - a));
+    rms[l] = nrm / std::sqrt((float)(b - a));
+  }
+  float mean = 0.0f;
+  for (uint64_t l = 0; l < L_count; ++l) mean = mean + rms[l];
+  mean = mean / (float)L_count;
+  for (uint64_t l = 0; l < L_count; ++l) {
+    s[l] = (rms[l] == 0.0f) ? 1.0f : mean / rms[l];
+    float ca = c_sum[l] / (float)warmup_steps;
+    c_avg[l] = ca;
+    r_prev[l] = 1.0f;
+    c_prev[l] = ca;
+    c_prev2[l] = ca;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): 10 rounds of
+//   (c0,c1,c2,c3) -> (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0))
+// with M0 = 0xD2511F53, M1 = 0xCD9E8D57, and the key advanced by the Weyl
+// constants (0x9E3779B9, 0xBB67AE85) between rounds.
+// ---------------------------------------------------------------------------
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
+                       uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+// The uniform used for element k of quantizer call `step`:
+// key = (seed low 32, seed high 32),
+// counter = (k>>2 low 32, k>>2 high 32, step low 32, step high 32),
+// word k & 3 of the output; u = (word >> 8) * 2^-24, an exact float in
+// [0, 1).  (The same counter split as a generator started at subsequence
+// `step` and offset k.)  Reading: the pages draw "ε ~ U(0,1)" per element
+// without naming a generator; Philox is the counter-based generator both
+// sides implement.
+float orc_uniform(uint64_t seed, uint64_t step, uint64_t k) {
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint64_t grp = k >> 2;
+  uint32_t ctr[4] = {(uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
+                     (uint32_t)(step >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  uint32_t wd = out[k & 3];
+  return (float)(wd >> 8) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Block-wise INT8 stochastic-rounding quantizer ([TUT] "FP32 → INT8 量化"
+// and the GradientQuantizeINT8 example)
+// ---------------------------------------------------------------------------
+// Per block of `block` elements (the last may be short):
+//   mx = max |g|  (a NaN never wins the comparison);  scale = mx / 127
+//   mx == 0: q = 0 and scale = 0
+//   else x = g/scale; f = floor(x); frac = x - f; q = f + (u < frac ? 1 : 0)
+//        clamped to [-127, 127]
+// deq (optional) = q * scale.  Reading: the example's "floor + Bernoulli"
+// form is used (not floor(x + eps)); the two agree in distribution.
+void orc_quant_int8(const float* g, uint64_t n, uint64_t block, uint64_t seed,
+                    uint64_t step, int8_t* q, float* block_scales, float* deq) {
+  for (uint64_t b0 = 0, bi = 0; b0 < n; b0 += block, ++bi) {
+    uint64_t b1 = b0 + block < n ? b0 + block : n;
+    float mx = 0.0f;
+    for (uint64_t k = b0; k < b1; ++k) {
+      float a = std::fabs(g[k]);
+      if (a > mx) mx = a;
+    }
+    if (mx == 0.0f) {
+      block_scales[bi] = 0.0f;
+      for (uint64_t k = b0; k < b1; ++k) {
+        q[k] = 0;
+        if (deq) deq[k] = 0.0f;
+      }
+      continue;
+    }
+    float scale = mx / 127.0f;
+    block_scales[bi] = scale;
+    for (uint64_t k = b0; k < b1; ++k) {
+      float x = g[k] / scale;
+      float f = std::floor(x);
+      float frac = x - f;
+      float u = orc_uniform(seed, step, k);
+      float qf = f + ((u < frac) ? 1.0f : 0.0f);
+      if (qf > 127.0f) qf = 127.0f;
+      if (qf < -127.0f) qf = -127.0f;
+      if (qf != qf) qf = 0.0f;  // a NaN input codes as 0 (reading)
+      q[k] = (int8_t)qf;
+      if (deq) deq[k] = qf * scale;
+    }
+  }
+}
+
+}  // extern "C"
