@@ -1,0 +1,255 @@
+/*
+ * ob.h -- C ABI of libob, the GB300 (sm_103a) implementation of the
+ * error-compensated 1-bit compressed optimizer step (1-bit Adam and 1-bit
+ * LAMB) and of a block-wise INT8 stochastic-rounding quantizer.
+ *
+ * Sources, cited by page title and section:
+ *   [BLOG] lqnn.cn, "1bit Adam" write-up: 2.1 error compensation, 6 warmup.
+ *   [TUT]  FreeGuideOnline, "梯度量化：将梯度从 FP32 压到 INT8 甚至 1-bit":
+ *          "FP32 → INT8 量化", "1-bit 梯度量化", GradientQuantizeINT8 example.
+ *   [LAMB] "1-bit LAMB (Error-Compensated LAMB-Preconditioned Large-Batch
+ *          Compressed Optimization)", paragraphs 1-4.
+ *
+ * Model.  W data-parallel workers are simulated as W resident buffer sets
+ * on one GPU.  One compressed step is
+ *     ob_compress       every worker compresses its momentum   ([LAMB] 2-3)
+ *     ob_server_reduce  server j averages partition j of all workers,
+ *                       adds its own error and compresses again ([LAMB] 3-4)
+ *     ob_adam_step      unpack + frozen-variance Adam            ([LAMB] 1)
+ *  or ob_lamb_step      unpack + 1-bit LAMB update               ([LAMB] 1-2)
+ * The worker-to-server "all-to-all" is the server kernel reading the
+ * workers' packed words straight from HBM.
+ *
+ * Layout.  n real elements, W workers, alignment A, chunk C (both multiples
+ * of 32).  P = roundup(ceil(n/W), A); n_pad = W*P; server j owns
+ * [jP, (j+1)P).  Each partition is cut into chunks of min(C, P) elements
+ * (the last one may be short); chunk g = j*cpp + kc, cpp = ceil(P/C).
+ * Elements k >= n are padding: they are excluded from every scale, their
+ * bit is 0, their error 0.
+ *   grads      W buffers of n_pad elements (fp32 or bf16)
+ *   err        W buffers of n_pad fp32 (worker error, deferred form)
+ *   bits       [W][n_pad/32] uint32; bit k%32 of word k/32 (LSB first) is
+ *              1 iff x[k] >= 0.0f (sign(+0) = sign(-0) = +1, NaN -> -1)
+ *   scales     [W][n_chunks] fp32, each worker's scale of every chunk
+ *   err_s      n_pad fp32 (server error, deferred form)
+ *   sbits      [n_pad/32] uint32; sscales [n_chunks] fp32
+ *   m, v, p    n_pad fp32 (momentum, frozen variance, parameters)
+ * Padding entries of m and of the errors are written as 0; padding entries
+ * of p and v are never written.
+ *
+ * Deferred errors.  ob_compress stores the compensated value x in err
+ * instead of e' = x - scale*sign(x): the scale needs the whole chunk, and
+ * storing x keeps the step single-pass.  The next ob_compress recovers e'
+ * from (x, bits, scales) bit for bit before using it.  The same holds for
+ * the server (err_s, sbits, sscales).  ob_materialize_errors writes e' into
+ * err/err_s and zeroes the scales, a state the next call reads the same
+ * way (e' - 0*sign = e').
+ *
+ * Arithmetic.  fp32, every operation rounded on its own (no contracted
+ * multiply-add, IEEE division and square root, no flush to zero).  Every
+ * sum that decides a scale or a norm follows one fixed order (4096-element
+ * tiles, 256 lanes adding elements 1024*i + 4*lane + c for i, c = 0..3,
+ * warp butterflies, a pairwise tree over 8 warps, tile totals added in
+ * order), so results are reproducible bit for bit.
+ *
+ * Conventions.
+ *   - Every function returns ob_status; ob_last_error(ctx) (or
+ *     ob_last_error(NULL) for calls without a ctx) gives a message.
+ *   - All device buffers are owned by the caller; the library allocates
+ *     no device memory.  ob_workspace_bytes() gives the size of the
+ *     scratch area the caller passes to ob_set_workspace().
+ *   - Calls are asynchronous on `stream`; nothing synchronises.  A launch
+ *     failure is reported as OB_ERR_CUDA.
+ *   - Device pointers must be 16-byte aligned (bits/sbits 4-byte, INT8
+ *     codes 4-byte).  Invalid arguments are rejected before any launch.
+ *   - A ctx is not thread-safe; distinct ctxs are independent.  Calls that
+ *     share a ctx (and so its workspace) must not overlap on the GPU.
+ */
+#ifndef OB_H
+#define OB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ob_stream_t; /* the same handle as cudaStream_t */
+typedef int ob_status;
+
+#define OB_OK 0
+#define OB_ERR_INVALID 1     /* bad argument or size */
+#define OB_ERR_ALIGN 2       /* misaligned pointer */
+#define OB_ERR_UNSUPPORTED 3 /* a configuration this build does not run */
+#define OB_ERR_CUDA 4        /* a CUDA call or launch failed */
+#define OB_ERR_STATE 5       /* call out of order (e.g. no workspace) */
+
+#define OB_GRAD_F32 0
+#define OB_GRAD_BF16 1
+
+#define OB_MODE_ADAM 0
+#define OB_MODE_LAMB 1
+
+#define OB_MAX_WORKERS 64
+
+/* ob_config.flags */
+#define OB_FLAG_NO_RATIO_EF (1u << 0) /* LAMB: error feedback factor rho = 1
+                                         instead of c_{t-2}/c_{t-1} */
+#define OB_FLAG_FROZEN_C (1u << 1)    /* LAMB: r = 1, c = c_avg ("LAMB +
+                                         basic 1-bit", [LAMB] 1) */
+
+typedef struct ob_config {
+  size_t n;                     /* real elements, >= 1, < 2^34 */
+  int W;                        /* workers, 1..OB_MAX_WORKERS */
+  size_t chunk;                 /* C: multiple of 32, >= 32 (clamped to P) */
+  size_t align;                 /* A: multiple of 32, >= 32 */
+  int grad_dtype;               /* OB_GRAD_F32 or OB_GRAD_BF16 */
+  int n_layers;                 /* 0: one layer [0, n) */
+  const size_t* layer_offsets;  /* host, n_layers+1 entries, 0 = off[0] <
+                                   off[1] < ... < off[n_layers] = n; copied */
+  float b1, b2, eps, lr;        /* Adam/LAMB hyperparameters */
+  float r_thr, r_min, r_max;    /* LAMB ratio clip ([LAMB] 1) */
+  float c_min, c_max;           /* LAMB coefficient clip ([LAMB] 3) */
+  uint32_t flags;               /* OB_FLAG_* */
+} ob_config;
+
+typedef struct ob_layout {
+  size_t n, n_pad, P, chunk;    /* chunk = min(C, P) */
+  size_t chunks_per_partition;  /* cpp */
+  size_t n_chunks;              /* W * cpp: length of sscales, and of each
+                                   worker's row of scales */
+  size_t words_per_worker;      /* n_pad / 32 */
+  size_t n_tiles;               /* 4096-element tiles, counted per chunk */
+  int W, n_layers;              /* n_layers >= 1 */
+} ob_layout;
+
+/* Per-layer state of 1-bit LAMB: device arrays of n_layers floats. */
+typedef struct ob_layer_state {
+  float* s;        /* fixed momentum scale sigma_l ([LAMB] 2) */
+  float* c_avg;    /* warmup average of LAMB's coefficient ([LAMB] 1) */
+  float* r_prev;   /* r_{t-1} */
+  float* c_prev;   /* c_{t-1} */
+  float* c_prev2;  /* c_{t-2} */
+  float* c_sum;    /* warmup: running sum of c */
+  float* c_t;      /* output: c of the latest step */
+} ob_layer_state;
+
+typedef struct ob_ctx ob_ctx;
+
+/* Validates cfg and builds the layout (host only; no CUDA call).
+ * OB_ERR_INVALID on a bad size, OB_ERR_UNSUPPORTED on W > OB_MAX_WORKERS. */
+ob_status ob_init(const ob_config* cfg, ob_ctx** out);
+ob_status ob_destroy(ob_ctx* ctx);
+const char* ob_last_error(const ob_ctx* ctx);
+ob_status ob_get_layout(const ob_ctx* ctx, ob_layout* out);
+
+/* Scratch: per-tile partial sums and arrival counters of the chunk scales,
+ * per-layer tables and accumulators.  Owned by the caller, device memory,
+ * 256-byte aligned, valid until the ctx is destroyed or another workspace
+ * is set.  ob_set_workspace enqueues its initialisation on `stream`. */
+ob_status ob_workspace_bytes(const ob_ctx* ctx, size_t* bytes);
+ob_status ob_set_workspace(ob_ctx* ctx, void* workspace, size_t bytes,
+                           ob_stream_t stream);
+
+/* One uncompressed warmup step ([BLOG] 6, [TUT] "预热训练"; [LAMB] 1):
+ *   g_bar = (sum_w g_w)/W; m = b1*m + (1-b1)*g_bar; v = b2*v + (1-b2)*g_bar^2
+ *   ADAM: p -= lr*(m/(sqrt(v)+eps))
+ *   LAMB: u = m/(sqrt(v)+eps); c_l = clip(||p_l||/||u_l||, c_min, c_max)
+ *         (1 if a norm is 0); p -= (lr*c_l)*u; ls->c_sum += c; ls->c_t = c
+ * grads: host array of W device pointers.  ls: NULL for ADAM. */
+ob_status ob_warmup_step(ob_ctx* ctx, const void* const* grads, float* m,
+                         float* v, float* p, int mode,
+                         const ob_layer_state* ls, ob_stream_t stream);
+
+/* End of warmup.  Zeroes err (W host-array pointers), err_s, bits, scales,
+ * sbits, sscales (the deferred form of e = 0).  v becomes the frozen
+ * variance v_Tw.  LAMB (ls != NULL): v_fresh = v; per layer
+ *   rms_l = ||m_l||/sqrt(n_l); s_l = mean(rms)/rms_l (1 if rms_l = 0)
+ *   c_avg = c_sum/warmup_steps; r_prev = 1; c_prev = c_prev2 = c_avg
+ * ([LAMB] 1-2).  m, v, v_fresh, ls may be NULL for ADAM. */
+ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s,
+                               uint32_t* bits, float* scales, uint32_t* sbits,
+                               float* sscales, const float* m, const float* v,
+                               float* v_fresh, const ob_layer_state* ls,
+                               int warmup_steps, ob_stream_t stream);
+
+/* Worker compression, all W workers ([BLOG] 2.1, [TUT] "1-bit 梯度量化",
+ * [LAMB] 2-3):
+ *   m_w = b1*m + (1-b1)*g_w
+ *   x   = sigma_l*m_w + rho_l*e_w    (ADAM: x = m_w + e_w)
+ *   scale(chunk) = mean |x| over the chunk's real elements
+ *   bit = x >= 0;  e_w' = x - scale*sign(x)   (stored deferred)
+ * sigma_l = ls->s, rho_l = ls->c_prev2/ls->c_prev (1 with
+ * OB_FLAG_NO_RATIO_EF); ls == NULL means 1-bit Adam.  m is not written. */
+ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m,
+                      float* const* err, uint32_t* bits, float* scales,
+                      const ob_layer_state* ls, ob_stream_t stream);
+
+/* Server average and re-compression, all partitions ([LAMB] 3-4):
+ *   z = (sum_w scale_w(chunk)*sign_w)/W;  y = rho_l*e_s + z
+ *   sscale(chunk) = mean |y|;  sbit = y >= 0;  e_s' = y - sscale*sign(y) */
+ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits,
+                           const float* scales, float* err_s, uint32_t* sbits,
+                           float* sscales, const ob_layer_state* ls,
+                           ob_stream_t stream);
+
+/* out = sscale*sign(sbit) (/ sigma_l if ls != NULL); padding -> 0. */
+ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits,
+                        const float* sscales, const ob_layer_state* ls,
+                        float* out, ob_stream_t stream);
+
+/* 1-bit Adam update with the frozen variance ([LAMB] 1, [BLOG] 2.1):
+ *   m = sscale*sign(sbit);  p -= lr*(m/(sqrt(v_frozen)+eps)) */
+ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits,
+                       const float* sscales, const float* v_frozen, float* m,
+                       float* p, ob_stream_t stream);
+
+/* 1-bit LAMB update ([LAMB] 1-3), in two element passes:
+ *   A: m_t = sscale*sign/sigma_l; g = (m_t - b1*m)/(1-b1);
+ *      v_fresh = b2*v_fresh + (1-b2)*g^2; R_l = max(v_frozen/v_fresh)
+ *      (NaN skipped)
+ *      then per layer r = clip(clip(R_l, (1-r_thr)r_prev, (1+r_thr)r_prev),
+ *      r_min, r_max); c = clip(c_avg*r, c_min, c_max); shift c_prev2 <-
+ *      c_prev <- c; r_prev <- r; ls->c_t = c
+ *   B: p -= (lr*c_l)*(m_t/(sqrt(v_frozen)+eps)) */
+ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits,
+                       const float* sscales, const float* v_frozen,
+                       float* v_fresh, float* m, float* p,
+                       const ob_layer_state* ls, ob_stream_t stream);
+
+/* compress + server_reduce + adam_step (ls == NULL) or lamb_step, in one
+ * call, in that order. */
+ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m,
+                  float* const* err, uint32_t* bits, float* scales,
+                  float* err_s, uint32_t* sbits, float* sscales,
+                  const float* v_frozen, float* v_fresh, float* p,
+                  const ob_layer_state* ls, ob_stream_t stream);
+
+/* Writes the true errors e' into err and err_s and zeroes scales and
+ * sscales.  Call only after a complete step (the update has consumed the
+ * scales). */
+ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err,
+                                const uint32_t* bits, float* scales,
+                                float* err_s, const uint32_t* sbits,
+                                float* sscales, ob_stream_t stream);
+
+/* Block-wise INT8 stochastic rounding ([TUT] "FP32 → INT8 量化" and the
+ * GradientQuantizeINT8 example), blocks of 256 elements (the last may be
+ * short):
+ *   mx = max |g| (NaN never wins); scale = mx/127 (0 if mx = 0, then q = 0)
+ *   x = g/scale; f = floor(x); q = f + (u < x - f); clamp to [-127, 127]
+ *   (a NaN codes as 0); deq = q*scale if deq != NULL
+ * u = (word >> 8) * 2^-24 from Philox4x32-10 (Salmon et al., SC'11) with
+ * key = seed, counter = (k>>2, step) as two 64-bit halves, word k&3.
+ * g and deq 16-byte aligned, q 4-byte aligned; n < 2^34.
+ * block_scales: ceil(n/256) floats. */
+ob_status ob_quant_int8(const float* g, size_t n, int8_t* q,
+                        float* block_scales, uint64_t seed, uint64_t step,
+                        float* deq, ob_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OB_H */

@@ -1,0 +1,338 @@
+"""Python binding of libob (include/ob.h): the GB300 implementation of the
+error-compensated 1-bit compressed optimizer step (1-bit Adam / 1-bit
+LAMB) and of the block-wise INT8 stochastic-rounding quantizer.
+
+This module only marshals arguments: torch tensors become device pointers
+and torch's current CUDA stream becomes the stream handle; every step of
+the path runs in the CUDA kernels of libob.so.  There is no CPU fallback:
+if libob.so is missing or cannot be loaded, `lib()` raises.
+
+Two layers:
+  * `ob_*` functions with the C names, taking an `ob_ctx` handle, tensors
+    (or lists of tensors) and an optional stream;
+  * `OneBitOptimizer`, which owns the device buffers of one simulated
+    data-parallel job (W workers on one GPU) and calls the `ob_*` functions
+    in the order of the method.
+"""
+import ctypes as ct
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libob.so")
+
+OB_OK, OB_ERR_INVALID, OB_ERR_ALIGN, OB_ERR_UNSUPPORTED, OB_ERR_CUDA, OB_ERR_STATE = range(6)
+OB_GRAD_F32, OB_GRAD_BF16 = 0, 1
+OB_MODE_ADAM, OB_MODE_LAMB = 0, 1
+OB_MAX_WORKERS = 64
+OB_FLAG_NO_RATIO_EF = 1 << 0
+OB_FLAG_FROZEN_C = 1 << 1
+
+# Every entry point include/ob.h declares.
+EXPORTS = (
+    "ob_init", "ob_destroy", "ob_last_error", "ob_get_layout", "ob_workspace_bytes",
+    "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
+    "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
+    "ob_materialize_errors", "ob_quant_int8",
+)
+
+
+class OBError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"libob status {status}: {msg}")
+        self.status = status
+
+
+class ob_config(ct.Structure):
+    _fields_ = [("n", ct.c_size_t), ("W", ct.c_int), ("chunk", ct.c_size_t),
+                ("align", ct.c_size_t), ("grad_dtype", ct.c_int), ("n_layers", ct.c_int),
+                ("layer_offsets", ct.POINTER(ct.c_size_t)),
+                ("b1", ct.c_float), ("b2", ct.c_float), ("eps", ct.c_float),
+                ("lr", ct.c_float), ("r_thr", ct.c_float), ("r_min", ct.c_float),
+                ("r_max", ct.c_float), ("c_min", ct.c_float), ("c_max", ct.c_float),
+                ("flags", ct.c_uint32)]
+
+
+class ob_layout(ct.Structure):
+    _fields_ = [("n", ct.c_size_t), ("n_pad", ct.c_size_t), ("P", ct.c_size_t),
+                ("chunk", ct.c_size_t), ("chunks_per_partition", ct.c_size_t),
+                ("n_chunks", ct.c_size_t), ("words_per_worker", ct.c_size_t),
+                ("n_tiles", ct.c_size_t), ("W", ct.c_int), ("n_layers", ct.c_int)]
+
+
+class ob_layer_state(ct.Structure):
+    _fields_ = [(k, ct.c_void_p) for k in
+                ("s", "c_avg", "r_prev", "c_prev", "c_prev2", "c_sum", "c_t")]
+
+
+_lib = None
+
+
+def lib():
+    """Loads libob.so (built by __graft_entry__.build() or _build.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                "g.build()'` (nvcc, sm_103a); there is no CPU fallback")
+        L = ct.CDLL(LIB_PATH)
+        vp, sz, i32, u64 = ct.c_void_p, ct.c_size_t, ct.c_int, ct.c_uint64
+        L.ob_init.argtypes = [ct.POINTER(ob_config), ct.POINTER(vp)]
+        L.ob_destroy.argtypes = [vp]
+        L.ob_last_error.argtypes = [vp]
+        L.ob_last_error.restype = ct.c_char_p
+        L.ob_get_layout.argtypes = [vp, ct.POINTER(ob_layout)]
+        L.ob_workspace_bytes.argtypes = [vp, ct.POINTER(sz)]
+        L.ob_set_workspace.argtypes = [vp, vp, sz, vp]
+        L.ob_warmup_step.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp]
+        L.ob_begin_compression.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp]
+        L.ob_compress.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ob_server_reduce.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ob_decompress.argtypes = [vp, vp, vp, vp, vp, vp]
+        L.ob_adam_step.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.ob_lamb_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ob_step.argtypes = [vp] * 14
+        L.ob_materialize_errors.argtypes = [vp] * 8
+        L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
+        for name in EXPORTS:
+            if name != "ob_last_error":
+                getattr(L, name).restype = ct.c_int
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# Marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(x):
+    """Device (or host) address of a tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(xs):
+    arr = (ct.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    return arr
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status, ctx=None):
+    if status != OB_OK:
+        msg = lib().ob_last_error(ctx).decode(errors="replace")
+        raise OBError(status, msg)
+
+
+class LayerState:
+    """Per-layer 1-bit LAMB state: seven float32 device tensors of n_layers
+    entries (s, c_avg, r_prev, c_prev, c_prev2, c_sum, c_t)."""
+
+    FIELDS = ("s", "c_avg", "r_prev", "c_prev", "c_prev2", "c_sum", "c_t")
+
+    def __init__(self, n_layers, device="cuda"):
+        import torch
+        for f in self.FIELDS:
+            setattr(self, f, torch.zeros(n_layers, dtype=torch.float32, device=device))
+
+    def struct(self):
+        return ob_layer_state(*[_ptr(getattr(self, f)) for f in self.FIELDS])
+
+
+def _ls(ls):
+    if ls is None:
+        return None
+    return ct.byref(ls.struct() if isinstance(ls, LayerState) else ls)
+
+
+# ---------------------------------------------------------------------------
+# The C entry points, same names
+# ---------------------------------------------------------------------------
+
+def ob_init(n, W, chunk, align=4096, grad_dtype=OB_GRAD_F32, layer_offsets=None,
+            b1=0.9, b2=0.999, eps=1e-8, lr=1e-4, r_thr=0.1, r_min=0.5, r_max=4.0,
+            c_min=0.01, c_max=10.0, flags=0):
+    """Returns an opaque ctx handle (int).  layer_offsets: sequence of
+    n_layers+1 ints, or None for one layer."""
+    cfg = ob_config(n=n, W=W, chunk=chunk, align=align, grad_dtype=grad_dtype,
+                    b1=b1, b2=b2, eps=eps, lr=lr, r_thr=r_thr, r_min=r_min, r_max=r_max,
+                    c_min=c_min, c_max=c_max, flags=flags)
+    keep = None
+    if layer_offsets is not None:
+        keep = (ct.c_size_t * len(layer_offsets))(*[int(x) for x in layer_offsets])
+        cfg.n_layers = len(layer_offsets) - 1
+        cfg.layer_offsets = ct.cast(keep, ct.POINTER(ct.c_size_t))
+    h = ct.c_void_p()
+    _check(lib().ob_init(ct.byref(cfg), ct.byref(h)))
+    return h.value
+
+
+def ob_destroy(ctx):
+    lib().ob_destroy(ctx)
+
+
+def ob_last_error(ctx=None):
+    return lib().ob_last_error(ctx).decode(errors="replace")
+
+
+def ob_get_layout(ctx):
+    lay = ob_layout()
+    _check(lib().ob_get_layout(ctx, ct.byref(lay)), ctx)
+    return {k: getattr(lay, k) for k, _ in ob_layout._fields_}
+
+
+def ob_workspace_bytes(ctx):
+    b = ct.c_size_t()
+    _check(lib().ob_workspace_bytes(ctx, ct.byref(b)), ctx)
+    return b.value
+
+
+def ob_set_workspace(ctx, workspace, nbytes=None, stream=None):
+    if nbytes is None:
+        nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().ob_set_workspace(ctx, _ptr(workspace), nbytes, _stream(stream)), ctx)
+
+
+def ob_warmup_step(ctx, grads, m, v, p, mode=OB_MODE_ADAM, ls=None, stream=None):
+    _check(lib().ob_warmup_step(ctx, _ptr_array(grads), _ptr(m), _ptr(v), _ptr(p), mode,
+                                _ls(ls), _stream(stream)), ctx)
+
+
+def ob_begin_compression(ctx, err, err_s, bits, scales, sbits, sscales, m=None, v=None,
+                         v_fresh=None, ls=None, warmup_steps=0, stream=None):
+    _check(lib().ob_begin_compression(ctx, _ptr_array(err), _ptr(err_s), _ptr(bits),
+                                      _ptr(scales), _ptr(sbits), _ptr(sscales), _ptr(m),
+                                      _ptr(v), _ptr(v_fresh), _ls(ls), warmup_steps,
+                                      _stream(stream)), ctx)
+
+
+def ob_compress(ctx, grads, m, err, bits, scales, ls=None, stream=None):
+    _check(lib().ob_compress(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err), _ptr(bits),
+                             _ptr(scales), _ls(ls), _stream(stream)), ctx)
+
+
+def ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls=None, stream=None):
+    _check(lib().ob_server_reduce(ctx, _ptr(bits), _ptr(scales), _ptr(err_s), _ptr(sbits),
+                                  _ptr(sscales), _ls(ls), _stream(stream)), ctx)
+
+
+def ob_decompress(ctx, sbits, sscales, out, ls=None, stream=None):
+    _check(lib().ob_decompress(ctx, _ptr(sbits), _ptr(sscales), _ls(ls), _ptr(out),
+                               _stream(stream)), ctx)
+
+
+def ob_adam_step(ctx, sbits, sscales, v_frozen, m, p, stream=None):
+    _check(lib().ob_adam_step(ctx, _ptr(sbits), _ptr(sscales), _ptr(v_frozen), _ptr(m),
+                              _ptr(p), _stream(stream)), ctx)
+
+
+def ob_lamb_step(ctx, sbits, sscales, v_frozen, v_fresh, m, p, ls, stream=None):
+    _check(lib().ob_lamb_step(ctx, _ptr(sbits), _ptr(sscales), _ptr(v_frozen), _ptr(v_fresh),
+                              _ptr(m), _ptr(p), _ls(ls), _stream(stream)), ctx)
+
+
+def ob_step(ctx, grads, m, err, bits, scales, err_s, sbits, sscales, v_frozen, v_fresh, p,
+            ls=None, stream=None):
+    _check(lib().ob_step(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err), _ptr(bits),
+                         _ptr(scales), _ptr(err_s), _ptr(sbits), _ptr(sscales),
+                         _ptr(v_frozen), _ptr(v_fresh), _ptr(p), _ls(ls), _stream(stream)),
+           ctx)
+
+
+def ob_materialize_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=None):
+    _check(lib().ob_materialize_errors(ctx, _ptr_array(err), _ptr(bits), _ptr(scales),
+                                       _ptr(err_s), _ptr(sbits), _ptr(sscales),
+                                       _stream(stream)), ctx)
+
+
+def ob_quant_int8(g, q, block_scales, seed, step, deq=None, n=None, stream=None):
+    if n is None:
+        n = g.numel()
+    _check(lib().ob_quant_int8(_ptr(g), n, _ptr(q), _ptr(block_scales), seed, step, _ptr(deq),
+                               _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# One simulated data-parallel job
+# ---------------------------------------------------------------------------
+
+class OneBitOptimizer:
+    """Device buffers and call order of one 1-bit Adam / 1-bit LAMB job with
+    W workers simulated on one GPU.
+
+    Buffers (torch, on `device`): m, v (frozen after warmup), p, v_fresh
+    (LAMB), err[W], err_s, bits [W, words], scales [W, n_chunks], sbits,
+    sscales, the workspace, and the per-layer LAMB state."""
+
+    def __init__(self, n, W, chunk, align=4096, grad_dtype="f32", layer_offsets=None,
+                 lamb=False, device="cuda", **hp):
+        import torch
+        self.lamb = lamb
+        self.grad_dtype = grad_dtype
+        self.ctx = ob_init(n, W, chunk, align,
+                           OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32,
+                           layer_offsets, **hp)
+        lay = ob_get_layout(self.ctx)
+        self.layout = lay
+        self.n, self.W, self.n_pad = n, W, lay["n_pad"]
+        z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)
+        self.m, self.v, self.p = z(self.n_pad), z(self.n_pad), z(self.n_pad)
+        self.v_fresh = z(self.n_pad) if lamb else None
+        self.err = [z(self.n_pad) for _ in range(W)]
+        self.err_s = z(self.n_pad)
+        words = lay["words_per_worker"]
+        self.bits = z(W, words, dt=torch.int32)
+        self.scales = z(W, lay["n_chunks"])
+        self.sbits = z(words, dt=torch.int32)
+        self.sscales = z(lay["n_chunks"])
+        nbytes = ob_workspace_bytes(self.ctx)
+        self.workspace = torch.zeros((nbytes + 255) // 256 * 256 // 4, dtype=torch.float32,
+                                     device=device)
+        ob_set_workspace(self.ctx, self.workspace, nbytes)
+        self.ls = LayerState(lay["n_layers"], device) if lamb else None
+        self.warmup_steps = 0
+
+    def close(self):
+        if self.ctx:
+            ob_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def grad_buffers(self):
+        import torch
+        dt = torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
+        return [torch.zeros(self.n_pad, dtype=dt, device=self.m.device) for _ in range(self.W)]
+
+    def warmup_step(self, grads, stream=None):
+        ob_warmup_step(self.ctx, grads, self.m, self.v, self.p,
+                       OB_MODE_LAMB if self.lamb else OB_MODE_ADAM, self.ls, stream)
+        self.warmup_steps += 1
+
+    def begin_compression(self, stream=None):
+        ob_begin_compression(self.ctx, self.err, self.err_s, self.bits, self.scales, self.sbits,
+                             self.sscales, self.m, self.v, self.v_fresh,
+                             self.ls if self.lamb else None, max(self.warmup_steps, 1), stream)
+
+    def compressed_step(self, grads, stream=None):
+        ob_step(self.ctx, grads, self.m, self.err, self.bits, self.scales, self.err_s,
+                self.sbits, self.sscales, self.v, self.v_fresh, self.p,
+                self.ls if self.lamb else None, stream)
+
+    def materialize_errors(self, stream=None):
+        ob_materialize_errors(self.ctx, self.err, self.bits, self.scales, self.err_s,
+                              self.sbits, self.sscales, stream)

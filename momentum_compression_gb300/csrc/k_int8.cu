@@ -1,0 +1,134 @@
+// Block-wise INT8 stochastic-rounding quantizer (gradient quantization
+// tutorial, "FP32 → INT8 量化": scale = max|g|/127 per block, stochastic
+// rounding; and its GradientQuantizeINT8 example: floor plus a Bernoulli
+// draw on the fractional part, clamp to ±127).
+//
+// One warp per block of 256 elements: lane j holds elements 4j..4j+3 and
+// 128+4j..128+4j+3 (two 128-bit loads), the block max is a warp max, and
+// each group of four elements draws one Philox4x32-10 output (four 32-bit
+// words) from counter (k>>2, step).
+//
+// Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64-bit
+// products with multipliers 0xD2511F53 and 0xCD9E8D57, the key advanced by
+// 0x9E3779B9 and 0xBB67AE85 between rounds.
+#include "ob_internal.cuh"
+
+namespace ob {
+namespace {
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
+  return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
+}
+
+// Quantizes the 4 elements of group `grp` (elements 4*grp .. 4*grp+3).
+__device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64_t grp,
+                                           uint64_t step, uint32_t k0, uint32_t k1,
+                                           int nvalid, float4& dq) {
+  const uint4 ctr = make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
+                               (uint32_t)(step >> 32));
+  const uint4 rnd = philox4x32_10(ctr, k0, k1);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float qf = 0.0f;
+    if (c < nvalid && scale != 0.0f) {
+      const float x = __fdiv_rn(f4get(gv, c), scale);
+      const float f = floorf(x);
+      const float fr = __fsub_rn(x, f);
+      const float u = __fmul_rn((float)(word_of(rnd, c) >> 8), 5.9604644775390625e-08f);
+      qf = __fadd_rn(f, (u < fr) ? 1.0f : 0.0f);
+      qf = qf > 127.0f ? 127.0f : qf;
+      qf = qf < -127.0f ? -127.0f : qf;
+      if (qf != qf) qf = 0.0f;
+    }
+    f4at(dq, c) = __fmul_rn(qf, scale);
+    packed |= ((uint32_t)(int32_t)qf & 0xffu) << (8 * c);
+  }
+  return packed;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
+                 float* __restrict__ scales, uint64_t seed, uint64_t step,
+                 float* __restrict__ deq) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t nblk = (n + 255) / 256;
+  const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
+  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (uint64_t b = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); b < nblk;
+       b += warps) {
+    float4 gv[2];
+    int nv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t k = b * 256 + 128 * h + 4 * lane;
+      nv[h] = k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
+      if (nv[h] == 4) {
+        gv[h] = __ldcs(reinterpret_cast<const float4*>(g + k));
+      } else {
+        gv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < nv[h]; ++c) f4at(gv[h], c) = g[k + c];
+      }
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float a = fabsf(f4at(gv[h], c));
+        if (c < nv[h] && a > mx) mx = a;  // a NaN never wins
+      }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float other = __shfl_xor_sync(kFull, mx, o);
+      if (other > mx) mx = other;
+    }
+    const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, 127.0f);
+    if (lane == 0) scales[b] = scale;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (nv[h] == 0) continue;
+      const uint64_t k = b * 256 + 128 * h + 4 * lane;
+      float4 dq;
+      const uint32_t packed = quant4(gv[h], scale, k >> 2, step, k0, k1, nv[h], dq);
+      if (nv[h] == 4) {
+        *reinterpret_cast<uint32_t*>(q + k) = packed;
+        if (deq) __stcs(reinterpret_cast<float4*>(deq + k), dq);
+      } else {
+        for (int c = 0; c < nv[h]; ++c) {
+          q[k + c] = (int8_t)((packed >> (8 * c)) & 0xffu);
+          if (deq) deq[k + c] = f4at(dq, c);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_int8(const float* g, uint64_t n, int8_t* q, float* scales,
+                              uint64_t seed, uint64_t step, float* deq, int sms,
+                              cudaStream_t s) {
+  const uint64_t nblk = (n + 255) / 256;
+  const uint64_t ctas = (nblk + kThreads / 32 - 1) / (kThreads / 32);
+  k_quant_int8<<<grid_for(k_quant_int8, sms, ctas), kThreads, 0, s>>>(g, n, q, scales, seed,
+                                                                      step, deq);
+  return cudaGetLastError();
+}
+
+}  // namespace ob

@@ -1,0 +1,302 @@
+// Unpack + update kernels of the 1-bit compressed optimizer step, and the
+// standalone decompression and error materialisation.
+//
+//   1-bit Adam (1-bit LAMB summary, paragraph 1: the frozen denominator
+//   sqrt(v_Tw); "1bit Adam" write-up, 2.1):
+//     m = sscale*sign(sbit);  p = p - lr*(m/(sqrt(v_Tw)+eps))
+//   1-bit LAMB (1-bit LAMB summary, paragraphs 1-3), pass A:
+//     m_t = sscale*sign/sigma_l; g = (m_t - b1*m_{t-1})/(1-b1)
+//     v_t = b2*v_t + (1-b2)*g^2;  R_l = max over the layer of v_Tw/v_t
+//   then per layer (by the last CTA of pass A):
+//     r = clip(clip(R_l, (1-r_thr)r_prev, (1+r_thr)r_prev), r_min, r_max)
+//     c = clip(c_avg*r, c_min, c_max); c_prev2 <- c_prev <- c; r_prev <- r
+//   pass B:
+//     p = p - (lr*c_l)*(m_t/(sqrt(v_Tw)+eps))
+// All operations are rounded one by one (no contraction), with IEEE
+// division and square root.
+#include "ob_internal.cuh"
+
+namespace ob {
+namespace {
+
+__global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    if (tl.start >= G.n) {
+      // whole tile is padding: m = 0
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (off < tl.len)
+          __stcs(reinterpret_cast<float4*>(A.m + tl.start + off), make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+      continue;
+    }
+    const float osc = __ldcg(A.sscales + tl.g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      const uint32_t wd = __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7));
+      const float4 vv = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
+      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+      float4 mo;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (k0 + c < G.n) {
+          const float mk = ((wd >> c) & 1u) ? osc : -osc;
+          const float d = __fadd_rn(__fsqrt_rn(f4get(vv, c)), A.eps);
+          const float u = __fdiv_rn(mk, d);
+          f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(A.lr, u));
+          f4at(mo, c) = mk;
+        } else {
+          f4at(mo, c) = 0.0f;
+        }
+      }
+      __stcs(reinterpret_cast<float4*>(A.m + k0), mo);
+      if (k0 < G.n) __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+    }
+  }
+}
+
+// Per-layer ratio and coefficient, run by one CTA.
+__device__ void lamb_ratio_all(const UpdateArgs& A) {
+  const LambHP& h = A.hp;
+  for (uint32_t l = threadIdx.x; l < A.geo.L; l += kThreads) {
+    const float R = __uint_as_float(__ldcg(A.ws.Rbits + l));
+    const float rp = A.ls.r_prev[l];
+    float r;
+    if (h.frozen) {
+      r = 1.0f;
+    } else {
+      const float lo = __fmul_rn(__fsub_rn(1.0f, h.r_thr), rp);
+      const float hi = __fmul_rn(__fadd_rn(1.0f, h.r_thr), rp);
+      r = fmin_plain(fmax_plain(R, lo), hi);
+      r = fmin_plain(fmax_plain(r, h.r_min), h.r_max);
+    }
+    float c = __fmul_rn(A.ls.c_avg[l], r);
+    c = fmin_plain(fmax_plain(c, h.c_min), h.c_max);
+    A.ls.c_prev2[l] = A.ls.c_prev[l];
+    A.ls.c_prev[l] = c;
+    A.ls.r_prev[l] = r;
+    A.ls.c_t[l] = c;
+    A.ws.Rbits[l] = 0u;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
+  __shared__ int s_last;
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    const float osc = __ldcg(A.sscales + tl.g);
+    uint32_t l = __ldg(A.ws.tile_layer + T);
+    uint64_t lend = __ldg(A.ws.layer_off + l + 1);
+    float sg_l = __ldg(A.ls.s + l);
+    float rmax = 0.0f;  // running max of the ratio for layer l
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      if (k0 >= G.n) {
+        __stcs(reinterpret_cast<float4*>(A.m + k0), make_float4(0.f, 0.f, 0.f, 0.f));
+        continue;
+      }
+      const uint32_t wd = __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7));
+      float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
+      float4 vt = __ldcs(reinterpret_cast<const float4*>(A.v_fresh + k0));
+      const float4 vf = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t k = k0 + c;
+        if (k >= G.n) {
+          f4at(mv, c) = 0.0f;
+          continue;
+        }
+        const uint32_t l_old = l;
+        if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
+          if (rmax > 0.0f) atomicMax(A.ws.Rbits + l_old, __float_as_uint(rmax));
+          rmax = 0.0f;
+          sg_l = __ldg(A.ls.s + l);
+        }
+        const float M = ((wd >> c) & 1u) ? osc : -osc;
+        const float mt = __fdiv_rn(M, sg_l);
+        const float gt = __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, f4at(mv, c))), A.ob1);
+        const float v = __fadd_rn(__fmul_rn(A.b2, f4at(vt, c)),
+                                  __fmul_rn(A.ob2, __fmul_rn(gt, gt)));
+        f4at(mv, c) = mt;
+        f4at(vt, c) = v;
+        const float ratio = __fdiv_rn(f4get(vf, c), v);
+        if (ratio > rmax) rmax = ratio;  // NaN never wins
+      }
+      __stcs(reinterpret_cast<float4*>(A.m + k0), mv);
+      __stcs(reinterpret_cast<float4*>(A.v_fresh + k0), vt);
+    }
+    // Flush the running max: one atomic per warp when all its lanes ended
+    // in the same layer, else one per lane.
+    const uint32_t l0 = __shfl_sync(kFull, l, 0);
+    if (__all_sync(kFull, l == l0)) {
+      float wmax = rmax;
+      for (int o = 16; o >= 1; o >>= 1) wmax = fmax_plain(wmax, __shfl_xor_sync(kFull, wmax, o));
+      if ((p & 31) == 0 && wmax > 0.0f) atomicMax(A.ws.Rbits + l, __float_as_uint(wmax));
+    } else if (rmax > 0.0f) {
+      atomicMax(A.ws.Rbits + l, __float_as_uint(rmax));
+    }
+  }
+  // Last CTA of the grid: per-layer ratio and coefficient.
+  __threadfence();
+  __syncthreads();
+  if (p == 0) {
+    unsigned prev = atomicAdd(A.ws.gcnt + 0, 1u);
+    s_last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    lamb_ratio_all(A);
+    if (p == 0) A.ws.gcnt[0] = 0u;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    if (tl.start >= G.n) continue;
+    uint32_t l = __ldg(A.ws.tile_layer + T);
+    uint64_t lend = __ldg(A.ws.layer_off + l + 1);
+    float t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      if (k0 >= G.n) continue;
+      const float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
+      const float4 vf = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
+      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t k = k0 + c;
+        if (k >= G.n) continue;
+        if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+          t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+        const float d = __fadd_rn(__fsqrt_rn(f4get(vf, c)), A.eps);
+        const float u = __fdiv_rn(f4get(mv, c), d);
+        f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(t1, u));
+      }
+      __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+    }
+  }
+}
+
+template <bool LAYERED>
+__global__ void __launch_bounds__(kThreads) k_decompress(const UpdateArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    const float osc = __ldcg(A.sscales + tl.g);
+    uint32_t l = 0;
+    uint64_t lend = 0;
+    float sg_l = 1.0f;
+    if constexpr (LAYERED) {
+      l = __ldg(A.ws.tile_layer + T);
+      lend = __ldg(A.ws.layer_off + l + 1);
+      sg_l = __ldg(A.ls.s + l);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      const uint32_t wd = __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7));
+      float4 o;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t k = k0 + c;
+        float M = 0.0f;
+        if (k < G.n) {
+          M = ((wd >> c) & 1u) ? osc : -osc;
+          if constexpr (LAYERED) {
+            if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) sg_l = __ldg(A.ls.s + l);
+            M = __fdiv_rn(M, sg_l);
+          }
+        }
+        f4at(o, c) = M;
+      }
+      __stcs(reinterpret_cast<float4*>(A.out + k0), o);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_materialize(const MaterializeArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    if (tl.start >= G.n) continue;
+    for (uint32_t w = 0; w <= G.W; ++w) {
+      // w < W: worker errors; w == W: the server error
+      float* e = w < G.W ? A.e[w] : A.e_s;
+      const uint32_t* bw = w < G.W ? A.bits + (uint64_t)w * G.words : A.sbits;
+      const float sc = w < G.W ? __ldcg(A.scales + (uint64_t)w * G.nc + tl.g)
+                               : __ldcg(A.sscales + tl.g);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (off >= tl.len) continue;
+        const uint64_t k0 = tl.start + off;
+        if (k0 >= G.n) continue;
+        const uint32_t wd = bw[k0 >> 5] >> (4 * (p & 7));
+        float4 ev = *reinterpret_cast<const float4*>(e + k0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (k0 + c >= G.n) continue;
+          const float so = ((wd >> c) & 1u) ? sc : -sc;
+          f4at(ev, c) = __fsub_rn(f4at(ev, c), so);
+        }
+        *reinterpret_cast<float4*>(e + k0) = ev;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s) {
+  k_adam_update<<<grid_for(k_adam_update, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lamb_pass_a(const UpdateArgs& a, int sms, cudaStream_t s) {
+  k_lamb_pass_a<<<grid_for(k_lamb_pass_a, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s) {
+  k_lamb_pass_b<<<grid_for(k_lamb_pass_b, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
+                              cudaStream_t s) {
+  if (layered)
+    k_decompress<true><<<grid_for(k_decompress<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  else
+    k_decompress<false><<<grid_for(k_decompress<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s) {
+  k_materialize<<<grid_for(k_materialize, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ob

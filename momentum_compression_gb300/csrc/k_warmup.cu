@@ -1,0 +1,316 @@
+// Uncompressed warmup steps and the switch to compression.
+//
+// The "1bit Adam" write-up (6, tuning) and the gradient quantization
+// tutorial ("预热训练") run the first steps at full precision; the 1-bit
+// LAMB summary (paragraph 1) freezes v at the end of warmup and keeps the
+// warmup average c_avg of LAMB's coefficient, and (paragraph 2) fixes a
+// per-layer momentum scale from the momentum norms at that point.
+//
+//   g_bar = (sum over w, in order, from 0, of g_w) / W
+//   m = b1*m + (1-b1)*g_bar;  v = b2*v + (1-b2)*g_bar^2
+//   Adam:  p = p - lr*(m/(sqrt(v)+eps))
+//   LAMB:  u = m/(sqrt(v)+eps); c_l = clip(||p_l||/||u_l||, c_min, c_max)
+//          (1 if a norm is 0); p = p - (lr*c_l)*u
+//   begin: rms_l = ||m_l||/sqrt(n_l); s_l = mean(rms)/rms_l;
+//          c_avg = c_sum/T_w; r_prev = 1; c_prev = c_prev2 = c_avg
+//
+// Layer norms use the fixed tile order counted from each layer's own
+// start, so those kernels walk "layer tiles" with scalar loads (a layer may
+// start at any element).
+#include "ob_internal.cuh"
+
+namespace ob {
+namespace {
+
+template <bool BF16>
+__device__ __forceinline__ float load_grad1(const void* g, uint64_t k) {
+  if constexpr (BF16) return bf16_to_f32(__ldcs(static_cast<const unsigned short*>(g) + k));
+  else return __ldcs(static_cast<const float*>(g) + k);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) k_warmup_adam(const WarmupArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      if (k0 >= G.n) {
+        __stcs(reinterpret_cast<float4*>(A.m + k0), make_float4(0.f, 0.f, 0.f, 0.f));
+        continue;
+      }
+      float4 gb = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t w = 0; w < G.W; ++w) {
+        const float4 gv = load_grad4<BF16>(A.g[w], k0);
+        gb.x = __fadd_rn(gb.x, gv.x);
+        gb.y = __fadd_rn(gb.y, gv.y);
+        gb.z = __fadd_rn(gb.z, gv.z);
+        gb.w = __fadd_rn(gb.w, gv.w);
+      }
+      float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
+      float4 vv = __ldcs(reinterpret_cast<const float4*>(A.v + k0));
+      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (k0 + c >= G.n) {
+          f4at(mv, c) = 0.0f;
+          continue;
+        }
+        const float g = __fdiv_rn(f4at(gb, c), A.fW);
+        const float m = __fadd_rn(__fmul_rn(A.b1, f4at(mv, c)), __fmul_rn(A.ob1, g));
+        const float v = __fadd_rn(__fmul_rn(A.b2, f4at(vv, c)),
+                                  __fmul_rn(A.ob2, __fmul_rn(g, g)));
+        const float d = __fadd_rn(__fsqrt_rn(v), A.eps);
+        const float u = __fdiv_rn(m, d);
+        f4at(mv, c) = m;
+        f4at(vv, c) = v;
+        f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(A.lr, u));
+      }
+      __stcs(reinterpret_cast<float4*>(A.m + k0), mv);
+      __stcs(reinterpret_cast<float4*>(A.v + k0), vv);
+      __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+    }
+  }
+}
+
+// Layer tile LT -> (layer, tile inside the layer, first element, length).
+struct LTile {
+  uint32_t l, t, len;
+  uint64_t start;
+};
+
+__device__ __forceinline__ LTile decode_ltile(const Workspace& ws, uint32_t L, uint32_t LT) {
+  uint32_t lo = 0, hi = L;  // pref[lo] <= LT < pref[hi]
+  while (hi - lo > 1) {
+    uint32_t mid = (lo + hi) >> 1;
+    if (__ldg(ws.ltile_pref + mid) <= LT) lo = mid; else hi = mid;
+  }
+  LTile r;
+  r.l = lo;
+  r.t = LT - __ldg(ws.ltile_pref + lo);
+  const uint64_t a = __ldg(ws.layer_off + lo), b = __ldg(ws.layer_off + lo + 1);
+  r.start = a + (uint64_t)r.t * kTile;
+  const uint64_t left = b - r.start;
+  r.len = (uint32_t)(left < kTile ? left : kTile);
+  return r;
+}
+
+// Block total of two lane sums in the fixed order; valid in thread 0.
+__device__ __forceinline__ void block_sum2(float a, float b, float (*ws)[8], float& ta,
+                                           float& tb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_butterfly_sum(a);
+  b = warp_butterfly_sum(b);
+  if (lane == 0) {
+    ws[0][warp] = a;
+    ws[1][warp] = b;
+  }
+  __syncthreads();
+  ta = tree8(ws[0]);
+  tb = tree8(ws[1]);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) k_warmup_lamb_a(const WarmupArgs A) {
+  __shared__ float ws[2][8];
+  __shared__ int s_last;
+  const Geo& G = A.geo;
+  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
+    const LTile lt = decode_ltile(A.ws, G.L, LT);
+    float accp = 0.0f, accu = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t idx = 1024u * i + 4u * p + c;
+        if (idx >= lt.len) continue;
+        const uint64_t k = lt.start + idx;
+        float gb = 0.0f;
+        for (uint32_t w = 0; w < G.W; ++w) gb = __fadd_rn(gb, load_grad1<BF16>(A.g[w], k));
+        gb = __fdiv_rn(gb, A.fW);
+        const float m = __fadd_rn(__fmul_rn(A.b1, A.m[k]), __fmul_rn(A.ob1, gb));
+        const float v = __fadd_rn(__fmul_rn(A.b2, A.v[k]), __fmul_rn(A.ob2, __fmul_rn(gb, gb)));
+        const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));
+        A.m[k] = m;
+        A.v[k] = v;
+        const float pk = A.p[k];
+        accp = __fadd_rn(accp, __fmul_rn(pk, pk));
+        accu = __fadd_rn(accu, __fmul_rn(u, u));
+      }
+    float tp, tu;
+    block_sum2(accp, accu, ws, tp, tu);
+    if (p == 0) {
+      A.ws.lpart[LT] = tp;
+      A.ws.lpart[G.n_ltiles + LT] = tu;
+    }
+    __threadfence();
+    __syncthreads();
+    if (p == 0) {
+      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - __ldg(A.ws.ltile_pref + lt.l);
+      unsigned prev = atomicAdd(A.ws.lcnt + lt.l, 1u);
+      s_last = (prev == ntl - 1);
+    }
+    __syncthreads();
+    if (s_last && warp == 0) {
+      __threadfence();
+      const uint32_t b = __ldg(A.ws.ltile_pref + lt.l);
+      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - b;
+      const float np = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
+      const float nu = __fsqrt_rn(ordered_sum(A.ws.lpart + G.n_ltiles + b, ntl, lane));
+      if (lane == 0) {
+        float c;
+        if (np == 0.0f || nu == 0.0f) {
+          c = 1.0f;
+        } else {
+          c = __fdiv_rn(np, nu);
+          c = fmin_plain(fmax_plain(c, A.c_min), A.c_max);
+        }
+        A.ls.c_t[lt.l] = c;
+        A.ls.c_sum[lt.l] = __fadd_rn(A.ls.c_sum[lt.l], c);
+        A.ws.lcnt[lt.l] = 0u;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_warmup_lamb_b(const WarmupArgs A) {
+  const Geo& G = A.geo;
+  const int p = threadIdx.x;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    const Tile tl = decode_tile(G, T);
+    uint32_t l = __ldg(A.ws.tile_layer + T);
+    uint64_t lend = __ldg(A.ws.layer_off + l + 1);
+    float t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      if (off >= tl.len) continue;
+      const uint64_t k0 = tl.start + off;
+      if (k0 >= G.n) {
+        __stcs(reinterpret_cast<float4*>(A.m + k0), make_float4(0.f, 0.f, 0.f, 0.f));
+        continue;
+      }
+      float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
+      const float4 vv = __ldcs(reinterpret_cast<const float4*>(A.v + k0));
+      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t k = k0 + c;
+        if (k >= G.n) {
+          f4at(mv, c) = 0.0f;
+          continue;
+        }
+        if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+          t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+        const float u = __fdiv_rn(f4at(mv, c), __fadd_rn(__fsqrt_rn(f4get(vv, c)), A.eps));
+        f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(t1, u));
+      }
+      if (k0 + 3 >= G.n) __stcs(reinterpret_cast<float4*>(A.m + k0), mv);
+      __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_lamb_begin(const WarmupArgs A) {
+  __shared__ float ws[2][8];
+  __shared__ int s_last;
+  __shared__ int s_all;
+  __shared__ float s_mean;
+  const Geo& G = A.geo;
+  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
+    const LTile lt = decode_ltile(A.ws, G.L, LT);
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t idx = 1024u * i + 4u * p + c;
+        if (idx >= lt.len) continue;
+        const float mk = A.m[lt.start + idx];
+        acc = __fadd_rn(acc, __fmul_rn(mk, mk));
+      }
+    float tm, unused;
+    block_sum2(acc, 0.0f, ws, tm, unused);
+    if (p == 0) A.ws.lpart[LT] = tm;
+    __threadfence();
+    __syncthreads();
+    if (p == 0) {
+      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - __ldg(A.ws.ltile_pref + lt.l);
+      unsigned prev = atomicAdd(A.ws.lcnt + lt.l, 1u);
+      s_last = (prev == ntl - 1);
+      s_all = 0;
+    }
+    __syncthreads();
+    if (s_last) {
+      if (warp == 0) {
+        __threadfence();
+        const uint32_t b = __ldg(A.ws.ltile_pref + lt.l);
+        const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - b;
+        const float nrm = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
+        if (lane == 0) {
+          const uint64_t nl = __ldg(A.ws.layer_off + lt.l + 1) - __ldg(A.ws.layer_off + lt.l);
+          A.ws.rms[lt.l] = __fdiv_rn(nrm, __fsqrt_rn(__ull2float_rn(nl)));
+          A.ws.lcnt[lt.l] = 0u;
+          __threadfence();
+          unsigned prev = atomicAdd(A.ws.gcnt + 1, 1u);
+          s_all = (prev == G.L - 1);
+        }
+      }
+      __syncthreads();
+      if (s_all) {
+        __threadfence();
+        if (p == 0) {
+          float mean = 0.0f;
+          for (uint32_t l = 0; l < G.L; ++l) mean = __fadd_rn(mean, __ldcg(A.ws.rms + l));
+          s_mean = __fdiv_rn(mean, (float)G.L);
+          A.ws.gcnt[1] = 0u;
+        }
+        __syncthreads();
+        const float fT = (float)A.warmup_steps;
+        for (uint32_t l = p; l < G.L; l += kThreads) {
+          const float rms = __ldcg(A.ws.rms + l);
+          A.ls.s[l] = rms == 0.0f ? 1.0f : __fdiv_rn(s_mean, rms);
+          const float ca = __fdiv_rn(A.ls.c_sum[l], fT);
+          A.ls.c_avg[l] = ca;
+          A.ls.r_prev[l] = 1.0f;
+          A.ls.c_prev[l] = ca;
+          A.ls.c_prev2[l] = ca;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_warmup_adam(const WarmupArgs& a, bool bf16, int sms, cudaStream_t s) {
+  const uint64_t nt = a.geo.n_tiles;
+  if (bf16) k_warmup_adam<true><<<grid_for(k_warmup_adam<true>, sms, nt), kThreads, 0, s>>>(a);
+  else k_warmup_adam<false><<<grid_for(k_warmup_adam<false>, sms, nt), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_warmup_lamb(const WarmupArgs& a, bool bf16, int sms, cudaStream_t s) {
+  const uint64_t nlt = a.geo.n_ltiles;
+  if (bf16) k_warmup_lamb_a<true><<<grid_for(k_warmup_lamb_a<true>, sms, nlt), kThreads, 0, s>>>(a);
+  else k_warmup_lamb_a<false><<<grid_for(k_warmup_lamb_a<false>, sms, nlt), kThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_warmup_lamb_b<<<grid_for(k_warmup_lamb_b, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lamb_begin(const WarmupArgs& a, int sms, cudaStream_t s) {
+  k_lamb_begin<<<grid_for(k_lamb_begin, sms, a.geo.n_ltiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ob

@@ -1,0 +1,285 @@
+// Internal declarations shared by the libob translation units: the layout
+// ("geometry") handed to every kernel, the kernel argument blocks, the
+// device helpers for tile decoding, the fixed-order tile reduction and sign
+// packing, and the host-side launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ob.h"
+
+namespace ob {
+
+constexpr int kThreads = 256;      // one CTA = the 256 lanes of a tile
+constexpr uint32_t kTile = 4096;   // elements per tile
+constexpr unsigned kFull = 0xffffffffu;
+
+// Layout of the fused buffer, as the kernels see it.
+struct Geo {
+  uint64_t n;        // real elements
+  uint64_t P;        // partition size (multiple of 32)
+  uint64_t C;        // chunk size, <= P, multiple of 32
+  uint64_t Cl;       // length of the last chunk of a partition
+  uint64_t n_pad;    // W * P
+  uint64_t words;    // n_pad / 32, words per worker
+  uint32_t W;        // workers
+  uint32_t cpp;      // chunks per partition
+  uint32_t tpc;      // tiles in a full chunk (also the stride of partials)
+  uint32_t tpl;      // tiles in the last chunk of a partition
+  uint32_t tpp;      // tiles per partition
+  uint32_t nc;       // chunks in total, W * cpp
+  uint32_t n_tiles;  // tiles in total, W * tpp
+  uint32_t L;        // layers (>= 1)
+  uint32_t n_ltiles; // tiles counted per layer (from each layer's start)
+};
+
+// One tile of 4096 (or fewer) elements inside one chunk.
+struct Tile {
+  uint64_t start;   // first element
+  uint64_t cstart;  // first element of its chunk
+  uint64_t real;    // real (non-padding) elements of its chunk
+  uint32_t len;     // elements in the tile, multiple of 32, <= 4096
+  uint32_t g;       // chunk id
+  uint32_t t;       // index of the tile inside its chunk
+  uint32_t ntc;     // tiles in its chunk
+};
+
+__device__ __forceinline__ Tile decode_tile(const Geo& G, uint32_t T) {
+  Tile r;
+  uint32_t j = T / G.tpp;
+  uint32_t rem = T - j * G.tpp;
+  uint32_t kc = rem / G.tpc;  // the last chunk has tpl <= tpc tiles
+  r.t = rem - kc * G.tpc;
+  bool last = (kc == G.cpp - 1);
+  uint64_t clen = last ? G.Cl : G.C;
+  r.ntc = last ? G.tpl : G.tpc;
+  r.g = j * G.cpp + kc;
+  r.cstart = (uint64_t)j * G.P + (uint64_t)kc * G.C;
+  r.start = r.cstart + (uint64_t)r.t * kTile;
+  uint64_t left = clen - (uint64_t)r.t * kTile;
+  r.len = (uint32_t)(left < kTile ? left : kTile);
+  r.real = G.n > r.cstart ? (G.n - r.cstart < clen ? G.n - r.cstart : clen) : 0;
+  return r;
+}
+
+// Workspace regions (byte offsets from the workspace base).
+struct Workspace {
+  float* wpart;          // [W][nc][tpc] worker tile totals
+  unsigned* wcnt;        // [nc] arrivals per chunk (worker scales)
+  float* spart;          // [nc][tpc] server tile totals
+  unsigned* scnt;        // [nc] arrivals per chunk (server scales)
+  uint32_t* tile_layer;  // [n_tiles] layer of each tile's first element
+  uint64_t* layer_off;   // [L+1]
+  uint32_t* ltile_pref;  // [L+1] prefix count of per-layer tiles
+  float* lpart;          // [2][n_ltiles] per-layer tile totals
+  unsigned* lcnt;        // [L] arrivals per layer
+  unsigned* Rbits;       // [L] LAMB max ratio, as float bit patterns
+  float* rms;            // [L] begin: momentum RMS per layer
+  unsigned* gcnt;        // [4] whole-grid arrival counters
+};
+
+// LAMB per-layer parameters handed to kernels.
+struct LambHP {
+  float r_thr, r_min, r_max, c_min, c_max;
+  int ratio_ef;  // 1: rho = c_{t-2}/c_{t-1}; 0: rho = 1
+  int frozen;    // 1: r = 1, c = c_avg
+};
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// Warp butterfly: every lane ends with the same value; lane l adds the
+// value of lane l^o for o = 16, 8, 4, 2, 1.
+__device__ __forceinline__ float warp_butterfly_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// Pairwise tree over the 8 warp totals of a tile.
+__device__ __forceinline__ float tree8(const float* w) {
+  float s01 = __fadd_rn(w[0], w[1]), s23 = __fadd_rn(w[2], w[3]);
+  float s45 = __fadd_rn(w[4], w[5]), s67 = __fadd_rn(w[6], w[7]);
+  return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+// OR of a 4-bit group over the 8 lanes that share one 32-bit word: lane l
+// holds bits 4*(l%8)..4*(l%8)+3 of word l/8 of its warp's 128 elements.
+__device__ __forceinline__ uint32_t pack_word(uint32_t nibble, int lane) {
+  uint32_t w = nibble << (4 * (lane & 7));
+  w |= __shfl_xor_sync(kFull, w, 1);
+  w |= __shfl_xor_sync(kFull, w, 2);
+  w |= __shfl_xor_sync(kFull, w, 4);
+  return w;
+}
+
+// Sequential sum of `cnt` tile totals (from 0, in order), done by one warp:
+// every lane returns the same value.
+__device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, int lane) {
+  float acc = 0.0f;
+  for (uint32_t t0 = 0; t0 < cnt; t0 += 32) {
+    float v = (t0 + lane < cnt) ? __ldcg(part + t0 + lane) : 0.0f;
+    uint32_t k = cnt - t0 < 32 ? cnt - t0 : 32;
+    for (uint32_t j = 0; j < k; ++j) acc = __fadd_rn(acc, __shfl_sync(kFull, v, j));
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float mean_of(float sum, uint64_t count) {
+  return count ? __fdiv_rn(sum, __ull2float_rn(count)) : 0.0f;
+}
+
+__device__ __forceinline__ float fmax_plain(float a, float b) { return a > b ? a : b; }
+__device__ __forceinline__ float fmin_plain(float a, float b) { return a < b ? a : b; }
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(((uint32_t)h) << 16);
+}
+
+// Loads 4 gradient values starting at element k (16-byte / 8-byte aligned).
+template <bool BF16>
+__device__ __forceinline__ float4 load_grad4(const void* g, uint64_t k) {
+  if constexpr (BF16) {
+    uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(g) + k));
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xffff0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xffff0000u);
+    return r;
+  } else {
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(g) + k));
+  }
+}
+
+__device__ __forceinline__ float& f4at(float4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float f4get(const float4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// Layer tracking: advances `l` until element k lies in [off[l], off[l+1]).
+__device__ __forceinline__ bool advance_layer(const uint64_t* off, uint32_t L,
+                                              uint64_t k, uint32_t& l,
+                                              uint64_t& lend) {
+  bool moved = false;
+  while (k >= lend && l + 1 < L) {
+    ++l;
+    lend = __ldg(off + l + 1);
+    moved = true;
+  }
+  return moved;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel argument blocks
+// ---------------------------------------------------------------------------
+
+struct CompressArgs {
+  Geo geo;
+  Workspace ws;
+  const void* g[OB_MAX_WORKERS];
+  float* e[OB_MAX_WORKERS];
+  const float* m;
+  uint32_t* bits;
+  float* scales;
+  const float* s;        // LAMB sigma, or null
+  const float* c_prev;   // LAMB c_{t-1}
+  const float* c_prev2;  // LAMB c_{t-2}
+  int ratio_ef;
+  float b1, ob1;
+};
+
+struct ServerArgs {
+  Geo geo;
+  Workspace ws;
+  const uint32_t* bits;
+  const float* scales;
+  float* e_s;
+  uint32_t* sbits;
+  float* sscales;
+  const float* c_prev;
+  const float* c_prev2;
+  int ratio_ef;
+};
+
+struct UpdateArgs {
+  Geo geo;
+  Workspace ws;
+  const uint32_t* sbits;
+  const float* sscales;
+  const float* v_frozen;
+  float* v_fresh;
+  float* m;
+  float* p;
+  float* out;            // decompress
+  ob_layer_state ls;     // LAMB arrays (device pointers)
+  LambHP hp;
+  float b1, ob1, b2, ob2, eps, lr;
+};
+
+struct MaterializeArgs {
+  Geo geo;
+  float* e[OB_MAX_WORKERS];
+  const uint32_t* bits;
+  const float* scales;
+  float* e_s;
+  const uint32_t* sbits;
+  const float* sscales;
+};
+
+struct WarmupArgs {
+  Geo geo;
+  Workspace ws;
+  const void* g[OB_MAX_WORKERS];
+  float* m;
+  float* v;
+  float* p;
+  ob_layer_state ls;
+  float b1, ob1, b2, ob2, eps, lr, c_min, c_max;
+  float fW;
+  int warmup_steps;
+};
+
+// ---------------------------------------------------------------------------
+// Launchers.  Each sizes its grid to the CTAs that fit on the device at once
+// (SM count x resident CTAs per SM, at most one CTA per tile) and returns
+// the cudaError_t of its launch.
+// ---------------------------------------------------------------------------
+
+template <typename K>
+inline int grid_for(K kernel, int sms, uint64_t items) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  uint64_t g = (uint64_t)sms * (uint64_t)occ;
+  if (g > items) g = items;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
+                            cudaStream_t s);
+cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s);
+cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_lamb_pass_a(const UpdateArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
+                              cudaStream_t s);
+cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_warmup_adam(const WarmupArgs& a, bool bf16, int sms,
+                               cudaStream_t s);
+cudaError_t launch_warmup_lamb(const WarmupArgs& a, bool bf16, int sms,
+                               cudaStream_t s);
+cudaError_t launch_lamb_begin(const WarmupArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_quant_int8(const float* g, uint64_t n, int8_t* q, float* scales,
+                              uint64_t seed, uint64_t step, float* deq, int sms,
+                              cudaStream_t s);
+
+}  // namespace ob

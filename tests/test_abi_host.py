@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: libob.so loads, exports every entry point that
+include/ob.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes as ct
+import os
+import re
+
+import pytest
+
+import momentum_compression_gb300 as ob
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from momentum_compression_gb300 import _build
+    _build.build()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ob.h")).read()
+    return sorted(set(re.findall(r"^(?:ob_status|const char\*)\s+(ob_\w+)\(", src, re.M)))
+
+
+def test_header_and_binding_agree():
+    assert _declared() == sorted(ob.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported():
+    lib = ct.CDLL(ob.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_layout_matches_definition():
+    ctx = ob.ob_init(109_482_240, 8, 1 << 20)
+    lay = ob.ob_get_layout(ctx)
+    assert lay["P"] == 13_688_832 and lay["n_pad"] == 8 * 13_688_832
+    assert lay["chunks_per_partition"] == 14 and lay["n_chunks"] == 112
+    # 13 full chunks of 256 tiles + a last chunk of 57,344 elements (14 tiles)
+    assert lay["n_tiles"] == 8 * (13 * 256 + 14)
+    assert lay["words_per_worker"] == lay["n_pad"] // 32
+    ob.ob_destroy(ctx)
+    ctx = ob.ob_init(5000, 3, 992, 32)
+    lay = ob.ob_get_layout(ctx)
+    assert lay["P"] == 1696 and lay["chunk"] == 992 and lay["chunks_per_partition"] == 2
+    ob.ob_destroy(ctx)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=0, W=4, chunk=1024), ob.OB_ERR_INVALID),
+    (dict(n=1 << 34, W=4, chunk=1024), ob.OB_ERR_INVALID),
+    (dict(n=100, W=0, chunk=1024), ob.OB_ERR_INVALID),
+    (dict(n=100, W=65, chunk=1024), ob.OB_ERR_UNSUPPORTED),
+    (dict(n=100, W=2, chunk=1000), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=0), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, align=48), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, grad_dtype=7), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, b1=1.0), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, eps=-1.0), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, layer_offsets=[0, 50, 50, 100]), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, layer_offsets=[0, 50, 99]), ob.OB_ERR_INVALID),
+    (dict(n=100, W=2, chunk=1024, layer_offsets=[1, 50, 100]), ob.OB_ERR_INVALID),
+])
+def test_init_rejects(kw, status):
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_init(**kw)
+    assert ei.value.status == status
+    assert ob.ob_last_error(None)
+
+
+def test_calls_need_a_workspace():
+    ctx = ob.ob_init(1 << 16, 2, 4096)
+    for call in (
+        lambda: ob.ob_compress(ctx, [16, 16], 16, [16, 16], 16, 16, stream=0),
+        lambda: ob.ob_server_reduce(ctx, 16, 16, 16, 16, 16, stream=0),
+        lambda: ob.ob_adam_step(ctx, 16, 16, 16, 16, 16, stream=0),
+        lambda: ob.ob_warmup_step(ctx, [16, 16], 16, 16, 16, stream=0),
+    ):
+        with pytest.raises(ob.OBError) as ei:
+            call()
+        assert ei.value.status == ob.OB_ERR_STATE
+        assert "workspace" in ob.ob_last_error(ctx)
+    ob.ob_destroy(ctx)
+
+
+def test_set_workspace_checks_before_cuda():
+    ctx = ob.ob_init(1 << 16, 2, 4096)
+    need = ob.ob_workspace_bytes(ctx)
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_set_workspace(ctx, 0x1000 + 16, need, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_set_workspace(ctx, 0x1000, need - 1, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    ob.ob_destroy(ctx)
+
+
+def test_quant_int8_checks_before_cuda():
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_quant_int8(0x1004, 0x2000, 0x3000, 1, 0, n=100, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_quant_int8(0x1000, 0x2001, 0x3000, 1, 0, n=100, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_quant_int8(0x1000, 0x2000, 0x3000, 1, 0, n=0, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_quant_int8(None, 0x2000, 0x3000, 1, 0, n=10, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+
+
+def test_null_ctx():
+    lib = ob.lib()
+    assert lib.ob_get_layout(None, None) == ob.OB_ERR_INVALID
+    assert lib.ob_compress(None, None, None, None, None, None, None, None) == ob.OB_ERR_INVALID
+    assert b"NULL" in lib.ob_last_error(None)

@@ -1,0 +1,399 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by
+element, on the same seeded inputs.
+
+Bar: packed sign words, INT8 codes and scales bit-exact; every float buffer
+bit-exact as well for single kernels (both sides round every operation the
+same way and sum in the same fixed order), and within rel 1e-5 / abs 1e-7
+after multi-step runs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import momentum_compression_gb300 as ob
+import oracle as O
+import synth
+from helpers import (assert_bits_equal, assert_close, bf16_tensor, dev, host)
+
+pytestmark = pytest.mark.gpu
+
+f32 = np.float32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    from momentum_compression_gb300 import _build
+    _build.build()
+    yield
+    torch.cuda.synchronize()
+
+
+# (n, W, align, chunk, grad dtype)
+CASES = [
+    (1 << 20, 4, 4096, 1 << 18, "f32"),      # the flat 2^20 workload
+    (50_037, 3, 32, 992, "f32"),             # chunk not a multiple of the tile
+    (4097, 2, 32, 64, "bf16"),
+    (1, 1, 32, 32, "f32"),
+    (31, 2, 32, 32, "f32"),
+    (33, 3, 32, 64, "f32"),
+    (4095, 1, 4096, 4096, "f32"),
+    (100, 4, 4096, 1 << 20, "f32"),          # partitions 1..3 are all padding
+    (70_001, 16, 4096, 4096, "bf16"),
+    (9_000, 64, 32, 32, "f32"),              # the largest W
+    (300_000, 5, 4096, 3 * 4096 + 32, "f32"),  # ragged last tile of each chunk
+]
+
+
+def _ids(c):
+    return "n{}-W{}-A{}-C{}-{}".format(*c)
+
+
+class Case:
+    def __init__(self, n, W, A, C, dt, seed=0):
+        self.n, self.W, self.A, self.C, self.dt = n, W, A, C, dt
+        self.lay = O.Layout(n, W, A, C)
+        self.ctx = ob.ob_init(n, W, C, A, ob.OB_GRAD_BF16 if dt == "bf16" else ob.OB_GRAD_F32,
+                              b1=0.9, b2=0.999, eps=1e-8, lr=1e-4)
+        lay = ob.ob_get_layout(self.ctx)
+        assert (lay["n_pad"], lay["P"], lay["n_chunks"]) == (self.lay.n_pad, self.lay.P,
+                                                            self.lay.nc)
+        nb = ob.ob_workspace_bytes(self.ctx)
+        self.ws = torch.zeros((nb + 255) // 4, dtype=torch.float32, device="cuda")
+        ob.ob_set_workspace(self.ctx, self.ws, nb)
+        self.rng = np.random.default_rng(seed + n + 7 * W)
+
+    def vec(self, scale, fill=0.0):
+        a = np.full(self.lay.n_pad, fill, f32)
+        a[: self.n] = self.rng.standard_normal(self.n).astype(f32) * f32(scale)
+        return a
+
+    def grads(self, scale=1e-3):
+        g = [self.vec(scale) for _ in range(self.W)]
+        if self.dt == "bf16":
+            bits = [synth.bf16_bits(x) for x in g]
+            return [synth.bf16_to_f32(b) for b in bits], [bf16_tensor(b) for b in bits]
+        return g, [dev(x) for x in g]
+
+    def close(self):
+        ob.ob_destroy(self.ctx)
+
+
+def _materialize(c, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t):
+    ob.ob_materialize_errors(c.ctx, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t)
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_compress_server_update_single_kernels(case):
+    c = Case(*case)
+    lay = c.lay
+    g_host, g_dev = c.grads()
+    m = c.vec(1e-3)
+    e = [c.vec(1e-4) for _ in range(c.W)]
+    # --- worker compression
+    err_t = [dev(x) for x in e]  # deferred form with zero scales = true errors
+    bits_t = torch.zeros((c.W, lay.words), dtype=torch.int32, device="cuda")
+    scales_t = torch.zeros((c.W, lay.nc), dtype=torch.float32, device="cuda")
+    m_t = dev(m)
+    ob.ob_compress(c.ctx, g_dev, m_t, err_t, bits_t, scales_t)
+    bits_o = np.zeros((c.W, lay.words), np.uint32)
+    scales_o = np.zeros((c.W, lay.nc), f32)
+    e_o = [x.copy() for x in e]
+    for w in range(c.W):
+        b, s, x = O.compress_worker(lay, g_host[w], m, e_o[w], 0.9)
+        bits_o[w], scales_o[w] = b, s
+        assert_bits_equal(host(err_t[w]), x, f"x of worker {w}")
+    assert_bits_equal(host(bits_t), bits_o, "worker sign words")
+    assert_bits_equal(host(scales_t), scales_o, "worker scales")
+    assert_bits_equal(host(m_t), m, "m is read only")
+    # --- server
+    es = c.vec(1e-4)
+    es_t = dev(es)
+    sbits_t = torch.zeros(lay.words, dtype=torch.int32, device="cuda")
+    sscales_t = torch.zeros(lay.nc, dtype=torch.float32, device="cuda")
+    ob.ob_server_reduce(c.ctx, bits_t, scales_t, es_t, sbits_t, sscales_t)
+    es_o = es.copy()
+    sbits_o, sscales_o, y_o = O.server_reduce(lay, bits_o, scales_o, es_o)
+    assert_bits_equal(host(es_t), y_o, "server y")
+    assert_bits_equal(host(sbits_t), sbits_o, "server sign words")
+    assert_bits_equal(host(sscales_t), sscales_o, "server scales")
+    # --- decompression and the Adam update
+    out_t = torch.full((lay.n_pad,), 7.0, device="cuda")
+    ob.ob_decompress(c.ctx, sbits_t, sscales_t, out_t)
+    assert_bits_equal(host(out_t), O.decompress(lay, sbits_o, sscales_o), "decompress")
+    v = np.abs(c.vec(1e-6)) + f32(1e-12)
+    p = c.vec(0.02)
+    v_t, p_t = dev(v), dev(p)
+    m2_t = torch.full((lay.n_pad,), 3.0, device="cuda")
+    ob.ob_adam_step(c.ctx, sbits_t, sscales_t, v_t, m2_t, p_t)
+    m_o = np.full(lay.n_pad, 3.0, f32)
+    p_o = p.copy()
+    O.adam_update(lay, sbits_o, sscales_o, v, 1e-8, 1e-4, m_o, p_o)
+    assert_bits_equal(host(m2_t), m_o, "m after update")
+    assert_bits_equal(host(p_t), p_o, "p after update")
+    # --- deferred errors made explicit
+    _materialize(c, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t)
+    for w in range(c.W):
+        assert_bits_equal(host(err_t[w]), e_o[w], f"e' of worker {w}")
+    assert_bits_equal(host(es_t), es_o, "server e'")
+    assert not host(scales_t).any() and not host(sscales_t).any()
+    c.close()
+
+
+def _run_adam(wl, warm, steps, check_every=False):
+    """Runs `warm` warmup and `steps` compressed steps of workload wl on the
+    GPU and in the oracle from the same seeded inputs."""
+    n, W = wl.n, wl.W
+    opt = ob.OneBitOptimizer(n, W, wl.chunk, wl.align, wl.grad_dtype, **wl.hp)
+    lay = O.Layout(n, W, wl.align, wl.chunk)
+    st = O.State(lay)
+    p0 = np.zeros(lay.n_pad, f32)
+    p0[:n] = synth.params0_slice(wl, 0, n)
+    st.p[:] = p0
+    opt.p.copy_(torch.from_numpy(p0))
+
+    def grads(step):
+        gh = []
+        gd = []
+        for w in range(W):
+            a = np.zeros(lay.n_pad, f32)
+            a[:n] = synth.grad_slice(wl, step, w, 0, n)
+            if wl.grad_dtype == "bf16":
+                b = synth.bf16_bits(a)
+                gh.append(synth.bf16_to_f32(b))
+                gd.append(bf16_tensor(b))
+            else:
+                gh.append(a)
+                gd.append(dev(a))
+        return gh, gd
+
+    for t in range(warm):
+        gh, gd = grads(t)
+        opt.warmup_step(gd)
+        O.warmup_step(lay, gh, 0, wl.hp, st.m, st.v, st.p)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(opt.m), st.m, "m after warmup")
+    assert_bits_equal(host(opt.v), st.v, "v after warmup")
+    assert_bits_equal(host(opt.p), st.p, "p after warmup")
+    opt.begin_compression()
+    O.begin_compression(st, warm)
+    for t in range(warm, warm + steps):
+        gh, gd = grads(t)
+        opt.compressed_step(gd)
+        O.compressed_step(st, gh, wl.hp)
+        if check_every:
+            torch.cuda.synchronize()
+            assert_bits_equal(host(opt.sbits), st.sbits, f"sbits at step {t}")
+    torch.cuda.synchronize()
+    return opt, st, lay
+
+
+def _compare_state(opt, st, lay, exact=True):
+    assert_bits_equal(host(opt.sbits), st.sbits, "server sign words")
+    assert_bits_equal(host(opt.sscales), st.sscales, "server scales")
+    assert_bits_equal(host(opt.bits), st.bits, "worker sign words")
+    assert_bits_equal(host(opt.scales), st.scales, "worker scales")
+    opt.materialize_errors()
+    torch.cuda.synchronize()
+    pairs = [("m", opt.m, st.m), ("p", opt.p, st.p), ("e_s", opt.err_s, st.e_s)]
+    pairs += [(f"e[{w}]", opt.err[w], st.e[w]) for w in range(lay.W)]
+    if opt.v_fresh is not None:
+        pairs.append(("v_fresh", opt.v_fresh, st.v_fresh))
+    for name, g, o in pairs:
+        assert_close(host(g), o, name)
+        if exact:
+            assert_bits_equal(host(g), o, name)
+
+
+def test_flat_1m_adam_5_warmup_10_compressed():
+    """The flat 2^20-element workload: W = 4, chunk 2^18, 5 uncompressed
+    warmup steps then 10 compressed steps."""
+    wl = synth.workload("flat-1m")
+    opt, st, lay = _run_adam(wl, wl.warmup_steps, wl.compressed_steps, check_every=True)
+    _compare_state(opt, st, lay)
+    opt.close()
+
+
+def test_bf16_gpt_shaped_slice_adam():
+    """bf16 gradients on the first 300,000 parameters of the GPT-1.3B list
+    (wte rows), W = 4, chunk 2^14, 2 warmup + 4 compressed steps."""
+    wl = synth.workload("gpt-1.3b")
+    wl.tensors = None
+    wl.n = 300_000
+    wl.chunk = 1 << 14
+    opt, st, lay = _run_adam(wl, 2, 4)
+    _compare_state(opt, st, lay)
+    opt.close()
+
+
+def test_deferred_resume_is_bit_identical():
+    """Materialising the errors between steps (as before a checkpoint) does
+    not change any later result."""
+    wl = synth.workload("flat", n=200_003, W=3, chunk=1 << 14)
+    a, st, lay = _run_adam(wl, 2, 3)
+    gd = [dev(synth.grad_slice(wl, 9, w, 0, lay.n_pad)) for w in range(3)]
+    a.materialize_errors()
+    a.compressed_step(gd)
+    b, _, _ = _run_adam(wl, 2, 3)
+    b.compressed_step(gd)
+    torch.cuda.synchronize()
+    for x, y in ((a.p, b.p), (a.m, b.m), (a.sbits, b.sbits)):
+        assert torch.equal(x, y)
+    a.materialize_errors()
+    b.materialize_errors()
+    torch.cuda.synchronize()
+    for w in range(3):
+        assert torch.equal(a.err[w], b.err[w])
+    a.close()
+    b.close()
+
+
+# ---------------------------------------------------------------------------
+# 1-bit LAMB
+# ---------------------------------------------------------------------------
+
+LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=4.0,
+               c_min=0.01, c_max=10.0)
+
+
+@pytest.mark.parametrize("flags", [0, ob.OB_FLAG_NO_RATIO_EF, ob.OB_FLAG_FROZEN_C])
+def test_lamb_small_layers(flags):
+    """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
+    W = 4, chunk 2048, 3 warmup + 6 compressed steps with the gradient std
+    falling 3x per step, so that r_t moves and the step-ratio error
+    feedback differs from 1."""
+    sizes = [7, 1, 2, 4095, 4097, 33, 1000, 20000, 3, 30000]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.uint64)
+    n, W, A, C = int(off[-1]), 4, 32, 2048
+    opt = ob.OneBitOptimizer(n, W, C, A, "f32", [int(x) for x in off], lamb=True, flags=flags,
+                             **LAMB_HP)
+    lay = O.Layout(n, W, A, C)
+    layers = O.Layers(off)
+    st = O.State(lay, layers, lamb=True)
+    rng = np.random.default_rng(3)
+    p0 = np.zeros(lay.n_pad, f32)
+    p0[:n] = rng.standard_normal(n).astype(f32) * f32(0.02)
+    st.p[:] = p0
+    opt.p.copy_(torch.from_numpy(p0))
+    layer_std = np.repeat(10.0 ** rng.uniform(-4, -2, size=len(sizes)), sizes).astype(f32)
+    warm, steps = 3, 6
+
+    def grads(t):
+        f = f32(3.0 ** -max(0, t - warm))
+        gh = []
+        for w in range(W):
+            a = np.zeros(lay.n_pad, f32)
+            a[:n] = rng.standard_normal(n).astype(f32) * layer_std * f
+            gh.append(a)
+        return gh, [dev(x) for x in gh]
+
+    hp = dict(LAMB_HP)
+    for t in range(warm):
+        gh, gd = grads(t)
+        opt.warmup_step(gd)
+        c = O.warmup_step(lay, gh, 1, hp, st.m, st.v, st.p, layers, st.c_sum)
+        torch.cuda.synchronize()
+        assert_bits_equal(host(opt.ls.c_t), c, f"warmup c at step {t}")
+    assert_bits_equal(host(opt.m), st.m, "m after warmup")
+    assert_bits_equal(host(opt.v), st.v, "v after warmup")
+    assert_bits_equal(host(opt.p), st.p, "p after warmup")
+    assert_bits_equal(host(opt.ls.c_sum), st.c_sum, "c_sum after warmup")
+    opt.begin_compression()
+    O.begin_compression(st, warm, lamb=True)
+    torch.cuda.synchronize()
+    for k in ("s", "c_avg", "r_prev", "c_prev", "c_prev2"):
+        assert_bits_equal(host(getattr(opt.ls, k)), st.ls[k], f"begin: {k}")
+    ratio_ef = not (flags & ob.OB_FLAG_NO_RATIO_EF)
+    frozen = bool(flags & ob.OB_FLAG_FROZEN_C)
+    for t in range(warm, warm + steps):
+        gh, gd = grads(t)
+        opt.compressed_step(gd)
+        O.compressed_step(st, gh, hp, lamb=True, ratio_ef=ratio_ef, frozen=frozen)
+        torch.cuda.synchronize()
+        assert_bits_equal(host(opt.sbits), st.sbits, f"sbits at step {t}")
+        assert_bits_equal(host(opt.ls.c_t), st.c, f"c_t at step {t}")
+    for k in ("r_prev", "c_prev", "c_prev2"):
+        assert_bits_equal(host(getattr(opt.ls, k)), st.ls[k], f"end: {k}")
+    if not frozen:
+        assert np.any(st.ls["r_prev"] != 1.0)
+    _compare_state(opt, st, lay)
+    opt.close()
+
+
+# ---------------------------------------------------------------------------
+# INT8
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 255, 256, 257, 1000, 4097, (1 << 20) + 3])
+def test_int8_parity(n):
+    rng = np.random.default_rng(n)
+    g = (rng.standard_normal(n) * 1e-3).astype(f32)
+    if n > 600:
+        g[256:512] = 0.0  # an all-zero block
+        g[700] = np.float32(5.0)  # a block dominated by one value
+    nb = (n + 255) // 256
+    g_t = dev(g)
+    q_t = torch.zeros(n + 16, dtype=torch.int8, device="cuda")
+    s_t = torch.zeros(nb, dtype=torch.float32, device="cuda")
+    d_t = torch.zeros(n + 4, dtype=torch.float32, device="cuda")
+    for step in (0, 1, 2 ** 33 + 5):
+        ob.ob_quant_int8(g_t, q_t, s_t, 1234, step, d_t, n=n)
+        q_o, s_o, d_o = O.quant_int8(g, 256, 1234, step, deq=True)
+        assert np.array_equal(host(q_t)[:n], q_o), f"codes, step {step}"
+        assert_bits_equal(host(s_t), s_o, "block scales")
+        assert_bits_equal(host(d_t)[:n], d_o, "dequantised")
+    assert not host(q_t)[n:].any()
+
+
+def test_int8_large_seed_and_no_deq():
+    n = 3 * 256 + 17
+    g = (np.random.default_rng(1).standard_normal(n) * 10).astype(f32)
+    g_t = dev(g)
+    q_t = torch.zeros(n, dtype=torch.int8, device="cuda")
+    s_t = torch.zeros(4, dtype=torch.float32, device="cuda")
+    seed = 0xFEDCBA9876543210
+    ob.ob_quant_int8(g_t, q_t, s_t, seed, 77)
+    q_o, s_o = O.quant_int8(g, 256, seed, 77)
+    assert np.array_equal(host(q_t), q_o)
+    assert_bits_equal(host(s_t), s_o)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+
+def test_nan_gradient_propagates_like_the_oracle():
+    """A NaN gradient packs as -1 and poisons its chunk's scale, on both
+    sides alike; no trap, and other chunks are untouched."""
+    c = Case(40_000, 2, 32, 4096, "f32", seed=5)
+    lay = c.lay
+    g_host, _ = c.grads()
+    g_host[1][5000] = np.nan
+    g_dev = [dev(x) for x in g_host]
+    m = c.vec(1e-3)
+    err_t = [torch.zeros(lay.n_pad, device="cuda") for _ in range(2)]
+    bits_t = torch.zeros((2, lay.words), dtype=torch.int32, device="cuda")
+    scales_t = torch.zeros((2, lay.nc), dtype=torch.float32, device="cuda")
+    ob.ob_compress(c.ctx, g_dev, dev(m), err_t, bits_t, scales_t)
+    for w in range(2):
+        b, s, x = O.compress_worker(lay, g_host[w], m, np.zeros(lay.n_pad, f32), 0.9)
+        assert np.array_equal(host(bits_t[w]).view(np.uint32), b)
+        got = host(scales_t[w])
+        assert np.array_equal(np.isnan(got), np.isnan(s))
+        assert_bits_equal(got[~np.isnan(s)], s[~np.isnan(s)])
+    assert np.isnan(host(scales_t[1])).sum() == 1
+    c.close()
+
+
+def test_misaligned_pointers_rejected_before_launch():
+    c = Case(4096, 2, 32, 1024, "f32")
+    buf = torch.zeros(8192 + 8, device="cuda")
+    bad = buf.data_ptr() + 4
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_adam_step(c.ctx, buf, buf, bad, buf, buf)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_compress(c.ctx, [buf, bad], buf, [buf, buf], buf, buf)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    c.close()
