@@ -1,0 +1,470 @@
+"""Throughput of the fused 1-bit compressed optimizer step on GB300.
+
+One step = worker compression of all W workers (ob_compress), the server
+average and re-compression (ob_server_reduce) and the unpack + frozen
+variance Adam update (ob_adam_step), on the BERT-base-shaped workload:
+109,482,240 fp32 parameters in 199 tensors fused into one buffer, W = 8
+simulated data-parallel workers, chunk 2^20.  Inputs are resident in HBM
+(13.9 GB touched per step, far above the 129 MB L2, so no flush is
+needed).
+
+Prints ONE JSON line (rank 0): elements/s of the whole job, GB/s and the
+roofline fraction of the dominant kernel, the oracle's CPU throughput on a
+bounded sample, an end-to-end number through host buffers, and the SM
+clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload bert-base|flat-1m|gpt-1.3b|bert-large]
+
+N > 1 runs under torchrun as independent replicas (one per GPU, no
+collective on the data path); timing is the max over ranks.
+--impl reference times the oracle (plain single-threaded C++) on the host
+cores, on a bounded sample of the same workload.
+"""
+import argparse
+import ctypes as ct
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("fused 1-bit compress+update elements/s and HBM GB/s (% of roofline) at 1 GPU")
+NOMINAL_HBM_GBS = 8000.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes per real element (G = gradient bytes, W workers)
+# ---------------------------------------------------------------------------
+
+def bytes_per_element(W, G, lamb=False):
+    """compress: m read 4 + per worker g read G, e read 4 + write 4, old
+    sign word read 1/8 + new word write 1/8; server: W/8 word reads, e_s read
+    4 + write 4, sign word 1/8 + 1/8; Adam: sign word 1/8, v 4, p 4 + 4,
+    m write 4.  LAMB pass A: sign word 1/8, m 4+4, v_fresh 4+4, v_Tw 4;
+    pass B: m 4, v_Tw 4, p 4+4."""
+    comp = 4 + W * (G + 8 + 0.25)
+    serv = W / 8 + 8 + 0.25
+    upd = (0.125 + 20 + 16) if lamb else (0.125 + 4 + 8 + 4)
+    return {"compress": comp, "server": serv, "update": upd, "total": comp + serv + upd}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling (NVML through ctypes; falls back to nvidia-smi)
+# ---------------------------------------------------------------------------
+
+REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+           0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+           0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of one GPU every
+    ~2 ms in a thread while active (reads only; changes no setting)."""
+
+    def __init__(self, uuid):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self._nvml = None
+        self._h = None
+        try:
+            nv = ct.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            h = ct.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ct.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(0, ct.byref(h)) != 0:
+                    raise OSError("nvml handle")
+            mx = ct.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self._reasons_fn = fn or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError) as e:
+            log(f"[bench] NVML unavailable ({e}); clocks via nvidia-smi")
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                r = rs.value if self._reasons_fn(h, ct.byref(rs)) == 0 else 0
+                self.samples.append((mhz.value, r))
+            time.sleep(0.002)
+
+    def _run_smi(self):
+        import subprocess
+        q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=5).stdout
+                a = out.strip().splitlines()[0].split(",")
+                self.max_mhz = int(float(a[1]))
+                self.samples.append((int(float(a[0])), int(a[2].strip(), 16)))
+            except Exception:
+                pass
+            time.sleep(0.05)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run if self._nvml else self._run_smi, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mhz = [s for s, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [v for k, v in sorted(REASONS.items()) if bits & k and v != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# Device-side synthetic inputs (same recipe as synth: per-tensor std
+# 1e-3 * 10^U(-1, 1), Gaussian values; drawn on the GPU for speed)
+# ---------------------------------------------------------------------------
+
+def device_grads(torch, wl, n_pad, step, dtype, device):
+    std = torch.zeros(n_pad, dtype=torch.float32, device=device)
+    if wl.tensors is None:
+        std[: wl.n] = wl.flat_std
+    else:
+        sizes = torch.tensor([s for _, s, _ in wl.tensors], device=device)
+        std[: wl.n] = torch.repeat_interleave(
+            torch.tensor(wl.layer_std, dtype=torch.float32, device=device), sizes)
+    out = []
+    for w in range(wl.W):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(synth.SEED_BASE + 1000 * step + w)
+        g = torch.randn(n_pad, generator=gen, device=device, dtype=torch.float32) * std
+        out.append(g.to(dtype))
+    return out
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("k_compress.cu", "ob_internal.cuh"):
+        with open(os.path.join(ROOT, "momentum_compression_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per element of the compress kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "compress_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("source_hash") != kernel_source_hash():
+            return None
+        if kv.get("workload_W") != str(workload.W) or kv.get("grad_bytes") != (
+                "2" if workload.grad_dtype == "bf16" else "4"):
+            return None
+        return float(kv["dram_bytes_per_element"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, single-threaded, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step_time(wl, sample, steps):
+    import oracle as O
+    lay = O.Layout(sample, wl.W, wl.align, wl.chunk)
+    st = O.State(lay)
+    st.v[:sample] = synth.state_slice(wl, "v", 0, sample)
+    st.m[:sample] = synth.state_slice(wl, "m", 0, sample)
+    grads = []
+    for w in range(wl.W):
+        a = np.zeros(lay.n_pad, np.float32)
+        a[:sample] = synth.grad_slice(wl, 0, w, 0, sample)
+        if wl.grad_dtype == "bf16":
+            a = synth.bf16_to_f32(synth.bf16_bits(a))
+        grads.append(a)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        O.compressed_step(st, grads, wl.hp)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_model():
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return f"{line.split(':', 1)[1].strip()} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    sample = 1 << 21
+    steps = max(args.steps, 1)
+    times = oracle_sample_step_time(wl, sample, args.warmup + steps)[args.warmup:]
+    t = sum(times) / len(times)
+    value = sample / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name} (oracle on a {sample}-element sample)", "n": wl.n,
+                   "W": wl.W, "chunk": wl.chunk, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {sample} elements of {wl.name}, W={wl.W}, "
+                                   f"one compressed step per timed step", "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+
+    import momentum_compression_gb300 as ob
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    G = 2 if wl.grad_dtype == "bf16" else 4
+    gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype, wl.layer_offsets,
+                             lamb=(wl.mode == "lamb"), device=device, **wl.hp)
+    n, n_pad = wl.n, opt.n_pad
+    log(f"[bench] rank {rank}: {wl.name} n={n} W={wl.W} n_pad={n_pad} "
+        f"tiles={opt.layout['n_tiles']}")
+    # parameters and two resident gradient sets
+    p0 = torch.zeros(n_pad, device=device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(synth.SEED_BASE + 17)
+    p0[:n] = torch.randn(n, generator=gen, device=device) * 0.02
+    opt.p.copy_(p0)
+    del p0
+    gsets = [device_grads(torch, wl, n_pad, s, gdt, device) for s in range(2)]
+    # prerequisite: a few uncompressed warmup steps freeze v
+    for t in range(3):
+        opt.warmup_step(gsets[t % 2])
+    opt.begin_compression()
+    stream = torch.cuda.current_stream()
+    for t in range(args.warmup):
+        opt.compressed_step(gsets[t % 2])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid)
+    lamb = opt.lamb
+    with ClockSampler(uuid) as clk:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for t in range(K):
+            g = gsets[t % 2]
+            e = ev[t]
+            e[0].record(stream)
+            ob.ob_compress(opt.ctx, g, opt.m, opt.err, opt.bits, opt.scales, opt.ls)
+            e[1].record(stream)
+            ob.ob_server_reduce(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
+                                opt.ls)
+            e[2].record(stream)
+            if lamb:
+                ob.ob_lamb_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.v_fresh, opt.m, opt.p,
+                                opt.ls)
+            else:
+                ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.m, opt.p)
+            e[3].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per = {k: [ev[t][i].elapsed_time(ev[t][i + 1]) for t in range(K)]
+           for i, k in enumerate(("compress", "server", "update"))}
+    launches = K * (4 if lamb else 3)
+    if pg:
+        tt = torch.tensor([total_ms], device=device)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms = total_ms / K
+    bpe = bytes_per_element(wl.W, G, lamb)
+    value = world * n / (ms * 1e-3)
+    peak, peak_kind = measured_peak()
+    kms = {k: sum(v) / K for k, v in per.items()}
+    dom = max(kms, key=kms.get)
+    dom_bytes = bpe[dom] * n
+    achieved = dom_bytes / (kms[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic(wl) if dom == "compress" else None
+
+    # end to end through host buffers: H2D of every worker's gradient, the
+    # step, D2H of the updated parameters
+    e2e = None
+    host_g = [torch.empty(n_pad, dtype=gdt, pin_memory=True) for _ in range(wl.W)]
+    for w in range(wl.W):
+        host_g[w].copy_(gsets[0][w])
+    host_p = torch.empty(n_pad, dtype=torch.float32, pin_memory=True)
+    dev_g = gsets[1]
+    K2 = max(2, min(K, 10))
+    for t in range(2):
+        for w in range(wl.W):
+            dev_g[w].copy_(host_g[w], non_blocking=True)
+        opt.compressed_step(dev_g)
+        host_p.copy_(opt.p, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for t in range(K2):
+        for w in range(wl.W):
+            dev_g[w].copy_(host_g[w], non_blocking=True)
+        opt.compressed_step(dev_g)
+        host_p.copy_(opt.p, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / K2
+    if pg:
+        tt = torch.tensor([e2e_ms], device=device)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": world * n / (e2e_ms * 1e-3), "unit": "elements/s",
+           "h2d_bytes_per_step": wl.W * n_pad * G, "d2h_bytes_per_step": n_pad * 4,
+           "ms_per_step": e2e_ms}
+    del host_g, host_p
+
+    cpu = None
+    if rank == 0 and world == 1:
+        sample, steps = min(1 << 24, n), 4
+        times = oracle_sample_step_time(wl, sample, steps)
+        cpu = {"value": sample * steps / sum(times), "unit": "elements/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"first {sample} elements of {wl.name}, W={wl.W}, {steps} compressed "
+                         f"steps ({sum(times):.1f} s)", "cpu": cpu_model()}
+
+    if rank != 0:
+        return
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if G == 4 else "f32 (bf16 gradients)",
+        "data": "synthetic",
+        "config": {"workload": wl_label(wl), "n": n, "W": wl.W, "chunk": wl.chunk,
+                   "n_layers": wl.n_layers, "grad_dtype": wl.grad_dtype,
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "l2": f"inputs larger than L2 ({bpe['total'] * n / 1e9:.1f} GB touched per "
+                         f"step); no flush"},
+        "gbs": bpe["total"] * n / (ms * 1e-3) / 1e9,
+        "worker_elements_per_s": world * n * wl.W / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
+                     "bytes_per_element": bpe[dom],
+                     "traffic": None if traffic is None else traffic * n},
+        "step_roofline_frac": bpe["total"] * n / (ms * 1e-3) / 1e9 / peak,
+        "kernels_ms": kms,
+        "kernels_gbs": {k: bpe[k] * n / (kms[k] * 1e-3) / 1e9 for k in kms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    opt.close()
+
+
+def wl_label(wl):
+    kind = "1-bit LAMB" if wl.mode == "lamb" else "1-bit Adam"
+    shape = f"{wl.n_layers} tensors" if wl.tensors else "flat"
+    return (f"{wl.name} {kind}: {wl.n:,} params ({shape}) fused, W={wl.W} simulated workers, "
+            f"chunk {wl.chunk}, {wl.grad_dtype} grads")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default="bert-base")
+    ap.add_argument("--n", type=int, help="elements (flat workload only)")
+    ap.add_argument("--W", type=int, help="workers (flat workload only)")
+    ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.workload == "flat":
+        wl = synth.workload("flat", n=args.n or (1 << 24), W=args.W or 8,
+                            chunk=args.chunk or (1 << 20))
+    else:
+        wl = synth.workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()
