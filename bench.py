@@ -253,7 +253,7 @@ def run_reference(args, wl):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    sample = 1 << 21
+    sample = min(1 << 21, wl.n)
     steps = max(args.steps, 1)
     times = oracle_sample_step_time(wl, sample, args.warmup + steps)[args.warmup:]
     t = sum(times) / len(times)
