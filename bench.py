@@ -346,7 +346,9 @@ def run_ours(args, wl):
     total_ms = t_start.elapsed_time(t_end)
     per = {k: [ev[t][i].elapsed_time(ev[t][i + 1]) for t in range(K)]
            for i, k in enumerate(("compress", "server", "update"))}
-    launches = K * (4 if lamb else 3)
+    # compress + scale finalisation, server + scale finalisation, update
+    # (LAMB: pass A and pass B)
+    launches = K * (6 if lamb else 5)
     if pg:
         tt = torch.tensor([total_ms], device=device)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)

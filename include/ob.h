@@ -18,7 +18,13 @@
  *     ob_adam_step      unpack + frozen-variance Adam            ([LAMB] 1)
  *  or ob_lamb_step      unpack + 1-bit LAMB update               ([LAMB] 1-2)
  * The worker-to-server "all-to-all" is the server kernel reading the
- * workers' packed words straight from HBM.
+ * workers' packed words straight from HBM (bulk copies of each worker's
+ * 16-byte aligned run of words for a tile).
+ *
+ * Device errors.  Pipelined kernels wait on shared-memory barriers for
+ * their own bulk copies; every wait is bounded (about a second), and a
+ * wait that runs out records a code in the workspace and lets the kernel
+ * return.  ob_device_error() reads (and clears) that code.
  *
  * Layout.  n real elements, W workers, alignment A, chunk C (both multiples
  * of 32).  P = roundup(ceil(n/W), A); n_pad = W*P; server j owns
@@ -28,11 +34,13 @@
  * bit is 0, their error 0.
  *   grads      W buffers of n_pad elements (fp32 or bf16)
  *   err        W buffers of n_pad fp32 (worker error, deferred form)
- *   bits       [W][n_pad/32] uint32; bit k%32 of word k/32 (LSB first) is
- *              1 iff x[k] >= 0.0f (sign(+0) = sign(-0) = +1, NaN -> -1)
+ *   bits       [W][words] uint32, words = n_pad/32 rounded up to a multiple
+ *              of 4 (16-byte rows); bit k%32 of word k/32 of a row (LSB
+ *              first) is 1 iff x[k] >= 0.0f (sign(+0) = sign(-0) = +1,
+ *              NaN -> -1); the rounding words are never written
  *   scales     [W][n_chunks] fp32, each worker's scale of every chunk
  *   err_s      n_pad fp32 (server error, deferred form)
- *   sbits      [n_pad/32] uint32; sscales [n_chunks] fp32
+ *   sbits      [words] uint32; sscales [n_chunks] fp32
  *   m, v, p    n_pad fp32 (momentum, frozen variance, parameters)
  * Padding entries of m and of the errors are written as 0; padding entries
  * of p and v are never written.
@@ -60,8 +68,8 @@
  *     scratch area the caller passes to ob_set_workspace().
  *   - Calls are asynchronous on `stream`; nothing synchronises.  A launch
  *     failure is reported as OB_ERR_CUDA.
- *   - Device pointers must be 16-byte aligned (bits/sbits 4-byte, INT8
- *     codes 4-byte).  Invalid arguments are rejected before any launch.
+ *   - Device pointers must be 16-byte aligned (scales 4-byte, INT8 codes
+ *     4-byte).  Invalid arguments are rejected before any launch.
  *   - A ctx is not thread-safe; distinct ctxs are independent.  Calls that
  *     share a ctx (and so its workspace) must not overlap on the GPU.
  */
@@ -119,7 +127,8 @@ typedef struct ob_layout {
   size_t chunks_per_partition;  /* cpp */
   size_t n_chunks;              /* W * cpp: length of sscales, and of each
                                    worker's row of scales */
-  size_t words_per_worker;      /* n_pad / 32 */
+  size_t words_per_worker;      /* row stride of bits: n_pad/32 rounded up
+                                   to a multiple of 4 */
   size_t n_tiles;               /* 4096-element tiles, counted per chunk */
   int W, n_layers;              /* n_layers >= 1 */
 } ob_layout;
@@ -233,6 +242,12 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err,
                                 const uint32_t* bits, float* scales,
                                 float* err_s, const uint32_t* sbits,
                                 float* sscales, ob_stream_t stream);
+
+/* Reads and clears the device error word of the workspace (0 = none;
+ * 1 = a consumer's wait for a copy ran out, 2 = the producer's wait for a
+ * free stage ran out, 3 = copies still in flight at exit).  Synchronises
+ * `stream`. */
+ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream);
 
 /* Block-wise INT8 stochastic rounding ([TUT] "FP32 → INT8 量化" and the
  * GradientQuantizeINT8 example), blocks of 256 elements (the last may be

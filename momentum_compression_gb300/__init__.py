@@ -32,7 +32,7 @@ EXPORTS = (
     "ob_init", "ob_destroy", "ob_last_error", "ob_get_layout", "ob_workspace_bytes",
     "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
-    "ob_materialize_errors", "ob_quant_int8",
+    "ob_materialize_errors", "ob_device_error", "ob_quant_int8",
 )
 
 
@@ -93,6 +93,7 @@ def lib():
         L.ob_lamb_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_step.argtypes = [vp] * 14
         L.ob_materialize_errors.argtypes = [vp] * 8
+        L.ob_device_error.argtypes = [vp, ct.POINTER(ct.c_uint), vp]
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
         for name in EXPORTS:
             if name != "ob_last_error":
@@ -253,6 +254,13 @@ def ob_materialize_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=
     _check(lib().ob_materialize_errors(ctx, _ptr_array(err), _ptr(bits), _ptr(scales),
                                        _ptr(err_s), _ptr(sbits), _ptr(sscales),
                                        _stream(stream)), ctx)
+
+
+def ob_device_error(ctx, stream=None):
+    """Reads and clears the device error word (0 = none)."""
+    v = ct.c_uint()
+    _check(lib().ob_device_error(ctx, ct.byref(v), _stream(stream)), ctx)
+    return v.value
 
 
 def ob_quant_int8(g, q, block_scales, seed, step, deq=None, n=None, stream=None):

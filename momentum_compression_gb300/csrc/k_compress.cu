@@ -9,42 +9,132 @@
 //   m_w   = b1*m + (1-b1)*g_w
 //   x     = sigma_l*m_w + rho_l*e_w            (1-bit Adam: m_w + e_w)
 //   bit   = x >= 0; x is stored in place of e_w
-//   scale(chunk) = mean |x| over the chunk (finalised by the last CTA of
-//   the chunk to arrive)
+//   scale(chunk) = mean |x| over the chunk: this kernel writes one total
+//   per (worker, tile); k_finalize_scales adds them in tile order
 //
-// One CTA of 256 threads owns one tile of 4096 elements and all W workers
-// of it, so the momentum m is read once per element.  Lane p handles
-// elements 1024*i + 4*p + c (i, c = 0..3) with 128-bit loads; that is also
-// the fixed summation order of the tile total.  Signs are packed with
-// three xor-shuffles per 32-bit word.  No device-side wait: the chunk scale
-// is finalised by whichever CTA brings the chunk's arrival count to its
-// tile count.
+// Work decomposition: a CTA owns a sequence of 4096-element tiles and, for
+// each, all W workers, so the momentum m is read once per element.  The
+// CTA is warp-specialised: one producer thread streams, for every
+// (tile, worker) item, the gradient and error tiles into a ring of
+// shared-memory stages with cp.async.bulk (completion counted in bytes on
+// an mbarrier), and the m tile into its own buffer; eight consumer warps
+// take the items in order.  Consumer lane p handles elements
+// 1024*i + 4*p + c (i, c = 0..3) -- 128-bit shared-memory reads, and the
+// fixed summation order of the tile total.  Signs are packed with three
+// xor-shuffles per 32-bit word; the new x goes back to global memory with
+// streaming 128-bit stores.  No wait is unbounded (ptx.cuh), and no CTA
+// ever waits for another.
 #include "ob_internal.cuh"
+#include "ptx.cuh"
 
 namespace ob {
 namespace {
 
-template <bool BF16, bool LAMB>
-__global__ void __launch_bounds__(kThreads)
-    k_compress(const CompressArgs A) {
-  __shared__ float ws[OB_MAX_WORKERS][8];
-  __shared__ int s_last;
-  const Geo& G = A.geo;
-  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
-  const float b1 = A.b1, ob1 = A.ob1;
+constexpr int kConsumers = kThreads;            // 8 warps
+constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 
-  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+// Two CTAs per SM: 2 stages of 32 KB (fp32 gradients) or 3 of 24 KB (bf16)
+// plus the m tile, so that 4-6 (tile, worker) items are in flight per SM.
+template <bool BF16>
+struct CompressSmem {
+  static constexpr int kStages = BF16 ? 3 : 2;
+  static constexpr uint32_t kG = BF16 ? 2u : 4u;
+  static constexpr size_t kStageG = kTile * kG;
+  static constexpr size_t kStageE = kTile * 4;
+  static constexpr size_t kStage = kStageG + kStageE;
+  static constexpr size_t kM = kTile * 4;
+  static constexpr size_t kBars = (2 * kStages + 2) * 8;
+  static constexpr size_t kWs = OB_MAX_WORKERS * 8 * 4;
+  static constexpr size_t kBytes = kM + kStages * kStage + kBars + kWs;
+};
+
+template <bool BF16, bool LAMB>
+__global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const CompressArgs A) {
+  using S = CompressSmem<BF16>;
+  constexpr int kStages = S::kStages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* mbuf = reinterpret_cast<float*>(smem);  // [4096]
+  unsigned char* stage0 = smem + S::kM;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage0 + kStages * S::kStage);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* mfull = bars + 2 * kStages;
+  uint64_t* mempty = bars + 2 * kStages + 1;
+  float(*ws)[8] = reinterpret_cast<float(*)[8]>(bars + 2 * kStages + 2);
+  __shared__ volatile int s_abort;
+
+  const Geo& G = A.geo;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned* err = A.ws.err;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers / 32);
+    }
+    mbar_init(mfull, 1);
+    mbar_init(mempty, kConsumers / 32);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer
+  if (warp == kConsumers / 32) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    uint32_t item = 0, ti = 0;
+    bool ok = true;
+    for (uint32_t T = blockIdx.x; ok && T < G.n_tiles; T += gridDim.x, ++ti) {
+      const Tile tl = decode_tile(G, T);
+      if (ti >= 1) ok = mbar_wait(mempty, (ti - 1) & 1, err, kErrWaitEmpty);
+      if (!ok || s_abort) break;
+      mbar_arrive_expect_tx(mfull, tl.len * 4);
+      bulk_g2s_stream(mbuf, A.m + tl.start, tl.len * 4, mfull, pol);
+      for (uint32_t w = 0; w < G.W; ++w, ++item) {
+        const uint32_t s = item % kStages, r = item / kStages;
+        if (r >= 1) ok = mbar_wait(&empty[s], (r - 1) & 1, err, kErrWaitEmpty);
+        if (!ok || s_abort) {
+          ok = false;
+          break;
+        }
+        unsigned char* st = stage0 + s * S::kStage;
+        mbar_arrive_expect_tx(&full[s], tl.len * (S::kG + 4));
+        bulk_g2s_stream(st, static_cast<const unsigned char*>(A.g[w]) + tl.start * S::kG,
+                        tl.len * S::kG, &full[s], pol);
+        bulk_g2s_stream(st + S::kStageG, A.e[w] + tl.start, tl.len * 4, &full[s], pol);
+      }
+    }
+    if (!ok) s_abort = 1;
+    // Drain: every copy this thread issued must have landed before exit.
+    for (uint32_t k = 0; k < kStages && k < item; ++k) {
+      const uint32_t it = item - 1 - k;
+      if (!mbar_wait(&full[it % kStages], (it / kStages) & 1, err, kErrDrain)) break;
+    }
+    if (ti >= 1) mbar_wait(mfull, (ti - 1) & 1, err, kErrDrain);
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const float b1 = A.b1, ob1 = A.ob1;
+  const int p = tid;
+  uint32_t item = 0, ti = 0;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
     const Tile tl = decode_tile(G, T);
+    bool ok = s_abort == 0 && mbar_wait(mfull, ti & 1, err, kErrWaitFull);
+    if (!ok) s_abort = 1;
 
     float4 mv[4];
     bool valid[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      uint32_t off = 1024u * i + 4u * p;
+      const uint32_t off = 1024u * i + 4u * p;
       valid[i] = off < tl.len;
-      if (valid[i]) mv[i] = __ldcs(reinterpret_cast<const float4*>(A.m + tl.start + off));
-      else mv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      mv[i] = valid[i] ? *reinterpret_cast<const float4*>(mbuf + off)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(mempty);
 
     // Per-element layer factors (1-bit LAMB only).
     float sig[4][4], rho[4][4];
@@ -57,9 +147,8 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint64_t k = tl.start + 1024u * i + 4u * p + c;
-          if (valid[i] && k < G.n &&
-              advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
+          const uint64_t k = tl.start + 1024u * i + 4u * p + c;
+          if (valid[i] && k < G.n && advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
             s_l = __ldg(A.s + l);
             r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
           }
@@ -68,33 +157,51 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
 
-    for (uint32_t w = 0; w < G.W; ++w) {
+    for (uint32_t w = 0; w < G.W; ++w, ++item) {
+      const uint32_t s = item % kStages;
       const float osc = __ldcg(A.scales + (uint64_t)w * G.nc + tl.g);
-      float* __restrict__ e = A.e[w];
       uint32_t* __restrict__ bw = A.bits + (uint64_t)w * G.words;
+      float* __restrict__ e = A.e[w];
+      uint32_t owd[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) owd[i] = valid[i] ? bw[(tl.start + 1024u * i + 4u * p) >> 5] : 0u;
+      ok = s_abort == 0 && mbar_wait(&full[s], (item / kStages) & 1, err, kErrWaitFull);
+      if (!ok) s_abort = 1;
+      const unsigned char* st = stage0 + s * S::kStage;
+      float4 gv[4], ev[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (valid[i]) {
+          if constexpr (BF16) {
+            const uint2 u = *reinterpret_cast<const uint2*>(st + off * 2);
+            gv[i] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+          } else {
+            gv[i] = *reinterpret_cast<const float4*>(st + off * 4);
+          }
+          ev[i] = *reinterpret_cast<const float4*>(st + S::kStageG + off * 4);
+        } else {
+          gv[i] = ev[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers now
+
       float acc = 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;
-        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f), ev = gv;
-        uint32_t owd = 0;
-        if (valid[i]) {
-          gv = load_grad4<BF16>(A.g[w], k0);
-          ev = __ldcs(reinterpret_cast<const float4*>(e + k0));
-          owd = bw[k0 >> 5];
-        }
         float4 xv;
         uint32_t nib = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint64_t k = k0 + c;
           float x = 0.0f;
-          if (valid[i] && k < G.n) {
-            const int sh = 4 * (p & 7) + c;
-            const float so = ((owd >> sh) & 1u) ? osc : -osc;  // scale*sign
-            const float et = __fsub_rn(f4at(ev, c), so);
-            const float mw = __fadd_rn(__fmul_rn(b1, f4at(mv[i], c)),
-                                       __fmul_rn(ob1, f4at(gv, c)));
+          if (valid[i] && k0 + c < G.n) {
+            const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;  // scale*sign
+            const float et = __fsub_rn(f4get(ev[i], c), so);
+            const float mw = __fadd_rn(__fmul_rn(b1, f4get(mv[i], c)),
+                                       __fmul_rn(ob1, f4get(gv[i], c)));
             if constexpr (LAMB) {
               x = __fadd_rn(__fmul_rn(sig[i][c], mw), __fmul_rn(rho[i][c], et));
             } else {
@@ -114,38 +221,27 @@ __global__ void __launch_bounds__(kThreads)
       acc = warp_butterfly_sum(acc);
       if (lane == 0) ws[w][warp] = acc;
     }
-    __syncthreads();
-    if ((uint32_t)p < G.W) {
+
+    named_sync(1, kConsumers);
+    if ((uint32_t)p < G.W)
       A.ws.wpart[((uint64_t)p * G.nc + tl.g) * G.tpc + tl.t] = tree8(ws[p]);
-    }
-    __threadfence();
-    __syncthreads();
-    if (p == 0) {
-      unsigned prev = atomicAdd(A.ws.wcnt + tl.g, 1u);
-      s_last = (prev == tl.ntc - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      for (uint32_t w = warp; w < G.W; w += kThreads / 32) {
-        float sum = ordered_sum(A.ws.wpart + ((uint64_t)w * G.nc + tl.g) * G.tpc,
-                                tl.ntc, lane);
-        if (lane == 0) A.scales[(uint64_t)w * G.nc + tl.g] = mean_of(sum, tl.real);
-      }
-      if (p == 0) A.ws.wcnt[tl.g] = 0u;
-    }
-    __syncthreads();
+    if (named_sync_or(1, kConsumers, s_abort != 0)) break;
   }
 }
 
-}  // namespace
-
 template <bool BF16, bool LAMB>
-static cudaError_t run_compress(const CompressArgs& a, int sms, cudaStream_t s) {
-  const int grid = grid_for(k_compress<BF16, LAMB>, sms, a.geo.n_tiles);
-  k_compress<BF16, LAMB><<<grid, kThreads, 0, s>>>(a);
+cudaError_t run_compress(const CompressArgs& a, int sms, cudaStream_t s) {
+  using S = CompressSmem<BF16>;
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      k_compress<BF16, LAMB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+  if (attr != cudaSuccess) return attr;
+  const int grid =
+      grid_for(k_compress<BF16, LAMB>, sms, a.geo.n_tiles, kCompressThreads, S::kBytes);
+  k_compress<BF16, LAMB><<<grid, kCompressThreads, S::kBytes, s>>>(a);
   return cudaGetLastError();
 }
+
+}  // namespace
 
 cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
                             cudaStream_t s) {

@@ -1,0 +1,45 @@
+// Chunk scales from per-tile totals: scale = (sum of the chunk's tile
+// totals, in tile order, from 0) / (real elements of the chunk), 0 for an
+// all-padding chunk.  This is the last step of the fixed summation order
+// of the mean |x| ("1-bit 梯度量化": mean(|g|) * sign(g)); running it as its
+// own small kernel after the streaming kernels keeps those free of
+// cross-CTA fences and counters.
+//
+// One warp per (row, chunk) sequence; rows are workers (compress) or the
+// single server row.
+#include "ob_internal.cuh"
+
+namespace ob {
+namespace {
+
+__global__ void __launch_bounds__(kThreads)
+    k_finalize_scales(const Geo G, const float* __restrict__ part, uint32_t rows,
+                      float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t nseq = rows * G.nc;
+  for (uint32_t q = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); q < nseq;
+       q += gridDim.x * (kThreads / 32)) {
+    const uint32_t g = q % G.nc;
+    const uint32_t kc = g % G.cpp;
+    const uint32_t j = g / G.cpp;
+    const bool last = kc == G.cpp - 1;
+    const uint64_t clen = last ? G.Cl : G.C;
+    const uint32_t ntc = last ? G.tpl : G.tpc;
+    const uint64_t cstart = (uint64_t)j * G.P + (uint64_t)kc * G.C;
+    const uint64_t real = G.n > cstart ? (G.n - cstart < clen ? G.n - cstart : clen) : 0;
+    const float sum = ordered_sum(part + (uint64_t)q * G.tpc, ntc, lane);
+    if (lane == 0) scales[q] = mean_of(sum, real);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
+                                   float* scales, int sms, cudaStream_t s) {
+  const uint64_t ctas = ((uint64_t)rows * G.nc + kThreads / 32 - 1) / (kThreads / 32);
+  k_finalize_scales<<<grid_for(k_finalize_scales, sms, ctas), kThreads, 0, s>>>(G, part, rows,
+                                                                               scales);
+  return cudaGetLastError();
+}
+
+}  // namespace ob

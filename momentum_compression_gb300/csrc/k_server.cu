@@ -8,37 +8,146 @@
 //   e_s  = y_prev - sscale_prev*sign(y_prev)   (deferred server error)
 //   y    = rho_l*e_s + z                        (1-bit Adam: e_s + z)
 //   sbit = y >= 0; y is stored in place of e_s
-//   sscale(g) = mean |y| over the chunk
+//   sscale(g) = mean |y| over the chunk: this kernel writes one total per
+//   tile; k_finalize_scales adds them in tile order
 //
-// The workers' words are laid out worker-major ([W][n_pad/32]), so the
-// W-way gather of one tile is W contiguous 512-byte runs; a CTA stages them
-// in shared memory and every lane reads the four words it needs from there.
+// The workers' words are laid out worker-major with a 16-byte aligned row
+// stride, so the W-way gather of one tile is W contiguous runs of 512
+// bytes.  A producer thread streams, per tile, the e_s tile and the W runs
+// (rounded out to 16-byte boundaries) into a ring of shared-memory stages
+// with cp.async.bulk; eight consumer warps read the four words each lane
+// needs from shared memory.  Waits are bounded (ptx.cuh).
 #include "ob_internal.cuh"
+#include "ptx.cuh"
 
 namespace ob {
 namespace {
 
+constexpr int kSStages = 3;
+constexpr int kSConsumers = kThreads;
+constexpr int kServerThreads = kThreads + 32;
+constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
+
+struct ServerSmem {
+  __host__ __device__ static size_t stage_bytes(uint32_t W) { return kTile * 4 + (size_t)W * kRunWords * 4; }
+  __host__ __device__ static size_t bytes(uint32_t W) {
+    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 2 * OB_MAX_WORKERS * 4;
+  }
+};
+
 template <bool LAMB>
-__global__ void __launch_bounds__(kThreads) k_server(const ServerArgs A) {
-  __shared__ uint32_t sbw[OB_MAX_WORKERS * (kTile / 32)];
-  __shared__ float sc[OB_MAX_WORKERS];
-  __shared__ float ws[8];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const Geo& G = A.geo;
-  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  const size_t stage_bytes = ServerSmem::stage_bytes(G.W);
+  unsigned char* stage0 = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSStages * stage_bytes);
+  uint64_t* empty = full + kSStages;
+  float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(empty + kSStages);
+  __shared__ float ws[8];
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned* err = A.ws.err;
   const float fW = (float)G.W;
 
-  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
-    const Tile tl = decode_tile(G, T);
-    const uint32_t nw = tl.len / 32;
-    const uint64_t word0 = tl.start >> 5;
-    if ((uint32_t)p < G.W) sc[p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
-    for (uint32_t idx = p; idx < G.W * nw; idx += kThreads) {
-      uint32_t w = idx / nw, q = idx - w * nw;
-      sbw[w * (kTile / 32) + q] = __ldcs(A.bits + (uint64_t)w * G.words + word0 + q);
+  if (tid == 0) {
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSConsumers / 32);
     }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer
+  if (warp == kSConsumers / 32) {
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    uint32_t ti = 0;
+    bool ok = true;
+    for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
+      const Tile tl = decode_tile(G, T);
+      const uint32_t s = ti % kSStages, r = ti / kSStages;
+      if (r >= 1) ok = mbar_wait(&empty[s], (r - 1) & 1, err, kErrWaitEmpty);
+      if (!ok || s_abort) {
+        ok = false;
+        break;
+      }
+      const uint64_t w0 = (tl.start >> 5) & ~uint64_t(3);
+      const uint64_t w1 = ((tl.start + tl.len) / 32 + 3) & ~uint64_t(3);
+      const uint32_t run = (uint32_t)(w1 - w0) * 4;
+      unsigned char* st = stage0 + s * stage_bytes;
+      mbar_arrive_expect_tx(&full[s], tl.len * 4 + G.W * run);
+      bulk_g2s_stream(st, A.e_s + tl.start, tl.len * 4, &full[s], pol);
+      for (uint32_t w = 0; w < G.W; ++w)
+        bulk_g2s(st + kTile * 4 + (size_t)w * kRunWords * 4, A.bits + (uint64_t)w * G.words + w0,
+                 run, &full[s]);
+    }
+    if (!ok) s_abort = 1;
+    for (uint32_t k = 0; k < kSStages && k < ti; ++k) {
+      const uint32_t t = ti - 1 - k;
+      if (!mbar_wait(&full[t % kSStages], (t / kSStages) & 1, err, kErrDrain)) break;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int p = tid;
+  // scales of the first tile
+  if (blockIdx.x < G.n_tiles && (uint32_t)p < G.W) {
+    const Tile tl = decode_tile(G, blockIdx.x);
+    s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
+  }
+  named_sync(1, kSConsumers);
+  uint32_t ti = 0;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
+    const Tile tl = decode_tile(G, T);
+    const uint32_t s = ti % kSStages;
+    // prefetch the next tile's worker scales
+    float next_sc = 0.0f;
+    const uint32_t Tn = T + gridDim.x;
+    if (Tn < G.n_tiles && (uint32_t)p < G.W)
+      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tn).g);
     const float osc = __ldcg(A.sscales + tl.g);
-    __syncthreads();
+    uint32_t owd[4];
+    bool valid[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      valid[i] = off < tl.len;
+      owd[i] = valid[i] ? A.sbits[(tl.start + off) >> 5] : 0u;
+    }
+    bool ok = s_abort == 0 && mbar_wait(&full[s], (ti / kSStages) & 1, err, kErrWaitFull);
+    if (!ok) s_abort = 1;
+    const unsigned char* st = stage0 + s * stage_bytes;
+    const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
+    const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
+    const float* sc = s_sc[ti & 1];
+
+    float4 ev[4];
+    float z[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      ev[i] = valid[i] ? *reinterpret_cast<const float4*>(st + off * 4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) z[i][c] = 0.0f;
+      if (valid[i]) {
+        const uint32_t widx = (off >> 5) + wshift;
+        const int sh = 4 * (p & 7);
+        for (uint32_t w = 0; w < G.W; ++w) {
+          const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
+          const float scw = sc[w];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) z[i][c] = __fadd_rn(z[i][c], ((wd >> c) & 1u) ? scw : -scw);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
 
     float acc = 0.0f;
     uint32_t l = 0;
@@ -51,35 +160,17 @@ __global__ void __launch_bounds__(kThreads) k_server(const ServerArgs A) {
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t off = 1024u * i + 4u * p;
-      const bool valid = off < tl.len;
-      const uint64_t k0 = tl.start + off;
-      float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
-      uint32_t owd = 0;
-      float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (valid) {
-        ev = __ldcs(reinterpret_cast<const float4*>(A.e_s + k0));
-        owd = A.sbits[k0 >> 5];
-        const uint32_t widx = off >> 5;
-        const int sh = 4 * (p & 7);
-        for (uint32_t w = 0; w < G.W; ++w) {
-          const uint32_t wd = sbw[w * (kTile / 32) + widx] >> sh;
-          const float s = sc[w];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) z[c] = __fadd_rn(z[c], ((wd >> c) & 1u) ? s : -s);
-        }
-      }
+      const uint64_t k0 = tl.start + 1024u * i + 4u * p;
       float4 yv;
       uint32_t nib = 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint64_t k = k0 + c;
         float y = 0.0f;
-        if (valid && k < G.n) {
-          const float zc = __fdiv_rn(z[c], fW);
-          const int sh = 4 * (p & 7) + c;
-          const float so = ((owd >> sh) & 1u) ? osc : -osc;
-          const float et = __fsub_rn(f4at(ev, c), so);
+        if (valid[i] && k < G.n) {
+          const float zc = __fdiv_rn(z[i][c], fW);
+          const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
+          const float et = __fsub_rn(f4get(ev[i], c), so);
           if constexpr (LAMB) {
             if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
               r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
@@ -93,45 +184,36 @@ __global__ void __launch_bounds__(kThreads) k_server(const ServerArgs A) {
         f4at(yv, c) = y;
       }
       const uint32_t word = pack_word(nib, lane);
-      if (valid) {
+      if (valid[i]) {
         __stcs(reinterpret_cast<float4*>(A.e_s + k0), yv);
         if ((p & 7) == 0) A.sbits[k0 >> 5] = word;
       }
     }
     acc = warp_butterfly_sum(acc);
     if (lane == 0) ws[warp] = acc;
-    __syncthreads();
+    if (Tn < G.n_tiles && (uint32_t)p < G.W) s_sc[(ti + 1) & 1][p] = next_sc;
+    named_sync(1, kSConsumers);
     if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws);
-    __threadfence();
-    __syncthreads();
-    if (p == 0) {
-      unsigned prev = atomicAdd(A.ws.scnt + tl.g, 1u);
-      s_last = (prev == tl.ntc - 1);
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      if (warp == 0) {
-        float sum = ordered_sum(A.ws.spart + (uint64_t)tl.g * G.tpc, tl.ntc, lane);
-        if (lane == 0) {
-          A.sscales[tl.g] = mean_of(sum, tl.real);
-          A.ws.scnt[tl.g] = 0u;
-        }
-      }
-    }
-    __syncthreads();
+    if (named_sync_or(1, kSConsumers, s_abort != 0)) break;
   }
+}
+
+template <bool LAMB>
+cudaError_t run_server(const ServerArgs& a, int sms, cudaStream_t s) {
+  const size_t bytes = ServerSmem::bytes(a.geo.W);
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      k_server<LAMB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)ServerSmem::bytes(OB_MAX_WORKERS));
+  if (attr != cudaSuccess) return attr;
+  const int grid = grid_for(k_server<LAMB>, sms, a.geo.n_tiles, kServerThreads, bytes);
+  k_server<LAMB><<<grid, kServerThreads, bytes, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s) {
-  if (lamb) {
-    k_server<true><<<grid_for(k_server<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
-  } else {
-    k_server<false><<<grid_for(k_server<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  return lamb ? run_server<true>(a, sms, s) : run_server<false>(a, sms, s);
 }
 
 }  // namespace ob

@@ -58,7 +58,7 @@ size_t region(size_t& cursor, size_t bytes) {
 
 struct Regions {
   size_t wpart, wcnt, spart, scnt, tile_layer, layer_off, ltile_pref, lpart, lcnt, Rbits,
-      rms, gcnt, total;
+      rms, gcnt, err, total;
 };
 
 Regions regions_of(const Geo& G) {
@@ -76,6 +76,7 @@ Regions regions_of(const Geo& G) {
   r.Rbits = region(c, (size_t)G.L * sizeof(unsigned));
   r.rms = region(c, (size_t)G.L * sizeof(float));
   r.gcnt = region(c, 4 * sizeof(unsigned));
+  r.err = region(c, sizeof(unsigned));
   r.total = c;
   return r;
 }
@@ -187,7 +188,7 @@ ob_status ob_init(const ob_config* cfg, ob_ctx** out) {
   const uint64_t cpp = cdiv(G.P, G.C);
   G.Cl = G.P - (cpp - 1) * G.C;
   G.n_pad = W * G.P;
-  G.words = G.n_pad / 32;
+  G.words = cdiv(G.n_pad / 32, 4) * 4;  // 16-byte aligned rows
   const uint64_t tpc = cdiv(G.C, kTile), tpl = cdiv(G.Cl, kTile);
   const uint64_t tpp = (cpp - 1) * tpc + tpl;
   const uint64_t n_tiles = W * tpp, nc = W * cpp;
@@ -297,6 +298,7 @@ ob_status ob_set_workspace(ob_ctx* ctx, void* workspace, size_t bytes, ob_stream
   w.Rbits = reinterpret_cast<unsigned*>(b + r.Rbits);
   w.rms = reinterpret_cast<float*>(b + r.rms);
   w.gcnt = reinterpret_cast<unsigned*>(b + r.gcnt);
+  w.err = reinterpret_cast<unsigned*>(b + r.err);
   ctx->ws_base = workspace;
   ctx->ws_bytes = bytes;
   ctx->sms = sms;
@@ -346,9 +348,9 @@ ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s, uin
   if (st) return st;
   if ((st = check_errs(ctx, err))) return st;
   OB_CHECK_PTR(ctx, err_s, 16, "err_s");
-  OB_CHECK_PTR(ctx, bits, 4, "bits");
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   const Geo& G = ctx->geo;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -386,7 +388,7 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, flo
   if (st) return st;
   if ((st = check_grads(ctx, grads)) || (st = check_errs(ctx, err))) return st;
   OB_CHECK_PTR(ctx, m, 16, "m");
-  OB_CHECK_PTR(ctx, bits, 4, "bits");
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
   if (ls && (st = check_ls(ctx, ls, false))) return st;
   ob::CompressArgs a{};
@@ -407,10 +409,16 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, flo
   a.ratio_ef = (ctx->cfg.flags & OB_FLAG_NO_RATIO_EF) ? 0 : 1;
   a.b1 = ctx->cfg.b1;
   a.ob1 = 1.0f - ctx->cfg.b1;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launched(ctx,
+                     ob::launch_compress(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ls != nullptr,
+                                         ctx->sms, s),
+                     "compress")))
+    return st;
   return launched(ctx,
-                  ob::launch_compress(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ls != nullptr,
-                                      ctx->sms, reinterpret_cast<cudaStream_t>(stream)),
-                  "compress");
+                  ob::launch_finalize_scales(ctx->geo, ctx->ws.wpart, ctx->geo.W, scales,
+                                             ctx->sms, s),
+                  "compress: chunk scales");
 }
 
 ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scales, float* err_s,
@@ -418,10 +426,10 @@ ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scale
                            ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
-  OB_CHECK_PTR(ctx, bits, 4, "bits");
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
   OB_CHECK_PTR(ctx, err_s, 16, "err_s");
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   if (ls && (st = check_ls(ctx, ls, false))) return st;
   ob::ServerArgs a{};
@@ -437,10 +445,11 @@ ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scale
     a.c_prev2 = ls->c_prev2;
   }
   a.ratio_ef = (ctx->cfg.flags & OB_FLAG_NO_RATIO_EF) ? 0 : 1;
-  return launched(ctx,
-                  ob::launch_server(a, ls != nullptr, ctx->sms,
-                                    reinterpret_cast<cudaStream_t>(stream)),
-                  "server_reduce");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launched(ctx, ob::launch_server(a, ls != nullptr, ctx->sms, s), "server_reduce")))
+    return st;
+  return launched(ctx, ob::launch_finalize_scales(ctx->geo, ctx->ws.spart, 1, sscales, ctx->sms, s),
+                  "server_reduce: chunk scales");
 }
 
 static void fill_update(const ob_ctx* ctx, ob::UpdateArgs& a) {
@@ -466,7 +475,7 @@ ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits, const float* sscales
                         const ob_layer_state* ls, float* out, ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, out, 16, "out");
   if (ls) OB_CHECK_PTR(ctx, ls->s, 4, "ls.s");
@@ -486,7 +495,7 @@ ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                        const float* v_frozen, float* m, float* p, ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, v_frozen, 16, "v_frozen");
   OB_CHECK_PTR(ctx, m, 16, "m");
@@ -508,7 +517,7 @@ ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                        const ob_layer_state* ls, ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, v_frozen, 16, "v_frozen");
   OB_CHECK_PTR(ctx, v_fresh, 16, "v_fresh");
@@ -546,10 +555,10 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* 
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_errs(ctx, err))) return st;
-  OB_CHECK_PTR(ctx, bits, 4, "bits");
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
   OB_CHECK_PTR(ctx, err_s, 16, "err_s");
-  OB_CHECK_PTR(ctx, sbits, 4, "sbits");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   const Geo& G = ctx->geo;
   ob::MaterializeArgs a{};
@@ -565,6 +574,20 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* 
   cudaError_t e = cudaMemsetAsync(scales, 0, (size_t)G.W * G.nc * sizeof(float), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(sscales, 0, (size_t)G.nc * sizeof(float), s);
   return launched(ctx, e, "materialize: clearing the scales");
+}
+
+ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream) {
+  ob_status st = ready(ctx);
+  if (st) return st;
+  if (!code) return fail(ctx, OB_ERR_INVALID, "code is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ctx->ws.err, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->ws.err, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "device_error");
+  *code = v;
+  return OB_OK;
 }
 
 ob_status ob_quant_int8(const float* g, size_t n, int8_t* q, float* block_scales, uint64_t seed,

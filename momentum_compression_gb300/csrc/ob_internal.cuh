@@ -24,7 +24,7 @@ struct Geo {
   uint64_t C;        // chunk size, <= P, multiple of 32
   uint64_t Cl;       // length of the last chunk of a partition
   uint64_t n_pad;    // W * P
-  uint64_t words;    // n_pad / 32, words per worker
+  uint64_t words;    // row stride of the sign words: n_pad/32 rounded up to 4
   uint32_t W;        // workers
   uint32_t cpp;      // chunks per partition
   uint32_t tpc;      // tiles in a full chunk (also the stride of partials)
@@ -79,6 +79,7 @@ struct Workspace {
   unsigned* Rbits;       // [L] LAMB max ratio, as float bit patterns
   float* rms;            // [L] begin: momentum RMS per layer
   unsigned* gcnt;        // [4] whole-grid arrival counters
+  unsigned* err;         // [1] first device-side error code (0 = none)
 };
 
 // LAMB per-layer parameters handed to kernels.
@@ -253,9 +254,10 @@ struct WarmupArgs {
 // ---------------------------------------------------------------------------
 
 template <typename K>
-inline int grid_for(K kernel, int sms, uint64_t items) {
+inline int grid_for(K kernel, int sms, uint64_t items, int threads = kThreads,
+                    size_t smem = 0) {
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess ||
       occ < 1)
     occ = 1;
   uint64_t g = (uint64_t)sms * (uint64_t)occ;
@@ -267,6 +269,8 @@ inline int grid_for(K kernel, int sms, uint64_t items) {
 cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
                             cudaStream_t s);
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s);
+cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
+                                   float* scales, int sms, cudaStream_t s);
 cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_lamb_pass_a(const UpdateArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s);

@@ -40,7 +40,7 @@ def test_layout_matches_definition():
     assert lay["chunks_per_partition"] == 14 and lay["n_chunks"] == 112
     # 13 full chunks of 256 tiles + a last chunk of 57,344 elements (14 tiles)
     assert lay["n_tiles"] == 8 * (13 * 256 + 14)
-    assert lay["words_per_worker"] == lay["n_pad"] // 32
+    assert lay["words_per_worker"] == (lay["n_pad"] // 32 + 3) // 4 * 4
     ob.ob_destroy(ctx)
     ctx = ob.ob_init(5000, 3, 992, 32)
     lay = ob.ob_get_layout(ctx)
