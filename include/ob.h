@@ -249,6 +249,26 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err,
  * `stream`. */
 ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream);
 
+/* No counterpart in the pages: an addition of this library for callers
+ * that cannot allocate device memory -- code inside a runtime whose own
+ * pool owns the device and gives extensions no allocator, or code that
+ * cannot afford the device-wide synchronisation of cudaMalloc/cudaFree.
+ * Same arguments and results as ob_compress with ls == NULL (1-bit Adam),
+ * and no workspace is needed: the scratch (per-tile totals and an error
+ * word) is a static device array of OB_NOALLOC_SCRATCH_BYTES that every
+ * GPU loading the library holds until exit.  Allocates nothing.
+ *   - Layouts whose W * n_chunks * tiles_per_chunk * 4 bytes (+ 512) exceed
+ *     OB_NOALLOC_SCRATCH_BYTES are rejected with OB_ERR_UNSUPPORTED
+ *     (e.g. up to about 2^28 elements at W = 8).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race. */
+#define OB_NOALLOC_SCRATCH_BYTES (4u << 20)
+ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads, const float* m,
+                              float* const* err, uint32_t* bits, float* scales,
+                              ob_stream_t stream);
+
 /* Block-wise INT8 stochastic rounding ([TUT] "FP32 → INT8 量化" and the
  * GradientQuantizeINT8 example), blocks of 256 elements (the last may be
  * short):

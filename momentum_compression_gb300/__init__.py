@@ -32,7 +32,7 @@ EXPORTS = (
     "ob_init", "ob_destroy", "ob_last_error", "ob_get_layout", "ob_workspace_bytes",
     "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
-    "ob_materialize_errors", "ob_device_error", "ob_quant_int8",
+    "ob_materialize_errors", "ob_device_error", "ob_quant_int8", "ob_compress_noalloc",
 )
 
 
@@ -95,6 +95,7 @@ def lib():
         L.ob_materialize_errors.argtypes = [vp] * 8
         L.ob_device_error.argtypes = [vp, ct.POINTER(ct.c_uint), vp]
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
+        L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -220,6 +221,13 @@ def ob_begin_compression(ctx, err, err_s, bits, scales, sbits, sscales, m=None, 
 def ob_compress(ctx, grads, m, err, bits, scales, ls=None, stream=None):
     _check(lib().ob_compress(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err), _ptr(bits),
                              _ptr(scales), _ls(ls), _stream(stream)), ctx)
+
+
+def ob_compress_noalloc(ctx, grads, m, err, bits, scales, stream=None):
+    """ob_compress (1-bit Adam) with the library's static scratch instead of
+    a workspace: for callers that cannot allocate device memory."""
+    _check(lib().ob_compress_noalloc(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err),
+                                     _ptr(bits), _ptr(scales), _stream(stream)), ctx)
 
 
 def ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls=None, stream=None):

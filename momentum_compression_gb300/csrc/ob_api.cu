@@ -129,6 +129,18 @@ ob_status launched(ob_ctx* ctx, cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace ob {
+
+// Read-only views of a ctx and its error slot, for the other translation
+// units of the library.
+const Geo* ctx_geo(const ob_ctx* ctx) { return &ctx->geo; }
+const ob_config* ctx_config(const ob_ctx* ctx) { return &ctx->cfg; }
+ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg) {
+  return fail(ctx, st, "%s", msg);
+}
+
+}  // namespace ob
+
 extern "C" {
 
 const char* ob_last_error(const ob_ctx* ctx) {

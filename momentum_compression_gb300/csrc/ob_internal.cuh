@@ -253,6 +253,11 @@ struct WarmupArgs {
 // the cudaError_t of its launch.
 // ---------------------------------------------------------------------------
 
+// Views of a ctx (defined with the C entry points).
+const Geo* ctx_geo(const ob_ctx* ctx);
+const ob_config* ctx_config(const ob_ctx* ctx);
+ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg);
+
 template <typename K>
 inline int grid_for(K kernel, int sms, uint64_t items, int threads = kThreads,
                     size_t smem = 0) {
