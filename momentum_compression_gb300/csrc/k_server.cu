@@ -17,6 +17,15 @@
 // (rounded out to 16-byte boundaries) into a ring of shared-memory stages
 // with cp.async.bulk; eight consumer warps read the four words each lane
 // needs from shared memory.  Waits are bounded (ptx.cuh).
+//
+// The W-way signed sum depends only on the element's W sign bits, and the
+// scales are constant within a tile.  So each tile first tabulates
+// z8[b] = (sum over w < min(W,8), in order, from 0, of (bit w of b ? s_w :
+// -s_w)) for all 2^min(W,8) patterns b -- the same additions in the same
+// order as element by element, hence the same bits -- divided by W when
+// W <= 8.  An element then gathers its first 8 workers' bits into a byte
+// (a 4-bit nibble per worker is spread to 4 bytes with one multiply) and
+// reads its z from the table; workers 8.. are added after it in order.
 #include "ob_internal.cuh"
 #include "ptx.cuh"
 
@@ -29,14 +38,25 @@ constexpr int kServerThreads = kThreads + 32;
 constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
 
 struct ServerSmem {
-  __host__ __device__ static size_t stage_bytes(uint32_t W) { return kTile * 4 + (size_t)W * kRunWords * 4; }
+  __host__ __device__ static size_t stage_bytes(uint32_t W) {
+    return kTile * 4 + (size_t)W * kRunWords * 4;
+  }
   __host__ __device__ static size_t bytes(uint32_t W) {
-    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 2 * OB_MAX_WORKERS * 4;
+    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 2 * OB_MAX_WORKERS * 4 +
+           2 * 256 * 4;
   }
 };
 
+// Table entry b for the first W8 = min(W, 8) workers (see the file header).
+__device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, uint32_t b) {
+  const uint32_t W8 = W < 8 ? W : 8;
+  float z = 0.0f;
+  for (uint32_t w = 0; w < W8; ++w) z = __fadd_rn(z, ((b >> w) & 1u) ? sc[w] : -sc[w]);
+  return W <= 8 ? __fdiv_rn(z, (float)W) : z;
+}
+
 template <bool LAMB>
-__global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A) {
+__global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo& G = A.geo;
   const size_t stage_bytes = ServerSmem::stage_bytes(G.W);
@@ -44,6 +64,7 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSStages * stage_bytes);
   uint64_t* empty = full + kSStages;
   float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(empty + kSStages);
+  float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 2);
   __shared__ float ws[8];
   __shared__ volatile int s_abort;
 
@@ -96,10 +117,13 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
   // ------------------------------------------------------------ consumers
   const int p = tid;
   // scales of the first tile
+  const uint32_t W8 = G.W < 8 ? G.W : 8;
   if (blockIdx.x < G.n_tiles && (uint32_t)p < G.W) {
     const Tile tl = decode_tile(G, blockIdx.x);
     s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
   }
+  named_sync(1, kSConsumers);
+  if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], G.W, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
@@ -126,6 +150,7 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
     const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
     const float* sc = s_sc[ti & 1];
 
+    const float* z8 = s_z8[ti & 1];
     float4 ev[4];
     float z[4][4];
 #pragma unroll
@@ -138,7 +163,18 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
       if (valid[i]) {
         const uint32_t widx = (off >> 5) + wshift;
         const int sh = 4 * (p & 7);
-        for (uint32_t w = 0; w < G.W; ++w) {
+        // byte c of idx = the first W8 workers' bits of element c
+        uint32_t idx = 0;
+#pragma unroll
+        for (uint32_t w = 0; w < 8; ++w) {
+          if (w < W8) {
+            const uint32_t nib = (sbw[w * kRunWords + widx] >> sh) & 0xFu;
+            idx |= (nib * (0x00204081u << w)) & (0x01010101u << w);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
+        for (uint32_t w = 8; w < G.W; ++w) {
           const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
           const float scw = sc[w];
 #pragma unroll
@@ -168,7 +204,7 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
         const uint64_t k = k0 + c;
         float y = 0.0f;
         if (valid[i] && k < G.n) {
-          const float zc = __fdiv_rn(z[i][c], fW);
+          const float zc = G.W <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
           const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
           const float et = __fsub_rn(f4get(ev[i], c), so);
           if constexpr (LAMB) {
@@ -194,6 +230,8 @@ __global__ void __launch_bounds__(kServerThreads, 1) k_server(const ServerArgs A
     if (Tn < G.n_tiles && (uint32_t)p < G.W) s_sc[(ti + 1) & 1][p] = next_sc;
     named_sync(1, kSConsumers);
     if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws);
+    if (Tn < G.n_tiles && (uint32_t)p < (1u << W8))
+      s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) & 1], G.W, p);
     if (named_sync_or(1, kSConsumers, s_abort != 0)) break;
   }
 }

@@ -22,42 +22,45 @@ namespace {
 __global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
   const Geo& G = A.geo;
   const int p = threadIdx.x;
+  const float* __restrict__ vf = A.v_frozen;
+  float* __restrict__ pp = A.p;
+  float* __restrict__ mm = A.m;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
     const Tile tl = decode_tile(G, T);
-    if (tl.start >= G.n) {
-      // whole tile is padding: m = 0
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t off = 1024u * i + 4u * p;
-        if (off < tl.len)
-          __stcs(reinterpret_cast<float4*>(A.m + tl.start + off), make_float4(0.f, 0.f, 0.f, 0.f));
-      }
-      continue;
-    }
     const float osc = __ldcg(A.sscales + tl.g);
+    // all loads of the tile first (4 sign words, 4 x 2 128-bit rows), then
+    // the arithmetic, then the stores
+    uint32_t wd[4];
+    float4 vv[4], pv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      const uint64_t k0 = tl.start + off;
+      const bool live = off < tl.len && k0 < G.n;
+      wd[i] = live ? __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7)) : 0u;
+      vv[i] = live ? __ldcs(reinterpret_cast<const float4*>(vf + k0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      pv[i] = live ? __ldcs(reinterpret_cast<const float4*>(pp + k0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t off = 1024u * i + 4u * p;
       if (off >= tl.len) continue;
       const uint64_t k0 = tl.start + off;
-      const uint32_t wd = __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7));
-      const float4 vv = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
-      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
       float4 mo;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (k0 + c < G.n) {
-          const float mk = ((wd >> c) & 1u) ? osc : -osc;
-          const float d = __fadd_rn(__fsqrt_rn(f4get(vv, c)), A.eps);
+          const float mk = ((wd[i] >> c) & 1u) ? osc : -osc;
+          const float d = __fadd_rn(__fsqrt_rn(f4get(vv[i], c)), A.eps);
           const float u = __fdiv_rn(mk, d);
-          f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(A.lr, u));
+          f4at(pv[i], c) = __fsub_rn(f4get(pv[i], c), __fmul_rn(A.lr, u));
           f4at(mo, c) = mk;
         } else {
-          f4at(mo, c) = 0.0f;
+          f4at(mo, c) = 0.0f;  // padding: m = 0, p untouched
         }
       }
-      __stcs(reinterpret_cast<float4*>(A.m + k0), mo);
-      if (k0 < G.n) __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+      __stcs(reinterpret_cast<float4*>(mm + k0), mo);
+      if (k0 < G.n) __stcs(reinterpret_cast<float4*>(pp + k0), pv[i]);
     }
   }
 }
