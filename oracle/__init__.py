@@ -60,6 +60,7 @@ def lib():
         L.orc_uniform.restype = f32
         L.orc_quant_int8.argtypes = [f32p, u64, u64, u64, u64, i8p, f32p,
                                      vp]
+        L.orc_quant_int8_at.argtypes = [f32p, u64, u64, u64, u64, u64, i8p, f32p, vp]
         _lib = L
     return _lib
 
@@ -213,12 +214,14 @@ def uniform(seed, step, k):
     return np.float32(lib().orc_uniform(seed, step, k))
 
 
-def quant_int8(g, block=256, seed=1234, step=0, deq=False):
+def quant_int8(g, block=256, seed=1234, step=0, deq=False, k0=0):
+    """k0: index of g[0] in the whole tensor (a multiple of block)."""
     g = _f32(g)
+    assert k0 % block == 0
     q = np.zeros(g.size, np.int8)
     sc = np.zeros((g.size + block - 1) // block, np.float32)
     d = np.zeros(g.size, np.float32) if deq else None
-    lib().orc_quant_int8(g, g.size, block, seed, step, q, sc, _ptr(d))
+    lib().orc_quant_int8_at(g, g.size, k0, block, seed, step, q, sc, _ptr(d))
     return (q, sc, d) if deq else (q, sc)
 
 

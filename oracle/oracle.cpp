@@ -578,8 +578,21 @@ float orc_uniform(uint64_t seed, uint64_t step, uint64_t k) {
 //        clamped to [-127, 127]
 // deq (optional) = q * scale.  Reading: the example's "floor + Bernoulli"
 // form is used (not floor(x + eps)); the two agree in distribution.
+// orc_quant_int8_at quantises g[0..n) as the elements k0 .. k0+n-1 of a
+// larger tensor (k0 a multiple of `block`): blocks and uniforms are those of
+// the whole tensor.  orc_quant_int8 is the whole tensor (k0 = 0).
+void orc_quant_int8_at(const float* g, uint64_t n, uint64_t k0, uint64_t block,
+                       uint64_t seed, uint64_t step, int8_t* q, float* block_scales,
+                       float* deq);
+
 void orc_quant_int8(const float* g, uint64_t n, uint64_t block, uint64_t seed,
                     uint64_t step, int8_t* q, float* block_scales, float* deq) {
+  orc_quant_int8_at(g, n, 0, block, seed, step, q, block_scales, deq);
+}
+
+void orc_quant_int8_at(const float* g, uint64_t n, uint64_t k0, uint64_t block,
+                       uint64_t seed, uint64_t step, int8_t* q, float* block_scales,
+                       float* deq) {
   for (uint64_t b0 = 0, bi = 0; b0 < n; b0 += block, ++bi) {
     uint64_t b1 = b0 + block < n ? b0 + block : n;
     float mx = 0.0f;
@@ -601,7 +614,7 @@ void orc_quant_int8(const float* g, uint64_t n, uint64_t block, uint64_t seed,
       float x = g[k] / scale;
       float f = std::floor(x);
       float frac = x - f;
-      float u = orc_uniform(seed, step, k);
+      float u = orc_uniform(seed, step, k0 + k);
       float qf = f + ((u < frac) ? 1.0f : 0.0f);
       if (qf > 127.0f) qf = 127.0f;
       if (qf < -127.0f) qf = -127.0f;
