@@ -274,6 +274,52 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def run_int8(args):
+    """The block-256 INT8 stochastic-rounding quantizer on the sweep's
+    largest size, n = 2^30 fp32 values (4 GB in, 1 GB of codes and 16 MB of
+    scales out per call; larger than L2)."""
+    import torch
+
+    import momentum_compression_gb300 as ob
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    n = args.n or (1 << 30)
+    g = torch.randn(n, device="cuda") * 1e-3
+    q = torch.empty(n, dtype=torch.int8, device="cuda")
+    sc = torch.empty((n + 255) // 256, device="cuda")
+    for t in range(args.warmup):
+        ob.ob_quant_int8(g, q, sc, 1234, t)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(local)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid)
+    with ClockSampler(uuid) as clk:
+        torch.cuda.synchronize()
+        a.record(stream)
+        for t in range(args.steps):
+            ob.ob_quant_int8(g, q, sc, 1234, 1000 + t)
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    bpe = 4 + 1 + 4 / 256
+    peak, kind = measured_peak()
+    gbs = bpe * n / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "INT8 block-256 stochastic-rounding quantizer elements/s", "value": n / (ms * 1e-3),
+            "unit": "elements/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32 -> int8", "data": "synthetic",
+            "config": {"workload": f"int8 quantizer, n = {n}, block 256, Philox4x32-10",
+                       "l2": "inputs larger than L2; no flush"},
+            "roofline": {"bound": "hbm", "kernel": "quant_int8", "achieved": gbs, "peak": peak,
+                         "peak_kind": kind, "unit": "GB/s", "frac": gbs / peak,
+                         "bytes_per_element": bpe, "traffic": None},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def run_ours(args, wl):
     import torch
 
@@ -302,9 +348,17 @@ def run_ours(args, wl):
     opt.p.copy_(p0)
     del p0
     gsets = [device_grads(torch, wl, n_pad, s, gdt, device) for s in range(2)]
-    # prerequisite: a few uncompressed warmup steps freeze v
-    for t in range(3):
+    # prerequisite: a few uncompressed warmup steps freeze v (timed on their
+    # own: the warmup step is a row of the path, not the metric)
+    stream0 = torch.cuda.current_stream()
+    wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    opt.warmup_step(gsets[0])
+    wa.record(stream0)
+    for t in range(1, 4):
         opt.warmup_step(gsets[t % 2])
+    wb.record(stream0)
+    torch.cuda.synchronize()
+    warm_ms = wa.elapsed_time(wb) / 3
     opt.begin_compression()
     stream = torch.cuda.current_stream()
     for t in range(args.warmup):
@@ -355,6 +409,9 @@ def run_ours(args, wl):
         total_ms = float(tt.item())
     ms = total_ms / K
     bpe = bytes_per_element(wl.W, G, lamb)
+    # warmup: W gradients read; m, v, p read + written (LAMB: pass 1 reads
+    # g, m, v, p and writes m, v; pass 2 reads m, v, p and writes p)
+    warm_bpe = wl.W * G + (36 if lamb else 24)
     value = world * n / (ms * 1e-3)
     peak, peak_kind = measured_peak()
     kms = {k: sum(v) / K for k, v in per.items()}
@@ -427,6 +484,8 @@ def run_ours(args, wl):
                      "bytes_per_element": bpe[dom],
                      "traffic": None if traffic is None else traffic * n},
         "step_roofline_frac": bpe["total"] * n / (ms * 1e-3) / 1e9 / peak,
+        "warmup_step": {"ms": warm_ms, "bytes_per_element": warm_bpe,
+                        "gbs": warm_bpe * n / (warm_ms * 1e-3) / 1e9},
         "kernels_ms": kms,
         "kernels_gbs": {k: bpe[k] * n / (kms[k] * 1e-3) / 1e9 for k in kms},
         "gpu_launches": launches,
@@ -457,6 +516,9 @@ def main():
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.impl == "ours" and args.workload == "int8":
+        run_int8(args)
+        return
     if args.workload == "flat":
         wl = synth.workload("flat", n=args.n or (1 << 24), W=args.W or 8,
                             chunk=args.chunk or (1 << 20))

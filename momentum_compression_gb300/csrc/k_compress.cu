@@ -24,6 +24,8 @@
 // xor-shuffles per 32-bit word; the new x goes back to global memory with
 // streaming 128-bit stores.  No wait is unbounded (ptx.cuh), and no CTA
 // ever waits for another.
+#include <type_traits>
+
 #include "ob_internal.cuh"
 #include "ptx.cuh"
 
@@ -136,26 +138,18 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     __syncwarp();
     if (lane == 0) mbar_arrive(mempty);
 
-    // Per-element layer factors (1-bit LAMB only).
-    float sig[4][4], rho[4][4];
+    // 1-bit LAMB: the layer of the tile's first element; every worker pass
+    // walks the layers forward from it (layers change rarely inside a tile)
+    uint32_t l_t = 0;
+    uint64_t lend_t = 0;
+    float s_t = 1.0f, r_t = 1.0f;
     if constexpr (LAMB) {
-      uint32_t l = __ldg(A.ws.tile_layer + T);
-      uint64_t lend = __ldg(A.ws.layer_off + l + 1);
-      float s_l = __ldg(A.s + l);
-      float r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint64_t k = tl.start + 1024u * i + 4u * p + c;
-          if (valid[i] && k < G.n && advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
-            s_l = __ldg(A.s + l);
-            r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
-          }
-          sig[i][c] = s_l;
-          rho[i][c] = r_l;
-        }
+      l_t = __ldg(A.ws.tile_layer + T);
+      lend_t = __ldg(A.ws.layer_off + l_t + 1);
+      s_t = __ldg(A.s + l_t);
+      r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
     }
+    const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
 
     for (uint32_t w = 0; w < G.W; ++w, ++item) {
       const uint32_t s = item % kStages;
@@ -188,36 +182,53 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers now
 
-      float acc = 0.0f;
+      // UNI: the whole tile lies in one layer (sigma, rho scalar); else the
+      // layers are walked element by element
+      auto body = [&](auto uni_tag) -> float {
+        constexpr bool UNI = decltype(uni_tag)::value;
+        float acc = 0.0f;
+        uint32_t l = l_t;
+        uint64_t lend = lend_t;
+        float s_l = s_t, r_l = r_t;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint64_t k0 = tl.start + 1024u * i + 4u * p;
-        float4 xv;
-        uint32_t nib = 0;
+        for (int i = 0; i < 4; ++i) {
+          const uint64_t k0 = tl.start + 1024u * i + 4u * p;
+          float4 xv;
+          uint32_t nib = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x = 0.0f;
-          if (valid[i] && k0 + c < G.n) {
-            const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;  // scale*sign
-            const float et = __fsub_rn(f4get(ev[i], c), so);
-            const float mw = __fadd_rn(__fmul_rn(b1, f4get(mv[i], c)),
-                                       __fmul_rn(ob1, f4get(gv[i], c)));
-            if constexpr (LAMB) {
-              x = __fadd_rn(__fmul_rn(sig[i][c], mw), __fmul_rn(rho[i][c], et));
-            } else {
-              x = __fadd_rn(mw, et);
+          for (int c = 0; c < 4; ++c) {
+            float x = 0.0f;
+            if (valid[i] && k0 + c < G.n) {
+              const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;  // scale*sign
+              const float et = __fsub_rn(f4get(ev[i], c), so);
+              const float mw = __fadd_rn(__fmul_rn(b1, f4get(mv[i], c)),
+                                         __fmul_rn(ob1, f4get(gv[i], c)));
+              if constexpr (LAMB) {
+                if constexpr (!UNI) {
+                  if (advance_layer(A.ws.layer_off, G.L, k0 + c, l, lend)) {
+                    s_l = __ldg(A.s + l);
+                    r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l))
+                                     : 1.0f;
+                  }
+                }
+                x = __fadd_rn(__fmul_rn(s_l, mw), __fmul_rn(r_l, et));
+              } else {
+                x = __fadd_rn(mw, et);
+              }
+              acc = __fadd_rn(acc, fabsf(x));
+              if (x >= 0.0f) nib |= 1u << c;
             }
-            acc = __fadd_rn(acc, fabsf(x));
-            if (x >= 0.0f) nib |= 1u << c;
+            f4at(xv, c) = x;
           }
-          f4at(xv, c) = x;
+          const uint32_t word = pack_word(nib, lane);
+          if (valid[i]) {
+            __stcs(reinterpret_cast<float4*>(e + k0), xv);
+            if ((p & 7) == 0) bw[k0 >> 5] = word;
+          }
         }
-        const uint32_t word = pack_word(nib, lane);
-        if (valid[i]) {
-          __stcs(reinterpret_cast<float4*>(e + k0), xv);
-          if ((p & 7) == 0) bw[k0 >> 5] = word;
-        }
-      }
+        return acc;
+      };
+      float acc = uni ? body(std::true_type{}) : body(std::false_type{});
       acc = warp_butterfly_sum(acc);
       if (lane == 0) ws[w][warp] = acc;
     }

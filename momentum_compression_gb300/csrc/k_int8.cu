@@ -4,9 +4,10 @@
 // draw on the fractional part, clamp to ±127).
 //
 // One warp per block of 256 elements: lane j holds elements 4j..4j+3 and
-// 128+4j..128+4j+3 (two 128-bit loads), the block max is a warp max, and
-// each group of four elements draws one Philox4x32-10 output (four 32-bit
-// words) from counter (k>>2, step).
+// 128+4j..128+4j+3 (two 128-bit loads, the next block's issued before this
+// one is quantised), the block max is a warp max, and each group of four
+// elements draws one Philox4x32-10 output (four 32-bit words) from counter
+// (k>>2, step).
 //
 // Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel random
 // numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64-bit
@@ -17,16 +18,29 @@
 namespace ob {
 namespace {
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Round keys of Philox4x32-10: key k advanced by (0x9E3779B9, 0xBB67AE85)
+// before every round but the first; computed once per thread.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys K;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    K.k0[r] = k0 + (uint32_t)r * 0x9E3779B9u;
+    K.k1[r] = k1 + (uint32_t)r * 0xBB67AE85u;
+  }
+  return K;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& K) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k0[r], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ K.k1[r], (uint32_t)p0);
   }
   return c;
 }
@@ -36,18 +50,20 @@ __device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
 }
 
 // Quantizes the 4 elements of group `grp` (elements 4*grp .. 4*grp+3).
+template <bool DEQ>
 __device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64_t grp,
-                                           uint64_t step, uint32_t k0, uint32_t k1,
-                                           int nvalid, float4& dq) {
+                                           uint64_t step, const PhiloxKeys& K, int nvalid,
+                                           float4& dq) {
   const uint4 ctr = make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
                                (uint32_t)(step >> 32));
-  const uint4 rnd = philox4x32_10(ctr, k0, k1);
+  const uint4 rnd = philox4x32_10(ctr, K);
   uint32_t packed = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     float qf = 0.0f;
     if (c < nvalid && scale != 0.0f) {
-      const float x = __fdiv_rn(f4get(gv, c), scale);
+      const float g = f4get(gv, c);
+      const float x = __fdiv_rn(g, scale);
       const float f = floorf(x);
       const float fr = __fsub_rn(x, f);
       const float u = __fmul_rn((float)(word_of(rnd, c) >> 8), 5.9604644775390625e-08f);
@@ -56,12 +72,30 @@ __device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64
       qf = qf < -127.0f ? -127.0f : qf;
       if (qf != qf) qf = 0.0f;
     }
-    f4at(dq, c) = __fmul_rn(qf, scale);
+    if constexpr (DEQ) f4at(dq, c) = __fmul_rn(qf, scale);
     packed |= ((uint32_t)(int32_t)qf & 0xffu) << (8 * c);
   }
   return packed;
 }
 
+// Loads the two 4-element groups lane `lane` owns in block b (zeros and a
+// valid count of 0..4 per group beyond n).
+__device__ __forceinline__ void load_block(const float* __restrict__ g, uint64_t n, uint64_t b,
+                                           int lane, float4 (&gv)[2], int (&nv)[2]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint64_t k = b * 256 + 128 * h + 4 * lane;
+    nv[h] = k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
+    if (nv[h] == 4) {
+      gv[h] = __ldcs(reinterpret_cast<const float4*>(g + k));
+    } else {
+      gv[h] = make_float4(nv[h] > 0 ? g[k] : 0.f, nv[h] > 1 ? g[k + 1] : 0.f,
+                          nv[h] > 2 ? g[k + 2] : 0.f, 0.f);
+    }
+  }
+}
+
+template <bool DEQ>
 __global__ void __launch_bounds__(kThreads)
     k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
                  float* __restrict__ scales, uint64_t seed, uint64_t step,
@@ -69,35 +103,25 @@ __global__ void __launch_bounds__(kThreads)
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
-  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-  for (uint64_t b = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); b < nblk;
-       b += warps) {
-    float4 gv[2];
-    int nv[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint64_t k = b * 256 + 128 * h + 4 * lane;
-      nv[h] = k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
-      if (nv[h] == 4) {
-        gv[h] = __ldcs(reinterpret_cast<const float4*>(g + k));
-      } else {
-        gv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < nv[h]; ++c) f4at(gv[h], c) = g[k + c];
-      }
-    }
+  const PhiloxKeys K = philox_keys((uint32_t)seed, (uint32_t)(seed >> 32));
+  uint64_t b = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  float4 gv[2];
+  int nv[2];
+  if (b < nblk) load_block(g, n, b, lane, gv, nv);
+  for (; b < nblk; b += warps) {
+    // the next block's loads are in flight while this block is quantised
+    float4 gn[2];
+    int nn[2] = {0, 0};
+    if (b + warps < nblk) load_block(g, n, b + warps, lane, gn, nn);
+    // fmaxf returns the other operand when one is NaN: a NaN never wins
     float mx = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float a = fabsf(f4at(gv[h], c));
-        if (c < nv[h] && a > mx) mx = a;  // a NaN never wins
-      }
+      for (int c = 0; c < 4; ++c)
+        if (c < nv[h]) mx = fmaxf(mx, fabsf(f4get(gv[h], c)));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float other = __shfl_xor_sync(kFull, mx, o);
-      if (other > mx) mx = other;
-    }
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, 127.0f);
     if (lane == 0) scales[b] = scale;
 #pragma unroll
@@ -105,17 +129,24 @@ __global__ void __launch_bounds__(kThreads)
       if (nv[h] == 0) continue;
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
       float4 dq;
-      const uint32_t packed = quant4(gv[h], scale, k >> 2, step, k0, k1, nv[h], dq);
+      const uint32_t packed = quant4<DEQ>(gv[h], scale, k >> 2, step, K, nv[h], dq);
       if (nv[h] == 4) {
         *reinterpret_cast<uint32_t*>(q + k) = packed;
-        if (deq) __stcs(reinterpret_cast<float4*>(deq + k), dq);
+        if constexpr (DEQ) __stcs(reinterpret_cast<float4*>(deq + k), dq);
       } else {
-        for (int c = 0; c < nv[h]; ++c) {
-          q[k + c] = (int8_t)((packed >> (8 * c)) & 0xffu);
-          if (deq) deq[k + c] = f4at(dq, c);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          if (c < nv[h]) {
+            q[k + c] = (int8_t)((packed >> (8 * c)) & 0xffu);
+            if constexpr (DEQ) deq[k + c] = f4get(dq, c);
+          }
         }
       }
     }
+    gv[0] = gn[0];
+    gv[1] = gn[1];
+    nv[0] = nn[0];
+    nv[1] = nn[1];
   }
 }
 
@@ -126,8 +157,12 @@ cudaError_t launch_quant_int8(const float* g, uint64_t n, int8_t* q, float* scal
                               cudaStream_t s) {
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t ctas = (nblk + kThreads / 32 - 1) / (kThreads / 32);
-  k_quant_int8<<<grid_for(k_quant_int8, sms, ctas), kThreads, 0, s>>>(g, n, q, scales, seed,
-                                                                      step, deq);
+  if (deq)
+    k_quant_int8<true><<<grid_for(k_quant_int8<true>, sms, ctas), kThreads, 0, s>>>(
+        g, n, q, scales, seed, step, deq);
+  else
+    k_quant_int8<false><<<grid_for(k_quant_int8<false>, sms, ctas), kThreads, 0, s>>>(
+        g, n, q, scales, seed, step, deq);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,8 @@
 // W <= 8.  An element then gathers its first 8 workers' bits into a byte
 // (a 4-bit nibble per worker is spread to 4 bytes with one multiply) and
 // reads its z from the table; workers 8.. are added after it in order.
+#include <type_traits>
+
 #include "ob_internal.cuh"
 #include "ptx.cuh"
 
@@ -185,46 +187,59 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 
-    float acc = 0.0f;
-    uint32_t l = 0;
-    uint64_t lend = 0;
-    float r_l = 1.0f;
+    uint32_t l_t = 0;
+    uint64_t lend_t = 0;
+    float r_t = 1.0f;
     if constexpr (LAMB) {
-      l = __ldg(A.ws.tile_layer + T);
-      lend = __ldg(A.ws.layer_off + l + 1);
-      r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
+      l_t = __ldg(A.ws.tile_layer + T);
+      lend_t = __ldg(A.ws.layer_off + l_t + 1);
+      r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
     }
+    // UNI: the whole tile lies in one layer (rho scalar); else the layers
+    // are walked element by element
+    auto body = [&](auto uni_tag) -> float {
+      constexpr bool UNI = decltype(uni_tag)::value;
+      float acc = 0.0f;
+      uint32_t l = l_t;
+      uint64_t lend = lend_t;
+      float r_l = r_t;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint64_t k0 = tl.start + 1024u * i + 4u * p;
-      float4 yv;
-      uint32_t nib = 0;
+      for (int i = 0; i < 4; ++i) {
+        const uint64_t k0 = tl.start + 1024u * i + 4u * p;
+        float4 yv;
+        uint32_t nib = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint64_t k = k0 + c;
-        float y = 0.0f;
-        if (valid[i] && k < G.n) {
-          const float zc = G.W <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
-          const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
-          const float et = __fsub_rn(f4get(ev[i], c), so);
-          if constexpr (LAMB) {
-            if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
-              r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
-            y = __fadd_rn(__fmul_rn(r_l, et), zc);
-          } else {
-            y = __fadd_rn(et, zc);
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t k = k0 + c;
+          float y = 0.0f;
+          if (valid[i] && k < G.n) {
+            const float zc = G.W <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
+            const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
+            const float et = __fsub_rn(f4get(ev[i], c), so);
+            if constexpr (LAMB) {
+              if constexpr (!UNI) {
+                if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+                  r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
+              }
+              y = __fadd_rn(__fmul_rn(r_l, et), zc);
+            } else {
+              y = __fadd_rn(et, zc);
+            }
+            acc = __fadd_rn(acc, fabsf(y));
+            if (y >= 0.0f) nib |= 1u << c;
           }
-          acc = __fadd_rn(acc, fabsf(y));
-          if (y >= 0.0f) nib |= 1u << c;
+          f4at(yv, c) = y;
         }
-        f4at(yv, c) = y;
+        const uint32_t word = pack_word(nib, lane);
+        if (valid[i]) {
+          __stcs(reinterpret_cast<float4*>(A.e_s + k0), yv);
+          if ((p & 7) == 0) A.sbits[k0 >> 5] = word;
+        }
       }
-      const uint32_t word = pack_word(nib, lane);
-      if (valid[i]) {
-        __stcs(reinterpret_cast<float4*>(A.e_s + k0), yv);
-        if ((p & 7) == 0) A.sbits[k0 >> 5] = word;
-      }
-    }
+      return acc;
+    };
+    const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
+    float acc = uni ? body(std::true_type{}) : body(std::false_type{});
     acc = warp_butterfly_sum(acc);
     if (lane == 0) ws[warp] = acc;
     if (Tn < G.n_tiles && (uint32_t)p < G.W) s_sc[(ti + 1) & 1][p] = next_sc;

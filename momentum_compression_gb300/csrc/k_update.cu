@@ -14,6 +14,8 @@
 //     p = p - (lr*c_l)*(m_t/(sqrt(v_Tw)+eps))
 // All operations are rounded one by one (no contraction), with IEEE
 // division and square root.
+#include <type_traits>
+
 #include "ob_internal.cuh"
 
 namespace ob {
@@ -97,48 +99,72 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
     const Tile tl = decode_tile(G, T);
     const float osc = __ldcg(A.sscales + tl.g);
-    uint32_t l = __ldg(A.ws.tile_layer + T);
-    uint64_t lend = __ldg(A.ws.layer_off + l + 1);
-    float sg_l = __ldg(A.ls.s + l);
+    const uint32_t l_t = __ldg(A.ws.tile_layer + T);
+    const uint64_t lend_t = __ldg(A.ws.layer_off + l_t + 1);
+    const float s_t = __ldg(A.ls.s + l_t);
+    // all loads of the tile first
+    uint32_t wd[4];
+    float4 mv[4], vt[4], vf[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      const uint64_t k0 = tl.start + off;
+      const bool live = off < tl.len && k0 < G.n;
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      wd[i] = live ? __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7)) : 0u;
+      mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
+      vt[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_fresh + k0)) : z4;
+      vf[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0)) : z4;
+    }
+    // UNI: the whole tile lies in one layer; else the layers are walked
+    // element by element and each layer's running max is flushed when the
+    // walk leaves it
+    uint32_t l = l_t;
     float rmax = 0.0f;  // running max of the ratio for layer l
+    auto body = [&](auto uni_tag) {
+      constexpr bool UNI = decltype(uni_tag)::value;
+      uint64_t lend = lend_t;
+      float sg_l = s_t;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint64_t k0 = tl.start + 1024u * i + 4u * p;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t k = k0 + c;
+          if (1024u * i + 4u * p >= tl.len || k >= G.n) {
+            f4at(mv[i], c) = 0.0f;
+            continue;
+          }
+          if constexpr (!UNI) {
+            const uint32_t l_old = l;
+            if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
+              if (rmax > 0.0f) atomicMax(A.ws.Rbits + l_old, __float_as_uint(rmax));
+              rmax = 0.0f;
+              sg_l = __ldg(A.ls.s + l);
+            }
+          }
+          const float M = ((wd[i] >> c) & 1u) ? osc : -osc;
+          const float mt = __fdiv_rn(M, sg_l);
+          const float gt =
+              __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, f4get(mv[i], c))), A.ob1);
+          const float v = __fadd_rn(__fmul_rn(A.b2, f4get(vt[i], c)),
+                                    __fmul_rn(A.ob2, __fmul_rn(gt, gt)));
+          f4at(mv[i], c) = mt;
+          f4at(vt[i], c) = v;
+          const float ratio = __fdiv_rn(f4get(vf[i], c), v);
+          if (ratio > rmax) rmax = ratio;  // NaN never wins
+        }
+      }
+    };
+    if (tl.start + tl.len <= lend_t || G.n <= lend_t) body(std::true_type{});
+    else body(std::false_type{});
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t off = 1024u * i + 4u * p;
       if (off >= tl.len) continue;
       const uint64_t k0 = tl.start + off;
-      if (k0 >= G.n) {
-        __stcs(reinterpret_cast<float4*>(A.m + k0), make_float4(0.f, 0.f, 0.f, 0.f));
-        continue;
-      }
-      const uint32_t wd = __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7));
-      float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
-      float4 vt = __ldcs(reinterpret_cast<const float4*>(A.v_fresh + k0));
-      const float4 vf = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint64_t k = k0 + c;
-        if (k >= G.n) {
-          f4at(mv, c) = 0.0f;
-          continue;
-        }
-        const uint32_t l_old = l;
-        if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
-          if (rmax > 0.0f) atomicMax(A.ws.Rbits + l_old, __float_as_uint(rmax));
-          rmax = 0.0f;
-          sg_l = __ldg(A.ls.s + l);
-        }
-        const float M = ((wd >> c) & 1u) ? osc : -osc;
-        const float mt = __fdiv_rn(M, sg_l);
-        const float gt = __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, f4at(mv, c))), A.ob1);
-        const float v = __fadd_rn(__fmul_rn(A.b2, f4at(vt, c)),
-                                  __fmul_rn(A.ob2, __fmul_rn(gt, gt)));
-        f4at(mv, c) = mt;
-        f4at(vt, c) = v;
-        const float ratio = __fdiv_rn(f4get(vf, c), v);
-        if (ratio > rmax) rmax = ratio;  // NaN never wins
-      }
-      __stcs(reinterpret_cast<float4*>(A.m + k0), mv);
-      __stcs(reinterpret_cast<float4*>(A.v_fresh + k0), vt);
+      __stcs(reinterpret_cast<float4*>(A.m + k0), mv[i]);
+      if (k0 < G.n) __stcs(reinterpret_cast<float4*>(A.v_fresh + k0), vt[i]);
     }
     // Flush the running max: one atomic per warp when all its lanes ended
     // in the same layer, else one per lane.
@@ -172,29 +198,49 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
     const Tile tl = decode_tile(G, T);
     if (tl.start >= G.n) continue;
-    uint32_t l = __ldg(A.ws.tile_layer + T);
-    uint64_t lend = __ldg(A.ws.layer_off + l + 1);
-    float t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+    const uint32_t l_t = __ldg(A.ws.tile_layer + T);
+    const uint64_t lend_t = __ldg(A.ws.layer_off + l_t + 1);
+    const float t1_t = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l_t));
+    float4 mv[4], vf[4], pv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t off = 1024u * i + 4u * p;
-      if (off >= tl.len) continue;
       const uint64_t k0 = tl.start + off;
-      if (k0 >= G.n) continue;
-      const float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
-      const float4 vf = __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0));
-      float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+      const bool live = off < tl.len && k0 < G.n;
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
+      vf[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0)) : z4;
+      pv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.p + k0)) : z4;
+    }
+    auto body = [&](auto uni_tag) {
+      constexpr bool UNI = decltype(uni_tag)::value;
+      uint32_t l = l_t;
+      uint64_t lend = lend_t;
+      float t1 = t1_t;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint64_t k = k0 + c;
-        if (k >= G.n) continue;
-        if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
-          t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
-        const float d = __fadd_rn(__fsqrt_rn(f4get(vf, c)), A.eps);
-        const float u = __fdiv_rn(f4get(mv, c), d);
-        f4at(pv, c) = __fsub_rn(f4at(pv, c), __fmul_rn(t1, u));
+      for (int i = 0; i < 4; ++i) {
+        const uint64_t k0 = tl.start + 1024u * i + 4u * p;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t k = k0 + c;
+          if (1024u * i + 4u * p >= tl.len || k >= G.n) continue;
+          if constexpr (!UNI) {
+            if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+              t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+          }
+          const float d = __fadd_rn(__fsqrt_rn(f4get(vf[i], c)), A.eps);
+          const float u = __fdiv_rn(f4get(mv[i], c), d);
+          f4at(pv[i], c) = __fsub_rn(f4get(pv[i], c), __fmul_rn(t1, u));
+        }
       }
-      __stcs(reinterpret_cast<float4*>(A.p + k0), pv);
+    };
+    if (tl.start + tl.len <= lend_t || G.n <= lend_t) body(std::true_type{});
+    else body(std::false_type{});
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t off = 1024u * i + 4u * p;
+      const uint64_t k0 = tl.start + off;
+      if (off < tl.len && k0 < G.n) __stcs(reinterpret_cast<float4*>(A.p + k0), pv[i]);
     }
   }
 }
