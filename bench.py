@@ -50,15 +50,16 @@ def log(*a):
 # Algorithmic bytes per real element (G = gradient bytes, W workers)
 # ---------------------------------------------------------------------------
 
-def bytes_per_element(W, G, lamb=False):
-    """compress: m read 4 + per worker g read G, e read 4 + write 4, old
-    sign word read 1/8 + new word write 1/8; server: W/8 word reads, e_s read
-    4 + write 4, sign word 1/8 + 1/8; Adam: sign word 1/8, v 4, p 4 + 4,
-    m write 4.  LAMB pass A: sign word 1/8, m 4+4, v_fresh 4+4, v_Tw 4;
-    pass B: m 4, v_Tw 4, p 4+4."""
-    comp = 4 + W * (G + 8 + 0.25)
+def bytes_per_element(W, G, lamb=False, sign_m=False):
+    """compress: m read 4 (sign form: the server's word, 1/8) + per worker
+    g read G, e read 4 + write 4, old sign word read 1/8 + new word write
+    1/8; server: W/8 word reads, e_s read 4 + write 4, sign word 1/8 + 1/8;
+    Adam: sign word 1/8, v 4, p 4 + 4, m write 4 (none in sign form).  LAMB
+    pass A: sign word 1/8, m 4+4, v_fresh 4+4, v_Tw 4; pass B: m 4, v_Tw 4,
+    p 4+4."""
+    comp = (0.125 if sign_m else 4) + W * (G + 8 + 0.25)
     serv = W / 8 + 8 + 0.25
-    upd = (0.125 + 20 + 16) if lamb else (0.125 + 4 + 8 + 4)
+    upd = (0.125 + 20 + 16) if lamb else (0.125 + 4 + 8 + (0 if sign_m else 4))
     return {"compress": comp, "server": serv, "update": upd, "total": comp + serv + upd}
 
 
@@ -335,8 +336,10 @@ def run_ours(args, wl):
         pg = dist
     G = 2 if wl.grad_dtype == "bf16" else 4
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
+    sign_m = wl.mode != "lamb" and not args.dense_m
     opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype, wl.layer_offsets,
-                             lamb=(wl.mode == "lamb"), device=device, **wl.hp)
+                             lamb=(wl.mode == "lamb"), device=device, sign_momentum=sign_m,
+                             **wl.hp)
     n, n_pad = wl.n, opt.n_pad
     log(f"[bench] rank {rank}: {wl.name} n={n} W={wl.W} n_pad={n_pad} "
         f"tiles={opt.layout['n_tiles']}")
@@ -382,7 +385,11 @@ def run_ours(args, wl):
             g = gsets[t % 2]
             e = ev[t]
             e[0].record(stream)
-            ob.ob_compress(opt.ctx, g, opt.m, opt.err, opt.bits, opt.scales, opt.ls)
+            if sign_m:
+                ob.ob_compress_signm(opt.ctx, g, opt.sbits, opt.sscales, opt.err, opt.bits,
+                                     opt.scales)
+            else:
+                ob.ob_compress(opt.ctx, g, opt.m, opt.err, opt.bits, opt.scales, opt.ls)
             e[1].record(stream)
             ob.ob_server_reduce(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
                                 opt.ls)
@@ -391,7 +398,8 @@ def run_ours(args, wl):
                 ob.ob_lamb_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.v_fresh, opt.m, opt.p,
                                 opt.ls)
             else:
-                ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.m, opt.p)
+                ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, None if sign_m else opt.m,
+                                opt.p)
             e[3].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -408,7 +416,7 @@ def run_ours(args, wl):
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         total_ms = float(tt.item())
     ms = total_ms / K
-    bpe = bytes_per_element(wl.W, G, lamb)
+    bpe = bytes_per_element(wl.W, G, lamb, sign_m)
     # warmup: W gradients read; m, v, p read + written (LAMB: pass 1 reads
     # g, m, v, p and writes m, v; pass 2 reads m, v, p and writes p)
     warm_bpe = wl.W * G + (36 if lamb else 24)
@@ -472,6 +480,8 @@ def run_ours(args, wl):
         "vs_baseline": None, "dtype": "f32" if G == 4 else "f32 (bf16 gradients)",
         "data": "synthetic",
         "config": {"workload": wl_label(wl), "n": n, "W": wl.W, "chunk": wl.chunk,
+                   "momentum": ("sign form: sbits + chunk scales, exact (ob_compress_signm)"
+                                if sign_m else "dense fp32"),
                    "n_layers": wl.n_layers, "grad_dtype": wl.grad_dtype,
                    "parallelism": "replicas" if world > 1 else "1 GPU",
                    "l2": f"inputs larger than L2 ({bpe['total'] * n / 1e9:.1f} GB touched per "
@@ -514,6 +524,8 @@ def main():
     ap.add_argument("--n", type=int, help="elements (flat workload only)")
     ap.add_argument("--W", type=int, help="workers (flat workload only)")
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
+    ap.add_argument("--dense-m", action="store_true",
+                    help="1-bit Adam: keep the momentum as a dense fp32 buffer")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "ours" and args.workload == "int8":

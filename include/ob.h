@@ -195,6 +195,20 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m,
                       float* const* err, uint32_t* bits, float* scales,
                       const ob_layer_state* ls, ob_stream_t stream);
 
+/* ob_compress for 1-bit Adam with the momentum in its sign form: after a
+ * compressed Adam step the momentum is exactly sscale*sign(sbit) of that
+ * step's server output, so the next compression can read those words
+ * (1/8 byte per element) instead of a dense fp32 m (4 bytes), and the
+ * update need not write m (ob_adam_step with m == NULL); ob_decompress
+ * gives m whenever it is wanted.  sbits/sscales are read before the
+ * following ob_server_reduce overwrites them.  Not for the first
+ * compressed step after ob_begin_compression (m comes from warmup then),
+ * nor after ob_materialize_errors (which zeroes sscales): use ob_compress
+ * with the dense m there. */
+ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
+                            const float* sscales, float* const* err, uint32_t* bits,
+                            float* scales, ob_stream_t stream);
+
 /* Server average and re-compression, all partitions ([LAMB] 3-4):
  *   z = (sum_w scale_w(chunk)*sign_w)/W;  y = rho_l*e_s + z
  *   sscale(chunk) = mean |y|;  sbit = y >= 0;  e_s' = y - sscale*sign(y) */
@@ -209,7 +223,9 @@ ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits,
                         float* out, ob_stream_t stream);
 
 /* 1-bit Adam update with the frozen variance ([LAMB] 1, [BLOG] 2.1):
- *   m = sscale*sign(sbit);  p -= lr*(m/(sqrt(v_frozen)+eps)) */
+ *   m = sscale*sign(sbit);  p -= lr*(m/(sqrt(v_frozen)+eps))
+ * m may be NULL: then it is not written, and the momentum stays held
+ * exactly by (sbits, sscales) -- see ob_compress_signm. */
 ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits,
                        const float* sscales, const float* v_frozen, float* m,
                        float* p, ob_stream_t stream);
@@ -228,7 +244,9 @@ ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits,
                        const ob_layer_state* ls, ob_stream_t stream);
 
 /* compress + server_reduce + adam_step (ls == NULL) or lamb_step, in one
- * call, in that order. */
+ * call, in that order.  With m == NULL (1-bit Adam only) the momentum is
+ * held in its sign form: ob_compress_signm + server + ob_adam_step without
+ * m. */
 ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m,
                   float* const* err, uint32_t* bits, float* scales,
                   float* err_s, uint32_t* sbits, float* sscales,

@@ -33,6 +33,7 @@ EXPORTS = (
     "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
     "ob_materialize_errors", "ob_device_error", "ob_quant_int8", "ob_compress_noalloc",
+    "ob_compress_signm",
 )
 
 
@@ -96,6 +97,7 @@ def lib():
         L.ob_device_error.argtypes = [vp, ct.POINTER(ct.c_uint), vp]
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
         L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -230,6 +232,13 @@ def ob_compress_noalloc(ctx, grads, m, err, bits, scales, stream=None):
                                      _ptr(bits), _ptr(scales), _stream(stream)), ctx)
 
 
+def ob_compress_signm(ctx, grads, sbits, sscales, err, bits, scales, stream=None):
+    """ob_compress for 1-bit Adam reading the momentum as sscale*sign(sbit)."""
+    _check(lib().ob_compress_signm(ctx, _ptr_array(grads), _ptr(sbits), _ptr(sscales),
+                                   _ptr_array(err), _ptr(bits), _ptr(scales), _stream(stream)),
+           ctx)
+
+
 def ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls=None, stream=None):
     _check(lib().ob_server_reduce(ctx, _ptr(bits), _ptr(scales), _ptr(err_s), _ptr(sbits),
                                   _ptr(sscales), _ls(ls), _stream(stream)), ctx)
@@ -291,9 +300,14 @@ class OneBitOptimizer:
     sscales, the workspace, and the per-layer LAMB state."""
 
     def __init__(self, n, W, chunk, align=4096, grad_dtype="f32", layer_offsets=None,
-                 lamb=False, device="cuda", **hp):
+                 lamb=False, device="cuda", sign_momentum=False, **hp):
+        """sign_momentum (1-bit Adam only): after the first compressed step
+        the momentum is held as (sbits, sscales) -- exactly sscale*sign --
+        and the dense m buffer is only refreshed by materialize_m()."""
         import torch
         self.lamb = lamb
+        self.sign_momentum = sign_momentum and not lamb
+        self.m_in_signs = False
         self.grad_dtype = grad_dtype
         self.ctx = ob_init(n, W, chunk, align,
                            OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32,
@@ -343,12 +357,23 @@ class OneBitOptimizer:
         ob_begin_compression(self.ctx, self.err, self.err_s, self.bits, self.scales, self.sbits,
                              self.sscales, self.m, self.v, self.v_fresh,
                              self.ls if self.lamb else None, max(self.warmup_steps, 1), stream)
+        self.m_in_signs = False
 
     def compressed_step(self, grads, stream=None):
-        ob_step(self.ctx, grads, self.m, self.err, self.bits, self.scales, self.err_s,
+        m = None if self.m_in_signs else self.m
+        ob_step(self.ctx, grads, m, self.err, self.bits, self.scales, self.err_s,
                 self.sbits, self.sscales, self.v, self.v_fresh, self.p,
                 self.ls if self.lamb else None, stream)
+        if self.sign_momentum and not self.m_in_signs:
+            self.m_in_signs = True  # the next steps read the momentum from the signs
+
+    def materialize_m(self, stream=None):
+        """Writes the dense momentum (it is exact: sscale*sign)."""
+        if self.m_in_signs:
+            ob_decompress(self.ctx, self.sbits, self.sscales, self.m, None, stream)
+            self.m_in_signs = False
 
     def materialize_errors(self, stream=None):
+        self.materialize_m(stream)  # the sign form is lost once sscales are cleared
         ob_materialize_errors(self.ctx, self.err, self.bits, self.scales, self.err_s,
                               self.sbits, self.sscales, stream)

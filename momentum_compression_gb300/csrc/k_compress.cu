@@ -36,23 +36,26 @@ constexpr int kConsumers = kThreads;            // 8 warps
 constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 
 // Two CTAs per SM: 2 stages of 32 KB (fp32 gradients) or 3 of 24 KB (bf16)
-// plus the m tile, so that 4-6 (tile, worker) items are in flight per SM.
-template <bool BF16>
+// plus the m tile, so that 4-6 (tile, worker) items are in flight per SM;
+// with the momentum in sign form the m tile's room holds one more stage.
+template <bool BF16, bool MSIGN>
 struct CompressSmem {
-  static constexpr int kStages = BF16 ? 3 : 2;
+  static constexpr int kStages = (BF16 ? 3 : 2) + (MSIGN ? 1 : 0);
   static constexpr uint32_t kG = BF16 ? 2u : 4u;
   static constexpr size_t kStageG = kTile * kG;
   static constexpr size_t kStageE = kTile * 4;
   static constexpr size_t kStage = kStageG + kStageE;
-  static constexpr size_t kM = kTile * 4;
+  static constexpr size_t kM = MSIGN ? 0 : kTile * 4;
   static constexpr size_t kBars = (2 * kStages + 2) * 8;
   static constexpr size_t kWs = OB_MAX_WORKERS * 8 * 4;
   static constexpr size_t kBytes = kM + kStages * kStage + kBars + kWs;
 };
 
-template <bool BF16, bool LAMB>
+// MSIGN: the momentum is read in its sign form (msscale*sign(msbit), what
+// the previous server step produced) instead of as a dense fp32 tile.
+template <bool BF16, bool LAMB, bool MSIGN>
 __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const CompressArgs A) {
-  using S = CompressSmem<BF16>;
+  using S = CompressSmem<BF16, MSIGN>;
   constexpr int kStages = S::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
   float* mbuf = reinterpret_cast<float*>(smem);  // [4096]
@@ -89,10 +92,12 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     bool ok = true;
     for (uint32_t T = blockIdx.x; ok && T < G.n_tiles; T += gridDim.x, ++ti) {
       const Tile tl = decode_tile(G, T);
-      if (ti >= 1) ok = mbar_wait(mempty, (ti - 1) & 1, err, kErrWaitEmpty);
-      if (!ok || s_abort) break;
-      mbar_arrive_expect_tx(mfull, tl.len * 4);
-      bulk_g2s_stream(mbuf, A.m + tl.start, tl.len * 4, mfull, pol);
+      if constexpr (!MSIGN) {
+        if (ti >= 1) ok = mbar_wait(mempty, (ti - 1) & 1, err, kErrWaitEmpty);
+        if (!ok || s_abort) break;
+        mbar_arrive_expect_tx(mfull, tl.len * 4);
+        bulk_g2s_stream(mbuf, A.m + tl.start, tl.len * 4, mfull, pol);
+      }
       for (uint32_t w = 0; w < G.W; ++w, ++item) {
         const uint32_t s = item % kStages, r = item / kStages;
         if (r >= 1) ok = mbar_wait(&empty[s], (r - 1) & 1, err, kErrWaitEmpty);
@@ -113,30 +118,62 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       const uint32_t it = item - 1 - k;
       if (!mbar_wait(&full[it % kStages], (it / kStages) & 1, err, kErrDrain)) break;
     }
-    if (ti >= 1) mbar_wait(mfull, (ti - 1) & 1, err, kErrDrain);
+    if (!MSIGN && ti >= 1) mbar_wait(mfull, (ti - 1) & 1, err, kErrDrain);
     return;
   }
 
   // ------------------------------------------------------------ consumers
   const float b1 = A.b1, ob1 = A.ob1;
   const int p = tid;
-  uint32_t item = 0, ti = 0;
-  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
-    const Tile tl = decode_tile(G, T);
-    bool ok = s_abort == 0 && mbar_wait(mfull, ti & 1, err, kErrWaitFull);
-    if (!ok) s_abort = 1;
-
-    float4 mv[4];
-    bool valid[4];
+  // MSIGN: the momentum's sign words and chunk scale of the next tile are
+  // loaded one tile ahead, so their latency hides behind the current tile
+  uint32_t mw_next[4] = {0u, 0u, 0u, 0u};
+  float mss_next = 0.0f;
+  auto load_msign = [&](uint32_t Tn) {
+    const Tile tn = decode_tile(G, Tn);
+    mss_next = __ldcg(A.msscales + tn.g);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t off = 1024u * i + 4u * p;
-      valid[i] = off < tl.len;
-      mv[i] = valid[i] ? *reinterpret_cast<const float4*>(mbuf + off)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      mw_next[i] = off < tn.len ? __ldg(A.msbits + ((tn.start + off) >> 5)) : 0u;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(mempty);
+  };
+  if constexpr (MSIGN) {
+    if (blockIdx.x < G.n_tiles) load_msign(blockIdx.x);
+  }
+  uint32_t item = 0, ti = 0;
+  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
+    const Tile tl = decode_tile(G, T);
+    bool ok = true;
+    float4 mv[4];
+    bool valid[4];
+    if constexpr (MSIGN) {
+      const float mss = mss_next;
+      uint32_t mw_cur[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mw_cur[i] = mw_next[i];
+      if (T + gridDim.x < G.n_tiles) load_msign(T + gridDim.x);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        valid[i] = off < tl.len;
+        const uint32_t wd = mw_cur[i] >> (4 * (p & 7));
+        mv[i] = make_float4((wd & 1u) ? mss : -mss, (wd & 2u) ? mss : -mss,
+                            (wd & 4u) ? mss : -mss, (wd & 8u) ? mss : -mss);
+      }
+    } else {
+      ok = s_abort == 0 && mbar_wait(mfull, ti & 1, err, kErrWaitFull);
+      if (!ok) s_abort = 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        valid[i] = off < tl.len;
+        mv[i] = valid[i] ? *reinterpret_cast<const float4*>(mbuf + off)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(mempty);
+    }
 
     // 1-bit LAMB: the layer of the tile's first element; every worker pass
     // walks the layers forward from it (layers change rarely inside a tile)
@@ -240,15 +277,16 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   }
 }
 
-template <bool BF16, bool LAMB>
+template <bool BF16, bool LAMB, bool MSIGN>
 cudaError_t run_compress(const CompressArgs& a, int sms, cudaStream_t s) {
-  using S = CompressSmem<BF16>;
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      k_compress<BF16, LAMB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+  using S = CompressSmem<BF16, MSIGN>;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_compress<BF16, LAMB, MSIGN>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
   if (attr != cudaSuccess) return attr;
   const int grid =
-      grid_for(k_compress<BF16, LAMB>, sms, a.geo.n_tiles, kCompressThreads, S::kBytes);
-  k_compress<BF16, LAMB><<<grid, kCompressThreads, S::kBytes, s>>>(a);
+      grid_for(k_compress<BF16, LAMB, MSIGN>, sms, a.geo.n_tiles, kCompressThreads, S::kBytes);
+  k_compress<BF16, LAMB, MSIGN><<<grid, kCompressThreads, S::kBytes, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -256,8 +294,16 @@ cudaError_t run_compress(const CompressArgs& a, int sms, cudaStream_t s) {
 
 cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
                             cudaStream_t s) {
-  if (bf16) return lamb ? run_compress<true, true>(a, sms, s) : run_compress<true, false>(a, sms, s);
-  return lamb ? run_compress<false, true>(a, sms, s) : run_compress<false, false>(a, sms, s);
+  if (bf16)
+    return lamb ? run_compress<true, true, false>(a, sms, s)
+                : run_compress<true, false, false>(a, sms, s);
+  return lamb ? run_compress<false, true, false>(a, sms, s)
+              : run_compress<false, false, false>(a, sms, s);
+}
+
+cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, int sms, cudaStream_t s) {
+  return bf16 ? run_compress<true, false, true>(a, sms, s)
+              : run_compress<false, false, true>(a, sms, s);
 }
 
 }  // namespace ob

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
           f4at(mo, c) = 0.0f;  // padding: m = 0, p untouched
         }
       }
-      __stcs(reinterpret_cast<float4*>(mm + k0), mo);
+      if (mm) __stcs(reinterpret_cast<float4*>(mm + k0), mo);  // m == null: kept as signs
       if (k0 < G.n) __stcs(reinterpret_cast<float4*>(pp + k0), pv[i]);
     }
   }

@@ -510,14 +510,14 @@ ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
   OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, v_frozen, 16, "v_frozen");
-  OB_CHECK_PTR(ctx, m, 16, "m");
+  if (m && !aligned(m, 16)) return fail(ctx, OB_ERR_ALIGN, "m is not 16-byte aligned");
   OB_CHECK_PTR(ctx, p, 16, "p");
   ob::UpdateArgs a{};
   fill_update(ctx, a);
   a.sbits = sbits;
   a.sscales = sscales;
   a.v_frozen = v_frozen;
-  a.m = m;
+  a.m = m;  // may be null: the momentum stays in its sign form
   a.p = p;
   return launched(ctx,
                   ob::launch_adam_update(a, ctx->sms, reinterpret_cast<cudaStream_t>(stream)),
@@ -550,11 +550,54 @@ ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
   return launched(ctx, ob::launch_lamb_pass_b(a, ctx->sms, s), "lamb_step pass B");
 }
 
+ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
+                            const float* sscales, float* const* err, uint32_t* bits,
+                            float* scales, ob_stream_t stream) {
+  ob_status st = ready(ctx);
+  if (st) return st;
+  if ((st = check_grads(ctx, grads)) || (st = check_errs(ctx, err))) return st;
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
+  OB_CHECK_PTR(ctx, sscales, 4, "sscales");
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
+  OB_CHECK_PTR(ctx, scales, 4, "scales");
+  ob::CompressArgs a{};
+  a.geo = ctx->geo;
+  a.ws = ctx->ws;
+  for (int w = 0; w < ctx->cfg.W; ++w) {
+    a.g[w] = grads[w];
+    a.e[w] = err[w];
+  }
+  a.msbits = sbits;
+  a.msscales = sscales;
+  a.bits = bits;
+  a.scales = scales;
+  a.ratio_ef = 1;
+  a.b1 = ctx->cfg.b1;
+  a.ob1 = 1.0f - ctx->cfg.b1;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launched(ctx,
+                     ob::launch_compress_signm(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ctx->sms, s),
+                     "compress_signm")))
+    return st;
+  return launched(ctx,
+                  ob::launch_finalize_scales(ctx->geo, ctx->ws.wpart, ctx->geo.W, scales,
+                                             ctx->sms, s),
+                  "compress_signm: chunk scales");
+}
+
 ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m, float* const* err,
                   uint32_t* bits, float* scales, float* err_s, uint32_t* sbits, float* sscales,
                   const float* v_frozen, float* v_fresh, float* p, const ob_layer_state* ls,
                   ob_stream_t stream) {
-  ob_status st = ob_compress(ctx, grads, m, err, bits, scales, ls, stream);
+  ob_status st;
+  if (!m && !ls) {
+    // 1-bit Adam with the momentum held in its sign form
+    if ((st = ob_compress_signm(ctx, grads, sbits, sscales, err, bits, scales, stream))) return st;
+    if ((st = ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, nullptr, stream)))
+      return st;
+    return ob_adam_step(ctx, sbits, sscales, v_frozen, nullptr, p, stream);
+  }
+  st = ob_compress(ctx, grads, m, err, bits, scales, ls, stream);
   if (st) return st;
   if ((st = ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls, stream))) return st;
   if (!ls) return ob_adam_step(ctx, sbits, sscales, v_frozen, m, p, stream);

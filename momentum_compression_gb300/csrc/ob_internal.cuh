@@ -186,7 +186,9 @@ struct CompressArgs {
   Workspace ws;
   const void* g[OB_MAX_WORKERS];
   float* e[OB_MAX_WORKERS];
-  const float* m;
+  const float* m;          // dense momentum, or null: then m = msscale*sign(msbits)
+  const uint32_t* msbits;  // momentum in sign form (the previous server step)
+  const float* msscales;
   uint32_t* bits;
   float* scales;
   const float* s;        // LAMB sigma, or null
@@ -273,6 +275,7 @@ inline int grid_for(K kernel, int sms, uint64_t items, int threads = kThreads,
 
 cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
                             cudaStream_t s);
+cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, int sms, cudaStream_t s);
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s);
 cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
                                    float* scales, int sms, cudaStream_t s);

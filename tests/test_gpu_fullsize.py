@@ -189,10 +189,11 @@ def _compare_chunk_errors_and_p(opt, co, what, p_exact=True):
         assert_bits_equal(host(opt.p[s:s + r]), S.p[:r], f"{what} p")
 
 
-def _run_adam_fullsize(wl, steps=2, need_bytes=None):
+def _run_adam_fullsize(wl, steps=2, need_bytes=None, sign_momentum=False):
     if need_bytes and _free_bytes() < need_bytes:
         pytest.skip(f"needs {need_bytes / 1e9:.0f} GB of free device memory")
-    opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype, **wl.hp)
+    opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype,
+                             sign_momentum=sign_momentum, **wl.hp)
     std = _std_vector(wl, opt.n_pad)
     _fill_state(opt, wl, seed=99)
     chunks = _chunks(opt.layout, wl.n)
@@ -207,6 +208,7 @@ def _run_adam_fullsize(wl, steps=2, need_bytes=None):
         del grads
     torch.cuda.synchronize()
     assert ob.ob_device_error(opt.ctx) == 0
+    opt.materialize_m()
     for g, co in cos.items():
         _compare_chunk(opt, co, g, f"chunk {g}")
     opt.materialize_errors()
@@ -216,10 +218,13 @@ def _run_adam_fullsize(wl, steps=2, need_bytes=None):
     opt.close()
 
 
-def test_bert_base_full_size():
+@pytest.mark.parametrize("sign_momentum", [False, True])
+def test_bert_base_full_size(sign_momentum):
     """109,482,240 parameters (199 tensors), W = 8, chunk 2^20, fp32: the
-    workload bench.py times."""
-    _run_adam_fullsize(synth.workload("bert-base"), steps=2, need_bytes=20e9)
+    workload bench.py times (with the momentum in sign form, as bench.py
+    runs it, and dense)."""
+    _run_adam_fullsize(synth.workload("bert-base"), steps=3, need_bytes=20e9,
+                       sign_momentum=sign_momentum)
 
 
 def test_gpt_1p3b_bf16_full_size():

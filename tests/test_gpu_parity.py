@@ -145,11 +145,12 @@ def test_compress_server_update_single_kernels(case):
     c.close()
 
 
-def _run_adam(wl, warm, steps, check_every=False):
+def _run_adam(wl, warm, steps, check_every=False, sign_momentum=False):
     """Runs `warm` warmup and `steps` compressed steps of workload wl on the
     GPU and in the oracle from the same seeded inputs."""
     n, W = wl.n, wl.W
-    opt = ob.OneBitOptimizer(n, W, wl.chunk, wl.align, wl.grad_dtype, **wl.hp)
+    opt = ob.OneBitOptimizer(n, W, wl.chunk, wl.align, wl.grad_dtype,
+                             sign_momentum=sign_momentum, **wl.hp)
     lay = O.Layout(n, W, wl.align, wl.chunk)
     st = O.State(lay)
     p0 = np.zeros(lay.n_pad, f32)
@@ -195,6 +196,7 @@ def _run_adam(wl, warm, steps, check_every=False):
 
 def _compare_state(opt, st, lay, exact=True):
     assert ob.ob_device_error(opt.ctx) == 0
+    opt.materialize_m()
     assert_bits_equal(host(opt.sbits)[: lay.words], st.sbits, "server sign words")
     assert_bits_equal(host(opt.sscales), st.sscales, "server scales")
     assert_bits_equal(host(opt.bits)[:, : lay.words], st.bits, "worker sign words")
@@ -216,6 +218,23 @@ def test_flat_1m_adam_5_warmup_10_compressed():
     warmup steps then 10 compressed steps."""
     wl = synth.workload("flat-1m")
     opt, st, lay = _run_adam(wl, wl.warmup_steps, wl.compressed_steps, check_every=True)
+    _compare_state(opt, st, lay)
+    opt.close()
+
+
+@pytest.mark.parametrize("workload,dt", [("flat-1m", "f32"), ("gpt-1.3b", "bf16")])
+def test_sign_momentum_matches_oracle(workload, dt):
+    """1-bit Adam with the momentum held as the server's sign words and
+    chunk scales (ob_compress_signm, ob_adam_step without m): the same
+    results as the dense momentum, bit for bit; the dense m, rebuilt by
+    ob_decompress, equals the oracle's."""
+    wl = synth.workload(workload)
+    if dt == "bf16":
+        wl.tensors = None
+        wl.n = 250_000
+        wl.chunk = 1 << 13
+    opt, st, lay = _run_adam(wl, 2, 6, check_every=True, sign_momentum=True)
+    assert opt.m_in_signs
     _compare_state(opt, st, lay)
     opt.close()
 
