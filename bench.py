@@ -183,9 +183,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, sign_m):
     """DRAM bytes per element of the compress kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel source and workload."""
     path = os.path.join(ROOT, "profiles", "compress_traffic.txt")
     try:
         kv = {}
@@ -197,6 +197,9 @@ def recorded_traffic(workload):
             return None
         if kv.get("workload_W") != str(workload.W) or kv.get("grad_bytes") != (
                 "2" if workload.grad_dtype == "bf16" else "4"):
+            return None
+        if kv.get("workload") != workload.name or kv.get("momentum") != (
+                "sign" if sign_m else "dense"):
             return None
         return float(kv["dram_bytes_per_element"])
     except (OSError, KeyError, ValueError):
@@ -426,7 +429,7 @@ def run_ours(args, wl):
     dom = max(kms, key=kms.get)
     dom_bytes = bpe[dom] * n
     achieved = dom_bytes / (kms[dom] * 1e-3) / 1e9
-    traffic = recorded_traffic(wl) if dom == "compress" else None
+    traffic = recorded_traffic(wl, sign_m) if dom == "compress" else None
 
     # end to end through host buffers: H2D of every worker's gradient, the
     # step, D2H of the updated parameters
