@@ -253,6 +253,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest value of x over all ranks (x itself without a process
+    group).  Timing takes the max: the job is as slow as its slowest rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Units per second of the whole job: every rank processes
+    units_per_rank, the job takes ms (max over ranks)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_reference(args, wl):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -414,16 +431,13 @@ def run_ours(args, wl):
     # compress + scale finalisation, server + scale finalisation, update
     # (LAMB: pass A and pass B)
     launches = K * (6 if lamb else 5)
-    if pg:
-        tt = torch.tensor([total_ms], device=device)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, pg, device)
     ms = total_ms / K
     bpe = bytes_per_element(wl.W, G, lamb, sign_m)
     # warmup: W gradients read; m, v, p read + written (LAMB: pass 1 reads
     # g, m, v, p and writes m, v; pass 2 reads m, v, p and writes p)
     warm_bpe = wl.W * G + (36 if lamb else 24)
-    value = world * n / (ms * 1e-3)
+    value = job_rate(n, world, ms)
     peak, peak_kind = measured_peak()
     kms = {k: sum(v) / K for k, v in per.items()}
     dom = max(kms, key=kms.get)
@@ -455,12 +469,8 @@ def run_ours(args, wl):
         host_p.copy_(opt.p, non_blocking=True)
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / K2
-    if pg:
-        tt = torch.tensor([e2e_ms], device=device)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": world * n / (e2e_ms * 1e-3), "unit": "elements/s",
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, pg, device)
+    e2e = {"value": job_rate(n, world, e2e_ms), "unit": "elements/s",
            "h2d_bytes_per_step": wl.W * n_pad * G, "d2h_bytes_per_step": n_pad * 4,
            "ms_per_step": e2e_ms}
     del host_g, host_p
@@ -524,7 +534,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="bert-base")
-    ap.add_argument("--n", type=int, help="elements (flat workload only)")
+    ap.add_argument("--n", "--elements", dest="n", type=int,
+                    help="elements (flat and int8 workloads); use --elements under torchrun")
     ap.add_argument("--W", type=int, help="workers (flat workload only)")
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     ap.add_argument("--dense-m", action="store_true",

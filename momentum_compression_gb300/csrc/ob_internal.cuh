@@ -119,13 +119,27 @@ __device__ __forceinline__ uint32_t pack_word(uint32_t nibble, int lane) {
 }
 
 // Sequential sum of `cnt` tile totals (from 0, in order), done by one warp:
-// every lane returns the same value.
+// every lane returns the same value.  Each batch of 256 totals is loaded at
+// once (8 per lane) and handed to the adding chain by unrolled shuffles, so
+// only the additions are serialised.
 __device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, int lane) {
   float acc = 0.0f;
-  for (uint32_t t0 = 0; t0 < cnt; t0 += 32) {
-    float v = (t0 + lane < cnt) ? __ldcg(part + t0 + lane) : 0.0f;
-    uint32_t k = cnt - t0 < 32 ? cnt - t0 : 32;
-    for (uint32_t j = 0; j < k; ++j) acc = __fadd_rn(acc, __shfl_sync(kFull, v, j));
+  for (uint32_t t0 = 0; t0 < cnt; t0 += 256) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t t = t0 + 32u * j + lane;
+      v[j] = t < cnt ? __ldcg(part + t) : 0.0f;
+    }
+    const uint32_t rem = cnt - t0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int s = 0; s < 32; ++s) {
+        const float x = __shfl_sync(kFull, v[j], s);
+        if (32u * j + s < rem) acc = __fadd_rn(acc, x);
+      }
+    }
   }
   return acc;
 }

@@ -54,13 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase of `bar` with parity `parity` has completed, for at
-// most kWaitCycles; on timeout records `code` in *err and returns false.
+// most `limit` SM clocks; on timeout records `code` in *err (if it holds no
+// code yet) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
-                                          unsigned code) {
+                                          unsigned code, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       atomicCAS(err, 0u, code);
       return false;
     }
