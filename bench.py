@@ -582,6 +582,8 @@ def main():
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     ap.add_argument("--dense-m", action="store_true",
                     help="1-bit Adam: keep the momentum as a dense fp32 buffer")
+    ap.add_argument("--clip-value", type=float, default=0.0,
+                    help="clamp of the compensated values (the write-up's stability variant)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "ours" and args.workload == "int8":
@@ -592,6 +594,8 @@ def main():
                             chunk=args.chunk or (1 << 20))
     else:
         wl = synth.workload(args.workload)
+    if args.clip_value:
+        wl.hp["clip_value"] = args.clip_value
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -120,6 +120,9 @@ typedef struct ob_config {
   float r_thr, r_min, r_max;    /* LAMB ratio clip ([LAMB] 1) */
   float c_min, c_max;           /* LAMB coefficient clip ([LAMB] 3) */
   uint32_t flags;               /* OB_FLAG_* */
+  float clip_value;             /* > 0: workers' compensated values are
+                                   limited to [-clip_value, clip_value]
+                                   before compression ([BLOG] 4.1); 0 = off */
 } ob_config;
 
 typedef struct ob_layout {
@@ -187,6 +190,7 @@ ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s,
  * [LAMB] 2-3):
  *   m_w = b1*m + (1-b1)*g_w
  *   x   = sigma_l*m_w + rho_l*e_w    (ADAM: x = m_w + e_w)
+ *   x   = clamp(x, -clip_value, clip_value) if clip_value > 0 ([BLOG] 4.1)
  *   scale(chunk) = mean |x| over the chunk's real elements
  *   bit = x >= 0;  e_w' = x - scale*sign(x)   (stored deferred)
  * sigma_l = ls->s, rho_l = ls->c_prev2/ls->c_prev (1 with
@@ -260,6 +264,15 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err,
                                 const uint32_t* bits, float* scales,
                                 float* err_s, const uint32_t* sbits,
                                 float* sscales, ob_stream_t stream);
+
+/* The periodic error reset of [BLOG] 4.1 (every reset_interval steps the
+ * compensation term is set to zero): after this call the next compression
+ * sees worker and server errors of exactly 0.  The deferred form is kept
+ * (err := scale*sign, err_s := sscale*sign, so that err - scale*sign = 0),
+ * so bits and scales -- and a momentum held in sign form -- are untouched. */
+ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
+                          const float* scales, float* err_s, const uint32_t* sbits,
+                          const float* sscales, ob_stream_t stream);
 
 /* Reads and clears the device error word of the workspace (0 = none;
  * 1 = a consumer's wait for a copy ran out, 2 = the producer's wait for a

@@ -33,7 +33,7 @@ EXPORTS = (
     "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
     "ob_materialize_errors", "ob_device_error", "ob_quant_int8", "ob_compress_noalloc",
-    "ob_compress_signm",
+    "ob_compress_signm", "ob_reset_errors",
 )
 
 
@@ -50,7 +50,7 @@ class ob_config(ct.Structure):
                 ("b1", ct.c_float), ("b2", ct.c_float), ("eps", ct.c_float),
                 ("lr", ct.c_float), ("r_thr", ct.c_float), ("r_min", ct.c_float),
                 ("r_max", ct.c_float), ("c_min", ct.c_float), ("c_max", ct.c_float),
-                ("flags", ct.c_uint32)]
+                ("flags", ct.c_uint32), ("clip_value", ct.c_float)]
 
 
 class ob_layout(ct.Structure):
@@ -98,6 +98,7 @@ def lib():
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
         L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ob_reset_errors.argtypes = [vp] * 8
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -165,12 +166,12 @@ def _ls(ls):
 
 def ob_init(n, W, chunk, align=4096, grad_dtype=OB_GRAD_F32, layer_offsets=None,
             b1=0.9, b2=0.999, eps=1e-8, lr=1e-4, r_thr=0.1, r_min=0.5, r_max=4.0,
-            c_min=0.01, c_max=10.0, flags=0):
+            c_min=0.01, c_max=10.0, flags=0, clip_value=0.0):
     """Returns an opaque ctx handle (int).  layer_offsets: sequence of
     n_layers+1 ints, or None for one layer."""
     cfg = ob_config(n=n, W=W, chunk=chunk, align=align, grad_dtype=grad_dtype,
                     b1=b1, b2=b2, eps=eps, lr=lr, r_thr=r_thr, r_min=r_min, r_max=r_max,
-                    c_min=c_min, c_max=c_max, flags=flags)
+                    c_min=c_min, c_max=c_max, flags=flags, clip_value=clip_value)
     keep = None
     if layer_offsets is not None:
         keep = (ct.c_size_t * len(layer_offsets))(*[int(x) for x in layer_offsets])
@@ -273,6 +274,11 @@ def ob_materialize_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=
                                        _stream(stream)), ctx)
 
 
+def ob_reset_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=None):
+    _check(lib().ob_reset_errors(ctx, _ptr_array(err), _ptr(bits), _ptr(scales), _ptr(err_s),
+                                 _ptr(sbits), _ptr(sscales), _stream(stream)), ctx)
+
+
 def ob_device_error(ctx, stream=None):
     """Reads and clears the device error word (0 = none)."""
     v = ct.c_uint()
@@ -300,12 +306,17 @@ class OneBitOptimizer:
     sscales, the workspace, and the per-layer LAMB state."""
 
     def __init__(self, n, W, chunk, align=4096, grad_dtype="f32", layer_offsets=None,
-                 lamb=False, device="cuda", sign_momentum=False, **hp):
+                 lamb=False, device="cuda", sign_momentum=False, reset_interval=0, **hp):
         """sign_momentum (1-bit Adam only): after the first compressed step
         the momentum is held as (sbits, sscales) -- exactly sscale*sign --
-        and the dense m buffer is only refreshed by materialize_m()."""
+        and the dense m buffer is only refreshed by materialize_m().
+        reset_interval > 0: before every reset_interval-th compressed step
+        the worker and server errors are reset to 0 (ob_reset_errors).
+        hp may hold clip_value (> 0: clamp of the compensated values)."""
         import torch
         self.lamb = lamb
+        self.reset_interval = reset_interval
+        self.cstep = 0
         self.sign_momentum = sign_momentum and not lamb
         self.m_in_signs = False
         self.grad_dtype = grad_dtype
@@ -358,8 +369,16 @@ class OneBitOptimizer:
                              self.sscales, self.m, self.v, self.v_fresh,
                              self.ls if self.lamb else None, max(self.warmup_steps, 1), stream)
         self.m_in_signs = False
+        self.cstep = 0
+
+    def reset_errors(self, stream=None):
+        ob_reset_errors(self.ctx, self.err, self.bits, self.scales, self.err_s, self.sbits,
+                        self.sscales, stream)
 
     def compressed_step(self, grads, stream=None):
+        if self.reset_interval and self.cstep and self.cstep % self.reset_interval == 0:
+            self.reset_errors(stream)
+        self.cstep += 1
         m = None if self.m_in_signs else self.m
         ob_step(self.ctx, grads, m, self.err, self.bits, self.scales, self.err_s,
                 self.sbits, self.sscales, self.v, self.v_fresh, self.p,

@@ -7,7 +7,8 @@
 //   e_w   = x_prev - scale_prev*sign(x_prev)   (the deferred error of the
 //           previous step, rebuilt from the stored x, bits and scale)
 //   m_w   = b1*m + (1-b1)*g_w
-//   x     = sigma_l*m_w + rho_l*e_w            (1-bit Adam: m_w + e_w)
+//   x     = sigma_l*m_w + rho_l*e_w            (1-bit Adam: m_w + e_w),
+//           limited to [-clip, clip] when clip > 0 ("1bit Adam" write-up 4.1)
 //   bit   = x >= 0; x is stored in place of e_w
 //   scale(chunk) = mean |x| over the chunk: this kernel writes one total
 //   per (worker, tile); k_finalize_scales adds them in tile order
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   }
 
   // ------------------------------------------------------------ consumers
-  const float b1 = A.b1, ob1 = A.ob1;
+  const float b1 = A.b1, ob1 = A.ob1, clip = A.clip;
   const int p = tid;
   // MSIGN: the momentum's sign words and chunk scale of the next tile are
   // loaded one tile ahead, so their latency hides behind the current tile
@@ -251,6 +252,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
                 x = __fadd_rn(__fmul_rn(s_l, mw), __fmul_rn(r_l, et));
               } else {
                 x = __fadd_rn(mw, et);
+              }
+              if (clip > 0.0f) {  // a NaN stays NaN
+                x = x > clip ? clip : x;
+                x = x < -clip ? -clip : x;
               }
               acc = __fadd_rn(acc, fabsf(x));
               if (x >= 0.0f) nib |= 1u << c;

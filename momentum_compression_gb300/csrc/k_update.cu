@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const UpdateArgs A) {
   }
 }
 
+// RESET = false: e := e - scale*sign (the deferred error made explicit).
+// RESET = true:  e := scale*sign, so that the next decode gives exactly 0
+//                (the periodic reset of the "1bit Adam" write-up, 4.1).
+template <bool RESET>
 __global__ void __launch_bounds__(kThreads) k_materialize(const MaterializeArgs A) {
   const Geo& G = A.geo;
   const int p = threadIdx.x;
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) k_materialize(const MaterializeArgs 
         for (int c = 0; c < 4; ++c) {
           if (k0 + c >= G.n) continue;
           const float so = ((wd >> c) & 1u) ? sc : -sc;
-          f4at(ev, c) = __fsub_rn(f4at(ev, c), so);
+          f4at(ev, c) = RESET ? so : __fsub_rn(f4at(ev, c), so);
         }
         *reinterpret_cast<float4*>(e + k0) = ev;
       }
@@ -344,7 +348,12 @@ cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
 }
 
 cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s) {
-  k_materialize<<<grid_for(k_materialize, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  k_materialize<false><<<grid_for(k_materialize<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_errors(const MaterializeArgs& a, int sms, cudaStream_t s) {
+  k_materialize<true><<<grid_for(k_materialize<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

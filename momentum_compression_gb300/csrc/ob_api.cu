@@ -167,6 +167,7 @@ ob_status ob_init(const ob_config* cfg, ob_ctx** out) {
   if (!(c.eps >= 0.0f) || !(c.lr == c.lr))
     return fail(nullptr, OB_ERR_INVALID, "eps must be >= 0 and lr a number");
   if (c.n_layers < 0) return fail(nullptr, OB_ERR_INVALID, "n_layers < 0");
+  if (!(c.clip_value >= 0.0f)) return fail(nullptr, OB_ERR_INVALID, "clip_value must be >= 0");
 
   ob_ctx* ctx = new ob_ctx();
   ctx->cfg = c;
@@ -421,6 +422,7 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, flo
   a.ratio_ef = (ctx->cfg.flags & OB_FLAG_NO_RATIO_EF) ? 0 : 1;
   a.b1 = ctx->cfg.b1;
   a.ob1 = 1.0f - ctx->cfg.b1;
+  a.clip = ctx->cfg.clip_value;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launched(ctx,
                      ob::launch_compress(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ls != nullptr,
@@ -574,6 +576,7 @@ ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_
   a.ratio_ef = 1;
   a.b1 = ctx->cfg.b1;
   a.ob1 = 1.0f - ctx->cfg.b1;
+  a.clip = ctx->cfg.clip_value;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launched(ctx,
                      ob::launch_compress_signm(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ctx->sms, s),
@@ -629,6 +632,31 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* 
   cudaError_t e = cudaMemsetAsync(scales, 0, (size_t)G.W * G.nc * sizeof(float), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(sscales, 0, (size_t)G.nc * sizeof(float), s);
   return launched(ctx, e, "materialize: clearing the scales");
+}
+
+ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
+                          const float* scales, float* err_s, const uint32_t* sbits,
+                          const float* sscales, ob_stream_t stream) {
+  ob_status st = ready(ctx);
+  if (st) return st;
+  if ((st = check_errs(ctx, err))) return st;
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
+  OB_CHECK_PTR(ctx, scales, 4, "scales");
+  OB_CHECK_PTR(ctx, err_s, 16, "err_s");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
+  OB_CHECK_PTR(ctx, sscales, 4, "sscales");
+  const Geo& G = ctx->geo;
+  ob::MaterializeArgs a{};
+  a.geo = G;
+  for (uint32_t w = 0; w < G.W; ++w) a.e[w] = err[w];
+  a.bits = bits;
+  a.scales = scales;
+  a.e_s = err_s;
+  a.sbits = sbits;
+  a.sscales = sscales;
+  return launched(ctx,
+                  ob::launch_reset_errors(a, ctx->sms, reinterpret_cast<cudaStream_t>(stream)),
+                  "reset_errors");
 }
 
 ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream) {

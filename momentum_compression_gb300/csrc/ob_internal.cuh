@@ -210,6 +210,7 @@ struct CompressArgs {
   const float* c_prev2;  // LAMB c_{t-2}
   int ratio_ef;
   float b1, ob1;
+  float clip;  // > 0: compensated values limited to [-clip, clip]
 };
 
 struct ServerArgs {
@@ -299,6 +300,7 @@ cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
                               cudaStream_t s);
 cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_reset_errors(const MaterializeArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_warmup_adam(const WarmupArgs& a, bool bf16, int sms,
                                cudaStream_t s);
 cudaError_t launch_warmup_lamb(const WarmupArgs& a, bool bf16, int sms,

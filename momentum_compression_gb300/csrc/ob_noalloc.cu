@@ -103,6 +103,7 @@ extern "C" ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads,
   a.ratio_ef = 1;
   a.b1 = cfg.b1;
   a.ob1 = 1.0f - cfg.b1;
+  a.clip = cfg.clip_value;
   e = ob::launch_compress(a, cfg.grad_dtype == OB_GRAD_BF16, false, sms, s);
   if (e == cudaSuccess) e = ob::launch_finalize_scales(G, part, G.W, scales, sms, s);
   if (e != cudaSuccess) return ob::ctx_fail(ctx, OB_ERR_CUDA, cudaGetErrorString(e));

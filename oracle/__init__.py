@@ -39,6 +39,8 @@ def lib():
         lay = ct.POINTER(_Layout)
         L.orc_compress_worker.argtypes = [lay, vp, u64, vp, vp, f32, f32p, f32p,
                                           f32p, u32p, f32p, vp]
+        L.orc_compress_worker_clip.argtypes = [lay, vp, u64, vp, vp, f32, f32, f32p, f32p,
+                                               f32p, u32p, f32p, vp]
         L.orc_server_reduce.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p,
                                         u32p, f32p, vp]
         L.orc_decompress.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p]
@@ -111,8 +113,9 @@ def cr_sum(a):
     return np.float32(lib().orc_cr_sum(a, a.size))
 
 
-def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None):
-    """One worker's compression.  e (n_pad,) is updated in place.
+def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None, clip=0.0):
+    """One worker's compression.  e (n_pad,) is updated in place.  clip > 0
+    limits the compensated value to [-clip, clip].
     Returns (bits[words] u32, scales[nc] f32, x[n_pad] f32)."""
     layers = layers or Layers()
     bits = np.zeros(lay.words, np.uint32)
@@ -120,9 +123,9 @@ def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None):
     x = np.zeros(lay.n_pad, np.float32)
     sg = None if sigma is None else _f32(sigma)
     rh = None if rho is None else _f32(rho)
-    lib().orc_compress_worker(lay._s, _ptr(layers.off), layers.nl, _ptr(sg),
-                              _ptr(rh), b1, _f32(g), _f32(m), e, bits, scales,
-                              _ptr(x))
+    lib().orc_compress_worker_clip(lay._s, _ptr(layers.off), layers.nl, _ptr(sg),
+                                   _ptr(rh), b1, clip, _f32(g), _f32(m), e, bits,
+                                   scales, _ptr(x))
     return bits, scales, x
 
 
@@ -262,13 +265,14 @@ def rho_of(ls, ratio_ef=True):
 
 
 def compressed_step(st, grads, hp, lamb=False, ratio_ef=True, frozen=False):
-    """One compressed step (1-bit Adam, or 1-bit LAMB if lamb=True)."""
+    """One compressed step (1-bit Adam, or 1-bit LAMB if lamb=True).
+    hp["clip"] > 0 limits the workers' compensated values."""
     lay, layers = st.lay, st.layers
     sigma = st.ls["s"] if lamb else None
     rho = rho_of(st.ls, ratio_ef) if lamb else None
     for w in range(lay.W):
         b, s, _ = compress_worker(lay, grads[w], st.m, st.e[w], hp["b1"],
-                                  layers, sigma, rho)
+                                  layers, sigma, rho, hp.get("clip", 0.0))
         st.bits[w], st.scales[w] = b, s
     st.sbits, st.sscales, _ = server_reduce(lay, st.bits, st.scales, st.e_s,
                                             layers, rho)
@@ -281,6 +285,14 @@ def compressed_step(st, grads, hp, lamb=False, ratio_ef=True, frozen=False):
     st.c = lamb_ratio(R, hp, st.ls, frozen)
     lamb_pass_b(lay, layers, st.c, st.m, st.v, hp["eps"], hp["lr"], st.p)
     st.R = R
+
+
+def reset_errors(st):
+    """The periodic error reset of the "1bit Adam" write-up (4.1: every 2000
+    steps the compensation term is set to zero): worker and server errors."""
+    for e in st.e:
+        e[:] = 0
+    st.e_s[:] = 0
 
 
 def begin_compression(st, warmup_steps, lamb=False):

@@ -188,10 +188,26 @@ static float sgn_of_bit(const uint32_t* words, uint64_t k) {
 //   bit = x >= 0;  e_w' = x - scale*sign(x)
 // `sigma`/`rho` are per-layer arrays or NULL (= 1).  e is updated in place.
 // `x_out`, if not NULL, receives x (used by tests).
+// clip > 0: the compensated value is limited to [-clip, clip] before it is
+// compressed ([BLOG] §4.1 "梯度裁剪": compensated_grad.clamp_(-clip_value,
+// clip_value), §6 clip_value 2.0); a NaN stays NaN.
+void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
+                              uint64_t nl, const float* sigma, const float* rho,
+                              float b1, float clip, const float* g, const float* m,
+                              float* e, uint32_t* bits, float* scales, float* x_out);
+
 void orc_compress_worker(const orc_layout* L, const uint64_t* layer_off,
                          uint64_t nl, const float* sigma, const float* rho,
                          float b1, const float* g, const float* m, float* e,
                          uint32_t* bits, float* scales, float* x_out) {
+  orc_compress_worker_clip(L, layer_off, nl, sigma, rho, b1, 0.0f, g, m, e, bits,
+                           scales, x_out);
+}
+
+void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
+                              uint64_t nl, const float* sigma, const float* rho,
+                              float b1, float clip, const float* g, const float* m,
+                              float* e, uint32_t* bits, float* scales, float* x_out) {
   const float ob1 = 1.0f - b1;
   std::vector<float> x(L->n_pad, 0.0f);
   for (uint64_t k = 0; k < L->n; ++k) {
@@ -199,7 +215,12 @@ void orc_compress_worker(const orc_layout* L, const uint64_t* layer_off,
     float s = sigma ? sigma[l] : 1.0f;
     float r = rho ? rho[l] : 1.0f;
     float mw = (b1 * m[k]) + (ob1 * g[k]);
-    x[k] = (s * mw) + (r * e[k]);
+    float xv = (s * mw) + (r * e[k]);
+    if (clip > 0.0f) {
+      if (xv > clip) xv = clip;
+      if (xv < -clip) xv = -clip;
+    }
+    x[k] = xv;
   }
   for (uint64_t wd = 0; wd < L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0); ++wd)
     bits[wd] = 0u;

@@ -145,12 +145,15 @@ def test_compress_server_update_single_kernels(case):
     c.close()
 
 
-def _run_adam(wl, warm, steps, check_every=False, sign_momentum=False):
+def _run_adam(wl, warm, steps, check_every=False, sign_momentum=False, reset_interval=0,
+              clip=0.0):
     """Runs `warm` warmup and `steps` compressed steps of workload wl on the
     GPU and in the oracle from the same seeded inputs."""
     n, W = wl.n, wl.W
     opt = ob.OneBitOptimizer(n, W, wl.chunk, wl.align, wl.grad_dtype,
-                             sign_momentum=sign_momentum, **wl.hp)
+                             sign_momentum=sign_momentum, reset_interval=reset_interval,
+                             clip_value=clip, **wl.hp)
+    hp_o = dict(wl.hp, clip=clip)
     lay = O.Layout(n, W, wl.align, wl.chunk)
     st = O.State(lay)
     p0 = np.zeros(lay.n_pad, f32)
@@ -186,7 +189,10 @@ def _run_adam(wl, warm, steps, check_every=False, sign_momentum=False):
     for t in range(warm, warm + steps):
         gh, gd = grads(t)
         opt.compressed_step(gd)
-        O.compressed_step(st, gh, wl.hp)
+        c = t - warm
+        if reset_interval and c and c % reset_interval == 0:
+            O.reset_errors(st)
+        O.compressed_step(st, gh, hp_o)
         if check_every:
             torch.cuda.synchronize()
             assert_bits_equal(host(opt.sbits)[: lay.words], st.sbits, f"sbits at step {t}")
@@ -235,6 +241,18 @@ def test_sign_momentum_matches_oracle(workload, dt):
         wl.chunk = 1 << 13
     opt, st, lay = _run_adam(wl, 2, 6, check_every=True, sign_momentum=True)
     assert opt.m_in_signs
+    _compare_state(opt, st, lay)
+    opt.close()
+
+
+@pytest.mark.parametrize("sign_momentum", [False, True])
+def test_stability_variants(sign_momentum):
+    """The "1bit Adam" write-up's stability variants (4.1): the compensated
+    value clamped to +-clip_value and the errors reset every 3 steps, for 8
+    steps -- against the oracle, bit for bit."""
+    wl = synth.workload("flat", n=200_003, W=3, chunk=1 << 14)
+    opt, st, lay = _run_adam(wl, 2, 8, check_every=True, sign_momentum=sign_momentum,
+                             reset_interval=3, clip=2.5e-4)
     _compare_state(opt, st, lay)
     opt.close()
 

@@ -661,3 +661,56 @@ def test_int8_whole_tensor_equals_page_function():
     qq = torch.clamp(gi, -127, 127)
     assert np.array_equal(qq.numpy().astype(np.int8), q)
     assert np.array_equal((qq * scale).numpy(), d)
+
+
+# ---------------------------------------------------------------------------
+# Stability variants of the "1bit Adam" write-up, 4.1
+# ---------------------------------------------------------------------------
+
+def test_clip_of_the_compensated_value_hand():
+    """b1 = 0 and e = 0 make x = g; clip 2 turns [3, -5, 1, 0.5] into
+    [2, -2, 1, 0.5]: scale (2+2+1+0.5)/4 = 1.375, e' = x - 1.375*sign(x)."""
+    lay = O.Layout(4, 1, 1, 4)
+    g = np.array([3.0, -5.0, 1.0, 0.5], f32)
+    e = np.zeros(4, f32)
+    b, s, x = O.compress_worker(lay, g, np.zeros(4, f32), e, 0.0, clip=2.0)
+    _eq(x, [2.0, -2.0, 1.0, 0.5])
+    _eq(s, [1.375])
+    _eq(e, [0.625, -0.625, -0.375, -0.875])
+    assert int(b[0]) == 0b1101
+    # a NaN stays NaN under the clamp
+    g[1] = np.nan
+    b, s, x = O.compress_worker(lay, g, np.zeros(4, f32), np.zeros(4, f32), 0.0, clip=2.0)
+    assert np.isnan(x[1]) and not (int(b[0]) >> 1) & 1
+
+
+def test_clip_zero_is_off():
+    lay, g, m, e = _rand_case()
+    e1, e2 = e[0].copy(), e[0].copy()
+    b1_, s1, x1 = O.compress_worker(lay, g[0], m, e1, 0.9)
+    b2_, s2, x2 = O.compress_worker(lay, g[0], m, e2, 0.9, clip=0.0)
+    _eq(x1, x2)
+    _eq(e1, e2)
+
+
+def test_reset_then_step_equals_fresh_start():
+    """After the periodic reset the next step sees e = 0, e_s = 0: it equals
+    a step from a state whose errors were never set."""
+    lay = O.Layout(3000, 2, 32, 512)
+    rng = np.random.default_rng(31)
+    hp = dict(b1=0.9, b2=0.999, eps=1e-8, lr=1e-4)
+    a = O.State(lay)
+    a.v[:3000] = np.abs(rng.standard_normal(3000)).astype(f32) * f32(1e-6) + f32(1e-8)
+    g = [np.zeros(lay.n_pad, f32) for _ in range(2)]
+    for w in range(2):
+        g[w][:3000] = rng.standard_normal(3000).astype(f32) * f32(1e-3)
+    O.compressed_step(a, g, hp)
+    b = a.copy()
+    O.reset_errors(a)
+    for e in b.e:
+        e[:] = 0
+    b.e_s[:] = 0
+    O.compressed_step(a, g, hp)
+    O.compressed_step(b, g, hp)
+    _eq(a.p, b.p)
+    assert all(np.array_equal(x, y) for x, y in zip(a.e, b.e))
