@@ -298,7 +298,9 @@ def run_reference(args, wl):
 def run_int8(args):
     """The block-256 INT8 stochastic-rounding quantizer on the sweep's
     largest size, n = 2^30 fp32 values (4 GB in, 1 GB of codes and 16 MB of
-    scales out per call; larger than L2)."""
+    scales out per call; larger than L2).  --ef: with error feedback (the
+    residual is read and written, 13 B per element) and the per-block
+    error monitor."""
     import torch
 
     import momentum_compression_gb300 as ob
@@ -308,8 +310,17 @@ def run_int8(args):
     g = torch.randn(n, device="cuda") * 1e-3
     q = torch.empty(n, dtype=torch.int8, device="cuda")
     sc = torch.empty((n + 255) // 256, device="cuda")
+    e = torch.zeros(n, device="cuda") if args.ef else None
+    e2 = torch.empty((n + 255) // 256, device="cuda") if args.ef else None
+
+    def call(t):
+        if args.ef:
+            ob.ob_quant_int8_ef(g, e, q, sc, 1234, t, None, e2)
+        else:
+            ob.ob_quant_int8(g, q, sc, 1234, t)
+
     for t in range(args.warmup):
-        ob.ob_quant_int8(g, q, sc, 1234, t)
+        call(t)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -320,20 +331,21 @@ def run_int8(args):
         torch.cuda.synchronize()
         a.record(stream)
         for t in range(args.steps):
-            ob.ob_quant_int8(g, q, sc, 1234, 1000 + t)
+            call(1000 + t)
         b.record(stream)
         torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    bpe = 4 + 1 + 4 / 256
+    bpe = (4 + 4 + 4 + 1 + 8 / 256) if args.ef else (4 + 1 + 4 / 256)
     peak, kind = measured_peak()
     gbs = bpe * n / (ms * 1e-3) / 1e9
     if rank == 0:
+        what = "with error feedback and error monitor" if args.ef else ""
         print(json.dumps({
             "metric": "INT8 block-256 stochastic-rounding quantizer elements/s", "value": n / (ms * 1e-3),
             "unit": "elements/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32 -> int8", "data": "synthetic",
-            "config": {"workload": f"int8 quantizer, n = {n}, block 256, Philox4x32-10",
+            "config": {"workload": f"int8 quantizer {what}, n = {n}, block 256, Philox4x32-10",
                        "l2": "inputs larger than L2; no flush"},
             "roofline": {"bound": "hbm", "kernel": "quant_int8", "achieved": gbs, "peak": peak,
                          "peak_kind": kind, "unit": "GB/s", "frac": gbs / peak,
@@ -582,6 +594,7 @@ def main():
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     ap.add_argument("--dense-m", action="store_true",
                     help="1-bit Adam: keep the momentum as a dense fp32 buffer")
+    ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")
     ap.add_argument("--clip-value", type=float, default=0.0,
                     help="clamp of the compensated values (the write-up's stability variant)")
     args = ap.parse_args()

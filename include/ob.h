@@ -314,6 +314,18 @@ ob_status ob_quant_int8(const float* g, size_t n, int8_t* q,
                         float* block_scales, uint64_t seed, uint64_t step,
                         float* deq, ob_stream_t stream);
 
+/* INT8 with error feedback ([TUT] "1-bit 梯度量化" error feedback and
+ * "精度恢复技巧": the residual is kept and added back before the next
+ * quantisation): x = g + e; per block of 256 the quantizer of ob_quant_int8
+ * is applied to x; e := x - q*scale (in place).  block_err2 (optional):
+ * per block, the sum of the squared residuals -- the quantisation-error
+ * monitor of [TUT] "监控与诊断" -- summed in a fixed order (lane j of 32
+ * adds its elements 4j..4j+3 then 128+4j..128+4j+3, then a warp
+ * butterfly).  e 16-byte aligned, n_pad-free: n elements. */
+ob_status ob_quant_int8_ef(const float* g, float* e, size_t n, int8_t* q, float* block_scales,
+                           uint64_t seed, uint64_t step, float* deq, float* block_err2,
+                           ob_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

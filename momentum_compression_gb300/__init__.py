@@ -33,7 +33,7 @@ EXPORTS = (
     "ob_set_workspace", "ob_warmup_step", "ob_begin_compression", "ob_compress",
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
     "ob_materialize_errors", "ob_device_error", "ob_quant_int8", "ob_compress_noalloc",
-    "ob_compress_signm", "ob_reset_errors",
+    "ob_compress_signm", "ob_reset_errors", "ob_quant_int8_ef",
 )
 
 
@@ -99,6 +99,7 @@ def lib():
         L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
+        L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -291,6 +292,14 @@ def ob_quant_int8(g, q, block_scales, seed, step, deq=None, n=None, stream=None)
         n = g.numel()
     _check(lib().ob_quant_int8(_ptr(g), n, _ptr(q), _ptr(block_scales), seed, step, _ptr(deq),
                                _stream(stream)))
+
+
+def ob_quant_int8_ef(g, e, q, block_scales, seed, step, deq=None, block_err2=None, n=None,
+                     stream=None):
+    if n is None:
+        n = g.numel()
+    _check(lib().ob_quant_int8_ef(_ptr(g), _ptr(e), n, _ptr(q), _ptr(block_scales), seed, step,
+                                  _ptr(deq), _ptr(block_err2), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -49,9 +49,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
   return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
 }
 
-// Quantizes the 4 elements of group `grp` (elements 4*grp .. 4*grp+3).
-template <bool DEQ>
-__device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64_t grp,
+// Quantizes the 4 values x of group `grp` (elements 4*grp .. 4*grp+3);
+// dq receives q*scale.
+__device__ __forceinline__ uint32_t quant4(const float4& xv, float scale, uint64_t grp,
                                            uint64_t step, const PhiloxKeys& K, int nvalid,
                                            float4& dq) {
   const uint4 ctr = make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
@@ -62,8 +62,7 @@ __device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64
   for (int c = 0; c < 4; ++c) {
     float qf = 0.0f;
     if (c < nvalid && scale != 0.0f) {
-      const float g = f4get(gv, c);
-      const float x = __fdiv_rn(g, scale);
+      const float x = __fdiv_rn(f4get(xv, c), scale);
       const float f = floorf(x);
       const float fr = __fsub_rn(x, f);
       const float u = __fmul_rn((float)(word_of(rnd, c) >> 8), 5.9604644775390625e-08f);
@@ -72,7 +71,7 @@ __device__ __forceinline__ uint32_t quant4(const float4& gv, float scale, uint64
       qf = qf < -127.0f ? -127.0f : qf;
       if (qf != qf) qf = 0.0f;
     }
-    if constexpr (DEQ) f4at(dq, c) = __fmul_rn(qf, scale);
+    f4at(dq, c) = __fmul_rn(qf, scale);
     packed |= ((uint32_t)(int32_t)qf & 0xffu) << (8 * c);
   }
   return packed;
@@ -95,59 +94,115 @@ __device__ __forceinline__ void load_block(const float* __restrict__ g, uint64_t
   }
 }
 
-template <bool DEQ>
+__device__ __forceinline__ void store4(float* __restrict__ dst, uint64_t k, int nv,
+                                       const float4& v) {
+  if (nv == 4) {
+    __stcs(reinterpret_cast<float4*>(dst + k), v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 3; ++c)
+      if (c < nv) dst[k + c] = f4get(v, c);
+  }
+}
+
+// DEQ: write q*scale.  EF: error feedback -- x = g + e is quantised and
+// e := x - q*scale.  ERR2: per-block sum of the squared residual (lane j
+// adds its 8 squares in element order, then a warp butterfly).
+template <bool DEQ, bool EF, bool ERR2>
 __global__ void __launch_bounds__(kThreads)
-    k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
-                 float* __restrict__ scales, uint64_t seed, uint64_t step,
-                 float* __restrict__ deq) {
+    k_quant_int8(const float* __restrict__ g, float* __restrict__ e, uint64_t n,
+                 int8_t* __restrict__ q, float* __restrict__ scales, uint64_t seed,
+                 uint64_t step, float* __restrict__ deq, float* __restrict__ err2) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
   const PhiloxKeys K = philox_keys((uint32_t)seed, (uint32_t)(seed >> 32));
   uint64_t b = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-  float4 gv[2];
+  float4 gv[2], ev[2];
   int nv[2];
-  if (b < nblk) load_block(g, n, b, lane, gv, nv);
+  if (b < nblk) {
+    load_block(g, n, b, lane, gv, nv);
+    if constexpr (EF) load_block(e, n, b, lane, ev, nv);
+  }
   for (; b < nblk; b += warps) {
     // the next block's loads are in flight while this block is quantised
-    float4 gn[2];
+    float4 gn[2], en[2];
     int nn[2] = {0, 0};
-    if (b + warps < nblk) load_block(g, n, b + warps, lane, gn, nn);
+    if (b + warps < nblk) {
+      load_block(g, n, b + warps, lane, gn, nn);
+      if constexpr (EF) load_block(e, n, b + warps, lane, en, nn);
+    }
+    float4 xv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if constexpr (EF) {
+        xv[h] = make_float4(__fadd_rn(gv[h].x, ev[h].x), __fadd_rn(gv[h].y, ev[h].y),
+                            __fadd_rn(gv[h].z, ev[h].z), __fadd_rn(gv[h].w, ev[h].w));
+      } else {
+        xv[h] = gv[h];
+      }
+    }
     // fmaxf returns the other operand when one is NaN: a NaN never wins
     float mx = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        if (c < nv[h]) mx = fmaxf(mx, fabsf(f4get(gv[h], c)));
+        if (c < nv[h]) mx = fmaxf(mx, fabsf(f4get(xv[h], c)));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, 127.0f);
     if (lane == 0) scales[b] = scale;
+    float acc2 = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      if (nv[h] == 0) continue;
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
-      float4 dq;
-      const uint32_t packed = quant4<DEQ>(gv[h], scale, k >> 2, step, K, nv[h], dq);
-      if (nv[h] == 4) {
-        *reinterpret_cast<uint32_t*>(q + k) = packed;
-        if constexpr (DEQ) __stcs(reinterpret_cast<float4*>(deq + k), dq);
-      } else {
+      float4 dq = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (nv[h] > 0) {
+        const uint32_t packed = quant4(xv[h], scale, k >> 2, step, K, nv[h], dq);
+        if (nv[h] == 4) {
+          *reinterpret_cast<uint32_t*>(q + k) = packed;
+        } else {
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          if (c < nv[h]) {
-            q[k + c] = (int8_t)((packed >> (8 * c)) & 0xffu);
-            if constexpr (DEQ) deq[k + c] = f4get(dq, c);
-          }
+          for (int c = 0; c < 3; ++c)
+            if (c < nv[h]) q[k + c] = (int8_t)((packed >> (8 * c)) & 0xffu);
         }
+        if constexpr (DEQ) store4(deq, k, nv[h], dq);
       }
+      if constexpr (EF) {
+        float4 r;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          f4at(r, c) = __fsub_rn(f4get(xv[h], c), f4get(dq, c));
+          if (ERR2 && c < nv[h]) acc2 = __fadd_rn(acc2, __fmul_rn(f4get(r, c), f4get(r, c)));
+        }
+        if (nv[h] > 0) store4(e, k, nv[h], r);
+      }
+    }
+    if constexpr (ERR2) {
+      acc2 = warp_butterfly_sum(acc2);
+      if (lane == 0) err2[b] = acc2;
     }
     gv[0] = gn[0];
     gv[1] = gn[1];
+    if constexpr (EF) {
+      ev[0] = en[0];
+      ev[1] = en[1];
+    }
     nv[0] = nn[0];
     nv[1] = nn[1];
   }
+}
+
+template <bool DEQ, bool EF, bool ERR2>
+cudaError_t run_int8(const float* g, float* e, uint64_t n, int8_t* q, float* scales,
+                     uint64_t seed, uint64_t step, float* deq, float* err2, int sms,
+                     cudaStream_t s) {
+  const uint64_t nblk = (n + 255) / 256;
+  const uint64_t ctas = (nblk + kThreads / 32 - 1) / (kThreads / 32);
+  k_quant_int8<DEQ, EF, ERR2><<<grid_for(k_quant_int8<DEQ, EF, ERR2>, sms, ctas), kThreads, 0,
+                                s>>>(g, e, n, q, scales, seed, step, deq, err2);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -155,15 +210,21 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_quant_int8(const float* g, uint64_t n, int8_t* q, float* scales,
                               uint64_t seed, uint64_t step, float* deq, int sms,
                               cudaStream_t s) {
-  const uint64_t nblk = (n + 255) / 256;
-  const uint64_t ctas = (nblk + kThreads / 32 - 1) / (kThreads / 32);
-  if (deq)
-    k_quant_int8<true><<<grid_for(k_quant_int8<true>, sms, ctas), kThreads, 0, s>>>(
-        g, n, q, scales, seed, step, deq);
-  else
-    k_quant_int8<false><<<grid_for(k_quant_int8<false>, sms, ctas), kThreads, 0, s>>>(
-        g, n, q, scales, seed, step, deq);
-  return cudaGetLastError();
+  if (deq) return run_int8<true, false, false>(g, nullptr, n, q, scales, seed, step, deq,
+                                               nullptr, sms, s);
+  return run_int8<false, false, false>(g, nullptr, n, q, scales, seed, step, nullptr, nullptr,
+                                       sms, s);
+}
+
+cudaError_t launch_quant_int8_ef(const float* g, float* e, uint64_t n, int8_t* q, float* scales,
+                                 uint64_t seed, uint64_t step, float* deq, float* err2, int sms,
+                                 cudaStream_t s) {
+  if (deq) {
+    return err2 ? run_int8<true, true, true>(g, e, n, q, scales, seed, step, deq, err2, sms, s)
+                : run_int8<true, true, false>(g, e, n, q, scales, seed, step, deq, err2, sms, s);
+  }
+  return err2 ? run_int8<false, true, true>(g, e, n, q, scales, seed, step, deq, err2, sms, s)
+              : run_int8<false, true, false>(g, e, n, q, scales, seed, step, deq, err2, sms, s);
 }
 
 }  // namespace ob

@@ -691,4 +691,26 @@ ob_status ob_quant_int8(const float* g, size_t n, int8_t* q, float* block_scales
   return OB_OK;
 }
 
+ob_status ob_quant_int8_ef(const float* g, float* e, size_t n, int8_t* q, float* block_scales,
+                           uint64_t seed, uint64_t step, float* deq, float* block_err2,
+                           ob_stream_t stream) {
+  if (n < 1 || n >= (1ull << 34))
+    return fail(nullptr, OB_ERR_INVALID, "n = %zu must be in [1, 2^34)", n);
+  OB_CHECK_PTR(nullptr, g, 16, "g");
+  OB_CHECK_PTR(nullptr, e, 16, "e");
+  OB_CHECK_PTR(nullptr, q, 4, "q");
+  OB_CHECK_PTR(nullptr, block_scales, 4, "block_scales");
+  if (deq && !aligned(deq, 16)) return fail(nullptr, OB_ERR_ALIGN, "deq is not 16-byte aligned");
+  if (block_err2 && !aligned(block_err2, 4))
+    return fail(nullptr, OB_ERR_ALIGN, "block_err2 is not 4-byte aligned");
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return cuda_fail(nullptr, err, "device query");
+  err = ob::launch_quant_int8_ef(g, e, n, q, block_scales, seed, step, deq, block_err2, sms,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(nullptr, err, "quant_int8_ef");
+  return OB_OK;
+}
+
 }  // extern "C"

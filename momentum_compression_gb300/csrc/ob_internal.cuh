@@ -309,5 +309,8 @@ cudaError_t launch_lamb_begin(const WarmupArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_quant_int8(const float* g, uint64_t n, int8_t* q, float* scales,
                               uint64_t seed, uint64_t step, float* deq, int sms,
                               cudaStream_t s);
+cudaError_t launch_quant_int8_ef(const float* g, float* e, uint64_t n, int8_t* q, float* scales,
+                                 uint64_t seed, uint64_t step, float* deq, float* err2, int sms,
+                                 cudaStream_t s);
 
 }  // namespace ob

@@ -63,6 +63,7 @@ def lib():
         L.orc_quant_int8.argtypes = [f32p, u64, u64, u64, u64, i8p, f32p,
                                      vp]
         L.orc_quant_int8_at.argtypes = [f32p, u64, u64, u64, u64, u64, i8p, f32p, vp]
+        L.orc_quant_int8_ef_at.argtypes = [f32p, f32p, u64, u64, u64, u64, i8p, f32p, vp, vp]
         _lib = L
     return _lib
 
@@ -226,6 +227,25 @@ def quant_int8(g, block=256, seed=1234, step=0, deq=False, k0=0):
     d = np.zeros(g.size, np.float32) if deq else None
     lib().orc_quant_int8_at(g, g.size, k0, block, seed, step, q, sc, _ptr(d))
     return (q, sc, d) if deq else (q, sc)
+
+
+def quant_int8_ef(g, e, seed=1234, step=0, deq=False, err2=False, k0=0):
+    """INT8 (block 256) with error feedback; e is updated in place.
+    Returns (q, scales[, deq][, err2])."""
+    g = _f32(g)
+    assert e.dtype == np.float32 and e.flags.c_contiguous and k0 % 256 == 0
+    nb = (g.size + 255) // 256
+    q = np.zeros(g.size, np.int8)
+    sc = np.zeros(nb, np.float32)
+    d = np.zeros(g.size, np.float32) if deq else None
+    e2 = np.zeros(nb, np.float32) if err2 else None
+    lib().orc_quant_int8_ef_at(g, e, g.size, k0, seed, step, q, sc, _ptr(d), _ptr(e2))
+    out = [q, sc]
+    if deq:
+        out.append(d)
+    if err2:
+        out.append(e2)
+    return tuple(out)
 
 
 # ---------------------------------------------------------------------------

@@ -646,4 +646,68 @@ void orc_quant_int8_at(const float* g, uint64_t n, uint64_t k0, uint64_t block,
   }
 }
 
+// INT8 with error feedback ([TUT] "1-bit 梯度量化" error feedback and
+// "精度恢复技巧": keep the residual and add it before the next quantisation;
+// applied to the INT8 quantizer of "FP32 → INT8 量化"):
+//   x = g + e;  per block of 256: scale = max|x|/127 (0 if max is 0),
+//   q = stochastic rounding of x/scale as above;  e' = x - q*scale
+// Monitor ([TUT] "监控与诊断": the norm of the quantisation error): err2 (if
+// not NULL) receives per block the sum of e'^2 in a fixed order -- lane j
+// of 32 adds the squares of elements 4j+c, then 128+4j+c (c = 0..3) from 0,
+// then the 32 lane sums meet in a butterfly (v[l] + v[l^o], o = 16..1).
+// g, e, q, deq are the elements k0 .. k0+n-1 of a larger tensor (k0 a
+// multiple of 256).
+void orc_quant_int8_ef_at(const float* g, float* e, uint64_t n, uint64_t k0,
+                          uint64_t seed, uint64_t step, int8_t* q, float* block_scales,
+                          float* deq, float* err2) {
+  const uint64_t block = 256;
+  std::vector<float> x(block);
+  for (uint64_t b0 = 0, bi = 0; b0 < n; b0 += block, ++bi) {
+    uint64_t b1 = b0 + block < n ? b0 + block : n;
+    float mx = 0.0f;
+    for (uint64_t k = b0; k < b1; ++k) {
+      x[k - b0] = g[k] + e[k];
+      float a = std::fabs(x[k - b0]);
+      if (a > mx) mx = a;
+    }
+    float scale = mx == 0.0f ? 0.0f : mx / 127.0f;
+    block_scales[bi] = scale;
+    for (uint64_t k = b0; k < b1; ++k) {
+      float qf = 0.0f;
+      if (scale != 0.0f) {
+        float xs = x[k - b0] / scale;
+        float f = std::floor(xs);
+        float frac = xs - f;
+        float u = orc_uniform(seed, step, k0 + k);
+        qf = f + ((u < frac) ? 1.0f : 0.0f);
+        if (qf > 127.0f) qf = 127.0f;
+        if (qf < -127.0f) qf = -127.0f;
+        if (qf != qf) qf = 0.0f;
+      }
+      q[k] = (int8_t)qf;
+      float dq = qf * scale;
+      if (deq) deq[k] = dq;
+      e[k] = x[k - b0] - dq;
+    }
+    if (err2) {
+      float lane[32];
+      for (int j = 0; j < 32; ++j) {
+        float acc = 0.0f;
+        for (int h = 0; h < 2; ++h)
+          for (int c = 0; c < 4; ++c) {
+            uint64_t k = b0 + 128 * h + 4 * j + c;
+            if (k < b1) acc = acc + (e[k] * e[k]);
+          }
+        lane[j] = acc;
+      }
+      for (int o = 16; o >= 1; o >>= 1) {
+        float nv[32];
+        for (int l = 0; l < 32; ++l) nv[l] = lane[l] + lane[l ^ o];
+        for (int l = 0; l < 32; ++l) lane[l] = nv[l];
+      }
+      err2[bi] = lane[0];
+    }
+  }
+}
+
 }  // extern "C"

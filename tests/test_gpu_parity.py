@@ -439,3 +439,26 @@ def test_misaligned_pointers_rejected_before_launch():
         ob.ob_compress(c.ctx, [buf, bad], buf, [buf, buf], buf, buf)
     assert ei.value.status == ob.OB_ERR_ALIGN
     c.close()
+
+
+@pytest.mark.parametrize("n", [1, 255, 256, 1000, 4097, (1 << 20) + 5])
+def test_int8_error_feedback_parity(n):
+    """INT8 with error feedback and the per-block error monitor, three calls
+    in a row (the residual carries over), against the oracle bit for bit."""
+    rng = np.random.default_rng(n + 17)
+    e_o = (rng.standard_normal(n) * 1e-5).astype(f32)
+    e_t = dev(e_o)
+    nb = (n + 255) // 256
+    q_t = torch.zeros(n + 16, dtype=torch.int8, device="cuda")
+    s_t = torch.zeros(nb, device="cuda")
+    d_t = torch.zeros(n + 4, device="cuda")
+    e2_t = torch.zeros(nb, device="cuda")
+    for step in range(3):
+        g = (rng.standard_normal(n) * 1e-3).astype(f32)
+        ob.ob_quant_int8_ef(dev(g), e_t, q_t, s_t, 77, step, d_t, e2_t, n=n)
+        q_o, s_o, d_o, e2_o = O.quant_int8_ef(g, e_o, 77, step, deq=True, err2=True)
+        assert np.array_equal(host(q_t)[:n], q_o), f"codes, call {step}"
+        assert_bits_equal(host(s_t), s_o, "scales")
+        assert_bits_equal(host(d_t)[:n], d_o, "dequantised")
+        assert_bits_equal(host(e_t), e_o, "residual")
+        assert_bits_equal(host(e2_t), e2_o, "error monitor")

@@ -714,3 +714,53 @@ def test_reset_then_step_equals_fresh_start():
     O.compressed_step(b, g, hp)
     _eq(a.p, b.p)
     assert all(np.array_equal(x, y) for x, y in zip(a.e, b.e))
+
+
+# ---------------------------------------------------------------------------
+# INT8 with error feedback and the error monitor
+# ---------------------------------------------------------------------------
+
+def test_int8_ef_zero_error_is_plain_int8():
+    """With e = 0 the codes and scales are those of the plain quantizer, and
+    the residual is x - q*scale."""
+    rng = np.random.default_rng(40)
+    g = (rng.standard_normal(1000) * 1e-3).astype(f32)
+    e = np.zeros(1000, f32)
+    q, sc, d = O.quant_int8_ef(g, e, seed=3, step=4, deq=True)
+    q0, sc0, d0 = O.quant_int8(g, 256, 3, 4, deq=True)
+    assert np.array_equal(q, q0)
+    _eq(sc, sc0)
+    _eq(e, (g - d0).astype(f32))
+
+
+def test_int8_ef_hand_block():
+    """x = g + e = [254, -7, 1, 0.25 ...]: scale 2; x/scale = [127, -3.5, 0.5,
+    0.125]; codes 127 always, -3 or -4, 0 or 1, 0 or 1; residual x - q*2."""
+    g = np.zeros(256, f32)
+    e = np.zeros(256, f32)
+    g[:4] = [250.0, -7.0, 1.0, 0.0]
+    e[:4] = [4.0, 0.0, 0.0, 0.25]
+    q, sc, d, e2 = O.quant_int8_ef(g, e, seed=11, step=0, deq=True, err2=True)
+    assert sc[0] == 2.0 and q[0] == 127 and e[0] == 0.0
+    assert q[1] in (-3, -4) and e[1] == -7.0 - 2.0 * q[1]
+    assert q[2] in (0, 1) and e[2] == 1.0 - 2.0 * q[2]
+    assert q[3] in (0, 1) and e[3] == 0.25 - 2.0 * q[3]
+    # the monitor: one value per block, the sum of the squared residuals
+    assert e2[0] == f32(e[1] ** 2 + e[2] ** 2 + e[3] ** 2)
+
+
+def test_int8_ef_residual_stays_bounded_and_unbiased():
+    """Error feedback keeps |e| within one quantisation step, and the
+    dequantised sum tracks the true sum (the telescoping of the write-up's
+    2.1 claim, E[sum q] = E[sum g])."""
+    rng = np.random.default_rng(41)
+    g = (rng.standard_normal(512) * 1e-3).astype(f32)
+    e = np.zeros(512, f32)
+    total_q = np.zeros(512)
+    for t in range(200):
+        q, sc, d = O.quant_int8_ef(g, e, seed=1, step=t, deq=True)
+        total_q += d
+        step = np.repeat(sc, 256)
+        assert np.all(np.abs(e) <= step * (1 + 1e-6) + 1e-12)
+    # sum of the dequantised values = sum of g minus the final residual
+    assert np.allclose(total_q, 200 * g.astype(np.float64) - e, rtol=0, atol=1e-6)
