@@ -198,11 +198,11 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     // UNI: the whole tile lies in one layer (rho scalar); else the layers
     // are walked element by element
     auto body = [&](auto uni_tag) -> float {
-      constexpr bool UNI = decltype(uni_tag)::value;
+      [[maybe_unused]] constexpr bool UNI = decltype(uni_tag)::value;
       float acc = 0.0f;
-      uint32_t l = l_t;
-      uint64_t lend = lend_t;
-      float r_l = r_t;
+      [[maybe_unused]] uint32_t l = l_t;
+      [[maybe_unused]] uint64_t lend = lend_t;
+      [[maybe_unused]] float r_l = r_t;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;

@@ -114,21 +114,40 @@ __device__ __forceinline__ void block_sum2(float a, float b, float (*ws)[8], flo
   tb = tree8(ws[1]);
 }
 
+// Sums of the squares staged in shared memory in the fixed lane order:
+// lane p adds elements 1024*i + 4*p + c (i, c = 0..3) from 0.  Entries past
+// the tile's end hold +0, which leaves a non-negative sum unchanged.
+__device__ __forceinline__ float lane_sum_sq(const float* sq, int p) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = *reinterpret_cast<const float4*>(sq + 1024 * i + 4 * p);
+    acc = __fadd_rn(acc, v.x);
+    acc = __fadd_rn(acc, v.y);
+    acc = __fadd_rn(acc, v.z);
+    acc = __fadd_rn(acc, v.w);
+  }
+  return acc;
+}
+
+// LAMB warmup, pass A: per layer tile (counted from the layer's start) the
+// elementwise update of m and v, and the tile totals of p^2 and u^2 for the
+// layer norms.  Threads read and write element t + 256*j (coalesced), stage
+// the squares in shared memory and sum them there in the fixed lane order.
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) k_warmup_lamb_a(const WarmupArgs A) {
+  __shared__ __align__(16) float sp[kTile];
+  __shared__ __align__(16) float su[kTile];
   __shared__ float ws[2][8];
-  __shared__ int s_last;
   const Geo& G = A.geo;
-  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  const int p = threadIdx.x;
   for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
     const LTile lt = decode_ltile(A.ws, G.L, LT);
-    float accp = 0.0f, accu = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t idx = 1024u * i + 4u * p + c;
-        if (idx >= lt.len) continue;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t idx = p + kThreads * j;
+      float pq = 0.0f, uq = 0.0f;
+      if (idx < lt.len) {
         const uint64_t k = lt.start + idx;
         float gb = 0.0f;
         for (uint32_t w = 0; w < G.W; ++w) gb = __fadd_rn(gb, load_grad1<BF16>(A.g[w], k));
@@ -138,44 +157,47 @@ __global__ void __launch_bounds__(kThreads) k_warmup_lamb_a(const WarmupArgs A) 
         const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));
         A.m[k] = m;
         A.v[k] = v;
-        const float pk = A.p[k];
-        accp = __fadd_rn(accp, __fmul_rn(pk, pk));
-        accu = __fadd_rn(accu, __fmul_rn(u, u));
+        const float pk = __ldcs(A.p + k);
+        pq = __fmul_rn(pk, pk);
+        uq = __fmul_rn(u, u);
       }
+      sp[idx] = pq;
+      su[idx] = uq;
+    }
+    __syncthreads();
     float tp, tu;
-    block_sum2(accp, accu, ws, tp, tu);
+    block_sum2(lane_sum_sq(sp, p), lane_sum_sq(su, p), ws, tp, tu);
     if (p == 0) {
       A.ws.lpart[LT] = tp;
       A.ws.lpart[G.n_ltiles + LT] = tu;
     }
-    __threadfence();
     __syncthreads();
-    if (p == 0) {
-      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - __ldg(A.ws.ltile_pref + lt.l);
-      unsigned prev = atomicAdd(A.ws.lcnt + lt.l, 1u);
-      s_last = (prev == ntl - 1);
-    }
-    __syncthreads();
-    if (s_last && warp == 0) {
-      __threadfence();
-      const uint32_t b = __ldg(A.ws.ltile_pref + lt.l);
-      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - b;
-      const float np = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
-      const float nu = __fsqrt_rn(ordered_sum(A.ws.lpart + G.n_ltiles + b, ntl, lane));
-      if (lane == 0) {
-        float c;
-        if (np == 0.0f || nu == 0.0f) {
-          c = 1.0f;
-        } else {
-          c = __fdiv_rn(np, nu);
-          c = fmin_plain(fmax_plain(c, A.c_min), A.c_max);
-        }
-        A.ls.c_t[lt.l] = c;
-        A.ls.c_sum[lt.l] = __fadd_rn(A.ls.c_sum[lt.l], c);
-        A.ws.lcnt[lt.l] = 0u;
+  }
+}
+
+// LAMB warmup: per layer (one warp each) the norms ||p_l||, ||u_l|| from
+// the tile totals in order, c = clip(||p||/||u||, c_min, c_max) (1 if a norm
+// is 0); c_t = c, c_sum += c.
+__global__ void __launch_bounds__(kThreads) k_warmup_lamb_c(const WarmupArgs A) {
+  const Geo& G = A.geo;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t l = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); l < G.L;
+       l += gridDim.x * (kThreads / 32)) {
+    const uint32_t b = __ldg(A.ws.ltile_pref + l);
+    const uint32_t ntl = __ldg(A.ws.ltile_pref + l + 1) - b;
+    const float np = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
+    const float nu = __fsqrt_rn(ordered_sum(A.ws.lpart + G.n_ltiles + b, ntl, lane));
+    if (lane == 0) {
+      float c;
+      if (np == 0.0f || nu == 0.0f) {
+        c = 1.0f;
+      } else {
+        c = __fdiv_rn(np, nu);
+        c = fmin_plain(fmax_plain(c, A.c_min), A.c_max);
       }
+      A.ls.c_t[l] = c;
+      A.ls.c_sum[l] = __fadd_rn(A.ls.c_sum[l], c);
     }
-    __syncthreads();
   }
 }
 
@@ -217,75 +239,70 @@ __global__ void __launch_bounds__(kThreads) k_warmup_lamb_b(const WarmupArgs A) 
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_lamb_begin(const WarmupArgs A) {
+// End of warmup, pass 1: per layer tile the total of m^2 (coalesced loads,
+// fixed lane order from shared memory, as in k_warmup_lamb_a).
+__global__ void __launch_bounds__(kThreads) k_lamb_begin_tiles(const WarmupArgs A) {
+  __shared__ __align__(16) float sq[kTile];
   __shared__ float ws[2][8];
-  __shared__ int s_last;
-  __shared__ int s_all;
-  __shared__ float s_mean;
   const Geo& G = A.geo;
-  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  const int p = threadIdx.x;
   for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
     const LTile lt = decode_ltile(A.ws, G.L, LT);
-    float acc = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t idx = 1024u * i + 4u * p + c;
-        if (idx >= lt.len) continue;
-        const float mk = A.m[lt.start + idx];
-        acc = __fadd_rn(acc, __fmul_rn(mk, mk));
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t idx = p + kThreads * j;
+      float q = 0.0f;
+      if (idx < lt.len) {
+        const float mk = __ldcs(A.m + lt.start + idx);
+        q = __fmul_rn(mk, mk);
       }
+      sq[idx] = q;
+    }
+    __syncthreads();
     float tm, unused;
-    block_sum2(acc, 0.0f, ws, tm, unused);
+    block_sum2(lane_sum_sq(sq, p), 0.0f, ws, tm, unused);
     if (p == 0) A.ws.lpart[LT] = tm;
-    __threadfence();
     __syncthreads();
-    if (p == 0) {
-      const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - __ldg(A.ws.ltile_pref + lt.l);
-      unsigned prev = atomicAdd(A.ws.lcnt + lt.l, 1u);
-      s_last = (prev == ntl - 1);
-      s_all = 0;
+  }
+}
+
+// Pass 2, one warp per layer: rms_l = ||m_l|| / sqrt(n_l).
+__global__ void __launch_bounds__(kThreads) k_lamb_begin_rms(const WarmupArgs A) {
+  const Geo& G = A.geo;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t l = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); l < G.L;
+       l += gridDim.x * (kThreads / 32)) {
+    const uint32_t b = __ldg(A.ws.ltile_pref + l);
+    const uint32_t ntl = __ldg(A.ws.ltile_pref + l + 1) - b;
+    const float nrm = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
+    if (lane == 0) {
+      const uint64_t nl = __ldg(A.ws.layer_off + l + 1) - __ldg(A.ws.layer_off + l);
+      A.ws.rms[l] = __fdiv_rn(nrm, __fsqrt_rn(__ull2float_rn(nl)));
     }
-    __syncthreads();
-    if (s_last) {
-      if (warp == 0) {
-        __threadfence();
-        const uint32_t b = __ldg(A.ws.ltile_pref + lt.l);
-        const uint32_t ntl = __ldg(A.ws.ltile_pref + lt.l + 1) - b;
-        const float nrm = __fsqrt_rn(ordered_sum(A.ws.lpart + b, ntl, lane));
-        if (lane == 0) {
-          const uint64_t nl = __ldg(A.ws.layer_off + lt.l + 1) - __ldg(A.ws.layer_off + lt.l);
-          A.ws.rms[lt.l] = __fdiv_rn(nrm, __fsqrt_rn(__ull2float_rn(nl)));
-          A.ws.lcnt[lt.l] = 0u;
-          __threadfence();
-          unsigned prev = atomicAdd(A.ws.gcnt + 1, 1u);
-          s_all = (prev == G.L - 1);
-        }
-      }
-      __syncthreads();
-      if (s_all) {
-        __threadfence();
-        if (p == 0) {
-          float mean = 0.0f;
-          for (uint32_t l = 0; l < G.L; ++l) mean = __fadd_rn(mean, __ldcg(A.ws.rms + l));
-          s_mean = __fdiv_rn(mean, (float)G.L);
-          A.ws.gcnt[1] = 0u;
-        }
-        __syncthreads();
-        const float fT = (float)A.warmup_steps;
-        for (uint32_t l = p; l < G.L; l += kThreads) {
-          const float rms = __ldcg(A.ws.rms + l);
-          A.ls.s[l] = rms == 0.0f ? 1.0f : __fdiv_rn(s_mean, rms);
-          const float ca = __fdiv_rn(A.ls.c_sum[l], fT);
-          A.ls.c_avg[l] = ca;
-          A.ls.r_prev[l] = 1.0f;
-          A.ls.c_prev[l] = ca;
-          A.ls.c_prev2[l] = ca;
-        }
-      }
-    }
-    __syncthreads();
+  }
+}
+
+// Pass 3, one CTA: mean of the rms over layers (in layer order, from 0),
+// s_l = mean / rms_l (1 if rms_l = 0), c_avg = c_sum / T_w, r = 1,
+// c_prev = c_prev2 = c_avg.
+__global__ void __launch_bounds__(kThreads) k_lamb_begin_final(const WarmupArgs A) {
+  __shared__ float s_mean;
+  const Geo& G = A.geo;
+  if (threadIdx.x == 0) {
+    float mean = 0.0f;
+    for (uint32_t l = 0; l < G.L; ++l) mean = __fadd_rn(mean, A.ws.rms[l]);
+    s_mean = __fdiv_rn(mean, (float)G.L);
+  }
+  __syncthreads();
+  const float fT = (float)A.warmup_steps;
+  for (uint32_t l = threadIdx.x; l < G.L; l += kThreads) {
+    const float rms = A.ws.rms[l];
+    A.ls.s[l] = rms == 0.0f ? 1.0f : __fdiv_rn(s_mean, rms);
+    const float ca = __fdiv_rn(A.ls.c_sum[l], fT);
+    A.ls.c_avg[l] = ca;
+    A.ls.r_prev[l] = 1.0f;
+    A.ls.c_prev[l] = ca;
+    A.ls.c_prev2[l] = ca;
   }
 }
 
@@ -304,12 +321,21 @@ cudaError_t launch_warmup_lamb(const WarmupArgs& a, bool bf16, int sms, cudaStre
   else k_warmup_lamb_a<false><<<grid_for(k_warmup_lamb_a<false>, sms, nlt), kThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const uint64_t lw = (a.geo.L + kThreads / 32 - 1) / (kThreads / 32);
+  k_warmup_lamb_c<<<grid_for(k_warmup_lamb_c, sms, lw), kThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   k_warmup_lamb_b<<<grid_for(k_warmup_lamb_b, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lamb_begin(const WarmupArgs& a, int sms, cudaStream_t s) {
-  k_lamb_begin<<<grid_for(k_lamb_begin, sms, a.geo.n_ltiles), kThreads, 0, s>>>(a);
+  k_lamb_begin_tiles<<<grid_for(k_lamb_begin_tiles, sms, a.geo.n_ltiles), kThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const uint64_t lw = (a.geo.L + kThreads / 32 - 1) / (kThreads / 32);
+  k_lamb_begin_rms<<<grid_for(k_lamb_begin_rms, sms, lw), kThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_lamb_begin_final<<<1, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -57,22 +57,18 @@ size_t region(size_t& cursor, size_t bytes) {
 }
 
 struct Regions {
-  size_t wpart, wcnt, spart, scnt, tile_layer, layer_off, ltile_pref, lpart, lcnt, Rbits,
-      rms, gcnt, err, total;
+  size_t wpart, spart, tile_layer, layer_off, ltile_pref, lpart, Rbits, rms, gcnt, err, total;
 };
 
 Regions regions_of(const Geo& G) {
   Regions r{};
   size_t c = 0;
   r.wpart = region(c, (size_t)G.W * G.nc * G.tpc * sizeof(float));
-  r.wcnt = region(c, (size_t)G.nc * sizeof(unsigned));
   r.spart = region(c, (size_t)G.nc * G.tpc * sizeof(float));
-  r.scnt = region(c, (size_t)G.nc * sizeof(unsigned));
   r.tile_layer = region(c, (size_t)G.n_tiles * sizeof(uint32_t));
   r.layer_off = region(c, (size_t)(G.L + 1) * sizeof(uint64_t));
   r.ltile_pref = region(c, (size_t)(G.L + 1) * sizeof(uint32_t));
   r.lpart = region(c, (size_t)2 * G.n_ltiles * sizeof(float));
-  r.lcnt = region(c, (size_t)G.L * sizeof(unsigned));
   r.Rbits = region(c, (size_t)G.L * sizeof(unsigned));
   r.rms = region(c, (size_t)G.L * sizeof(float));
   r.gcnt = region(c, 4 * sizeof(unsigned));
@@ -300,14 +296,11 @@ ob_status ob_set_workspace(ob_ctx* ctx, void* workspace, size_t bytes, ob_stream
   if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace initialisation");
   ob::Workspace& w = ctx->ws;
   w.wpart = reinterpret_cast<float*>(b + r.wpart);
-  w.wcnt = reinterpret_cast<unsigned*>(b + r.wcnt);
   w.spart = reinterpret_cast<float*>(b + r.spart);
-  w.scnt = reinterpret_cast<unsigned*>(b + r.scnt);
   w.tile_layer = reinterpret_cast<uint32_t*>(b + r.tile_layer);
   w.layer_off = reinterpret_cast<uint64_t*>(b + r.layer_off);
   w.ltile_pref = reinterpret_cast<uint32_t*>(b + r.ltile_pref);
   w.lpart = reinterpret_cast<float*>(b + r.lpart);
-  w.lcnt = reinterpret_cast<unsigned*>(b + r.lcnt);
   w.Rbits = reinterpret_cast<unsigned*>(b + r.Rbits);
   w.rms = reinterpret_cast<float*>(b + r.rms);
   w.gcnt = reinterpret_cast<unsigned*>(b + r.gcnt);

@@ -68,17 +68,14 @@ __device__ __forceinline__ Tile decode_tile(const Geo& G, uint32_t T) {
 // Workspace regions (byte offsets from the workspace base).
 struct Workspace {
   float* wpart;          // [W][nc][tpc] worker tile totals
-  unsigned* wcnt;        // [nc] arrivals per chunk (worker scales)
   float* spart;          // [nc][tpc] server tile totals
-  unsigned* scnt;        // [nc] arrivals per chunk (server scales)
   uint32_t* tile_layer;  // [n_tiles] layer of each tile's first element
   uint64_t* layer_off;   // [L+1]
   uint32_t* ltile_pref;  // [L+1] prefix count of per-layer tiles
   float* lpart;          // [2][n_ltiles] per-layer tile totals
-  unsigned* lcnt;        // [L] arrivals per layer
   unsigned* Rbits;       // [L] LAMB max ratio, as float bit patterns
   float* rms;            // [L] begin: momentum RMS per layer
-  unsigned* gcnt;        // [4] whole-grid arrival counters
+  unsigned* gcnt;        // [4] whole-grid arrival counters (LAMB pass A)
   unsigned* err;         // [1] first device-side error code (0 = none)
 };
 
