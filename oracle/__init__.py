@@ -64,6 +64,22 @@ def lib():
                                      vp]
         L.orc_quant_int8_at.argtypes = [f32p, u64, u64, u64, u64, u64, i8p, f32p, vp]
         L.orc_quant_int8_ef_at.argtypes = [f32p, f32p, u64, u64, u64, u64, i8p, f32p, vp, vp]
+        u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+        ci = ct.c_int
+        L.orc_qb_compress_worker_at.argtypes = [lay, ci, f32, f32, u64, u64, u64, u64, u64,
+                                                f32p, f32p, f32p, u32p, f32p]
+        L.orc_qb_server_at.argtypes = [lay, ci, u64, u64, u64, u64, u32p, u64, f32p, u64,
+                                       f32p, u32p, f32p]
+        L.orc_qb_decode_at.argtypes = [lay, ci, u64, u64, u32p, f32p, f32p]
+        L.orc_qb_adam_at.argtypes = [lay, ci, f32, f32, u64, u64, u32p, f32p, f32p, f32p,
+                                     f32p]
+        L.orc_f32_to_f16.argtypes = [f32]
+        L.orc_f32_to_f16.restype = ct.c_uint16
+        L.orc_f16_to_f32.argtypes = [ct.c_uint16]
+        L.orc_f16_to_f32.restype = f32
+        L.orc_f16_compress_worker.argtypes = [lay, f32, f32, ci, f32p, f32p, f32p, u16p]
+        L.orc_f16_server.argtypes = [lay, u16p, f32p, u16p]
+        L.orc_f16_adam.argtypes = [lay, ci, f32, f32, u16p, f32p, f32p, f32p]
         _lib = L
     return _lib
 
@@ -246,6 +262,125 @@ def quant_int8_ef(g, e, seed=1234, step=0, deq=False, err2=False, k0=0):
     if err2:
         out.append(e2)
     return tuple(out)
+
+
+# ---------------------------------------------------------------------------
+# Layerwise mixed bit widths: the b-bit (b = 2, 4, 8) and FP16 codecs
+# ---------------------------------------------------------------------------
+
+def qb_words(n, bits):
+    """Words of packed b-bit codes for n elements (n a multiple of 256)."""
+    return n * bits // 32
+
+
+def qb_compress_worker(lay, bits, g, m, e, b1, w, seed, step, clip=0.0, k0=0, length=None):
+    """Worker w's b-bit compression of the elements [k0, k0+length) (the
+    arrays hold that range); e is updated in place.  Returns (codes u32,
+    block scales f32)."""
+    length = lay.n_pad - k0 if length is None else length
+    assert k0 % 256 == 0 and length % 256 == 0
+    assert e.dtype == np.float32 and e.flags.c_contiguous and e.size == length
+    codes = np.zeros(qb_words(length, bits), np.uint32)
+    sc = np.zeros(length // 256, np.float32)
+    lib().orc_qb_compress_worker_at(lay._s, bits, b1, clip, w, seed, step, k0, length,
+                                    _f32(g), _f32(m), e, codes, sc)
+    return codes, sc
+
+
+def qb_server(lay, bits, codes, bscales, e_s, seed, step, k0=0, length=None):
+    """The server's b-bit average and re-compression of [k0, k0+length).
+    codes: [W][words] (rows may be longer than the range: their stride is
+    codes.shape[1] and they start at word k0*b/32); bscales likewise.
+    e_s is updated in place.  Returns (scodes, sbscales)."""
+    length = lay.n_pad - k0 if length is None else length
+    assert k0 % 256 == 0 and length % 256 == 0
+    assert e_s.dtype == np.float32 and e_s.flags.c_contiguous and e_s.size == length
+    codes = np.ascontiguousarray(codes, np.uint32)
+    bscales = _f32(bscales)
+    sc = np.zeros(qb_words(length, bits), np.uint32)
+    ss = np.zeros(length // 256, np.float32)
+    lib().orc_qb_server_at(lay._s, bits, seed, step, k0, length, codes, codes.shape[1],
+                           bscales, bscales.shape[1], e_s, sc, ss)
+    return sc, ss
+
+
+def qb_decode(lay, bits, codes, bscales, k0=0, length=None):
+    length = lay.n_pad - k0 if length is None else length
+    out = np.zeros(length, np.float32)
+    lib().orc_qb_decode_at(lay._s, bits, k0, length, np.ascontiguousarray(codes, np.uint32),
+                           _f32(bscales), out)
+    return out
+
+
+def qb_adam(lay, bits, scodes, sbscales, v, eps, lr, m, p, k0=0, length=None):
+    """m, p (the range's arrays) are updated in place."""
+    length = lay.n_pad - k0 if length is None else length
+    lib().orc_qb_adam_at(lay._s, bits, eps, lr, k0, length,
+                         np.ascontiguousarray(scodes, np.uint32), _f32(sbscales), _f32(v),
+                         m, p)
+
+
+def f32_to_f16(x):
+    """uint16 bit patterns of IEEE binary16 (nearest, ties to even)."""
+    f = lib().orc_f32_to_f16
+    x = _f32(x)
+    return np.array([f(float(v)) for v in x.ravel()], np.uint16).reshape(x.shape)
+
+
+def f16_to_f32(h):
+    f = lib().orc_f16_to_f32
+    h = np.ascontiguousarray(h, np.uint16)
+    return np.array([f(int(v)) for v in h.ravel()], np.float32).reshape(h.shape)
+
+
+def f16_compress_worker(lay, g, m, e, b1, send, h=None, clip=0.0):
+    """e is updated in place; returns h (n_pad uint16), untouched (or zeros
+    if h is None) when not sending."""
+    h = np.zeros(lay.n_pad, np.uint16) if h is None else h
+    lib().orc_f16_compress_worker(lay._s, b1, clip, int(bool(send)), _f32(g), _f32(m), e, h)
+    return h
+
+
+def f16_server(lay, h, e_s):
+    """h: [W][n_pad] uint16; e_s updated in place; returns hs."""
+    hs = np.zeros(lay.n_pad, np.uint16)
+    lib().orc_f16_server(lay._s, np.ascontiguousarray(h, np.uint16), e_s, hs)
+    return hs
+
+
+def f16_adam(lay, send, hs, v, eps, lr, m, p):
+    lib().orc_f16_adam(lay._s, int(bool(send)), eps, lr, np.ascontiguousarray(hs, np.uint16),
+                       _f32(v), m, p)
+
+
+def codec_step(st, grads, hp, bits, t, seed, period=10):
+    """One compressed 1-bit Adam step of a group compressed with `bits`
+    (1: scaled sign, 2/4/8: block quantizer, 16: FP16 sent when t % period
+    == 0), t = 1, 2, ... the compressed step.  The uniforms of the b-bit
+    codec use (seed, step t)."""
+    lay = st.lay
+    if bits == 1:
+        return compressed_step(st, grads, hp)
+    clip = hp.get("clip", 0.0)
+    if bits == 16:
+        send = (t % period) == 0
+        if not hasattr(st, "h"):
+            st.h = np.zeros((lay.W, lay.n_pad), np.uint16)
+            st.hs = np.zeros(lay.n_pad, np.uint16)
+        for w in range(lay.W):
+            f16_compress_worker(lay, grads[w], st.m, st.e[w], hp["b1"], send, st.h[w], clip)
+        if send:
+            st.hs = f16_server(lay, st.h, st.e_s)
+        f16_adam(lay, send, st.hs, st.v, hp["eps"], hp["lr"], st.m, st.p)
+        return
+    codes, scs = [], []
+    for w in range(lay.W):
+        c, s = qb_compress_worker(lay, bits, grads[w], st.m, st.e[w], hp["b1"], w, seed, t, clip)
+        codes.append(c)
+        scs.append(s)
+    st.codes, st.bscales = np.stack(codes), np.stack(scs)
+    st.scodes, st.sbscales = qb_server(lay, bits, st.codes, st.bscales, st.e_s, seed, t)
+    qb_adam(lay, bits, st.scodes, st.sbscales, st.v, hp["eps"], hp["lr"], st.m, st.p)
 
 
 # ---------------------------------------------------------------------------

@@ -1,6 +1,6 @@
 // Oracle for the error-compensated 1-bit compressed optimizer step
-// (1-bit Adam / 1-bit LAMB) and the block-wise INT8 stochastic-rounding
-// quantizer.
+// (1-bit Adam / 1-bit LAMB), the block-wise INT8 stochastic-rounding
+// quantizer, and the layerwise mixed-width codecs (b-bit blocks, FP16).
 //
 // TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, single-threaded
 // restatement of the method, written to be checked by eye against the
@@ -707,6 +707,308 @@ void orc_quant_int8_ef_at(const float* g, float* e, uint64_t n, uint64_t k0,
       }
       err2[bi] = lane[0];
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Layerwise mixed bit widths
+// ---------------------------------------------------------------------------
+// [BLOG] §3.2 (混合精度训练策略) gives each parameter type its own bit width
+// and update period: embeddings and transformer FFN weights 1 bit every
+// step, CNN weights 2 bits every step, LayerNorm parameters FP16 every 10
+// steps; §6 repeats it as layerwise_bits [1, 2, 1, 16].  [TUT]
+// "更激进的组合策略" (分层混合精度) names the same idea.  Neither page
+// defines the 2-bit code or what happens between two FP16 updates.
+// Readings:
+//   - the layers of one width form a fused buffer of their own, with the
+//     layout above (n = that group's elements), compressed by one codec;
+//     width 1 is the scaled sign above;
+//   - width b in {2, 4, 8} is the b-bit form of [TUT]'s quantizer, whose
+//     GradientQuantizeINT8 example takes the width as an argument: per block
+//     of 256 elements scale = max|x| / (2^(b-1) - 1) (0 if the max is 0),
+//     stochastic rounding as in the INT8 quantizer, clamp to
+//     [-(2^(b-1) - 1), 2^(b-1) - 1], a NaN codes as 0, and error feedback
+//     e' = x - q*scale.  b = 2 gives the codes -1, 0, 1.  Blocks are counted
+//     over each worker's whole buffer (block k/256); the alignment A is a
+//     multiple of 256, so no block straddles two partitions and the server's
+//     blocks are the workers' blocks;
+//   - the uniform of worker w's element k is orc_uniform(seed, step,
+//     w*n_pad + k), that of the server's element k orc_uniform(seed, step,
+//     W*n_pad + k): the element's index in the W+1 messages laid end to end;
+//   - width 16 sends x as IEEE binary16 (round to nearest, ties to even)
+//     with error feedback e' = x - f32(h), on the steps where `send` is set
+//     (every 10th).  On the other steps nothing is exchanged: each worker
+//     keeps x whole as its error, the server keeps its error, the momentum
+//     is 0 and the parameters are left as they are;
+//   - 1-bit Adam only (the table sits in the 1bit Adam write-up); no sigma,
+//     no rho.
+// Codes: the field q mod 2^b of element k sits at bit (k*b) % 32 of word
+// (k*b)/32 (LSB first, two's complement); a row holds n_pad*b/32 words.
+// The *_at functions take the elements [k0, k0+len) of the buffer (k0 and
+// len multiples of 256): the arrays passed hold just that range (codes from
+// word k0*b/32, scales from block k0/256), so that a sample of blocks can be
+// checked on its own.  Elements k >= n are padding: code 0, error 0, m 0.
+
+static void qb_put(uint32_t* words, uint64_t k, int bits, int q) {
+  const uint64_t bit = k * (uint64_t)bits;
+  const uint32_t field = (uint32_t)q & ((1u << bits) - 1u);
+  words[bit / 32] |= field << (bit % 32);
+}
+
+static int qb_get(const uint32_t* words, uint64_t k, int bits) {
+  const uint64_t bit = k * (uint64_t)bits;
+  const int field = (int)((words[bit / 32] >> (bit % 32)) & ((1u << bits) - 1u));
+  return field >= (1 << (bits - 1)) ? field - (1 << bits) : field;
+}
+
+// Quantises the block of 256 values x[0..256) that are the elements
+// kb .. kb+255 of a buffer of n real elements; `u_base` + k is the uniform's
+// element index; codes are relative to the block's own first element (the
+// caller passes the row's words from that block on).
+static void qb_block(int bits, uint64_t n, uint64_t kb, const float* x, uint64_t seed,
+                     uint64_t step, uint64_t u_base, uint32_t* codes, float* scale_out,
+                     float* e) {
+  const float qmax = (float)((1 << (bits - 1)) - 1);
+  float mx = 0.0f;
+  for (uint64_t i = 0; i < 256; ++i) {
+    if (kb + i >= n) break;
+    float a = std::fabs(x[i]);
+    if (a > mx) mx = a;  // a NaN never wins
+  }
+  const float scale = mx == 0.0f ? 0.0f : mx / qmax;
+  *scale_out = scale;
+  for (uint64_t i = 0; i < 256; ++i) {
+    const uint64_t k = kb + i;
+    if (k >= n) {
+      e[i] = 0.0f;
+      continue;
+    }
+    float qf = 0.0f;
+    if (scale != 0.0f) {
+      float xs = x[i] / scale;
+      float f = std::floor(xs);
+      float frac = xs - f;
+      float u = orc_uniform(seed, step, u_base + k);
+      qf = f + ((u < frac) ? 1.0f : 0.0f);
+      if (qf > qmax) qf = qmax;
+      if (qf < -qmax) qf = -qmax;
+      if (qf != qf) qf = 0.0f;
+    }
+    qb_put(codes, i, bits, (int)qf);
+    e[i] = x[i] - (qf * scale);
+  }
+}
+
+// Worker w, b-bit codec:
+//   m_w = b1*m + (1-b1)*g;  x = m_w + e  (clamped to [-clip, clip] if clip > 0)
+//   per block: the quantizer above;  e := x - q*scale (plain, not deferred)
+// codes: the worker's row from word k0*b/32; bscales from block k0/256.
+void orc_qb_compress_worker_at(const orc_layout* L, int bits, float b1, float clip,
+                               uint64_t w, uint64_t seed, uint64_t step, uint64_t k0,
+                               uint64_t len, const float* g, const float* m, float* e,
+                               uint32_t* codes, float* bscales) {
+  const float ob1 = 1.0f - b1;
+  const uint64_t words = len * (uint64_t)bits / 32;
+  for (uint64_t i = 0; i < words; ++i) codes[i] = 0u;
+  std::vector<float> x(256);
+  for (uint64_t b0 = 0; b0 < len; b0 += 256) {
+    for (uint64_t i = 0; i < 256; ++i) {
+      const uint64_t k = k0 + b0 + i;
+      if (k >= L->n) {
+        x[i] = 0.0f;
+        continue;
+      }
+      float mw = (b1 * m[b0 + i]) + (ob1 * g[b0 + i]);
+      float xv = mw + e[b0 + i];
+      if (clip > 0.0f) {
+        if (xv > clip) xv = clip;
+        if (xv < -clip) xv = -clip;
+      }
+      x[i] = xv;
+    }
+    qb_block(bits, L->n, k0 + b0, x.data(), seed, step, w * L->n_pad,
+             codes + b0 * (uint64_t)bits / 32, &bscales[b0 / 256], e + b0);
+  }
+}
+
+void orc_qb_compress_worker(const orc_layout* L, int bits, float b1, float clip, uint64_t w,
+                            uint64_t seed, uint64_t step, const float* g, const float* m,
+                            float* e, uint32_t* codes, float* bscales) {
+  orc_qb_compress_worker_at(L, bits, b1, clip, w, seed, step, 0, L->n_pad, g, m, e, codes,
+                            bscales);
+}
+
+// Server, b-bit codec, elements [k0, k0+len) of every partition it covers:
+//   z = (sum over w = 0..W-1, in order, from 0, of q_w*scale_w) / W
+//   y = e_s + z;  per block the quantizer above;  e_s := y - q_s*sscale
+// codes: W rows of `row_words` words, each from word k0*b/32 of its row;
+// bscales: W rows of `row_blocks` scales, each from block k0/256.
+void orc_qb_server_at(const orc_layout* L, int bits, uint64_t seed, uint64_t step,
+                      uint64_t k0, uint64_t len, const uint32_t* codes, uint64_t row_words,
+                      const float* bscales, uint64_t row_blocks, float* e_s,
+                      uint32_t* scodes, float* sbscales) {
+  const float fW = (float)L->W;
+  const uint64_t words = len * (uint64_t)bits / 32;
+  for (uint64_t i = 0; i < words; ++i) scodes[i] = 0u;
+  std::vector<float> y(256);
+  for (uint64_t b0 = 0; b0 < len; b0 += 256) {
+    for (uint64_t i = 0; i < 256; ++i) {
+      const uint64_t k = k0 + b0 + i;
+      if (k >= L->n) {
+        y[i] = 0.0f;
+        continue;
+      }
+      float z = 0.0f;
+      for (uint64_t w = 0; w < L->W; ++w) {
+        const float q = (float)qb_get(codes + w * row_words, b0 + i, bits);
+        z = z + (q * bscales[w * row_blocks + b0 / 256]);
+      }
+      z = z / fW;
+      y[i] = e_s[b0 + i] + z;
+    }
+    qb_block(bits, L->n, k0 + b0, y.data(), seed, step, L->W * L->n_pad,
+             scodes + b0 * (uint64_t)bits / 32, &sbscales[b0 / 256], e_s + b0);
+  }
+}
+
+void orc_qb_server(const orc_layout* L, int bits, uint64_t seed, uint64_t step,
+                   const uint32_t* codes, const float* bscales, float* e_s, uint32_t* scodes,
+                   float* sbscales) {
+  orc_qb_server_at(L, bits, seed, step, 0, L->n_pad, codes, L->n_pad * (uint64_t)bits / 32,
+                   bscales, L->n_pad / 256, e_s, scodes, sbscales);
+}
+
+// out = q*scale (padding 0), elements [k0, k0+len).
+void orc_qb_decode_at(const orc_layout* L, int bits, uint64_t k0, uint64_t len,
+                      const uint32_t* codes, const float* bscales, float* out) {
+  for (uint64_t i = 0; i < len; ++i) {
+    if (k0 + i >= L->n) {
+      out[i] = 0.0f;
+      continue;
+    }
+    out[i] = (float)qb_get(codes, i, bits) * bscales[i / 256];
+  }
+}
+
+// 1-bit Adam update fed by the b-bit server message (frozen variance, as
+// orc_adam_update): m = q*sscale;  p = p - lr*(m/(sqrt(v) + eps)).
+void orc_qb_adam_at(const orc_layout* L, int bits, float eps, float lr, uint64_t k0,
+                    uint64_t len, const uint32_t* scodes, const float* sbscales,
+                    const float* v, float* m, float* p) {
+  for (uint64_t i = 0; i < len; ++i) {
+    if (k0 + i >= L->n) {
+      m[i] = 0.0f;
+      continue;
+    }
+    float mk = (float)qb_get(scodes, i, bits) * sbscales[i / 256];
+    float d = std::sqrt(v[i]);
+    d = d + eps;
+    float u = mk / d;
+    float t = lr * u;
+    m[i] = mk;
+    p[i] = p[i] - t;
+  }
+}
+
+// IEEE 754 binary16 from binary32, round to nearest, ties to even, written
+// from the format's definition: 1 sign bit, 5 exponent bits (bias 15), 10
+// fraction bits; normal values 2^-14 .. 65504, subnormal steps of 2^-24.
+// A value is rounded to a multiple of its binade's step (2^(e-10) for
+// 2^e <= |x| < 2^(e+1), 2^-24 below 2^-14); |x| >= 65520 (65504 plus half a
+// step, which rounds up to 2^16) becomes infinity.  A NaN becomes the quiet
+// NaN 0x7e00 with the input's sign.
+uint16_t orc_f32_to_f16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const double a = std::fabs((double)f);
+  if (f != f) return (uint16_t)(sign | 0x7e00u);
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+  int e2;
+  std::frexp(a, &e2);  // a = mant * 2^e2, mant in [0.5, 1): 2^(e2-1) <= a < 2^e2
+  const int e = e2 - 1;
+  const bool sub = (a < std::ldexp(1.0, -14));
+  const double step = sub ? std::ldexp(1.0, -24) : std::ldexp(1.0, e - 10);
+  const double r = std::nearbyint(a / step);  // exact quotient; ties to even
+  if (sub) return (uint16_t)(sign | (uint16_t)r);  // r = 1024 is 2^-14, normal
+  // r in [1024, 2048]; r = 2048 carries into the next binade by itself
+  return (uint16_t)(sign | (uint16_t)(((e + 15) << 10) + ((int)r - 1024)));
+}
+
+float orc_f16_to_f32(uint16_t h) {
+  const int s = (h >> 15) & 1, ex = (h >> 10) & 31, fr = h & 1023;
+  double v;
+  if (ex == 0) v = std::ldexp((double)fr, -24);
+  else if (ex == 31) v = fr ? NAN : INFINITY;
+  else v = std::ldexp((double)(1024 + fr), ex - 25);
+  return (float)(s ? -v : v);
+}
+
+// Worker, FP16 codec (elements [0, n_pad)):
+//   x = m_w + e (clamped if clip > 0);
+//   send:  h = f16(x), e := x - f32(h);   otherwise: e := x, h untouched.
+void orc_f16_compress_worker(const orc_layout* L, float b1, float clip, int send,
+                             const float* g, const float* m, float* e, uint16_t* h) {
+  const float ob1 = 1.0f - b1;
+  for (uint64_t k = 0; k < L->n_pad; ++k) {
+    if (k >= L->n) {
+      e[k] = 0.0f;
+      if (send) h[k] = 0;
+      continue;
+    }
+    float mw = (b1 * m[k]) + (ob1 * g[k]);
+    float x = mw + e[k];
+    if (clip > 0.0f) {
+      if (x > clip) x = clip;
+      if (x < -clip) x = -clip;
+    }
+    if (send) {
+      const uint16_t hk = orc_f32_to_f16(x);
+      h[k] = hk;
+      e[k] = x - orc_f16_to_f32(hk);
+    } else {
+      e[k] = x;
+    }
+  }
+}
+
+// Server, FP16 codec, on a sending step: h is [W][n_pad];
+//   z = (sum over w, in order, from 0, of f32(h_w)) / W;  y = e_s + z
+//   hs = f16(y);  e_s := y - f32(hs)
+void orc_f16_server(const orc_layout* L, const uint16_t* h, float* e_s, uint16_t* hs) {
+  const float fW = (float)L->W;
+  for (uint64_t k = 0; k < L->n_pad; ++k) {
+    if (k >= L->n) {
+      e_s[k] = 0.0f;
+      hs[k] = 0;
+      continue;
+    }
+    float z = 0.0f;
+    for (uint64_t w = 0; w < L->W; ++w) z = z + orc_f16_to_f32(h[w * L->n_pad + k]);
+    z = z / fW;
+    const float y = e_s[k] + z;
+    const uint16_t hk = orc_f32_to_f16(y);
+    hs[k] = hk;
+    e_s[k] = y - orc_f16_to_f32(hk);
+  }
+}
+
+// Update, FP16 codec: sending step m = f32(hs), p = p - lr*(m/(sqrt(v)+eps));
+// other steps m = 0 and p is left as it is.  Padding: m = 0.
+void orc_f16_adam(const orc_layout* L, int send, float eps, float lr, const uint16_t* hs,
+                  const float* v, float* m, float* p) {
+  for (uint64_t k = 0; k < L->n_pad; ++k) {
+    if (k >= L->n || !send) {
+      m[k] = 0.0f;
+      continue;
+    }
+    float mk = orc_f16_to_f32(hs[k]);
+    float d = std::sqrt(v[k]);
+    d = d + eps;
+    float u = mk / d;
+    float t = lr * u;
+    m[k] = mk;
+    p[k] = p[k] - t;
   }
 }
 

@@ -85,6 +85,48 @@ def gpt_1p3b_tensors() -> List[Tuple[str, int, str]]:
     return t
 
 
+def resnet50_params() -> List[Tuple[str, int, str, str]]:
+    """ResNet-50 (bottleneck blocks 3-4-6-3, widths 64-128-256-512, expansion
+    4, 1000 classes) as (name, numel, init kind, parameter type): 53
+    convolutions, 53 batch norms (weight and bias), the fc layer: 161
+    tensors, 25,557,032 values.  Types: "conv", "norm", "dense"."""
+    t = []
+
+    def conv(name, cin, cout, k):
+        t.append((name + ".weight", cin * cout * k * k, "w", "conv"))
+
+    def bn(name, c):
+        t.extend([(name + ".weight", c, "ln_w", "norm"), (name + ".bias", c, "b", "norm")])
+
+    conv("conv1", 3, 64, 7)
+    bn("bn1", 64)
+    cin = 64
+    for li, (mid, blocks) in enumerate([(64, 3), (128, 4), (256, 6), (512, 3)], 1):
+        out = 4 * mid
+        for b in range(blocks):
+            pre = f"layer{li}.{b}"
+            conv(pre + ".conv1", cin, mid, 1)
+            bn(pre + ".bn1", mid)
+            conv(pre + ".conv2", mid, mid, 3)
+            bn(pre + ".bn2", mid)
+            conv(pre + ".conv3", mid, out, 1)
+            bn(pre + ".bn3", out)
+            if b == 0:
+                conv(pre + ".downsample.0", cin, out, 1)
+                bn(pre + ".downsample.1", out)
+            cin = out
+    t.extend([("fc.weight", 2048 * 1000, "w", "dense"), ("fc.bias", 1000, "b", "dense")])
+    return t
+
+
+# Bit width per parameter type for layerwise mixed widths: embeddings and
+# dense (transformer FFN) layers 1 bit, convolution weights 2 bits,
+# normalisation parameters FP16 sent every NORM_PERIOD-th step (the "1bit
+# Adam" write-up, §3.2 table and §6 layerwise_bits [1, 2, 1, 16]).
+LAYERWISE_BITS = {"embedding": 1, "conv": 2, "dense": 1, "norm": 16}
+NORM_PERIOD = 10
+
+
 # ---------------------------------------------------------------------------
 # Workloads
 # ---------------------------------------------------------------------------
@@ -105,6 +147,7 @@ class Workload:
     warmup_steps: int = 5
     compressed_steps: int = 10
     hp: dict = field(default_factory=dict)
+    seed_tag: int = 0                # != 0: a separate family of random streams
 
     @property
     def layer_offsets(self) -> Optional[np.ndarray]:
@@ -180,9 +223,35 @@ def workload(name: str, **over) -> Workload:
     return wl
 
 
+def mixed_groups(name: str = "resnet50-mixed", W: int = 8, warmup_steps: int = 5,
+                 compressed_steps: int = 20) -> List[Tuple[int, Workload]]:
+    """Layerwise mixed widths: the model's tensors grouped by the bit width
+    of their type (LAYERWISE_BITS), each group a fused buffer of its own
+    (tensors in model order), as [(bits, Workload)] in increasing width.
+    Per-tensor gradient std 1e-3*10^U(-1,1) drawn over the whole model;
+    each group draws from its own random streams (seed_tag = bits)."""
+    if name != "resnet50-mixed":
+        raise KeyError(name)
+    params = resnet50_params()
+    std = _tensor_std(params)
+    groups = []
+    for bits in sorted(set(LAYERWISE_BITS[p[3]] for p in params)):
+        idx = [i for i, p in enumerate(params) if LAYERWISE_BITS[p[3]] == bits]
+        t = [params[i][:3] for i in idx]
+        wl = Workload(f"{name}/{bits}", n=sum(s for _, s, _ in t), W=W, chunk=1 << 20,
+                      tensors=t, layer_std=std[idx], warmup_steps=warmup_steps,
+                      compressed_steps=compressed_steps, hp=dict(ADAM_HP), seed_tag=bits)
+        groups.append((bits, wl))
+    return groups
+
+
 # ---------------------------------------------------------------------------
 # Drawing numbers
 # ---------------------------------------------------------------------------
+
+def _tag(wl: Workload) -> list:
+    return [wl.seed_tag] if wl.seed_tag else []
+
 
 def _std_per_element(wl: Workload, start: int, stop: int) -> np.ndarray:
     """float32 std for elements [start, stop) (0 beyond n)."""
@@ -210,7 +279,7 @@ def grad_slice(wl: Workload, step: int, worker: int, start: int,
     out = np.empty(stop - start, np.float32)
     b0, b1 = start // BLOCK, (stop - 1) // BLOCK if stop > start else -1
     for b in range(b0, b1 + 1):
-        ss = np.random.SeedSequence([SEED_BASE + 1000 * step + worker, b])
+        ss = np.random.SeedSequence([SEED_BASE + 1000 * step + worker, b] + _tag(wl))
         z = np.random.default_rng(ss).standard_normal(BLOCK, dtype=np.float32)
         a, c = max(b * BLOCK, start), min((b + 1) * BLOCK, stop)
         out[a - start: c - start] = z[a - b * BLOCK: c - b * BLOCK]
@@ -225,7 +294,7 @@ def params0_slice(wl: Workload, start: int, stop: int) -> np.ndarray:
     out = np.empty(stop - start, np.float32)
     b0, b1 = start // BLOCK, (stop - 1) // BLOCK if stop > start else -1
     for b in range(b0, b1 + 1):
-        ss = np.random.SeedSequence([SEED_BASE, 999_999, b])
+        ss = np.random.SeedSequence([SEED_BASE, 999_999, b] + _tag(wl))
         z = np.random.default_rng(ss).standard_normal(BLOCK, dtype=np.float32)
         a, c = max(b * BLOCK, start), min((b + 1) * BLOCK, stop)
         out[a - start: c - start] = z[a - b * BLOCK: c - b * BLOCK]
@@ -253,7 +322,7 @@ def state_slice(wl: Workload, what: str, start: int, stop: int,
     out = np.empty(stop - start, np.float32)
     b0, b1 = start // BLOCK, (stop - 1) // BLOCK if stop > start else -1
     for b in range(b0, b1 + 1):
-        ss = np.random.SeedSequence([SEED_BASE, 500_000 + tag, worker, b])
+        ss = np.random.SeedSequence([SEED_BASE, 500_000 + tag, worker, b] + _tag(wl))
         z = np.random.default_rng(ss).standard_normal(BLOCK, dtype=np.float32)
         a, c = max(b * BLOCK, start), min((b + 1) * BLOCK, stop)
         out[a - start: c - start] = z[a - b * BLOCK: c - b * BLOCK]
