@@ -326,6 +326,86 @@ ob_status ob_quant_int8_ef(const float* g, float* e, size_t n, int8_t* q, float*
                            uint64_t seed, uint64_t step, float* deq, float* block_err2,
                            ob_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Layerwise mixed bit widths ([BLOG] 3.2 table: a bit width and an update
+ * period per parameter type -- embeddings and transformer FFN 1 bit, CNN
+ * weights 2 bits, LayerNorm parameters FP16 every 10 steps; [BLOG] 6
+ * layerwise_bits [1, 2, 1, 16]; [TUT] "更激进的组合策略").
+ *
+ * The layers of one width form a fused buffer of their own with its own
+ * ctx (the layout above, n = that group's elements).  Width 1 uses the
+ * calls above.  Widths 2, 4 and 8 use the b-bit codec below, width 16 the
+ * FP16 codec; both run 1-bit Adam's frozen-variance update (no LAMB) with
+ * a dense m, and keep their errors in plain form (e' itself, not deferred).
+ * Their ctx needs A = cfg.align a multiple of 256 (else
+ * OB_ERR_UNSUPPORTED) and no workspace; cfg.b1, eps, lr and clip_value
+ * apply, cfg.chunk and the layers are not used.
+ *
+ * b-bit codec, per block of 256 elements (block k/256 of each worker's
+ * buffer; no block straddles two partitions since A % 256 == 0), the
+ * quantizer of [TUT] "FP32 → INT8 量化" with the width as an argument (as
+ * its GradientQuantizeINT8 example takes it):
+ *   scale = max|x| / (2^(b-1) - 1) over the block's real elements (0 if the
+ *   max is 0; a NaN never wins); q = floor(x/scale) + (u < frac) clamped to
+ *   +-(2^(b-1) - 1), a NaN codes as 0; e' = x - q*scale.
+ *   u as in ob_quant_int8 (Philox4x32-10, key = seed, counter = (i>>2,
+ *   step), word i&3) with i = w*n_pad + k for worker w's element k and
+ *   i = W*n_pad + k for the server's.
+ *   codes: [W][words_per_worker] uint32, words_per_worker = n_pad*b/32; the
+ *   field q mod 2^b of element k at bit (k*b)%32 of word (k*b)/32 (LSB
+ *   first, two's complement).  bscales: [W][n_blocks] floats,
+ *   n_blocks = n_pad/256.  Padding elements code 0 with error 0.
+ * ---------------------------------------------------------------------- */
+
+/* words_per_worker = n_pad*bits/32 and n_blocks = n_pad/256 (either may
+ * be NULL).  bits: 2, 4 or 8. */
+ob_status ob_qb_sizes(const ob_ctx* ctx, int bits, size_t* words_per_worker,
+                      size_t* n_blocks);
+
+/* e = 0 for every worker and e_s = 0 (start of the compressed phase, and
+ * the periodic reset of [BLOG] 4.1) for the codecs whose errors are kept in
+ * plain form. */
+ob_status ob_zero_errors(ob_ctx* ctx, float* const* err, float* err_s, ob_stream_t stream);
+
+/* Worker compression, all W workers:
+ *   m_w = b1*m + (1-b1)*g_w;  x = m_w + e_w (clamped if clip_value > 0)
+ *   per block: codes, bscales, e_w := x - q*scale.  m is not written. */
+ob_status ob_compress_qb(ob_ctx* ctx, int bits, const void* const* grads, const float* m,
+                         float* const* err, uint32_t* codes, float* bscales, uint64_t seed,
+                         uint64_t step, ob_stream_t stream);
+
+/* Server average and re-compression:
+ *   z = (sum over w in order, from 0, of q_w*scale_w)/W;  y = e_s + z
+ *   per block: scodes [words_per_worker], sbscales [n_blocks],
+ *   e_s := y - q*sscale. */
+ob_status ob_server_reduce_qb(ob_ctx* ctx, int bits, const uint32_t* codes,
+                              const float* bscales, float* err_s, uint32_t* scodes,
+                              float* sbscales, uint64_t seed, uint64_t step,
+                              ob_stream_t stream);
+
+/* m = q*sscale; p -= lr*(m/(sqrt(v_frozen)+eps)).  Padding: m = 0, p is
+ * not written. */
+ob_status ob_adam_step_qb(ob_ctx* ctx, int bits, const uint32_t* scodes, const float* sbscales,
+                          const float* v_frozen, float* m, float* p, ob_stream_t stream);
+
+/* FP16 codec.  send != 0 on the steps the group is exchanged (every 10th
+ * in [BLOG] 3.2); h: [W][n_pad] uint16 (IEEE binary16 bit patterns).
+ *   x = b1*m + (1-b1)*g_w + e_w (clamped if clip_value > 0)
+ *   send:  h_w = f16(x) (nearest, ties to even); e_w := x - f32(h_w)
+ *   else:  e_w := x; h untouched (may be NULL). */
+ob_status ob_compress_f16(ob_ctx* ctx, int send, const void* const* grads, const float* m,
+                          float* const* err, uint16_t* h, ob_stream_t stream);
+
+/* Sending steps only: z = (sum over w, in order, from 0, of f32(h_w))/W;
+ * y = e_s + z; hs = f16(y); e_s := y - f32(hs).  hs: [n_pad]. */
+ob_status ob_server_reduce_f16(ob_ctx* ctx, const uint16_t* h, float* err_s, uint16_t* hs,
+                               ob_stream_t stream);
+
+/* send: m = f32(hs); p -= lr*(m/(sqrt(v_frozen)+eps)).  Otherwise m = 0 and
+ * p is left as it is (hs, v_frozen, p may be NULL).  Padding: m = 0. */
+ob_status ob_adam_step_f16(ob_ctx* ctx, int send, const uint16_t* hs, const float* v_frozen,
+                           float* m, float* p, ob_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,8 @@ EXPORTS = (
     "ob_server_reduce", "ob_decompress", "ob_adam_step", "ob_lamb_step", "ob_step",
     "ob_materialize_errors", "ob_device_error", "ob_quant_int8", "ob_compress_noalloc",
     "ob_compress_signm", "ob_reset_errors", "ob_quant_int8_ef",
+    "ob_qb_sizes", "ob_zero_errors", "ob_compress_qb", "ob_server_reduce_qb", "ob_adam_step_qb",
+    "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
 )
 
 
@@ -100,6 +102,14 @@ def lib():
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
         L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
+        L.ob_qb_sizes.argtypes = [vp, i32, ct.POINTER(sz), ct.POINTER(sz)]
+        L.ob_zero_errors.argtypes = [vp, vp, vp, vp]
+        L.ob_compress_qb.argtypes = [vp, i32, vp, vp, vp, vp, vp, u64, u64, vp]
+        L.ob_server_reduce_qb.argtypes = [vp, i32, vp, vp, vp, vp, vp, u64, u64, vp]
+        L.ob_adam_step_qb.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+        L.ob_compress_f16.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+        L.ob_server_reduce_f16.argtypes = [vp, vp, vp, vp, vp]
+        L.ob_adam_step_f16.argtypes = [vp, i32, vp, vp, vp, vp, vp]
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -302,6 +312,48 @@ def ob_quant_int8_ef(g, e, q, block_scales, seed, step, deq=None, block_err2=Non
                                   _ptr(deq), _ptr(block_err2), _stream(stream)))
 
 
+def ob_qb_sizes(ctx, bits):
+    """(words_per_worker, n_blocks) of the b-bit codec."""
+    w, b = ct.c_size_t(), ct.c_size_t()
+    _check(lib().ob_qb_sizes(ctx, bits, ct.byref(w), ct.byref(b)), ctx)
+    return w.value, b.value
+
+
+def ob_zero_errors(ctx, err, err_s, stream=None):
+    _check(lib().ob_zero_errors(ctx, _ptr_array(err), _ptr(err_s), _stream(stream)), ctx)
+
+
+def ob_compress_qb(ctx, bits, grads, m, err, codes, bscales, seed, step, stream=None):
+    _check(lib().ob_compress_qb(ctx, bits, _ptr_array(grads), _ptr(m), _ptr_array(err),
+                                _ptr(codes), _ptr(bscales), seed, step, _stream(stream)), ctx)
+
+
+def ob_server_reduce_qb(ctx, bits, codes, bscales, err_s, scodes, sbscales, seed, step,
+                        stream=None):
+    _check(lib().ob_server_reduce_qb(ctx, bits, _ptr(codes), _ptr(bscales), _ptr(err_s),
+                                     _ptr(scodes), _ptr(sbscales), seed, step, _stream(stream)),
+           ctx)
+
+
+def ob_adam_step_qb(ctx, bits, scodes, sbscales, v_frozen, m, p, stream=None):
+    _check(lib().ob_adam_step_qb(ctx, bits, _ptr(scodes), _ptr(sbscales), _ptr(v_frozen), _ptr(m),
+                                 _ptr(p), _stream(stream)), ctx)
+
+
+def ob_compress_f16(ctx, send, grads, m, err, h, stream=None):
+    _check(lib().ob_compress_f16(ctx, int(bool(send)), _ptr_array(grads), _ptr(m),
+                                 _ptr_array(err), _ptr(h), _stream(stream)), ctx)
+
+
+def ob_server_reduce_f16(ctx, h, err_s, hs, stream=None):
+    _check(lib().ob_server_reduce_f16(ctx, _ptr(h), _ptr(err_s), _ptr(hs), _stream(stream)), ctx)
+
+
+def ob_adam_step_f16(ctx, send, hs, v_frozen, m, p, stream=None):
+    _check(lib().ob_adam_step_f16(ctx, int(bool(send)), _ptr(hs), _ptr(v_frozen), _ptr(m),
+                                  _ptr(p), _stream(stream)), ctx)
+
+
 # ---------------------------------------------------------------------------
 # One simulated data-parallel job
 # ---------------------------------------------------------------------------
@@ -405,3 +457,126 @@ class OneBitOptimizer:
         self.materialize_m(stream)  # the sign form is lost once sscales are cleared
         ob_materialize_errors(self.ctx, self.err, self.bits, self.scales, self.err_s,
                               self.sbits, self.sscales, stream)
+
+
+class CodecGroup:
+    """One group of layerwise mixed widths compressed with the b-bit codec
+    (bits 2, 4, 8) or the FP16 codec (bits 16, exchanged on every
+    `period`-th compressed step), with 1-bit Adam's frozen-variance update.
+    Buffers: m, v, p, err[W], err_s, and the messages (codes/bscales and
+    scodes/sbscales, or h and hs)."""
+
+    def __init__(self, n, W, bits, align=4096, grad_dtype="f32", device="cuda", period=10,
+                 seed=1234, reset_interval=0, **hp):
+        import torch
+        if bits not in (2, 4, 8, 16):
+            raise ValueError(f"bits = {bits}: the codec groups take 2, 4, 8 or 16")
+        self.bits, self.period, self.seed = bits, period, seed
+        self.reset_interval = reset_interval
+        self.grad_dtype = grad_dtype
+        self.ctx = ob_init(n, W, align, align,
+                           OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32, None, **hp)
+        lay = ob_get_layout(self.ctx)
+        self.layout = lay
+        self.n, self.W, self.n_pad = n, W, lay["n_pad"]
+        z = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device=device)
+        self.m, self.v, self.p = z(self.n_pad), z(self.n_pad), z(self.n_pad)
+        self.err = [z(self.n_pad) for _ in range(W)]
+        self.err_s = z(self.n_pad)
+        if bits == 16:
+            self.h = z(W, self.n_pad, dt=torch.int16)
+            self.hs = z(self.n_pad, dt=torch.int16)
+        else:
+            words, nblk = ob_qb_sizes(self.ctx, bits)
+            self.codes = z(W, words, dt=torch.int32)
+            self.bscales = z(W, nblk)
+            self.scodes = z(words, dt=torch.int32)
+            self.sbscales = z(nblk)
+        nbytes = ob_workspace_bytes(self.ctx)  # the warmup step's scratch
+        self.workspace = torch.zeros((nbytes + 255) // 256 * 256 // 4, dtype=torch.float32,
+                                     device=device)
+        ob_set_workspace(self.ctx, self.workspace, nbytes)
+        self.t = 0
+
+    def close(self):
+        if self.ctx:
+            ob_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def grad_buffers(self):
+        import torch
+        dt = torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
+        return [torch.zeros(self.n_pad, dtype=dt, device=self.m.device) for _ in range(self.W)]
+
+    def warmup_step(self, grads, stream=None):
+        ob_warmup_step(self.ctx, grads, self.m, self.v, self.p, OB_MODE_ADAM, None, stream)
+
+    def begin_compression(self, stream=None):
+        ob_zero_errors(self.ctx, self.err, self.err_s, stream)
+        self.t = 0
+
+    def compressed_step(self, grads, stream=None):
+        if self.reset_interval and self.t and self.t % self.reset_interval == 0:
+            ob_zero_errors(self.ctx, self.err, self.err_s, stream)
+        self.t += 1
+        if self.bits == 16:
+            send = self.t % self.period == 0
+            ob_compress_f16(self.ctx, send, grads, self.m, self.err, self.h, stream)
+            if send:
+                ob_server_reduce_f16(self.ctx, self.h, self.err_s, self.hs, stream)
+            ob_adam_step_f16(self.ctx, send, self.hs, self.v, self.m, self.p, stream)
+            return
+        b = self.bits
+        ob_compress_qb(self.ctx, b, grads, self.m, self.err, self.codes, self.bscales,
+                       self.seed, self.t, stream)
+        ob_server_reduce_qb(self.ctx, b, self.codes, self.bscales, self.err_s, self.scodes,
+                            self.sbscales, self.seed, self.t, stream)
+        ob_adam_step_qb(self.ctx, b, self.scodes, self.sbscales, self.v, self.m, self.p, stream)
+
+
+class MixedOptimizer:
+    """Layerwise mixed bit widths: one group per width, each a fused buffer
+    of its own (the "1bit Adam" write-up's §3.2 table: 1 bit for embeddings
+    and dense layers, 2 for convolution weights, FP16 every 10th step for
+    normalisation parameters).  `groups` is a list of (bits, n,
+    layer_offsets); width 1 runs the scaled-sign 1-bit Adam
+    (OneBitOptimizer), the others a CodecGroup whose uniforms use the key
+    seed + bits.  Steps run the groups in list order."""
+
+    def __init__(self, groups, W, chunk=1 << 20, align=4096, grad_dtype="f32", device="cuda",
+                 period=10, seed=1234, sign_momentum=False, reset_interval=0, **hp):
+        self.groups = []
+        for bits, n, off in groups:
+            if bits == 1:
+                g = OneBitOptimizer(n, W, chunk, align, grad_dtype, off, device=device,
+                                    sign_momentum=sign_momentum,
+                                    reset_interval=reset_interval, **hp)
+            else:
+                g = CodecGroup(n, W, bits, align, grad_dtype, device, period, seed + bits,
+                               reset_interval, **hp)
+            self.groups.append((bits, g))
+
+    def close(self):
+        for _, g in self.groups:
+            g.close()
+
+    def grad_buffers(self):
+        return [g.grad_buffers() for _, g in self.groups]
+
+    def warmup_step(self, grads, stream=None):
+        for (_, g), gr in zip(self.groups, grads):
+            g.warmup_step(gr, stream)
+
+    def begin_compression(self, stream=None):
+        for _, g in self.groups:
+            g.begin_compression(stream)
+
+    def compressed_step(self, grads, stream=None):
+        for (_, g), gr in zip(self.groups, grads):
+            g.compressed_step(gr, stream)

@@ -9,45 +9,12 @@
 // elements draws one Philox4x32-10 output (four 32-bit words) from counter
 // (k>>2, step).
 //
-// Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel random
-// numbers: as easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64-bit
-// products with multipliers 0xD2511F53 and 0xCD9E8D57, the key advanced by
-// 0x9E3779B9 and 0xBB67AE85 between rounds.
+// Philox4x32-10 is in philox.cuh.
 #include "ob_internal.cuh"
+#include "philox.cuh"
 
 namespace ob {
 namespace {
-
-// Round keys of Philox4x32-10: key k advanced by (0x9E3779B9, 0xBB67AE85)
-// before every round but the first; computed once per thread.
-struct PhiloxKeys {
-  uint32_t k0[10], k1[10];
-};
-
-__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
-  PhiloxKeys K;
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    K.k0[r] = k0 + (uint32_t)r * 0x9E3779B9u;
-    K.k1[r] = k1 + (uint32_t)r * 0xBB67AE85u;
-  }
-  return K;
-}
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& K) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
-    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k0[r], (uint32_t)p1,
-                   (uint32_t)(p0 >> 32) ^ c.w ^ K.k1[r], (uint32_t)p0);
-  }
-  return c;
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
-  return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
-}
 
 // Quantizes the 4 values x of group `grp` (elements 4*grp .. 4*grp+3);
 // dq receives q*scale.

@@ -261,6 +261,54 @@ struct WarmupArgs {
   int warmup_steps;
 };
 
+// Layerwise mixed widths: the b-bit codec (blocks of 256, codes packed BITS
+// to an element) and the FP16 codec.
+struct QbCompressArgs {
+  const void* g[OB_MAX_WORKERS];
+  float* e[OB_MAX_WORKERS];
+  const float* m;
+  uint32_t* codes;     // [W][row_words]
+  float* scales;       // [W][n_pad/256]
+  uint64_t n, n_pad, row_words, seed, step;
+  uint32_t W;
+  float b1, clip;
+};
+
+struct QbServerArgs {
+  const uint32_t* codes;
+  const float* scales;
+  float* e_s;
+  uint32_t* scodes;
+  float* sscales;
+  uint64_t n, n_pad, row_words, seed, step;
+  uint32_t W;
+};
+
+struct QbUpdateArgs {
+  const uint32_t* scodes;
+  const float* sscales;
+  const float* v;
+  float* m;
+  float* p;
+  uint64_t n, n_pad;
+  float lr, eps;
+};
+
+struct F16Args {
+  const void* g[OB_MAX_WORKERS];
+  float* e[OB_MAX_WORKERS];
+  float* m;            // read by the worker kernel, written by the update
+  uint16_t* h;         // [W][n_pad] worker messages
+  uint16_t* hs;        // [n_pad] server message
+  float* e_s;
+  const float* v;
+  float* p;
+  uint64_t n, n_pad;
+  uint32_t W;
+  int send;
+  float b1, clip, lr, eps;
+};
+
 // ---------------------------------------------------------------------------
 // Launchers.  Each sizes its grid to the CTAs that fit on the device at once
 // (SM count x resident CTAs per SM, at most one CTA per tile) and returns
@@ -298,6 +346,13 @@ cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
                               cudaStream_t s);
 cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_reset_errors(const MaterializeArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_qb_compress(const QbCompressArgs& a, int bits, bool bf16, int sms,
+                               cudaStream_t s);
+cudaError_t launch_qb_server(const QbServerArgs& a, int bits, int sms, cudaStream_t s);
+cudaError_t launch_qb_adam(const QbUpdateArgs& a, int bits, int sms, cudaStream_t s);
+cudaError_t launch_f16_compress(const F16Args& a, bool bf16, int sms, cudaStream_t s);
+cudaError_t launch_f16_server(const F16Args& a, int sms, cudaStream_t s);
+cudaError_t launch_f16_adam(const F16Args& a, int sms, cudaStream_t s);
 cudaError_t launch_warmup_adam(const WarmupArgs& a, bool bf16, int sms,
                                cudaStream_t s);
 cudaError_t launch_warmup_lamb(const WarmupArgs& a, bool bf16, int sms,

@@ -117,3 +117,43 @@ def test_null_ctx():
     assert lib.ob_get_layout(None, None) == ob.OB_ERR_INVALID
     assert lib.ob_compress(None, None, None, None, None, None, None, None) == ob.OB_ERR_INVALID
     assert b"NULL" in lib.ob_last_error(None)
+
+
+def test_codec_calls_check_before_cuda():
+    """The mixed-width codec calls reject a bad width, an alignment A that
+    is not a multiple of 256, NULL and misaligned pointers on the host."""
+    ctx = ob.ob_init(10_000, 2, 4096)
+    assert ob.ob_qb_sizes(ctx, 2) == (ob.ob_get_layout(ctx)["n_pad"] * 2 // 32,
+                                      ob.ob_get_layout(ctx)["n_pad"] // 256)
+    for bits in (0, 1, 3, 16):
+        with pytest.raises(ob.OBError) as ei:
+            ob.ob_compress_qb(ctx, bits, [16, 16], 16, [16, 16], 16, 16, 1, 1, stream=0)
+        assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_compress_qb(ctx, 2, [16, 24], 16, [16, 16], 16, 16, 1, 1, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_server_reduce_qb(ctx, 2, 16, 18, 16, 16, 16, 1, 1, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_adam_step_qb(ctx, 4, 16, 16, None, 16, 16, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_compress_f16(ctx, 1, [16, 16], 16, [16, 16], None, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_server_reduce_f16(ctx, 16, 16, 8, stream=0)
+    assert ei.value.status == ob.OB_ERR_ALIGN
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_zero_errors(ctx, [16, None], 16, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    ob.ob_destroy(ctx)
+    ctx = ob.ob_init(10_000, 2, 4096, align=32)
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_compress_qb(ctx, 2, [16, 16], 16, [16, 16], 16, 16, 1, 1, stream=0)
+    assert ei.value.status == ob.OB_ERR_UNSUPPORTED
+    assert "256" in ob.ob_last_error(ctx)
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_adam_step_f16(ctx, 0, None, None, 16, None, stream=0)
+    assert ei.value.status == ob.OB_ERR_UNSUPPORTED
+    ob.ob_destroy(ctx)
