@@ -14,7 +14,8 @@ bounded sample, an end-to-end number through host buffers, and the SM
 clocks seen during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload bert-base|flat-1m|gpt-1.3b|bert-large]
+                  [--workload bert-base|flat-1m|gpt-1.3b|bert-large|int8|flat|
+                              resnet50-mixed]
 
 N > 1 runs under torchrun as independent replicas (one per GPU, no
 collective on the data path); timing is the max over ranks.
@@ -574,6 +575,220 @@ def run_ours(args, wl):
     opt.close()
 
 
+def mixed_bytes(bits, W, G, send=True):
+    """Algorithmic bytes per real element of one mixed-width group, per
+    kernel: b-bit codes are b/8 bytes per element plus a 4-byte scale per
+    256; FP16 messages are 2 bytes, exchanged on sending steps only."""
+    if bits == 16:
+        comp = 4 + W * (G + 8 + (2 if send else 0))
+        serv = (W * 2 + 8 + 2) if send else 0
+        upd = (2 + 4 + 8 + 4) if send else 4
+    else:
+        code = bits / 8 + 4 / 256
+        comp = 4 + W * (G + 8 + code)
+        serv = W * code + 8 + code
+        upd = code + 4 + 8 + 4
+    return {"compress": comp, "server": serv, "update": upd, "total": comp + serv + upd}
+
+
+def run_mixed(args):
+    """Layerwise mixed bit widths on the ResNet-50 parameter list: 1-bit
+    scaled sign for the fc layer, the 2-bit block codec for the
+    convolutions, FP16 every 10th step for the batch-norm parameters, W = 8.
+    One step = one compressed step of every group."""
+    import torch
+
+    import momentum_compression_gb300 as ob
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    groups = synth.mixed_groups(W=args.W or 8)
+    W = groups[0][1].W
+    sign_m = not args.dense_m
+    specs = [(bits, wl.n, wl.layer_offsets) for bits, wl in groups]
+    opt = ob.MixedOptimizer(specs, W, chunk=1 << 20, period=synth.NORM_PERIOD, seed=1234,
+                            device=device, sign_momentum=sign_m, **synth.ADAM_HP)
+    n_tot = sum(wl.n for _, wl in groups)
+    log(f"[bench] rank {rank}: resnet50-mixed n={n_tot} W={W} groups "
+        + ", ".join(f"{b}-bit {wl.n}" for b, wl in groups))
+    gsets = [[device_grads(torch, wl, g.n_pad, s, torch.float32, device)
+              for (_, wl), (_, g) in zip(groups, opt.groups)] for s in range(2)]
+    for _, g in opt.groups:
+        g.p.normal_(0.0, 0.02)
+    for t in range(3):
+        opt.warmup_step(gsets[t % 2])
+    opt.begin_compression()
+    for t in range(args.warmup):
+        opt.compressed_step(gsets[t % 2])
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    ng = len(groups)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ng + 1)] for _ in range(K)]
+    kev = {}  # per-kernel events of the 2-bit group's step
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid)
+    sends = 0
+    with ClockSampler(uuid) as clk:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for t in range(K):
+            e = ev[t]
+            e[0].record(stream)
+            for i, ((bits, _), (_, g)) in enumerate(zip(groups, opt.groups)):
+                if bits == 2:
+                    # the group's three calls, with an event between each
+                    ke = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    g.t += 1
+                    ob.ob_compress_qb(g.ctx, 2, gsets[t % 2][i], g.m, g.err, g.codes, g.bscales,
+                                      g.seed, g.t)
+                    ke[0].record(stream)
+                    ob.ob_server_reduce_qb(g.ctx, 2, g.codes, g.bscales, g.err_s, g.scodes,
+                                           g.sbscales, g.seed, g.t)
+                    ke[1].record(stream)
+                    ob.ob_adam_step_qb(g.ctx, 2, g.scodes, g.sbscales, g.v, g.m, g.p)
+                    ke[2].record(stream)
+                    kev[t] = (e[i], ke)
+                else:
+                    if bits == 16 and (g.t + 1) % g.period == 0:
+                        sends += 1
+                    g.compressed_step(gsets[t % 2][i])
+                e[i + 1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), pg, device)
+    ms = total_ms / K
+    group_ms = {f"{bits}-bit": sum(ev[t][i].elapsed_time(ev[t][i + 1]) for t in range(K)) / K
+                for i, (bits, _) in enumerate(groups)}
+    kq = {}
+    for name, j in (("compress", 0), ("server", 1), ("update", 2)):
+        kq[name] = sum((kev[t][0] if j == 0 else kev[t][1][j - 1]).elapsed_time(kev[t][1][j])
+                       for t in range(K)) / K
+    nq = dict(groups)[2].n
+    bq = mixed_bytes(2, W, 4)
+    kq_gbs = {k: bq[k] * nq / (kq[k] * 1e-3) / 1e9 for k in kq}
+    launches = K * (5 + 3 + 2) + sends
+    peak, peak_kind = measured_peak()
+    frac_send = sends / K
+    total_bytes = 0.0
+    for bits, wl in groups:
+        if bits == 1:
+            total_bytes += bytes_per_element(W, 4, False, sign_m)["total"] * wl.n
+        elif bits == 16:
+            total_bytes += (frac_send * mixed_bytes(16, W, 4, True)["total"] +
+                            (1 - frac_send) * mixed_bytes(16, W, 4, False)["total"]) * wl.n
+        else:
+            total_bytes += mixed_bytes(bits, W, 4)["total"] * wl.n
+
+    # end to end through host buffers: every step copies all groups' W
+    # gradients host -> device from pinned memory, runs the step and reads
+    # all parameters back, in order on one stream
+    host_g = [[torch.empty_like(x, device="cpu").pin_memory() for x in gs] for gs in gsets[0]]
+    for hg, dg in zip(host_g, gsets[0]):
+        for h, d in zip(hg, dg):
+            h.copy_(d)
+    host_p = [torch.empty(g.n_pad, pin_memory=True) for _, g in opt.groups]
+
+    def e2e_step(t):
+        for hg, dg in zip(host_g, gsets[t % 2]):
+            for h, d in zip(hg, dg):
+                d.copy_(h, non_blocking=True)
+        opt.compressed_step(gsets[t % 2])
+        for hp_, (_, g) in zip(host_p, opt.groups):
+            hp_.copy_(g.p, non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize()
+    K2 = max(3, min(K, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for t in range(K2):
+        e2e_step(t)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, pg, device)
+    h2d = sum(x.numel() * x.element_size() for hg in host_g for x in hg)
+    d2h = sum(x.numel() * 4 for x in host_p)
+    e2e = {"value": job_rate(n_tot, world, e2e_ms), "unit": "elements/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "pipelined": False}
+    del host_g, host_p
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = mixed_oracle_sample(groups, steps=3)
+    if rank != 0:
+        opt.close()
+        return
+    achieved = kq_gbs["compress"]
+    line = {
+        "metric": "layerwise mixed-width compressed step elements/s (1-bit / 2-bit / FP16 "
+                  "groups)", "value": job_rate(n_tot, world, ms), "unit": "elements/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "resnet50-mixed: ResNet-50 parameter list (161 tensors, "
+                               f"{n_tot:,} params), W={W}; fc 1-bit, convolutions 2-bit "
+                               "(block 256), batch norms FP16 every 10th step",
+                   "groups": {f"{b}-bit": wl.n for b, wl in groups}, "W": W,
+                   "momentum_1bit": "sign form" if sign_m else "dense fp32",
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "l2": f"inputs larger than L2 ({total_bytes / 1e9:.1f} GB touched per step);"
+                         " no flush"},
+        "gbs": total_bytes / (ms * 1e-3) / 1e9,
+        "group_ms": group_ms,
+        "kernels_ms_2bit": kq, "kernels_gbs_2bit": kq_gbs,
+        "roofline": {"bound": "hbm", "kernel": "qb_compress (2-bit group)", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "bytes_per_element": bq["compress"],
+                     "traffic": None},
+        "step_roofline_frac": total_bytes / (ms * 1e-3) / 1e9 / peak,
+        "gpu_launches": launches, "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    opt.close()
+
+
+def mixed_oracle_sample(groups, steps):
+    """The oracle's mixed step on a bounded sample: the first 2^22 elements
+    of each group (all of a smaller one), W workers, `steps` compressed
+    steps; elements/s over the sampled elements."""
+    import oracle as O
+    total, t_all, names = 0, 0.0, []
+    for bits, wl in groups:
+        sample = min(1 << 22, wl.n)
+        lay = O.Layout(sample, wl.W, wl.align, wl.chunk)
+        st = O.State(lay)
+        st.v[:sample] = synth.state_slice(wl, "v", 0, sample)
+        st.m[:sample] = synth.state_slice(wl, "m", 0, sample)
+        grads = []
+        for w in range(wl.W):
+            a = np.zeros(lay.n_pad, np.float32)
+            a[:sample] = synth.grad_slice(wl, 0, w, 0, sample)
+            grads.append(a)
+        t0 = time.perf_counter()
+        for t in range(1, steps + 1):
+            O.codec_step(st, grads, wl.hp, bits, t, 1234 + bits, period=synth.NORM_PERIOD)
+        t_all += time.perf_counter() - t0
+        total += sample * steps
+        names.append(f"{sample} of the {bits}-bit group")
+    return {"value": total / t_all, "unit": "elements/s", "cores": 1, "kind": "oracle",
+            "sample": f"{', '.join(names)}, W={groups[0][1].W}, {steps} compressed steps "
+                      f"({t_all:.1f} s)", "cpu": cpu_model()}
+
+
 def wl_label(wl):
     kind = "1-bit LAMB" if wl.mode == "lamb" else "1-bit Adam"
     shape = f"{wl.n_layers} tensors" if wl.tensors else "flat"
@@ -601,6 +816,24 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.impl == "ours" and args.workload == "int8":
         run_int8(args)
+        return
+    if args.workload == "resnet50-mixed":
+        if args.impl == "reference":
+            world, rank, _ = dist_env()
+            if rank == 0:
+                cpu = mixed_oracle_sample(synth.mixed_groups(), steps=min(max(args.steps, 1), 3))
+                print(json.dumps({
+                    "impl": "reference", "metric": "layerwise mixed-width compressed step "
+                    "elements/s (1-bit / 2-bit / FP16 groups)", "value": cpu["value"],
+                    "unit": "elements/s", "n_gpus": args.gpus, "steps": args.steps,
+                    "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                    "config": {"workload": "resnet50-mixed (oracle on a sample)"},
+                    "cpu_baseline": cpu,
+                    "e2e": {"value": cpu["value"], "unit": "elements/s",
+                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+        else:
+            run_mixed(args)
         return
     if args.workload == "flat":
         wl = synth.workload("flat", n=args.n or (1 << 24), W=args.W or 8,

@@ -208,3 +208,105 @@ def test_mixed_optimizer_matches_oracle():
                 assert_bits_equal(host(g.m), st.m, f"{what}: m")
                 assert_bits_equal(host(g.err_s), st.e_s, f"{what}: e_s")
     opt.close()
+
+
+def _torch_state(g, n, seed):
+    """m ~ N(0, 1e-3), v ~ |N(0, 1e-6)| + 1e-12, p ~ N(0, 0.02), errors
+    ~ N(0, 1e-4), drawn on the GPU by torch's seeded generator (padding 0)."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    r = lambda s: torch.randn(n, generator=gen, device="cuda") * s
+    g.m[:n] = r(1e-3)
+    g.v[:n] = r(1e-6).abs() + 1e-12
+    g.p[:n] = r(0.02)
+    for e in g.err:
+        e[:n] = r(1e-4)
+    g.err_s[:n] = r(1e-4)
+
+
+@pytest.mark.slow
+def test_resnet50_mixed_full_size():
+    """The ResNet-50 mixed workload at W = 8 in bench.py's configuration.
+    2-bit group (23.5 M elements): one step on the GPU, the oracle on
+    sampled blocks of 256 -- a block's step reads only its own elements of
+    every worker, the server and the update -- the first, one in the
+    middle, the last real one and one of the padding tail.  FP16 group
+    (53 k elements): a sending step, checked whole."""
+    groups = synth.mixed_groups(W=8)
+    W = 8
+    specs = [(bits, wl.n, wl.layer_offsets) for bits, wl in groups]
+    opt = ob.MixedOptimizer(specs, W, chunk=1 << 20, period=synth.NORM_PERIOD, seed=1234,
+                            **synth.ADAM_HP)
+    gens = {}
+    for (bits, wl), (_, g) in zip(groups, opt.groups):
+        if bits == 1:
+            continue
+        _torch_state(g, wl.n, 77 + bits)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(synth.SEED_BASE + bits)
+        sizes = torch.tensor([s for _, s, _ in wl.tensors], device="cuda")
+        std = torch.zeros(g.n_pad, device="cuda")
+        std[: wl.n] = torch.repeat_interleave(
+            torch.tensor(wl.layer_std, dtype=torch.float32, device="cuda"), sizes)
+        gens[bits] = [torch.randn(g.n_pad, generator=gen, device="cuda") * std for _ in range(W)]
+    hp = dict(synth.ADAM_HP)
+
+    # 2-bit group: sampled blocks
+    wl2, g2 = dict(groups)[2], dict(opt.groups)[2]
+    lay2 = O.Layout(wl2.n, W, 4096, 4096)
+    assert lay2.n_pad == g2.n_pad
+    nblk = g2.n_pad // 256
+    picks = sorted({0, nblk // 2, (wl2.n - 1) // 256, nblk - 1})
+    before = {}
+    for b in picks:
+        s = slice(256 * b, 256 * b + 256)
+        before[b] = dict(m=host(g2.m[s]).copy(), v=host(g2.v[s]).copy(), p=host(g2.p[s]).copy(),
+                         e_s=host(g2.err_s[s]).copy(),
+                         e=[host(e[s]).copy() for e in g2.err],
+                         g=[host(x[s]).copy() for x in gens[2]])
+    # FP16 group: whole, a sending step (t = 10)
+    wl16, g16 = dict(groups)[16], dict(opt.groups)[16]
+    lay16 = O.Layout(wl16.n, W, 4096, 4096)
+    st16 = O.State(lay16)
+    st16.m[:], st16.v[:], st16.p[:] = host(g16.m), host(g16.v), host(g16.p)
+    st16.e_s[:] = host(g16.err_s)
+    for w in range(W):
+        st16.e[w][:] = host(g16.err[w])
+    g16h = [host(x).copy() for x in gens[16]]
+
+    g2.compressed_step(gens[2])
+    g16.t = 9
+    g16.compressed_step(gens[16])
+    torch.cuda.synchronize()
+
+    for b, d in before.items():
+        s = slice(256 * b, 256 * b + 256)
+        k0 = 256 * b
+        codes, scs = [], []
+        for w in range(W):
+            c, sc = O.qb_compress_worker(lay2, 2, d["g"][w], d["m"], d["e"][w], hp["b1"], w,
+                                         g2.seed, 1, k0=k0, length=256)
+            codes.append(c)
+            scs.append(sc)
+            assert_bits_equal(host(g2.codes[w, 16 * b: 16 * b + 16]).view(np.uint32), c,
+                              f"block {b} codes of worker {w}")
+            assert_bits_equal(host(g2.bscales[w, b: b + 1]), sc, f"block {b} scale {w}")
+            assert_bits_equal(host(g2.err[w][s]), d["e"][w], f"block {b} e[{w}]")
+        sc_, ss_ = O.qb_server(lay2, 2, np.stack(codes), np.stack(scs), d["e_s"], g2.seed, 1,
+                               k0=k0, length=256)
+        assert_bits_equal(host(g2.scodes[16 * b: 16 * b + 16]).view(np.uint32), sc_,
+                          f"block {b} server codes")
+        assert_bits_equal(host(g2.sbscales[b: b + 1]), ss_, f"block {b} server scale")
+        assert_bits_equal(host(g2.err_s[s]), d["e_s"], f"block {b} e_s")
+        m, p = d["m"].copy(), d["p"].copy()
+        O.qb_adam(lay2, 2, sc_, ss_, d["v"], hp["eps"], hp["lr"], m, p, k0=k0, length=256)
+        assert_bits_equal(host(g2.m[s]), m, f"block {b} m")
+        assert_bits_equal(host(g2.p[s]), p, f"block {b} p")
+
+    O.codec_step(st16, g16h, hp, 16, 10, g16.seed, period=synth.NORM_PERIOD)
+    assert_bits_equal(host(g16.p), st16.p, "FP16 group p")
+    assert_bits_equal(host(g16.m), st16.m, "FP16 group m")
+    assert_bits_equal(host(g16.err_s), st16.e_s, "FP16 group e_s")
+    for w in range(W):
+        assert_bits_equal(host(g16.err[w]), st16.e[w], f"FP16 group e[{w}]")
+    opt.close()
