@@ -56,20 +56,40 @@ struct CodeSlot {
   __device__ static int shift(int lane) { return 4 * BITS * (lane % kLPW); }
 };
 
-// Signed field c of the lane's group from its code word.
+// Signed field c (two's complement, BITS wide) of a code word already
+// shifted to the lane's first field, as a float: the field is sign-extended
+// by bfe.s32 and converted exactly through 1.5*2^23 (|q| < 2^22), which
+// keeps the conversion on the integer and FMA pipes.
 template <int BITS>
-__device__ __forceinline__ float code_of(uint32_t word, int lane, int c) {
-  const uint32_t f = (word >> (CodeSlot<BITS>::shift(lane) + BITS * c)) & CodeSlot<BITS>::kMask;
-  return (float)((int32_t)(f << (32 - BITS)) >> (32 - BITS));
+__device__ __forceinline__ float code_val(uint32_t v, int c) {
+  int32_t q;
+  asm("bfe.s32 %0, %1, %2, %3;" : "=r"(q) : "r"(v), "r"(BITS * c), "r"(BITS));
+  return __fsub_rn(__int_as_float(0x4B400000 + q), 12582912.0f);
 }
 
 // Quantises the lane's 8 values of one block (x, nv real values per half)
 // with error feedback; writes the code words (whole words, by the lanes
 // that own them), the block scale and the residual e' (padding 0).
-template <int BITS>
+// Round keys of the quantizer's Philox: held in registers (hoisted, 20 of
+// them) or formed round by round from the seed.
+struct KeysHoisted {
+  PhiloxKeys K;
+  __device__ explicit KeysHoisted(uint64_t seed)
+      : K(philox_keys((uint32_t)seed, (uint32_t)(seed >> 32))) {}
+  __device__ uint4 operator()(uint4 c) const { return philox4x32_10(c, K); }
+};
+
+struct KeysRolling {
+  uint32_t k0, k1;
+  __device__ explicit KeysRolling(uint64_t seed)
+      : k0((uint32_t)seed), k1((uint32_t)(seed >> 32)) {}
+  __device__ uint4 operator()(uint4 c) const { return philox4x32_10_rk(c, k0, k1); }
+};
+
+template <int BITS, class Keys>
 __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (&nv)[2],
                                                uint64_t u_index0, uint64_t step,
-                                               const PhiloxKeys& K, int lane,
+                                               const Keys& keys, int lane,
                                                uint32_t* __restrict__ codes, float* scale_out,
                                                float4 (&e_out)[2]) {
   constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
@@ -89,7 +109,11 @@ __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (
   for (int h = 0; h < 2; ++h) {
     const uint64_t ui = u_index0 + 128 * h + 4 * lane;  // a multiple of 4
     uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-    if (nv[h] > 0 && scale != 0.0f) rnd = philox_group(ui >> 2, step, K);
+    if (nv[h] > 0 && scale != 0.0f) {
+      const uint64_t grp = ui >> 2;
+      rnd = keys(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
+                            (uint32_t)(step >> 32)));
+    }
     uint32_t piece = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -118,13 +142,12 @@ __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (
 // ---------------------------------------------------------------------------
 
 template <bool BF16, int BITS>
-__global__ void __launch_bounds__(kThreads)
-    k_qb_compress(const QbCompressArgs A) {
+__global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArgs A) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
-  const PhiloxKeys K = philox_keys((uint32_t)A.seed, (uint32_t)(A.seed >> 32));
   const float ob1 = __fsub_rn(1.0f, A.b1);
+  const KeysHoisted keys(A.seed);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 mv[2], gv[2], ev[2];
@@ -162,7 +185,7 @@ __global__ void __launch_bounds__(kThreads)
           f4at(x[h], c) = c < nv[h] ? xv : 0.0f;
         }
       float4 r[2];
-      quantize_block<BITS>(x, nv, (uint64_t)w * A.n_pad + b * 256, A.step, K, lane,
+      quantize_block<BITS>(x, nv, (uint64_t)w * A.n_pad + b * 256, A.step, keys, lane,
                            A.codes + (uint64_t)w * A.row_words + b * CodeSlot<BITS>::kBlockWords,
                            A.scales + (uint64_t)w * nblk + b, r);
 #pragma unroll
@@ -178,14 +201,14 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int BITS>
+template <int BITS, class Keys>
 __global__ void __launch_bounds__(kThreads) k_qb_server(const QbServerArgs A) {
   using S = CodeSlot<BITS>;
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
-  const PhiloxKeys K = philox_keys((uint32_t)A.seed, (uint32_t)(A.seed >> 32));
   const float fW = (float)A.W;
+  const Keys keys(A.seed);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 es[2], z[2];
@@ -215,11 +238,12 @@ __global__ void __launch_bounds__(kThreads) k_qb_server(const QbServerArgs A) {
       for (int i = 0; i < 8; ++i) {
         if (w0 + i < A.W) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t v = wd[i][h] >> S::shift(lane);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              f4at(z[h], c) =
-                  __fadd_rn(f4get(z[h], c), __fmul_rn(code_of<BITS>(wd[i][h], lane, c), sc[i]));
+              f4at(z[h], c) = __fadd_rn(f4get(z[h], c), __fmul_rn(code_val<BITS>(v, c), sc[i]));
+          }
         }
       }
     }
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) k_qb_server(const QbServerArgs A) {
         f4at(y[h], c) =
             c < nv[h] ? __fadd_rn(f4get(es[h], c), __fdiv_rn(f4get(z[h], c), fW)) : 0.0f;
     float4 r[2];
-    quantize_block<BITS>(y, nv, (uint64_t)A.W * A.n_pad + b * 256, A.step, K, lane,
+    quantize_block<BITS>(y, nv, (uint64_t)A.W * A.n_pad + b * 256, A.step, keys, lane,
                          A.scodes + b * S::kBlockWords, A.sscales + b, r);
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -262,10 +286,11 @@ __global__ void __launch_bounds__(kThreads) k_qb_adam(const QbUpdateArgs A) {
     for (int h = 0; h < 2; ++h) {
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
       float4 mv;
+      const uint32_t v = wd[h] >> S::shift(lane);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (c < nv[h]) {
-          const float mk = __fmul_rn(code_of<BITS>(wd[h], lane, c), sc);
+          const float mk = __fmul_rn(code_val<BITS>(v, c), sc);
           const float u = __fdiv_rn(mk, __fadd_rn(__fsqrt_rn(f4get(vv[h], c)), A.eps));
           f4at(pv[h], c) = __fsub_rn(f4get(pv[h], c), __fmul_rn(A.lr, u));
           f4at(mv, c) = mk;
@@ -422,11 +447,21 @@ cudaError_t launch_qb_compress(const QbCompressArgs& a, int bits, bool bf16, int
   return cudaGetLastError();
 }
 
+// The server forms its Philox round keys round by round: with 80 registers
+// it keeps 3 CTAs per SM, where hoisted keys (100 registers) allow 2 and
+// measured 15% slower.  The worker kernel keeps them hoisted: there the
+// extra additions cost more than the occupancy gains.
+template <int B>
+void run_qb_server(const QbServerArgs& a, int sms, uint64_t ctas, cudaStream_t s) {
+  k_qb_server<B, KeysRolling>
+      <<<grid_for(k_qb_server<B, KeysRolling>, sms, ctas), kThreads, 0, s>>>(a);
+}
+
 cudaError_t launch_qb_server(const QbServerArgs& a, int bits, int sms, cudaStream_t s) {
   const uint64_t ctas = warp_ctas(a.n_pad);
-  if (bits == 2) k_qb_server<2><<<grid_for(k_qb_server<2>, sms, ctas), kThreads, 0, s>>>(a);
-  else if (bits == 4) k_qb_server<4><<<grid_for(k_qb_server<4>, sms, ctas), kThreads, 0, s>>>(a);
-  else k_qb_server<8><<<grid_for(k_qb_server<8>, sms, ctas), kThreads, 0, s>>>(a);
+  if (bits == 2) run_qb_server<2>(a, sms, ctas, s);
+  else if (bits == 4) run_qb_server<4>(a, sms, ctas, s);
+  else run_qb_server<8>(a, sms, ctas, s);
   return cudaGetLastError();
 }
 
