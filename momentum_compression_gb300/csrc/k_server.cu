@@ -57,7 +57,9 @@ __device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, uint32_t 
   return W <= 8 ? __fdiv_rn(z, (float)W) : z;
 }
 
-template <bool LAMB>
+// WT: the worker count when it is a compile-time 4 or 8 (the tables' and
+// loops' bounds are then constants), 0 for any other W.
+template <bool LAMB, uint32_t WT>
 __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo& G = A.geo;
@@ -118,14 +120,15 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 
   // ------------------------------------------------------------ consumers
   const int p = tid;
+  const uint32_t Wc = WT ? WT : G.W;
   // scales of the first tile
-  const uint32_t W8 = G.W < 8 ? G.W : 8;
-  if (blockIdx.x < G.n_tiles && (uint32_t)p < G.W) {
+  const uint32_t W8 = Wc < 8 ? Wc : 8;
+  if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc) {
     const Tile tl = decode_tile(G, blockIdx.x);
     s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
   }
   named_sync(1, kSConsumers);
-  if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], G.W, p);
+  if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     // prefetch the next tile's worker scales
     float next_sc = 0.0f;
     const uint32_t Tn = T + gridDim.x;
-    if (Tn < G.n_tiles && (uint32_t)p < G.W)
+    if (Tn < G.n_tiles && (uint32_t)p < Wc)
       next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tn).g);
     const float osc = __ldcg(A.sscales + tl.g);
     uint32_t owd[4];
@@ -153,39 +156,6 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     const float* sc = s_sc[ti & 1];
 
     const float* z8 = s_z8[ti & 1];
-    float4 ev[4];
-    float z[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t off = 1024u * i + 4u * p;
-      ev[i] = valid[i] ? *reinterpret_cast<const float4*>(st + off * 4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) z[i][c] = 0.0f;
-      if (valid[i]) {
-        const uint32_t widx = (off >> 5) + wshift;
-        const int sh = 4 * (p & 7);
-        // byte c of idx = the first W8 workers' bits of element c
-        uint32_t idx = 0;
-#pragma unroll
-        for (uint32_t w = 0; w < 8; ++w) {
-          if (w < W8) {
-            const uint32_t nib = (sbw[w * kRunWords + widx] >> sh) & 0xFu;
-            idx |= (nib * (0x00204081u << w)) & (0x01010101u << w);
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
-        for (uint32_t w = 8; w < G.W; ++w) {
-          const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
-          const float scw = sc[w];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) z[i][c] = __fadd_rn(z[i][c], ((wd >> c) & 1u) ? scw : -scw);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
 
     uint32_t l_t = 0;
     uint64_t lend_t = 0;
@@ -195,10 +165,50 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       lend_t = __ldg(A.ws.layer_off + l_t + 1);
       r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
     }
-    // UNI: the whole tile lies in one layer (rho scalar); else the layers
-    // are walked element by element
-    auto body = [&](auto uni_tag) -> float {
+    // FULL: all 4096 elements of the tile are real (no length or padding
+    // checks per element).  UNI: the whole tile lies in one layer (rho
+    // scalar); else the layers are walked element by element.
+    auto work = [&](auto full_tag, auto uni_tag) -> float {
+      constexpr bool FULL = decltype(full_tag)::value;
       [[maybe_unused]] constexpr bool UNI = decltype(uni_tag)::value;
+      float4 ev[4];
+      float z[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        const bool vi = FULL || valid[i];
+        ev[i] = vi ? *reinterpret_cast<const float4*>(st + off * 4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) z[i][c] = 0.0f;
+        if (vi) {
+          const uint32_t widx = (off >> 5) + wshift;
+          const int sh = 4 * (p & 7);
+          // byte c of idx = the first W8 workers' bits of element c
+          uint32_t idx = 0;
+#pragma unroll
+          for (uint32_t w = 0; w < 8; ++w) {
+            if (w < W8) {
+              const uint32_t nib = (sbw[w * kRunWords + widx] >> sh) & 0xFu;
+              idx |= (nib * (0x00204081u << w)) & (0x01010101u << w);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
+          if (WT == 0 || WT > 8) {
+            for (uint32_t w = 8; w < Wc; ++w) {
+              const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
+              const float scw = sc[w];
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                z[i][c] = __fadd_rn(z[i][c], ((wd >> c) & 1u) ? scw : -scw);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+
       float acc = 0.0f;
       [[maybe_unused]] uint32_t l = l_t;
       [[maybe_unused]] uint64_t lend = lend_t;
@@ -212,8 +222,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         for (int c = 0; c < 4; ++c) {
           const uint64_t k = k0 + c;
           float y = 0.0f;
-          if (valid[i] && k < G.n) {
-            const float zc = G.W <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
+          if (FULL || (valid[i] && k < G.n)) {
+            const float zc = Wc <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
             const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
             const float et = __fsub_rn(f4get(ev[i], c), so);
             if constexpr (LAMB) {
@@ -231,42 +241,57 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           f4at(yv, c) = y;
         }
         const uint32_t word = pack_word(nib, lane);
-        if (valid[i]) {
+        if (FULL || valid[i]) {
           __stcs(reinterpret_cast<float4*>(A.e_s + k0), yv);
           if ((p & 7) == 0) A.sbits[k0 >> 5] = word;
         }
       }
       return acc;
     };
+    const bool full_tile = tl.len == kTile && tl.start + kTile <= G.n;
     const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
-    float acc = uni ? body(std::true_type{}) : body(std::false_type{});
+    float acc;
+    if (full_tile) {
+      if (!LAMB || uni) acc = work(std::true_type{}, std::true_type{});
+      else acc = work(std::true_type{}, std::false_type{});
+    } else {
+      if (!LAMB || uni) acc = work(std::false_type{}, std::true_type{});
+      else acc = work(std::false_type{}, std::false_type{});
+    }
     acc = warp_butterfly_sum(acc);
     if (lane == 0) ws[warp] = acc;
-    if (Tn < G.n_tiles && (uint32_t)p < G.W) s_sc[(ti + 1) & 1][p] = next_sc;
+    if (Tn < G.n_tiles && (uint32_t)p < Wc) s_sc[(ti + 1) & 1][p] = next_sc;
     named_sync(1, kSConsumers);
     if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws);
     if (Tn < G.n_tiles && (uint32_t)p < (1u << W8))
-      s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) & 1], G.W, p);
+      s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) & 1], Wc, p);
     if (named_sync_or(1, kSConsumers, s_abort != 0)) break;
   }
 }
 
-template <bool LAMB>
+template <bool LAMB, uint32_t WT>
 cudaError_t run_server(const ServerArgs& a, int sms, cudaStream_t s) {
   const size_t bytes = ServerSmem::bytes(a.geo.W);
   static const cudaError_t attr = cudaFuncSetAttribute(
-      k_server<LAMB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      k_server<LAMB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)ServerSmem::bytes(OB_MAX_WORKERS));
   if (attr != cudaSuccess) return attr;
-  const int grid = grid_for(k_server<LAMB>, sms, a.geo.n_tiles, kServerThreads, bytes);
-  k_server<LAMB><<<grid, kServerThreads, bytes, s>>>(a);
+  const int grid = grid_for(k_server<LAMB, WT>, sms, a.geo.n_tiles, kServerThreads, bytes);
+  k_server<LAMB, WT><<<grid, kServerThreads, bytes, s>>>(a);
   return cudaGetLastError();
+}
+
+template <bool LAMB>
+cudaError_t run_server_w(const ServerArgs& a, int sms, cudaStream_t s) {
+  if (a.geo.W == 8) return run_server<LAMB, 8>(a, sms, s);
+  if (a.geo.W == 4) return run_server<LAMB, 4>(a, sms, s);
+  return run_server<LAMB, 0>(a, sms, s);
 }
 
 }  // namespace
 
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s) {
-  return lamb ? run_server<true>(a, sms, s) : run_server<false>(a, sms, s);
+  return lamb ? run_server_w<true>(a, sms, s) : run_server_w<false>(a, sms, s);
 }
 
 }  // namespace ob
