@@ -40,8 +40,9 @@ constexpr int kServerThreads = kThreads + 32;
 constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
 
 struct ServerSmem {
+  // the e_s tile, the W workers' word runs and the server's previous words
   __host__ __device__ static size_t stage_bytes(uint32_t W) {
-    return kTile * 4 + (size_t)W * kRunWords * 4;
+    return kTile * 4 + (size_t)(W + 1) * kRunWords * 4;
   }
   __host__ __device__ static size_t bytes(uint32_t W) {
     return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 2 * OB_MAX_WORKERS * 4 +
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 2);
   __shared__ float ws[8];
   __shared__ volatile int s_abort;
+  __shared__ Tile s_tile[2];  // the current and the next tile, decoded by thread 0
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned* err = A.ws.err;
@@ -104,11 +106,15 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       const uint64_t w1 = ((tl.start + tl.len) / 32 + 3) & ~uint64_t(3);
       const uint32_t run = (uint32_t)(w1 - w0) * 4;
       unsigned char* st = stage0 + s * stage_bytes;
-      mbar_arrive_expect_tx(&full[s], tl.len * 4 + G.W * run);
+      mbar_arrive_expect_tx(&full[s], tl.len * 4 + (G.W + 1) * run);
       bulk_g2s_stream(st, A.e_s + tl.start, tl.len * 4, &full[s], pol);
       for (uint32_t w = 0; w < G.W; ++w)
         bulk_g2s(st + kTile * 4 + (size_t)w * kRunWords * 4, A.bits + (uint64_t)w * G.words + w0,
                  run, &full[s]);
+      // the previous server words of this tile (only this CTA rewrites
+      // them, after this copy has landed; the rounding words read beyond
+      // the tile are not used)
+      bulk_g2s(st + kTile * 4 + (size_t)G.W * kRunWords * 4, A.sbits + w0, run, &full[s]);
     }
     if (!ok) s_abort = 1;
     for (uint32_t k = 0; k < kSStages && k < ti; ++k) {
@@ -126,32 +132,33 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc) {
     const Tile tl = decode_tile(G, blockIdx.x);
     s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
+    if (p == 0) s_tile[0] = tl;
   }
   named_sync(1, kSConsumers);
   if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
-    const Tile tl = decode_tile(G, T);
+    const Tile tl = s_tile[ti & 1];
     const uint32_t s = ti % kSStages;
-    // prefetch the next tile's worker scales
+    // prefetch the next tile's worker scales (thread 0 also keeps the
+    // decoded tile for everyone)
     float next_sc = 0.0f;
     const uint32_t Tn = T + gridDim.x;
-    if (Tn < G.n_tiles && (uint32_t)p < Wc)
-      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tn).g);
+    if (Tn < G.n_tiles && (uint32_t)p < Wc) {
+      const Tile tn = decode_tile(G, Tn);
+      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + tn.g);
+      if (p == 0) s_tile[(ti + 1) & 1] = tn;
+    }
     const float osc = __ldcg(A.sscales + tl.g);
-    uint32_t owd[4];
     bool valid[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t off = 1024u * i + 4u * p;
-      valid[i] = off < tl.len;
-      owd[i] = valid[i] ? A.sbits[(tl.start + off) >> 5] : 0u;
-    }
+    for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
     bool ok = s_abort == 0 && mbar_wait(&full[s], (ti / kSStages) & 1, err, kErrWaitFull);
     if (!ok) s_abort = 1;
     const unsigned char* st = stage0 + s * stage_bytes;
     const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
+    const uint32_t* sow = sbw + Wc * kRunWords;  // the server's previous words
     const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
     const float* sc = s_sc[ti & 1];
 
@@ -173,12 +180,14 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       [[maybe_unused]] constexpr bool UNI = decltype(uni_tag)::value;
       float4 ev[4];
       float z[4][4];
+      uint32_t owd[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t off = 1024u * i + 4u * p;
         const bool vi = FULL || valid[i];
         ev[i] = vi ? *reinterpret_cast<const float4*>(st + off * 4)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        owd[i] = vi ? sow[(off >> 5) + wshift] : 0u;
 #pragma unroll
         for (int c = 0; c < 4; ++c) z[i][c] = 0.0f;
         if (vi) {
