@@ -807,6 +807,8 @@ def main():
                     help="elements (flat and int8 workloads); use --elements under torchrun")
     ap.add_argument("--W", type=int, help="workers (flat workload only)")
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
+    ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32",
+                    help="gradient type (flat workload only)")
     ap.add_argument("--dense-m", action="store_true",
                     help="1-bit Adam: keep the momentum as a dense fp32 buffer")
     ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")
@@ -837,7 +839,7 @@ def main():
         return
     if args.workload == "flat":
         wl = synth.workload("flat", n=args.n or (1 << 24), W=args.W or 8,
-                            chunk=args.chunk or (1 << 20))
+                            chunk=args.chunk or (1 << 20), grad_dtype=args.grad_dtype)
     else:
         wl = synth.workload(args.workload)
     if args.clip_value:

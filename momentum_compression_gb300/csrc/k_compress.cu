@@ -39,17 +39,23 @@ constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 // Two CTAs per SM: 2 stages of 32 KB (fp32 gradients) or 3 of 24 KB (bf16)
 // plus the m tile, so that 4-6 (tile, worker) items are in flight per SM;
 // with the momentum in sign form the m tile's room holds one more stage.
+// A stage holds one (tile, worker) item: the gradient tile, the error tile
+// and the worker's previous sign words of the tile (a 16-byte aligned run).
+constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
+
 template <bool BF16, bool MSIGN>
 struct CompressSmem {
   static constexpr int kStages = (BF16 ? 3 : 2) + (MSIGN ? 1 : 0);
   static constexpr uint32_t kG = BF16 ? 2u : 4u;
   static constexpr size_t kStageG = kTile * kG;
   static constexpr size_t kStageE = kTile * 4;
-  static constexpr size_t kStage = kStageG + kStageE;
+  static constexpr size_t kStageB = kRunWords * 4;
+  static constexpr size_t kStage = kStageG + kStageE + kStageB;
   static constexpr size_t kM = MSIGN ? 0 : kTile * 4;
   static constexpr size_t kBars = (2 * kStages + 2) * 8;
   static constexpr size_t kWs = OB_MAX_WORKERS * 8 * 4;
-  static constexpr size_t kBytes = kM + kStages * kStage + kBars + kWs;
+  static constexpr size_t kSc = 2 * OB_MAX_WORKERS * 4;
+  static constexpr size_t kBytes = kM + kStages * kStage + kBars + kWs + kSc;
 };
 
 // MSIGN: the momentum is read in its sign form (msscale*sign(msbit), what
@@ -67,6 +73,8 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   uint64_t* mfull = bars + 2 * kStages;
   uint64_t* mempty = bars + 2 * kStages + 1;
   float(*ws)[8] = reinterpret_cast<float(*)[8]>(bars + 2 * kStages + 2);
+  // the workers' chunk scales of the current and the next tile
+  float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(ws + OB_MAX_WORKERS);
   __shared__ volatile int s_abort;
 
   const Geo& G = A.geo;
@@ -107,10 +115,16 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
           break;
         }
         unsigned char* st = stage0 + s * S::kStage;
-        mbar_arrive_expect_tx(&full[s], tl.len * (S::kG + 4));
+        // the previous words of (tile, worker): only this CTA rewrites them,
+        // after this copy has landed; the rounding words are not used
+        const uint64_t w0 = (tl.start >> 5) & ~uint64_t(3);
+        const uint32_t run = (uint32_t)((((tl.start + tl.len) / 32 + 3) & ~uint64_t(3)) - w0) * 4;
+        mbar_arrive_expect_tx(&full[s], tl.len * (S::kG + 4) + run);
         bulk_g2s_stream(st, static_cast<const unsigned char*>(A.g[w]) + tl.start * S::kG,
                         tl.len * S::kG, &full[s], pol);
         bulk_g2s_stream(st + S::kStageG, A.e[w] + tl.start, tl.len * 4, &full[s], pol);
+        bulk_g2s(st + S::kStageG + S::kStageE, A.bits + (uint64_t)w * G.words + w0, run,
+                 &full[s]);
       }
     }
     if (!ok) s_abort = 1;
@@ -142,10 +156,18 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   if constexpr (MSIGN) {
     if (blockIdx.x < G.n_tiles) load_msign(blockIdx.x);
   }
+  if (blockIdx.x < G.n_tiles && (uint32_t)p < G.W)
+    s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x).g);
+  named_sync(1, kConsumers);
   uint32_t item = 0, ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
     const Tile tl = decode_tile(G, T);
     bool ok = true;
+    // the next tile's worker scales, stored after this tile's last barrier
+    float sc_next = 0.0f;
+    const uint32_t Tn = T + gridDim.x;
+    if (Tn < G.n_tiles && (uint32_t)p < G.W)
+      sc_next = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tn).g);
     float4 mv[4];
     bool valid[4];
     if constexpr (MSIGN) {
@@ -189,21 +211,22 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     }
     const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
 
+    const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the word runs
     for (uint32_t w = 0; w < G.W; ++w, ++item) {
       const uint32_t s = item % kStages;
-      const float osc = __ldcg(A.scales + (uint64_t)w * G.nc + tl.g);
+      const float osc = s_sc[ti & 1][w];
       uint32_t* __restrict__ bw = A.bits + (uint64_t)w * G.words;
       float* __restrict__ e = A.e[w];
-      uint32_t owd[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) owd[i] = valid[i] ? bw[(tl.start + 1024u * i + 4u * p) >> 5] : 0u;
       ok = s_abort == 0 && mbar_wait(&full[s], (item / kStages) & 1, err, kErrWaitFull);
       if (!ok) s_abort = 1;
       const unsigned char* st = stage0 + s * S::kStage;
+      const uint32_t* sow = reinterpret_cast<const uint32_t*>(st + S::kStageG + S::kStageE);
       float4 gv[4], ev[4];
+      uint32_t owd[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t off = 1024u * i + 4u * p;
+        owd[i] = valid[i] ? sow[(off >> 5) + wshift] : 0u;
         if (valid[i]) {
           if constexpr (BF16) {
             const uint2 u = *reinterpret_cast<const uint2*>(st + off * 2);
@@ -275,6 +298,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       if (lane == 0) ws[w][warp] = acc;
     }
 
+    if (Tn < G.n_tiles && (uint32_t)p < G.W) s_sc[(ti + 1) & 1][p] = sc_next;
     named_sync(1, kConsumers);
     if ((uint32_t)p < G.W)
       A.ws.wpart[((uint64_t)p * G.nc + tl.g) * G.tpc + tl.t] = tree8(ws[p]);
