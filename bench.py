@@ -176,12 +176,36 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=("k_compress.cu", "ob_internal.cuh")):
     h = hashlib.sha256()
-    for f in ("k_compress.cu", "ob_internal.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "momentum_compression_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+INT8_SOURCES = ("k_int8.cu", "philox.cuh", "ob_internal.cuh")
+
+# Issue rate of the GPU: 152 SMs x 4 schedulers x one warp instruction (32
+# thread instructions) per clock each.
+ISSUE_THREADS_PER_CLK = 152 * 4 * 32
+
+
+def recorded_kv(name, source_files):
+    """key: value lines of a committed ncu summary under profiles/, if it was
+    taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("source_hash") != kernel_source_hash(source_files):
+            return None
+        return kv
+    except OSError:
+        return None
 
 
 def recorded_traffic(workload, sign_m):
@@ -339,6 +363,29 @@ def run_int8(args):
     bpe = (4 + 4 + 4 + 1 + 8 / 256) if args.ef else (4 + 1 + 4 / 256)
     peak, kind = measured_peak()
     gbs = bpe * n / (ms * 1e-3) / 1e9
+    clocks = clk.summary()
+    # The quantizer is bound by instruction issue, not by HBM: its roofline
+    # is the issue rate at the clock seen, against the thread instructions
+    # per element that ncu counted for this kernel source (profiles/).
+    kv = recorded_kv("int8_instructions.txt", INT8_SOURCES) or {}
+    ipe = kv.get("thread_instructions_per_element_ef" if args.ef else
+                 "thread_instructions_per_element")
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070
+    issue_peak = ISSUE_THREADS_PER_CLK * mhz * 1e6 / 1e12
+    if ipe is not None:
+        ach = float(ipe) * n / (ms * 1e-3) / 1e12
+        roofline = {"bound": "alu", "kernel": "quant_int8", "achieved": ach,
+                    "peak": issue_peak, "peak_kind": f"issue rate at the median SM clock "
+                    f"({mhz:.0f} MHz): 152 SMs x 4 schedulers x 32 lanes",
+                    "unit": "T thread-instructions/s", "frac": ach / issue_peak,
+                    "instructions_per_element": float(ipe),
+                    "hbm": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                            "bytes_per_element": bpe}, "traffic": None}
+    else:
+        roofline = {"bound": "hbm", "kernel": "quant_int8", "achieved": gbs, "peak": peak,
+                    "peak_kind": kind, "unit": "GB/s", "frac": gbs / peak,
+                    "bytes_per_element": bpe, "traffic": None,
+                    "note": "no instruction count recorded for this kernel source"}
     if rank == 0:
         what = "with error feedback and error monitor" if args.ef else ""
         print(json.dumps({
@@ -348,10 +395,7 @@ def run_int8(args):
             "dtype": "f32 -> int8", "data": "synthetic",
             "config": {"workload": f"int8 quantizer {what}, n = {n}, block 256, Philox4x32-10",
                        "l2": "inputs larger than L2; no flush"},
-            "roofline": {"bound": "hbm", "kernel": "quant_int8", "achieved": gbs, "peak": peak,
-                         "peak_kind": kind, "unit": "GB/s", "frac": gbs / peak,
-                         "bytes_per_element": bpe, "traffic": None},
-            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+            "roofline": roofline, "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
 
 def run_ours(args, wl):
