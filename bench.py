@@ -485,8 +485,34 @@ def run_ours(args, wl):
     total_ms = t_start.elapsed_time(t_end)
     per = {k: [ev[t][i].elapsed_time(ev[t][i + 1]) for t in range(K)]
            for i, k in enumerate(("compress", "server", "update"))}
+    graph_info = None
+    if args.graph:
+        # The same steps replayed from CUDA graphs (one per gradient set):
+        # one launch per step instead of five or six.  Per-kernel times come
+        # from the eager loop above; the step time from the replays.
+        graphs = [opt.capture_step(gsets[i]) for i in range(2)]
+        for t in range(2):
+            graphs[t % 2].replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(uuid) as gclk:
+            if pg:
+                pg.barrier()
+            torch.cuda.synchronize()
+            ga.record(stream)
+            for t in range(K):
+                graphs[t % 2].replay()
+            gb.record(stream)
+            torch.cuda.synchronize()
+            if pg:
+                pg.barrier()
+        eager_ms = max_over_ranks(total_ms, pg, device) / K
+        total_ms = ga.elapsed_time(gb)
+        graph_info = {"eager_ms_per_step": eager_ms, "graph_launches_per_step": 1,
+                      "clocks": gclk.summary()}
+        del graphs
     # compress + scale finalisation, server + scale finalisation, update
-    # (LAMB: pass A and pass B)
+    # (LAMB: pass A and pass B); the kernels inside a replayed graph count too
     launches = K * (6 if lamb else 5)
     total_ms = max_over_ranks(total_ms, pg, device)
     ms = total_ms / K
@@ -615,6 +641,9 @@ def run_ours(args, wl):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if graph_info is not None:
+        line["config"]["launch"] = "CUDA graph replay (one graph launch per step)"
+        line["graph"] = graph_info
     print(json.dumps(line), flush=True)
     opt.close()
 
@@ -853,6 +882,8 @@ def main():
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32",
                     help="gradient type (flat workload only)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as CUDA graph replays (1-bit workloads)")
     ap.add_argument("--dense-m", action="store_true",
                     help="1-bit Adam: keep the momentum as a dense fp32 buffer")
     ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")

@@ -447,6 +447,29 @@ class OneBitOptimizer:
         if self.sign_momentum and not self.m_in_signs:
             self.m_in_signs = True  # the next steps read the momentum from the signs
 
+    def capture_step(self, grads):
+        """Captures one compressed step on the gradient buffers `grads` into
+        a CUDA graph and returns it (torch.cuda.CUDAGraph); each replay()
+        runs that step with whatever the buffers hold -- one launch instead
+        of five or six, for sizes where launches dominate.  The step reads
+        every per-step quantity (scales, sign words, LAMB state) from device
+        memory, so replays are the same steps as eager calls.  Host-side
+        schedules are not replayed: capture after the first compressed step
+        when the momentum is held in sign form, and without reset_interval.
+        The library allocates nothing, so capture needs no memory pool."""
+        import torch
+        if self.reset_interval:
+            raise ValueError("capture_step: reset_interval is a host-side schedule")
+        if self.sign_momentum and not self.m_in_signs:
+            raise ValueError("capture_step: take the first compressed step eagerly")
+        graph = torch.cuda.CUDAGraph()
+        m = None if self.m_in_signs else self.m
+        with torch.cuda.graph(graph):
+            ob_step(self.ctx, grads, m, self.err, self.bits, self.scales, self.err_s,
+                    self.sbits, self.sscales, self.v, self.v_fresh, self.p,
+                    self.ls if self.lamb else None)
+        return graph
+
     def materialize_m(self, stream=None):
         """Writes the dense momentum (it is exact: sscale*sign)."""
         if self.m_in_signs:

@@ -1,0 +1,81 @@
+"""A compressed step captured in a CUDA graph and replayed gives the same
+bits as the same steps called eagerly (1-bit Adam with the momentum in sign
+form, and 1-bit LAMB).  The library's calls allocate nothing and take every
+per-step quantity from device memory, so a replay is the step itself."""
+import numpy as np
+import pytest
+import torch
+
+import momentum_compression_gb300 as ob
+from helpers import assert_bits_equal, host
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(b1=0.9, b2=0.999, eps=1e-8, lr=1e-4)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    from momentum_compression_gb300 import _build
+    _build.build()
+
+
+def _make(lamb, seed):
+    n, W = 300_001, 4
+    off = [0, 1000, 70_000, 250_000, n] if lamb else None
+    hp = dict(HP, **(dict(r_thr=0.1, r_min=0.5, r_max=4.0, c_min=0.01, c_max=10.0)
+                     if lamb else {}))
+    opt = ob.OneBitOptimizer(n, W, 1 << 16, 4096, "f32", off, lamb=lamb,
+                             sign_momentum=not lamb, **hp)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    opt.p[:n] = torch.randn(n, generator=gen, device="cuda") * 0.02
+    return opt, n, W
+
+
+def _grads(n_pad, n, W, step):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + step)
+    out = []
+    for _ in range(W):
+        g = torch.zeros(n_pad, device="cuda")
+        g[:n] = torch.randn(n, generator=gen, device="cuda") * 1e-3
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("lamb", [False, True])
+def test_graph_replay_matches_eager_steps(lamb):
+    a, n, W = _make(lamb, 1)
+    b, _, _ = _make(lamb, 1)
+    for opt in (a, b):
+        for t in range(3):
+            opt.warmup_step(_grads(opt.n_pad, n, W, t))
+        opt.begin_compression()
+        opt.compressed_step(_grads(opt.n_pad, n, W, 3))
+    bufs = [torch.zeros(b.n_pad, device="cuda") for _ in range(W)]
+    graph = b.capture_step(bufs)
+    for t in range(4, 10):
+        g = _grads(a.n_pad, n, W, t)
+        a.compressed_step(g)
+        for dst, src in zip(bufs, g):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(host(b.p), host(a.p), f"p after step {t}")
+        assert_bits_equal(host(b.sbits), host(a.sbits), f"sbits after step {t}")
+        assert_bits_equal(host(b.err_s), host(a.err_s), f"e_s after step {t}")
+        if lamb:
+            assert_bits_equal(host(b.ls.c_t), host(a.ls.c_t), f"c_t after step {t}")
+    a.close()
+    b.close()
+
+
+def test_capture_refuses_host_schedules():
+    opt, n, W = _make(False, 2)
+    opt.begin_compression()
+    with pytest.raises(ValueError):
+        opt.capture_step(_grads(opt.n_pad, n, W, 0))   # momentum still dense
+    opt.close()
