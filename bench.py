@@ -862,6 +862,74 @@ def mixed_oracle_sample(groups, steps):
                       f"({t_all:.1f} s)", "cpu": cpu_model()}
 
 
+def run_sweep(args):
+    """The flat bandwidth sweep: n in {2^20, 2^24, 2^28, 2^30} x W in {1, 2,
+    4, 8, 16} x chunk in {2^12, 2^20} (chunk clamped to the partition),
+    state drawn directly (m, e ~ N(0, 1e-3), v ~ |N(0, 1e-6)| + 1e-12, no
+    warmup), 1-bit Adam with the momentum in sign form after the first
+    step.  One JSON line per point: the step's elements/s and GB/s, and the
+    compress kernel's GB/s.  Points that do not fit in free memory are
+    skipped.  Small points are launch-bound and L2-resident."""
+    import torch
+
+    import momentum_compression_gb300 as ob
+    torch.cuda.set_device(0)
+    peak, kind = measured_peak()
+    for n_log in (20, 24, 28, 30):
+        for W in (1, 2, 4, 8, 16):
+            for c_log in (12, 20):
+                n, C = 1 << n_log, 1 << c_log
+                need = n * (8 * W + 24) * 1.1
+                free, _ = torch.cuda.mem_get_info()
+                if need > free * 0.9:
+                    log(f"[sweep] skip n=2^{n_log} W={W}: {need / 1e9:.0f} GB needed")
+                    continue
+                opt = ob.OneBitOptimizer(n, W, C, 4096, "f32", None, sign_momentum=True,
+                                         **synth.ADAM_HP)
+                gen = torch.Generator(device="cuda")
+                gen.manual_seed(synth.SEED_BASE + n_log * 100 + W)
+                opt.m[:n] = torch.randn(n, generator=gen, device="cuda") * 1e-3
+                opt.v[:n] = torch.randn(n, generator=gen, device="cuda").abs() * 1e-6 + 1e-12
+                for e in opt.err:
+                    e[:n] = torch.randn(n, generator=gen, device="cuda") * 1e-3
+                grads = [torch.zeros(opt.n_pad, device="cuda") for _ in range(W)]
+                for g in grads:
+                    g[:n] = torch.randn(n, generator=gen, device="cuda") * 1e-3
+                K = 50 if n_log <= 24 else 10
+                for _ in range(3):
+                    opt.compressed_step(grads)
+                torch.cuda.synchronize()
+                stream = torch.cuda.current_stream()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(K):
+                    opt.compressed_step(grads)
+                b.record(stream)
+                ca.record(stream)
+                for _ in range(K):
+                    ob.ob_compress_signm(opt.ctx, grads, opt.sbits, opt.sscales, opt.err,
+                                         opt.bits, opt.scales)
+                cb.record(stream)
+                torch.cuda.synchronize()
+                ms = a.elapsed_time(b) / K
+                cms = ca.elapsed_time(cb) / K
+                bpe = bytes_per_element(W, 4, False, True)
+                gbs = bpe["total"] * n / (ms * 1e-3) / 1e9
+                cgbs = bpe["compress"] * n / (cms * 1e-3) / 1e9
+                print(json.dumps({
+                    "sweep": "flat 1-bit Adam, sign-form momentum", "n": n, "W": W,
+                    "chunk": min(C, opt.layout["P"]), "steps": K, "ms_per_step": ms,
+                    "elements_per_s": n / (ms * 1e-3), "gbs": gbs, "frac": gbs / peak,
+                    "compress_ms": cms, "compress_gbs": cgbs, "compress_frac": cgbs / peak,
+                    "peak": peak, "peak_kind": kind,
+                    "l2": "L2-resident" if bpe["total"] * n < 2 * 129e6 else "larger than L2"}),
+                    flush=True)
+                opt.close()
+                del grads, opt
+                torch.cuda.empty_cache()
+
+
 def wl_label(wl):
     kind = "1-bit LAMB" if wl.mode == "lamb" else "1-bit Adam"
     shape = f"{wl.n_layers} tensors" if wl.tensors else "flat"
@@ -889,8 +957,13 @@ def main():
     ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")
     ap.add_argument("--clip-value", type=float, default=0.0,
                     help="clamp of the compensated values (the write-up's stability variant)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the flat n x W x chunk bandwidth sweep, one JSON line per point")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "ours" and args.workload == "int8":
         run_int8(args)
         return
