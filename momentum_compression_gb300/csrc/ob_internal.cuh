@@ -117,8 +117,10 @@ __device__ __forceinline__ uint32_t pack_word(uint32_t nibble, int lane) {
 
 // Sequential sum of `cnt` tile totals (from 0, in order), done by one warp:
 // every lane returns the same value.  Each batch of 256 totals is loaded at
-// once (8 per lane) and handed to the adding chain by unrolled shuffles, so
-// only the additions are serialised.
+// once (8 per lane) and handed to the adding chain by shuffles, so only the
+// additions are serialised: a full batch through unrolled shuffles, the
+// last partial one through as many shuffles as it has totals (a one-tile
+// chunk costs one).
 __device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, int lane) {
   float acc = 0.0f;
   for (uint32_t t0 = 0; t0 < cnt; t0 += 256) {
@@ -128,13 +130,18 @@ __device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, in
       const uint32_t t = t0 + 32u * j + lane;
       v[j] = t < cnt ? __ldcg(part + t) : 0.0f;
     }
-    const uint32_t rem = cnt - t0;
+    const uint32_t rem = cnt - t0;  // the same in every lane
+    if (rem >= 256) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int s = 0; s < 32; ++s) {
-        const float x = __shfl_sync(kFull, v[j], s);
-        if (32u * j + s < rem) acc = __fadd_rn(acc, x);
+        for (int s = 0; s < 32; ++s) acc = __fadd_rn(acc, __shfl_sync(kFull, v[j], s));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (32u * j >= rem) break;
+        const uint32_t lim = rem - 32u * j < 32u ? rem - 32u * j : 32u;
+        for (uint32_t s = 0; s < lim; ++s) acc = __fadd_rn(acc, __shfl_sync(kFull, v[j], s));
       }
     }
   }
