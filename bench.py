@@ -177,10 +177,16 @@ def measured_peak():
 
 
 def kernel_source_hash(files=("k_compress.cu", "ob_internal.cuh")):
+    """Hash of the kernel sources a recorded measurement was taken on, with
+    comments and blank space left out (they do not change the kernel)."""
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "momentum_compression_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "momentum_compression_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

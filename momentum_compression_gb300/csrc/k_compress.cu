@@ -36,11 +36,12 @@ namespace {
 constexpr int kConsumers = kThreads;            // 8 warps
 constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 
-// Two CTAs per SM: 2 stages of 32 KB (fp32 gradients) or 3 of 24 KB (bf16)
-// plus the m tile, so that 4-6 (tile, worker) items are in flight per SM;
-// with the momentum in sign form the m tile's room holds one more stage.
 // A stage holds one (tile, worker) item: the gradient tile, the error tile
-// and the worker's previous sign words of the tile (a 16-byte aligned run).
+// and the worker's previous sign words of the tile (a 16-byte aligned run),
+// 32.5 KB with fp32 gradients, 24.5 KB with bf16.  Two CTAs per SM, each
+// with 2 (fp32) or 3 (bf16) stages plus the m tile, so that 4-6 items are
+// in flight per SM; with the momentum in sign form the m tile's room holds
+// one more stage.
 constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
 
 template <bool BF16, bool MSIGN>
