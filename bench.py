@@ -956,6 +956,8 @@ def main():
     ap.add_argument("--chunk", type=int, help="chunk (flat workload only)")
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32",
                     help="gradient type (flat workload only)")
+    ap.add_argument("--mode", choices=("adam", "lamb"), default="adam",
+                    help="1-bit Adam or 1-bit LAMB (flat workload only; one layer)")
     ap.add_argument("--graph", action="store_true",
                     help="time the step as CUDA graph replays (1-bit workloads)")
     ap.add_argument("--dense-m", action="store_true",
@@ -994,6 +996,9 @@ def main():
     if args.workload == "flat":
         wl = synth.workload("flat", n=args.n or (1 << 24), W=args.W or 8,
                             chunk=args.chunk or (1 << 20), grad_dtype=args.grad_dtype)
+        if args.mode == "lamb":
+            wl.mode = "lamb"
+            wl.hp.update(r_thr=0.1, r_min=0.5, r_max=4.0, c_min=0.01, c_max=10.0)
     else:
         wl = synth.workload(args.workload)
     if args.clip_value:

@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
     auto body = [&](auto uni_tag) {
       constexpr bool UNI = decltype(uni_tag)::value;
       uint64_t lend = lend_t;
-      float sg_l = s_t;
+      // M/sigma = +-(sscale/sigma) exactly (IEEE division is symmetric in
+      // sign): one division per layer instead of one per element
+      float q_l = __fdiv_rn(osc, s_t);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;
@@ -140,11 +142,10 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
             if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
               if (rmax > 0.0f) atomicMax(A.ws.Rbits + l_old, __float_as_uint(rmax));
               rmax = 0.0f;
-              sg_l = __ldg(A.ls.s + l);
+              q_l = __fdiv_rn(osc, __ldg(A.ls.s + l));
             }
           }
-          const float M = ((wd[i] >> c) & 1u) ? osc : -osc;
-          const float mt = __fdiv_rn(M, sg_l);
+          const float mt = ((wd[i] >> c) & 1u) ? q_l : -q_l;
           const float gt =
               __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, f4get(mv[i], c))), A.ob1);
           const float v = __fadd_rn(__fmul_rn(A.b2, f4get(vt[i], c)),
