@@ -255,11 +255,14 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const UpdateArgs A) {
     const float osc = __ldcg(A.sscales + tl.g);
     uint32_t l = 0;
     uint64_t lend = 0;
-    float sg_l = 1.0f;
+    // the magnitude of every value of the layer: sscale, or sscale/sigma_l
+    // (+-sscale/sigma = (+-sscale)/sigma exactly: IEEE division is
+    // symmetric in sign)
+    float q_l = osc;
     if constexpr (LAYERED) {
       l = __ldg(A.ws.tile_layer + T);
       lend = __ldg(A.ws.layer_off + l + 1);
-      sg_l = __ldg(A.ls.s + l);
+      q_l = __fdiv_rn(osc, __ldg(A.ls.s + l));
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -273,11 +276,11 @@ __global__ void __launch_bounds__(kThreads) k_decompress(const UpdateArgs A) {
         const uint64_t k = k0 + c;
         float M = 0.0f;
         if (k < G.n) {
-          M = ((wd >> c) & 1u) ? osc : -osc;
           if constexpr (LAYERED) {
-            if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) sg_l = __ldg(A.ls.s + l);
-            M = __fdiv_rn(M, sg_l);
+            if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+              q_l = __fdiv_rn(osc, __ldg(A.ls.s + l));
           }
+          M = ((wd >> c) & 1u) ? q_l : -q_l;
         }
         f4at(o, c) = M;
       }
