@@ -299,16 +299,21 @@ LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=
                c_min=0.01, c_max=10.0)
 
 
-@pytest.mark.parametrize("flags", [0, ob.OB_FLAG_NO_RATIO_EF, ob.OB_FLAG_FROZEN_C])
-def test_lamb_small_layers(flags):
+@pytest.mark.parametrize("flags,W,dt", [
+    (0, 4, "f32"), (ob.OB_FLAG_NO_RATIO_EF, 4, "f32"), (ob.OB_FLAG_FROZEN_C, 4, "f32"),
+    (0, 8, "bf16"),   # the W = 8 server specialisation, bf16 worker kernel
+    (0, 3, "f32"),    # generic W
+    (0, 12, "bf16"),  # workers beyond the 8-worker sign table
+])
+def test_lamb_small_layers(flags, W, dt):
     """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
-    W = 4, chunk 2048, 3 warmup + 6 compressed steps with the gradient std
-    falling 3x per step, so that r_t moves and the step-ratio error
-    feedback differs from 1."""
+    chunk 2048, 3 warmup + 6 compressed steps with the gradient std falling
+    3x per step, so that r_t moves and the step-ratio error feedback
+    differs from 1."""
     sizes = [7, 1, 2, 4095, 4097, 33, 1000, 20000, 3, 30000]
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.uint64)
-    n, W, A, C = int(off[-1]), 4, 32, 2048
-    opt = ob.OneBitOptimizer(n, W, C, A, "f32", [int(x) for x in off], lamb=True, flags=flags,
+    n, A, C = int(off[-1]), 32, 2048
+    opt = ob.OneBitOptimizer(n, W, C, A, dt, [int(x) for x in off], lamb=True, flags=flags,
                              **LAMB_HP)
     lay = O.Layout(n, W, A, C)
     layers = O.Layers(off)
@@ -328,6 +333,9 @@ def test_lamb_small_layers(flags):
             a = np.zeros(lay.n_pad, f32)
             a[:n] = rng.standard_normal(n).astype(f32) * layer_std * f
             gh.append(a)
+        if dt == "bf16":
+            bits = [synth.bf16_bits(x) for x in gh]
+            return [synth.bf16_to_f32(b) for b in bits], [bf16_tensor(b) for b in bits]
         return gh, [dev(x) for x in gh]
 
     hp = dict(LAMB_HP)
