@@ -58,8 +58,8 @@ __device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, uint32_t 
   return W <= 8 ? __fdiv_rn(z, (float)W) : z;
 }
 
-// WT: the worker count when it is a compile-time 4 or 8 (the tables' and
-// loops' bounds are then constants), 0 for any other W.
+// WT: the worker count when it is a compile-time 4, 8 or 16 (the tables'
+// and loops' bounds are then constants), 0 for any other W.
 template <bool LAMB, uint32_t WT>
 __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 #pragma unroll
           for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
           if (WT == 0 || WT > 8) {
+#pragma unroll 8
             for (uint32_t w = 8; w < Wc; ++w) {
               const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
               const float scw = sc[w];
@@ -294,6 +295,7 @@ template <bool LAMB>
 cudaError_t run_server_w(const ServerArgs& a, int sms, cudaStream_t s) {
   if (a.geo.W == 8) return run_server<LAMB, 8>(a, sms, s);
   if (a.geo.W == 4) return run_server<LAMB, 4>(a, sms, s);
+  if (a.geo.W == 16) return run_server<LAMB, 16>(a, sms, s);
   return run_server<LAMB, 0>(a, sms, s);
 }
 
