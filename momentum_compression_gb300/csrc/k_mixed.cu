@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) k_qb_server(const QbServerArgs A) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
-  const float fW = (float)A.W;
+  const float fW = (float)A.W, inv_w = inv_workers(A.W);
   const Keys keys(A.seed);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kThreads) k_qb_server(const QbServerArgs A) {
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         f4at(y[h], c) =
-            c < nv[h] ? __fadd_rn(f4get(es[h], c), __fdiv_rn(f4get(z[h], c), fW)) : 0.0f;
+            c < nv[h] ? __fadd_rn(f4get(es[h], c), div_by_workers(f4get(z[h], c), fW, inv_w))
+                      : 0.0f;
     float4 r[2];
     quantize_block<BITS>(y, nv, (uint64_t)A.W * A.n_pad + b * 256, A.step, keys, lane,
                          A.scodes + b * S::kBlockWords, A.sscales + b, r);
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) k_f16_compress(const F16Args A) {
 
 __global__ void __launch_bounds__(kThreads) k_f16_server(const F16Args A) {
   const uint64_t groups = A.n_pad / 4;
-  const float fW = (float)A.W;
+  const float fW = (float)A.W, inv_w = inv_workers(A.W);
   for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < groups;
        i += (uint64_t)gridDim.x * kThreads) {
     const uint64_t k = 4 * i;
@@ -382,7 +383,8 @@ __global__ void __launch_bounds__(kThreads) k_f16_server(const F16Args A) {
     float4 y;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      f4at(y, c) = c < nv ? __fadd_rn(f4get(es, c), __fdiv_rn(f4get(z, c), fW)) : 0.0f;
+      f4at(y, c) = c < nv ? __fadd_rn(f4get(es, c), div_by_workers(f4get(z, c), fW, inv_w))
+                          : 0.0f;
     const uint2 hs = make_uint2(pack_half2(y.x, y.y), pack_half2(y.z, y.w));
     const float4 r = make_float4(__fsub_rn(y.x, half_lo(hs.x)), __fsub_rn(y.y, half_hi(hs.x)),
                                  __fsub_rn(y.z, half_lo(hs.y)), __fsub_rn(y.w, half_hi(hs.y)));

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned* err = A.ws.err;
-  const float fW = (float)G.W;
+  const float fW = (float)G.W, inv_w = inv_workers(G.W);
 
   if (tid == 0) {
     for (int s = 0; s < kSStages; ++s) {
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           const uint64_t k = k0 + c;
           float y = 0.0f;
           if (FULL || (valid[i] && k < G.n)) {
-            const float zc = Wc <= 8 ? z[i][c] : __fdiv_rn(z[i][c], fW);
+            const float zc = Wc <= 8 ? z[i][c] : div_by_workers(z[i][c], fW, inv_w);
             const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
             const float et = __fsub_rn(f4get(ev[i], c), so);
             if constexpr (LAMB) {

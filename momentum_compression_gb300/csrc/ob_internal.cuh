@@ -148,6 +148,18 @@ __device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, in
   return acc;
 }
 
+// z / W for the server averages.  When W is a power of two, 1/W is exact
+// and z * (1/W) is the same correctly rounded number as z / W (both round
+// the same real value), so a multiply replaces the division; inv_w is
+// 1/W then and 0 otherwise.
+__device__ __forceinline__ float div_by_workers(float z, float fW, float inv_w) {
+  return inv_w != 0.0f ? __fmul_rn(z, inv_w) : __fdiv_rn(z, fW);
+}
+
+__host__ __device__ inline float inv_workers(uint32_t W) {
+  return (W & (W - 1)) == 0 ? 1.0f / (float)W : 0.0f;
+}
+
 __device__ __forceinline__ float mean_of(float sum, uint64_t count) {
   return count ? __fdiv_rn(sum, __ull2float_rn(count)) : 0.0f;
 }
