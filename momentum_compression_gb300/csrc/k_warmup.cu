@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) k_warmup_adam(const WarmupArgs A) {
           f4at(mv, c) = 0.0f;
           continue;
         }
-        const float g = __fdiv_rn(f4at(gb, c), A.fW);
+        const float g = div_by_workers(f4at(gb, c), A.fW, A.inv_w);
         const float m = __fadd_rn(__fmul_rn(A.b1, f4at(mv, c)), __fmul_rn(A.ob1, g));
         const float v = __fadd_rn(__fmul_rn(A.b2, f4at(vv, c)),
                                   __fmul_rn(A.ob2, __fmul_rn(g, g)));
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) k_warmup_lamb_a(const WarmupArgs A) 
         const uint64_t k = lt.start + idx;
         float gb = 0.0f;
         for (uint32_t w = 0; w < G.W; ++w) gb = __fadd_rn(gb, load_grad1<BF16>(A.g[w], k));
-        gb = __fdiv_rn(gb, A.fW);
+        gb = div_by_workers(gb, A.fW, A.inv_w);
         const float m = __fadd_rn(__fmul_rn(A.b1, A.m[k]), __fmul_rn(A.ob1, gb));
         const float v = __fadd_rn(__fmul_rn(A.b2, A.v[k]), __fmul_rn(A.ob2, __fmul_rn(gb, gb)));
         const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));

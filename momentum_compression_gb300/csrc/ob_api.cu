@@ -340,6 +340,7 @@ ob_status ob_warmup_step(ob_ctx* ctx, const void* const* grads, float* m, float*
   a.c_min = c.c_min;
   a.c_max = c.c_max;
   a.fW = (float)c.W;
+  a.inv_w = ob::inv_workers((uint32_t)c.W);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool bf16 = c.grad_dtype == OB_GRAD_BF16;
   if (mode == OB_MODE_ADAM) return launched(ctx, ob::launch_warmup_adam(a, bf16, ctx->sms, s), "warmup");

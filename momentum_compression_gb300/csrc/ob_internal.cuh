@@ -276,7 +276,7 @@ struct WarmupArgs {
   float* p;
   ob_layer_state ls;
   float b1, ob1, b2, ob2, eps, lr, c_min, c_max;
-  float fW;
+  float fW, inv_w;  // W, and 1/W when W is a power of two (else 0)
   int warmup_steps;
 };
 
