@@ -143,30 +143,87 @@ __global__ void __launch_bounds__(kThreads) k_warmup_lamb_a(const WarmupArgs A) 
   const int p = threadIdx.x;
   for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
     const LTile lt = decode_ltile(A.ws, G.L, LT);
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t idx = p + kThreads * j;
-      float pq = 0.0f, uq = 0.0f;
-      if (idx < lt.len) {
-        const uint64_t k = lt.start + idx;
-        float gb = 0.0f;
-        for (uint32_t w = 0; w < G.W; ++w) gb = __fadd_rn(gb, load_grad1<BF16>(A.g[w], k));
-        gb = div_by_workers(gb, A.fW, A.inv_w);
-        const float m = __fadd_rn(__fmul_rn(A.b1, A.m[k]), __fmul_rn(A.ob1, gb));
-        const float v = __fadd_rn(__fmul_rn(A.b2, A.v[k]), __fmul_rn(A.ob2, __fmul_rn(gb, gb)));
-        const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));
-        A.m[k] = m;
-        A.v[k] = v;
-        const float pk = __ldcs(A.p + k);
-        pq = __fmul_rn(pk, pk);
-        uq = __fmul_rn(u, u);
+    float lp, lu;  // this lane's sums of p^2 and u^2 in the fixed order
+    if ((lt.start & 3) == 0) {
+      // the layer tile starts on a 16-byte boundary: lane p loads elements
+      // 1024*i + 4*p .. +3 with 128-bit loads -- exactly the elements it
+      // adds, in the order it adds them, so no staging is needed.  A last
+      // group that runs past the layer's end is stored element by element
+      // (the rest belongs to the next layer).
+      lp = 0.0f;
+      lu = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (off >= lt.len) continue;
+        const uint64_t k0 = lt.start + off;
+        const uint32_t nv = lt.len - off < 4u ? lt.len - off : 4u;
+        float4 gb = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint32_t w = 0; w < G.W; ++w) {
+          const float4 gv = load_grad4<BF16>(A.g[w], k0);
+          gb.x = __fadd_rn(gb.x, gv.x);
+          gb.y = __fadd_rn(gb.y, gv.y);
+          gb.z = __fadd_rn(gb.z, gv.z);
+          gb.w = __fadd_rn(gb.w, gv.w);
+        }
+        float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k0));
+        float4 vv = __ldcs(reinterpret_cast<const float4*>(A.v + k0));
+        const float4 pv = __ldcs(reinterpret_cast<const float4*>(A.p + k0));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if ((uint32_t)c >= nv) continue;
+          const float g = div_by_workers(f4at(gb, c), A.fW, A.inv_w);
+          const float m = __fadd_rn(__fmul_rn(A.b1, f4at(mv, c)), __fmul_rn(A.ob1, g));
+          const float v = __fadd_rn(__fmul_rn(A.b2, f4at(vv, c)),
+                                    __fmul_rn(A.ob2, __fmul_rn(g, g)));
+          const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));
+          f4at(mv, c) = m;
+          f4at(vv, c) = v;
+          lp = __fadd_rn(lp, __fmul_rn(f4get(pv, c), f4get(pv, c)));
+          lu = __fadd_rn(lu, __fmul_rn(u, u));
+        }
+        if (nv == 4) {
+          __stcs(reinterpret_cast<float4*>(A.m + k0), mv);
+          __stcs(reinterpret_cast<float4*>(A.v + k0), vv);
+        } else {
+          for (uint32_t c = 0; c < nv; ++c) {
+            A.m[k0 + c] = f4at(mv, c);
+            A.v[k0 + c] = f4at(vv, c);
+          }
+        }
       }
-      sp[idx] = pq;
-      su[idx] = uq;
+    } else {
+      // any other start: coalesced scalar accesses (thread t takes elements
+      // t + 256*j), the squares staged in shared memory at their tile
+      // positions and summed there in the fixed lane order
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t idx = p + kThreads * j;
+        float pq = 0.0f, uq = 0.0f;
+        if (idx < lt.len) {
+          const uint64_t k = lt.start + idx;
+          float gb = 0.0f;
+          for (uint32_t w = 0; w < G.W; ++w) gb = __fadd_rn(gb, load_grad1<BF16>(A.g[w], k));
+          gb = div_by_workers(gb, A.fW, A.inv_w);
+          const float m = __fadd_rn(__fmul_rn(A.b1, A.m[k]), __fmul_rn(A.ob1, gb));
+          const float v =
+              __fadd_rn(__fmul_rn(A.b2, A.v[k]), __fmul_rn(A.ob2, __fmul_rn(gb, gb)));
+          const float u = __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), A.eps));
+          A.m[k] = m;
+          A.v[k] = v;
+          const float pk = __ldcs(A.p + k);
+          pq = __fmul_rn(pk, pk);
+          uq = __fmul_rn(u, u);
+        }
+        sp[idx] = pq;
+        su[idx] = uq;
+      }
+      __syncthreads();
+      lp = lane_sum_sq(sp, p);
+      lu = lane_sum_sq(su, p);
     }
-    __syncthreads();
     float tp, tu;
-    block_sum2(lane_sum_sq(sp, p), lane_sum_sq(su, p), ws, tp, tu);
+    block_sum2(lp, lu, ws, tp, tu);
     if (p == 0) {
       A.ws.lpart[LT] = tp;
       A.ws.lpart[G.n_ltiles + LT] = tu;
@@ -248,19 +305,35 @@ __global__ void __launch_bounds__(kThreads) k_lamb_begin_tiles(const WarmupArgs 
   const int p = threadIdx.x;
   for (uint32_t LT = blockIdx.x; LT < G.n_ltiles; LT += gridDim.x) {
     const LTile lt = decode_ltile(A.ws, G.L, LT);
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t idx = p + kThreads * j;
-      float q = 0.0f;
-      if (idx < lt.len) {
-        const float mk = __ldcs(A.m + lt.start + idx);
-        q = __fmul_rn(mk, mk);
+    float lm = 0.0f;
+    if ((lt.start & 3) == 0) {
+      // 16-byte aligned layer tile: 128-bit loads in the fixed lane order
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (off >= lt.len) continue;
+        const uint32_t nv = lt.len - off < 4u ? lt.len - off : 4u;
+        const float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + lt.start + off));
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if ((uint32_t)c < nv) lm = __fadd_rn(lm, __fmul_rn(f4get(mv, c), f4get(mv, c)));
       }
-      sq[idx] = q;
+    } else {
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t idx = p + kThreads * j;
+        float q = 0.0f;
+        if (idx < lt.len) {
+          const float mk = __ldcs(A.m + lt.start + idx);
+          q = __fmul_rn(mk, mk);
+        }
+        sq[idx] = q;
+      }
+      __syncthreads();
+      lm = lane_sum_sq(sq, p);
     }
-    __syncthreads();
     float tm, unused;
-    block_sum2(lane_sum_sq(sq, p), 0.0f, ws, tm, unused);
+    block_sum2(lm, 0.0f, ws, tm, unused);
     if (p == 0) A.ws.lpart[LT] = tm;
     __syncthreads();
   }
