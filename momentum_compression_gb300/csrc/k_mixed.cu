@@ -38,11 +38,6 @@ __device__ __forceinline__ int valid4(uint64_t k, uint64_t n) {
   return k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
 }
 
-template <bool BF16>
-__device__ __forceinline__ float4 grad4(const void* g, uint64_t k) {
-  return load_grad4<BF16>(g, k);
-}
-
 // Code words of one lane-half: BITS*4 bits (4 fields); LPW lanes share a
 // word.  Returns the word index inside the block and the bit offset of the
 // lane's first field.
@@ -156,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArg
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
       nv[h] = valid4(k, A.n);
       mv[h] = __ldcs(reinterpret_cast<const float4*>(A.m + k));
-      gv[h] = grad4<BF16>(A.g[0], k);
+      gv[h] = load_grad4<BF16>(A.g[0], k);
       ev[h] = __ldcs(reinterpret_cast<const float4*>(A.e[0] + k));
     }
     for (uint32_t w = 0; w < A.W; ++w) {
@@ -166,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArg
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint64_t k = b * 256 + 128 * h + 4 * lane;
-          gn[h] = grad4<BF16>(A.g[w + 1], k);
+          gn[h] = load_grad4<BF16>(A.g[w + 1], k);
           en[h] = __ldcs(reinterpret_cast<const float4*>(A.e[w + 1] + k));
         }
       }
@@ -338,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) k_f16_compress(const F16Args A) {
     const int nv = valid4(k, A.n);
     const float4 mv = __ldcs(reinterpret_cast<const float4*>(A.m + k));
     for (uint32_t w = 0; w < A.W; ++w) {
-      const float4 gv = grad4<BF16>(A.g[w], k);
+      const float4 gv = load_grad4<BF16>(A.g[w], k);
       const float4 ev = __ldcs(reinterpret_cast<const float4*>(A.e[w] + k));
       float4 x, r;
 #pragma unroll

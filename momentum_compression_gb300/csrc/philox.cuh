@@ -58,13 +58,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
   return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
 }
 
-// The four uniforms of elements 4*grp .. 4*grp+3 at call `step`.
-__device__ __forceinline__ uint4 philox_group(uint64_t grp, uint64_t step, const PhiloxKeys& K) {
-  return philox4x32_10(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
-                                  (uint32_t)(step >> 32)),
-                       K);
-}
-
 __device__ __forceinline__ float uniform_of(uint32_t word) {
   return __fmul_rn((float)(word >> 8), 5.9604644775390625e-08f);  // 2^-24
 }
