@@ -470,3 +470,70 @@ def test_int8_error_feedback_parity(n):
         assert_bits_equal(host(d_t)[:n], d_o, "dequantised")
         assert_bits_equal(host(e_t), e_o, "residual")
         assert_bits_equal(host(e2_t), e2_o, "error monitor")
+
+
+# ---------------------------------------------------------------------------
+# Degenerate inputs
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("lamb", [False, True])
+def test_all_zero_inputs(lamb):
+    """All gradients, momentum and errors zero: every chunk scale is 0,
+    every sign is +1 (x = +0 >= 0), errors stay 0, and the update leaves p
+    as it is -- bit for bit as the oracle.  LAMB: zero norms give c = 1."""
+    n, W, A, C = 20_000, 4, 32, 4096
+    off = [0, 100, 20_000] if lamb else None
+    hp = dict(LAMB_HP) if lamb else dict(b1=0.9, b2=0.999, eps=1e-8, lr=1e-4)
+    opt = ob.OneBitOptimizer(n, W, C, A, "f32", off, lamb=lamb, **hp)
+    lay = O.Layout(n, W, A, C)
+    layers = O.Layers(np.array(off, np.uint64)) if lamb else None
+    st = O.State(lay, layers, lamb=lamb)
+    p0 = np.zeros(lay.n_pad, f32)
+    p0[:n] = np.linspace(-1, 1, n, dtype=f32)
+    st.p[:] = p0
+    opt.p.copy_(dev(p0))
+    st.v[:n] = f32(1e-6)
+    opt.v[:n] = 1e-6
+    zeros = [np.zeros(lay.n_pad, f32) for _ in range(W)]
+    if lamb:
+        opt.warmup_step([dev(z) for z in zeros])
+        O.warmup_step(lay, zeros, 1, hp, st.m, st.v, st.p, layers, st.c_sum)
+    opt.begin_compression()
+    O.begin_compression(st, 1, lamb=lamb)
+    for t in range(2):
+        opt.compressed_step([dev(z) for z in zeros])
+        O.compressed_step(st, zeros, hp, lamb=lamb)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(opt.sbits)[: lay.words], st.sbits, "sbits")
+    assert np.all(st.sscales == 0) and np.all(host(opt.sscales) == 0)
+    assert_bits_equal(host(opt.p), st.p, "p")
+    assert_bits_equal(host(opt.p)[:n], p0[:n], "p unchanged")
+    if lamb:
+        assert_bits_equal(host(opt.ls.c_t), st.c, "c_t")
+    opt.close()
+
+
+@pytest.mark.parametrize("bits", [2, 16])
+def test_codec_all_zero_inputs(bits):
+    """Zero blocks in the codec groups: scale 0, codes 0, errors 0."""
+    n, W = 5000, 3
+    g = ob.CodecGroup(n, W, bits, 256, period=1, seed=3, b1=0.9, b2=0.999, eps=1e-8, lr=1e-4)
+    lay = O.Layout(n, W, 256, 256)
+    st = O.State(lay)
+    p0 = np.zeros(lay.n_pad, f32)
+    p0[:n] = np.linspace(-1, 1, n, dtype=f32)
+    st.p[:] = p0
+    g.p.copy_(dev(p0))
+    st.v[:n] = f32(1e-6)
+    g.v[:n] = 1e-6
+    zeros = [np.zeros(lay.n_pad, f32) for _ in range(W)]
+    g.begin_compression()
+    for t in range(1, 3):
+        g.compressed_step([dev(z) for z in zeros])
+        O.codec_step(st, zeros, dict(b1=0.9, b2=0.999, eps=1e-8, lr=1e-4), bits, t, 3, period=1)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(g.p), st.p, "p")
+    assert_bits_equal(host(g.m), st.m, "m")
+    if bits != 16:
+        assert np.all(host(g.bscales) == 0) and np.all(host(g.codes) == 0)
+    g.close()
