@@ -310,9 +310,11 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
 template <bool BF16, bool LAMB, bool MSIGN>
 cudaError_t run_compress(const CompressArgs& a, int sms, cudaStream_t s) {
   using S = CompressSmem<BF16, MSIGN>;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(k_compress<BF16, LAMB, MSIGN>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+  static PerDeviceOnce once;
+  const cudaError_t attr = once.run([] {
+    return cudaFuncSetAttribute(k_compress<BF16, LAMB, MSIGN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kBytes);
+  });
   if (attr != cudaSuccess) return attr;
   const int grid =
       grid_for(k_compress<BF16, LAMB, MSIGN>, sms, a.geo.n_tiles, kCompressThreads, S::kBytes);

@@ -282,9 +282,11 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 template <bool LAMB, uint32_t WT>
 cudaError_t run_server(const ServerArgs& a, int sms, cudaStream_t s) {
   const size_t bytes = ServerSmem::bytes(a.geo.W);
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      k_server<LAMB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)ServerSmem::bytes(OB_MAX_WORKERS));
+  static PerDeviceOnce once;
+  const cudaError_t attr = once.run([] {
+    return cudaFuncSetAttribute(k_server<LAMB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ServerSmem::bytes(OB_MAX_WORKERS));
+  });
   if (attr != cudaSuccess) return attr;
   const int grid = grid_for(k_server<LAMB, WT>, sms, a.geo.n_tiles, kServerThreads, bytes);
   k_server<LAMB, WT><<<grid, kServerThreads, bytes, s>>>(a);

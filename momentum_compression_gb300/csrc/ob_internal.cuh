@@ -4,6 +4,7 @@
 // packing, and the host-side launchers.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -338,6 +339,24 @@ struct F16Args {
 const Geo* ctx_geo(const ob_ctx* ctx);
 const ob_config* ctx_config(const ob_ctx* ctx);
 ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg);
+
+// Runs a setup call (e.g. a kernel's dynamic shared-memory limit, which
+// is a per-device attribute) once on each device the process uses; one
+// instance per call site.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};  // bit d: done on device d (< 64)
+  template <typename F>
+  cudaError_t run(F f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = f();
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
 
 template <typename K>
 inline int grid_for(K kernel, int sms, uint64_t items, int threads = kThreads,
