@@ -1,4 +1,5 @@
-"""A compressed step captured in a CUDA graph and replayed gives the same
+"""CUDA graphs and streams.  A compressed step captured in a CUDA graph and
+replayed gives the same
 bits as the same steps called eagerly (1-bit Adam with the momentum in sign
 form, and 1-bit LAMB).  The library's calls allocate nothing and take every
 per-step quantity from device memory, so a replay is the step itself."""
@@ -79,3 +80,40 @@ def test_capture_refuses_host_schedules():
     with pytest.raises(ValueError):
         opt.capture_step(_grads(opt.n_pad, n, W, 0))   # momentum still dense
     opt.close()
+
+
+def test_two_contexts_on_two_streams_are_independent():
+    """Two jobs (own ctx, workspace and buffers) stepped concurrently on two
+    streams give the same bits as the same jobs stepped one after the
+    other: nothing in the library is shared between contexts."""
+    runs = []
+    for concurrent in (False, True):
+        jobs = [_make(False, 10 + j) for j in range(2)]
+        streams = [torch.cuda.Stream() for _ in range(2)]
+        torch.cuda.synchronize()  # the initial parameters were written on the default stream
+        for (opt, n, W), s in zip(jobs, streams):
+            with torch.cuda.stream(s):
+                for t in range(2):
+                    opt.warmup_step(_grads(opt.n_pad, n, W, t), stream=s)
+                opt.begin_compression(stream=s)
+        torch.cuda.synchronize()
+        grads = [[_grads(opt.n_pad, n, W, 10 * j + t) for t in range(4)]
+                 for j, (opt, n, W) in enumerate(jobs)]
+        torch.cuda.synchronize()
+        if concurrent:
+            for t in range(4):
+                for j, ((opt, n, W), s) in enumerate(zip(jobs, streams)):
+                    opt.compressed_step(grads[j][t], stream=s)
+        else:
+            for j, ((opt, n, W), s) in enumerate(zip(jobs, streams)):
+                for t in range(4):
+                    opt.compressed_step(grads[j][t], stream=s)
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        runs.append([(host(opt.p).copy(), host(opt.sbits).copy()) for opt, _, _ in jobs])
+        for opt, _, _ in jobs:
+            assert ob.ob_device_error(opt.ctx) == 0
+            opt.close()
+    for (p0, s0), (p1, s1) in zip(runs[0], runs[1]):
+        assert_bits_equal(p1, p0, "p")
+        assert_bits_equal(s1, s0, "sbits")
