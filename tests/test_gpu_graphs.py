@@ -1,8 +1,9 @@
 """CUDA graphs and streams.  A compressed step captured in a CUDA graph and
-replayed gives the same
-bits as the same steps called eagerly (1-bit Adam with the momentum in sign
-form, and 1-bit LAMB).  The library's calls allocate nothing and take every
-per-step quantity from device memory, so a replay is the step itself."""
+replayed gives the same bits as the same steps called eagerly (1-bit Adam
+with the momentum in sign form, and 1-bit LAMB): the library's calls
+allocate nothing and take every per-step quantity from device memory, so a
+replay is the step itself.  Two contexts stepped concurrently on two
+streams are independent."""
 import numpy as np
 import pytest
 import torch
