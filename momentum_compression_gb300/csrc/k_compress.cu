@@ -39,7 +39,9 @@ constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 // With the momentum in sign form (re-reading it costs 1/8 byte per element)
 // a tile's workers are taken in groups of at most kGroup, group-major over
 // the buffer: fewer workers' arrays are streamed at once, which measured
-// faster (compress at W = 3-4 ran at ~98% of the copy peak, at W = 8 ~90%).
+// faster (compress at W = 3-4 ran at ~98% of the copy peak, at W = 8 ~90%;
+// grouped, W = 8 and 16 run at ~97%).  With a dense m the groups measured
+// slower (m is re-read per group and its single buffer serialises them).
 constexpr uint32_t kGroup = 4;
 
 // A stage holds one (tile, worker) item: the gradient tile, the error tile
