@@ -52,13 +52,14 @@ def log(*a):
 # ---------------------------------------------------------------------------
 
 def bytes_per_element(W, G, lamb=False, sign_m=False):
-    """compress: m read 4 (sign form: the server's word, 1/8) + per worker
+    """compress: m read 4 (sign form: the server's word, 1/8, once per group
+    of up to 4 workers) + per worker
     g read G, e read 4 + write 4, old sign word read 1/8 + new word write
     1/8; server: W/8 word reads, e_s read 4 + write 4, sign word 1/8 + 1/8;
     Adam: sign word 1/8, v 4, p 4 + 4, m write 4 (none in sign form).  LAMB
     pass A: sign word 1/8, m 4+4, v_fresh 4+4, v_Tw 4; pass B: m 4, v_Tw 4,
     p 4+4."""
-    comp = (0.125 if sign_m else 4) + W * (G + 8 + 0.25)
+    comp = (0.125 * ((W + 3) // 4) if sign_m else 4) + W * (G + 8 + 0.25)
     serv = W / 8 + 8 + 0.25
     upd = (0.125 + 20 + 16) if lamb else (0.125 + 4 + 8 + (0 if sign_m else 4))
     return {"compress": comp, "server": serv, "update": upd, "total": comp + serv + upd}
