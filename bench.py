@@ -53,15 +53,20 @@ def log(*a):
 
 def bytes_per_element(W, G, lamb=False, sign_m=False):
     """compress: m read 4 (sign form: the server's word, 1/8, once per group
-    of up to 4 workers) + per worker
+    of up to 4 workers for Adam, once per tile for LAMB) + per worker
     g read G, e read 4 + write 4, old sign word read 1/8 + new word write
     1/8; server: W/8 word reads, e_s read 4 + write 4, sign word 1/8 + 1/8;
     Adam: sign word 1/8, v 4, p 4 + 4, m write 4 (none in sign form).  LAMB
     pass A: sign word 1/8, m 4+4, v_fresh 4+4, v_Tw 4; pass B: m 4, v_Tw 4,
-    p 4+4."""
-    comp = (0.125 * ((W + 3) // 4) if sign_m else 4) + W * (G + 8 + 0.25)
+    p 4+4.  LAMB in sign form: pass A reads the previous and the current
+    sign word (1/8 + 1/8) instead of m, pass B the current word instead of
+    m, and m is not written."""
+    comp = (0.125 * (1 if lamb else (W + 3) // 4) if sign_m else 4) + W * (G + 8 + 0.25)
     serv = W / 8 + 8 + 0.25
-    upd = (0.125 + 20 + 16) if lamb else (0.125 + 4 + 8 + (0 if sign_m else 4))
+    if lamb:
+        upd = (0.25 + 12 + 0.125 + 12) if sign_m else (0.125 + 20 + 16)
+    else:
+        upd = 0.125 + 4 + 8 + (0 if sign_m else 4)
     return {"compress": comp, "server": serv, "update": upd, "total": comp + serv + upd}
 
 
@@ -231,7 +236,7 @@ def recorded_traffic(workload, sign_m):
                 "2" if workload.grad_dtype == "bf16" else "4"):
             return None
         if kv.get("workload") != workload.name or kv.get("momentum") != (
-                "sign" if sign_m else "dense"):
+                "sign" if sign_m else "dense") or kv.get("mode", "adam") != workload.mode:
             return None
         return float(kv["dram_bytes_per_element"])
     except (OSError, KeyError, ValueError):
@@ -420,7 +425,7 @@ def run_ours(args, wl):
         pg = dist
     G = 2 if wl.grad_dtype == "bf16" else 4
     gdt = torch.bfloat16 if wl.grad_dtype == "bf16" else torch.float32
-    sign_m = wl.mode != "lamb" and not args.dense_m
+    sign_m = not args.dense_m
     opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype, wl.layer_offsets,
                              lamb=(wl.mode == "lamb"), device=device, sign_momentum=sign_m,
                              **wl.hp)
@@ -451,6 +456,9 @@ def run_ours(args, wl):
     for t in range(args.warmup):
         opt.compressed_step(gsets[t % 2])
     torch.cuda.synchronize()
+    if sign_m and not opt.m_in_signs:
+        raise SystemExit("bench: the sign-form momentum starts after one compressed step; "
+                         "give --warmup >= 1")
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -460,6 +468,39 @@ def run_ours(args, wl):
     uuid = getattr(props, "uuid", None)
     uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid)
     lamb = opt.lamb
+    db = opt.double_buffered  # LAMB in sign form: two server buffers
+
+    # the three rows of a compressed step through the public calls
+    def compress(g):
+        if db:
+            ob.ob_compress_signm_ls(opt.ctx, g, opt.sbits, opt.sscales, opt.err, opt.bits,
+                                    opt.scales, opt.ls)
+        elif sign_m:
+            ob.ob_compress_signm(opt.ctx, g, opt.sbits, opt.sscales, opt.err, opt.bits,
+                                 opt.scales)
+        else:
+            ob.ob_compress(opt.ctx, g, opt.m, opt.err, opt.bits, opt.scales, opt.ls)
+
+    def server():
+        if db:
+            ob.ob_server_reduce_db(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits,
+                                   opt.sscales, opt.sbits_alt, opt.sscales_alt, opt.ls)
+        else:
+            ob.ob_server_reduce(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
+                                opt.ls)
+
+    def update():
+        if db:
+            ob.ob_lamb_step_signm(opt.ctx, opt.sbits, opt.sscales, opt.sbits_alt,
+                                  opt.sscales_alt, opt.v, opt.v_fresh, opt.p, opt.ls)
+            opt._swap()  # this step's output becomes the current pair
+        elif lamb:
+            ob.ob_lamb_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.v_fresh, opt.m, opt.p,
+                            opt.ls)
+        else:
+            ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, None if sign_m else opt.m,
+                            opt.p)
+
     with ClockSampler(uuid) as clk:
         if pg:
             pg.barrier()
@@ -469,21 +510,11 @@ def run_ours(args, wl):
             g = gsets[t % 2]
             e = ev[t]
             e[0].record(stream)
-            if sign_m:
-                ob.ob_compress_signm(opt.ctx, g, opt.sbits, opt.sscales, opt.err, opt.bits,
-                                     opt.scales)
-            else:
-                ob.ob_compress(opt.ctx, g, opt.m, opt.err, opt.bits, opt.scales, opt.ls)
+            compress(g)
             e[1].record(stream)
-            ob.ob_server_reduce(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
-                                opt.ls)
+            server()
             e[2].record(stream)
-            if lamb:
-                ob.ob_lamb_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.v_fresh, opt.m, opt.p,
-                                opt.ls)
-            else:
-                ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, None if sign_m else opt.m,
-                                opt.p)
+            update()
             e[3].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -563,22 +594,12 @@ def run_ours(args, wl):
     def issue_step(t):
         b = t % 2
         stream.wait_event(ev_h2d[b])
-        if sign_m:
-            ob.ob_compress_signm(opt.ctx, gsets[b], opt.sbits, opt.sscales, opt.err, opt.bits,
-                                 opt.scales)
-        else:
-            ob.ob_compress(opt.ctx, gsets[b], opt.m, opt.err, opt.bits, opt.scales, opt.ls)
-        ob.ob_server_reduce(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
-                            opt.ls)
+        compress(gsets[b])
+        server()
         ev_used[b].record(stream)
         if t >= 1:
             stream.wait_event(ev_back)
-        if lamb:
-            ob.ob_lamb_step(opt.ctx, opt.sbits, opt.sscales, opt.v, opt.v_fresh, opt.m, opt.p,
-                            opt.ls)
-        else:
-            ob.ob_adam_step(opt.ctx, opt.sbits, opt.sscales, opt.v, None if sign_m else opt.m,
-                            opt.p)
+        update()
         ev_upd.record(stream)
         s_d2h.wait_event(ev_upd)
         with torch.cuda.stream(s_d2h):
@@ -625,7 +646,9 @@ def run_ours(args, wl):
         "vs_baseline": None, "dtype": "f32" if G == 4 else "f32 (bf16 gradients)",
         "data": "synthetic",
         "config": {"workload": wl_label(wl), "n": n, "W": wl.W, "chunk": wl.chunk,
-                   "momentum": ("sign form: sbits + chunk scales, exact (ob_compress_signm)"
+                   "momentum": (("sign form, server output double-buffered, exact "
+                                 "(ob_compress_signm_ls, ob_lamb_step_signm)") if db else
+                                "sign form: sbits + chunk scales, exact (ob_compress_signm)"
                                 if sign_m else "dense fp32"),
                    "n_layers": wl.n_layers, "grad_dtype": wl.grad_dtype,
                    "parallelism": "replicas" if world > 1 else "1 GPU",
@@ -962,7 +985,7 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="time the step as CUDA graph replays (1-bit workloads)")
     ap.add_argument("--dense-m", action="store_true",
-                    help="1-bit Adam: keep the momentum as a dense fp32 buffer")
+                    help="keep the momentum as a dense fp32 buffer (default: its exact sign form)")
     ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")
     ap.add_argument("--clip-value", type=float, default=0.0,
                     help="clamp of the compensated values (the write-up's stability variant)")

@@ -213,6 +213,17 @@ ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_
                             const float* sscales, float* const* err, uint32_t* bits,
                             float* scales, ob_stream_t stream);
 
+/* ob_compress_signm for 1-bit LAMB as well (ls != NULL): after a compressed
+ * LAMB step the momentum is exactly sscale*sign(sbit)/sigma_l of that
+ * step's server output (the update stores M/sigma_l, [LAMB] 1-2), and
+ * +-sscale/sigma_l is one correctly rounded division per layer.  ls == NULL
+ * is ob_compress_signm.  The same conditions apply; with LAMB the server
+ * output must be double-buffered (ob_server_reduce_db), because the
+ * update reads the previous step's words too (ob_lamb_step_signm). */
+ob_status ob_compress_signm_ls(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
+                               const float* sscales, float* const* err, uint32_t* bits,
+                               float* scales, const ob_layer_state* ls, ob_stream_t stream);
+
 /* Server average and re-compression, all partitions ([LAMB] 3-4):
  *   z = (sum_w scale_w(chunk)*sign_w)/W;  y = rho_l*e_s + z
  *   sscale(chunk) = mean |y|;  sbit = y >= 0;  e_s' = y - sscale*sign(y) */
@@ -220,6 +231,16 @@ ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits,
                            const float* scales, float* err_s, uint32_t* sbits,
                            float* sscales, const ob_layer_state* ls,
                            ob_stream_t stream);
+
+/* ob_server_reduce with the server output double-buffered: the deferred
+ * error e_s is decoded with the previous step's (sbits_old, sscales_old),
+ * and the new words and scales go to (sbits, sscales), leaving the old
+ * ones intact.  Each pair either is the same buffer (then this is
+ * ob_server_reduce) or does not overlap (OB_ERR_INVALID otherwise). */
+ob_status ob_server_reduce_db(ob_ctx* ctx, const uint32_t* bits, const float* scales,
+                              float* err_s, const uint32_t* sbits_old, const float* sscales_old,
+                              uint32_t* sbits, float* sscales, const ob_layer_state* ls,
+                              ob_stream_t stream);
 
 /* out = sscale*sign(sbit) (/ sigma_l if ls != NULL); padding -> 0. */
 ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits,
@@ -247,6 +268,16 @@ ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits,
                        float* v_fresh, float* m, float* p,
                        const ob_layer_state* ls, ob_stream_t stream);
 
+/* ob_lamb_step with the momentum in its sign form: the previous momentum
+ * is sscale_prev*sign(sbit_prev)/sigma_l from the previous step's server
+ * output, m_t = sscale*sign(sbit)/sigma_l from this step's, and no dense m
+ * is read or written.  The two server buffers must not overlap
+ * (OB_ERR_INVALID). */
+ob_status ob_lamb_step_signm(ob_ctx* ctx, const uint32_t* sbits_prev, const float* sscales_prev,
+                             const uint32_t* sbits, const float* sscales, const float* v_frozen,
+                             float* v_fresh, float* p, const ob_layer_state* ls,
+                             ob_stream_t stream);
+
 /* compress + server_reduce + adam_step (ls == NULL) or lamb_step, in one
  * call, in that order.  With m == NULL (1-bit Adam only) the momentum is
  * held in its sign form: ob_compress_signm + server + ob_adam_step without
@@ -256,6 +287,19 @@ ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m,
                   float* err_s, uint32_t* sbits, float* sscales,
                   const float* v_frozen, float* v_fresh, float* p,
                   const ob_layer_state* ls, ob_stream_t stream);
+
+/* One compressed step with the momentum in its sign form and the server
+ * output double-buffered, 1-bit Adam (ls == NULL) or 1-bit LAMB:
+ * ob_compress_signm_ls from (sbits_prev, sscales_prev), then
+ * ob_server_reduce_db into (sbits, sscales), then ob_adam_step without m or
+ * ob_lamb_step_signm.  The caller swaps the two buffers between steps.  The
+ * same conditions as ob_compress_signm apply (not the first compressed
+ * step after ob_begin_compression or ob_materialize_errors). */
+ob_status ob_step_db(ob_ctx* ctx, const void* const* grads, float* const* err, uint32_t* bits,
+                     float* scales, float* err_s, const uint32_t* sbits_prev,
+                     const float* sscales_prev, uint32_t* sbits, float* sscales,
+                     const float* v_frozen, float* v_fresh, float* p, const ob_layer_state* ls,
+                     ob_stream_t stream);
 
 /* Writes the true errors e' into err and err_s and zeroes scales and
  * sscales.  Call only after a complete step (the update has consumed the

@@ -36,6 +36,7 @@ EXPORTS = (
     "ob_compress_signm", "ob_reset_errors", "ob_quant_int8_ef",
     "ob_qb_sizes", "ob_zero_errors", "ob_compress_qb", "ob_server_reduce_qb", "ob_adam_step_qb",
     "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
+    "ob_compress_signm_ls", "ob_server_reduce_db", "ob_lamb_step_signm", "ob_step_db",
 )
 
 
@@ -110,6 +111,10 @@ def lib():
         L.ob_compress_f16.argtypes = [vp, i32, vp, vp, vp, vp, vp]
         L.ob_server_reduce_f16.argtypes = [vp, vp, vp, vp, vp]
         L.ob_adam_step_f16.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+        L.ob_compress_signm_ls.argtypes = [vp] * 9
+        L.ob_server_reduce_db.argtypes = [vp] * 10
+        L.ob_lamb_step_signm.argtypes = [vp] * 10
+        L.ob_step_db.argtypes = [vp] * 15
         for name in EXPORTS:
             if name != "ob_last_error":
                 getattr(L, name).restype = ct.c_int
@@ -251,6 +256,42 @@ def ob_compress_signm(ctx, grads, sbits, sscales, err, bits, scales, stream=None
            ctx)
 
 
+def ob_compress_signm_ls(ctx, grads, sbits, sscales, err, bits, scales, ls=None, stream=None):
+    """ob_compress_signm for 1-bit Adam (ls None) or 1-bit LAMB, the momentum
+    read as sscale*sign(sbit) (/ sigma_l for LAMB)."""
+    _check(lib().ob_compress_signm_ls(ctx, _ptr_array(grads), _ptr(sbits), _ptr(sscales),
+                                      _ptr_array(err), _ptr(bits), _ptr(scales), _ls(ls),
+                                      _stream(stream)), ctx)
+
+
+def ob_server_reduce_db(ctx, bits, scales, err_s, sbits_old, sscales_old, sbits, sscales,
+                        ls=None, stream=None):
+    """ob_server_reduce decoding e_s with (sbits_old, sscales_old) and writing
+    the new words and scales to (sbits, sscales)."""
+    _check(lib().ob_server_reduce_db(ctx, _ptr(bits), _ptr(scales), _ptr(err_s),
+                                     _ptr(sbits_old), _ptr(sscales_old), _ptr(sbits),
+                                     _ptr(sscales), _ls(ls), _stream(stream)), ctx)
+
+
+def ob_lamb_step_signm(ctx, sbits_prev, sscales_prev, sbits, sscales, v_frozen, v_fresh, p, ls,
+                       stream=None):
+    """ob_lamb_step with m_{t-1} and m_t read from the previous and the
+    current server output; no dense m."""
+    _check(lib().ob_lamb_step_signm(ctx, _ptr(sbits_prev), _ptr(sscales_prev), _ptr(sbits),
+                                    _ptr(sscales), _ptr(v_frozen), _ptr(v_fresh), _ptr(p),
+                                    _ls(ls), _stream(stream)), ctx)
+
+
+def ob_step_db(ctx, grads, err, bits, scales, err_s, sbits_prev, sscales_prev, sbits, sscales,
+               v_frozen, v_fresh, p, ls=None, stream=None):
+    """One compressed step, momentum in sign form, server output
+    double-buffered: reads (sbits_prev, sscales_prev), writes (sbits, sscales)."""
+    _check(lib().ob_step_db(ctx, _ptr_array(grads), _ptr_array(err), _ptr(bits), _ptr(scales),
+                            _ptr(err_s), _ptr(sbits_prev), _ptr(sscales_prev), _ptr(sbits),
+                            _ptr(sscales), _ptr(v_frozen), _ptr(v_fresh), _ptr(p), _ls(ls),
+                            _stream(stream)), ctx)
+
+
 def ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls=None, stream=None):
     _check(lib().ob_server_reduce(ctx, _ptr(bits), _ptr(scales), _ptr(err_s), _ptr(sbits),
                                   _ptr(sscales), _ls(ls), _stream(stream)), ctx)
@@ -368,9 +409,12 @@ class OneBitOptimizer:
 
     def __init__(self, n, W, chunk, align=4096, grad_dtype="f32", layer_offsets=None,
                  lamb=False, device="cuda", sign_momentum=False, reset_interval=0, **hp):
-        """sign_momentum (1-bit Adam only): after the first compressed step
-        the momentum is held as (sbits, sscales) -- exactly sscale*sign --
-        and the dense m buffer is only refreshed by materialize_m().
+        """sign_momentum: after the first compressed step the momentum is
+        held as (sbits, sscales) -- exactly sscale*sign, over sigma_l for
+        LAMB -- and the dense m buffer is only refreshed by materialize_m().
+        With LAMB the server output is double-buffered (the update reads
+        the previous step's words too): sbits/sscales always name the last
+        step's output, sbits_alt/sscales_alt the other pair.
         reset_interval > 0: before every reset_interval-th compressed step
         the worker and server errors are reset to 0 (ob_reset_errors).
         hp may hold clip_value (> 0: clamp of the compensated values)."""
@@ -378,7 +422,7 @@ class OneBitOptimizer:
         self.lamb = lamb
         self.reset_interval = reset_interval
         self.cstep = 0
-        self.sign_momentum = sign_momentum and not lamb
+        self.sign_momentum = sign_momentum
         self.m_in_signs = False
         self.grad_dtype = grad_dtype
         self.ctx = ob_init(n, W, chunk, align,
@@ -397,6 +441,9 @@ class OneBitOptimizer:
         self.scales = z(W, lay["n_chunks"])
         self.sbits = z(words, dt=torch.int32)
         self.sscales = z(lay["n_chunks"])
+        self.double_buffered = bool(sign_momentum and lamb)
+        self.sbits_alt = z(words, dt=torch.int32) if self.double_buffered else None
+        self.sscales_alt = z(lay["n_chunks"]) if self.double_buffered else None
         nbytes = ob_workspace_bytes(self.ctx)
         self.workspace = torch.zeros((nbytes + 255) // 256 * 256 // 4, dtype=torch.float32,
                                      device=device)
@@ -440,12 +487,27 @@ class OneBitOptimizer:
         if self.reset_interval and self.cstep and self.cstep % self.reset_interval == 0:
             self.reset_errors(stream)
         self.cstep += 1
+        if self.double_buffered and self.m_in_signs:
+            self._step_db(grads, stream)
+            return
         m = None if self.m_in_signs else self.m
         ob_step(self.ctx, grads, m, self.err, self.bits, self.scales, self.err_s,
                 self.sbits, self.sscales, self.v, self.v_fresh, self.p,
                 self.ls if self.lamb else None, stream)
         if self.sign_momentum and not self.m_in_signs:
             self.m_in_signs = True  # the next steps read the momentum from the signs
+
+    def _step_db(self, grads, stream=None):
+        """One double-buffered sign-form step; the new output becomes
+        (sbits, sscales)."""
+        ob_step_db(self.ctx, grads, self.err, self.bits, self.scales, self.err_s,
+                   self.sbits, self.sscales, self.sbits_alt, self.sscales_alt, self.v,
+                   self.v_fresh, self.p, self.ls if self.lamb else None, stream)
+        self._swap()
+
+    def _swap(self):
+        self.sbits, self.sbits_alt = self.sbits_alt, self.sbits
+        self.sscales, self.sscales_alt = self.sscales_alt, self.sscales
 
     def capture_step(self, grads):
         """Captures one compressed step on the gradient buffers `grads` into
@@ -462,6 +524,8 @@ class OneBitOptimizer:
             raise ValueError("capture_step: reset_interval is a host-side schedule")
         if self.sign_momentum and not self.m_in_signs:
             raise ValueError("capture_step: take the first compressed step eagerly")
+        if self.double_buffered:
+            return _AlternatingGraphs(self, grads)
         graph = torch.cuda.CUDAGraph()
         m = None if self.m_in_signs else self.m
         with torch.cuda.graph(graph):
@@ -473,13 +537,38 @@ class OneBitOptimizer:
     def materialize_m(self, stream=None):
         """Writes the dense momentum (it is exact: sscale*sign)."""
         if self.m_in_signs:
-            ob_decompress(self.ctx, self.sbits, self.sscales, self.m, None, stream)
+            ob_decompress(self.ctx, self.sbits, self.sscales, self.m,
+                          self.ls if self.lamb else None, stream)
             self.m_in_signs = False
 
     def materialize_errors(self, stream=None):
         self.materialize_m(stream)  # the sign form is lost once sscales are cleared
         ob_materialize_errors(self.ctx, self.err, self.bits, self.scales, self.err_s,
                               self.sbits, self.sscales, stream)
+
+
+class _AlternatingGraphs:
+    """Two CUDA graphs of one double-buffered sign-form step, one for each
+    orientation of the two server buffers; replay() runs the one that
+    matches the optimizer's current buffers and swaps them, so replays are
+    the same steps as eager calls."""
+
+    def __init__(self, opt, grads):
+        import torch
+        self.opt = opt
+        self.graphs = {}
+        for _ in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                ob_step_db(opt.ctx, grads, opt.err, opt.bits, opt.scales, opt.err_s,
+                           opt.sbits, opt.sscales, opt.sbits_alt, opt.sscales_alt, opt.v,
+                           opt.v_fresh, opt.p, opt.ls if opt.lamb else None)
+            self.graphs[opt.sbits.data_ptr()] = g
+            opt._swap()  # capture only records; the other orientation next
+
+    def replay(self):
+        self.graphs[self.opt.sbits.data_ptr()].replay()
+        self.opt._swap()
 
 
 class CodecGroup:

@@ -102,10 +102,13 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   }
   __syncthreads();
 
-  // work items: (worker group, tile), group-major; one group of all W
-  // workers when m is dense (it would be re-read per group)
-  const uint32_t gsz = MSIGN ? kGroup : G.W;
-  const uint32_t n_groups = MSIGN ? (G.W + kGroup - 1) / kGroup : 1u;
+  // work items: (worker group, tile), group-major.  Only 1-bit Adam with
+  // the sign-form m takes the workers in groups (fewer worker streams at
+  // once measured faster there); a dense m would be re-read per group, and
+  // 1-bit LAMB's per-tile layer setup measured slower repeated per group
+  constexpr bool kGrouped = MSIGN && !LAMB;
+  const uint32_t gsz = kGrouped ? kGroup : G.W;
+  const uint32_t n_groups = kGrouped ? (G.W + kGroup - 1) / kGroup : 1u;
   const uint32_t n_vt = G.n_tiles * n_groups;
 
   // ------------------------------------------------------------ producer
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     uint32_t item = 0, ti = 0;
     bool ok = true;
     for (uint32_t VT = blockIdx.x; ok && VT < n_vt; VT += gridDim.x, ++ti) {
-      const uint32_t gi = MSIGN ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
+      const uint32_t gi = kGrouped ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
       const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < G.W ? wbeg + gsz : G.W;
       const Tile tl = decode_tile(G, T);
       if constexpr (!MSIGN) {
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     }
   };
   if (blockIdx.x < n_vt) {
-    const uint32_t gi = MSIGN ? blockIdx.x / G.n_tiles : 0u, T0 = blockIdx.x - gi * G.n_tiles;
+    const uint32_t gi = kGrouped ? blockIdx.x / G.n_tiles : 0u, T0 = blockIdx.x - gi * G.n_tiles;
     if constexpr (MSIGN) load_msign(T0);
     const uint32_t wb = gi * gsz, nw = (wb + gsz < G.W ? wb + gsz : G.W) - wb;
     if ((uint32_t)p < nw)
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   named_sync(1, kConsumers);
   uint32_t item = 0, ti = 0;
   for (uint32_t VT = blockIdx.x; VT < n_vt; VT += gridDim.x, ++ti) {
-    const uint32_t gi = MSIGN ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
+    const uint32_t gi = kGrouped ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
     const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < G.W ? wbeg + gsz : G.W;
     const Tile tl = decode_tile(G, T);
     bool ok = true;
@@ -189,43 +192,13 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     const uint32_t VTn = VT + gridDim.x;
     uint32_t Tn = 0, nwn = 0;
     if (VTn < n_vt) {
-      const uint32_t gin = MSIGN ? VTn / G.n_tiles : 0u;
+      const uint32_t gin = kGrouped ? VTn / G.n_tiles : 0u;
       Tn = VTn - gin * G.n_tiles;
       const uint32_t wbn = gin * gsz;
       nwn = (wbn + gsz < G.W ? wbn + gsz : G.W) - wbn;
       if ((uint32_t)p < nwn)
         sc_next = __ldcg(A.scales + (uint64_t)(wbn + p) * G.nc + decode_tile(G, Tn).g);
     }
-    float4 mv[4];
-    bool valid[4];
-    if constexpr (MSIGN) {
-      const float mss = mss_next;
-      uint32_t mw_cur[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mw_cur[i] = mw_next[i];
-      if (VTn < n_vt) load_msign(Tn);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t off = 1024u * i + 4u * p;
-        valid[i] = off < tl.len;
-        const uint32_t wd = mw_cur[i] >> (4 * (p & 7));
-        mv[i] = make_float4((wd & 1u) ? mss : -mss, (wd & 2u) ? mss : -mss,
-                            (wd & 4u) ? mss : -mss, (wd & 8u) ? mss : -mss);
-      }
-    } else {
-      ok = s_abort == 0 && mbar_wait(mfull, ti & 1, err, kErrWaitFull);
-      if (!ok) s_abort = 1;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t off = 1024u * i + 4u * p;
-        valid[i] = off < tl.len;
-        mv[i] = valid[i] ? *reinterpret_cast<const float4*>(mbuf + off)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(mempty);
-    }
-
     // 1-bit LAMB: the layer of the tile's first element; every worker pass
     // walks the layers forward from it (layers change rarely inside a tile)
     uint32_t l_t = 0;
@@ -238,6 +211,60 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
     }
     const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
+    // the tile's m in registers, shared by its workers
+    float4 mv[4];
+    // row i (elements tl.start + 1024i + 4p + c) lies in the tile: padding
+    // rows inside the tile are still stored (as 0); an element is a real
+    // one if its row is valid and its index is below n.  1-bit LAMB tests
+    // the tile offset against a 32-bit limit instead (fewer registers
+    // there; for 1-bit Adam the 64-bit index test measured faster).
+    bool valid[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
+    [[maybe_unused]] const uint32_t lim =
+        !LAMB || G.n <= tl.start ? 0u
+                                 : (G.n - tl.start < tl.len ? (uint32_t)(G.n - tl.start) : tl.len);
+    auto real = [&](int i, int c, uint64_t k) {
+      if constexpr (LAMB) return 1024u * i + 4u * p + c < lim;
+      else return valid[i] && k < G.n;
+    };
+    if constexpr (MSIGN) {
+      // m = sscale*sign (1-bit Adam) or sscale*sign/sigma_l (1-bit LAMB);
+      // +-sscale/sigma = (+-sscale)/sigma exactly (IEEE division is
+      // symmetric in sign): one division per layer
+      const float mss = mss_next;
+      uint32_t mnib[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mnib[i] = mw_next[i] >> (4 * (p & 7));
+      if (VTn < n_vt) load_msign(Tn);
+      [[maybe_unused]] uint32_t lq = l_t;
+      [[maybe_unused]] uint64_t lqend = lend_t;
+      float q = LAMB ? __fdiv_rn(mss, s_t) : mss;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if constexpr (LAMB) {
+            const uint64_t k = tl.start + 1024u * i + 4u * p + c;
+            if (!uni && real(i, c, k) && advance_layer(A.ws.layer_off, G.L, k, lq, lqend))
+              q = __fdiv_rn(mss, __ldg(A.s + lq));
+          }
+          f4at(mv[i], c) = ((mnib[i] >> c) & 1u) ? q : -q;
+        }
+      }
+    } else {
+      ok = s_abort == 0 && mbar_wait(mfull, ti & 1, err, kErrWaitFull);
+      if (!ok) s_abort = 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t off = 1024u * i + 4u * p;
+        mv[i] = valid[i] ? *reinterpret_cast<const float4*>(mbuf + off)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(mempty);
+    }
+
 
     const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the word runs
     for (uint32_t w = wbeg; w < wend; ++w, ++item) {
@@ -249,27 +276,39 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       if (!ok) s_abort = 1;
       const unsigned char* st = stage0 + s * S::kStage;
       const uint32_t* sow = reinterpret_cast<const uint32_t*>(st + S::kStageG + S::kStageE);
-      float4 gv[4], ev[4];
+      // g and e of row i from the stage
+      auto fetch = [&](int i, float4& g4, float4& e4) {
+        const uint32_t off = 1024u * i + 4u * p;
+        if (valid[i]) {
+          if constexpr (BF16) {
+            const uint2 u = *reinterpret_cast<const uint2*>(st + off * 2);
+            g4 = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                             __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+          } else {
+            g4 = *reinterpret_cast<const float4*>(st + off * 4);
+          }
+          e4 = *reinterpret_cast<const float4*>(st + S::kStageG + off * 4);
+        } else {
+          g4 = e4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      };
+      // 1-bit Adam: the whole stage into registers and released at once;
+      // 1-bit LAMB (more live state per element): row by row inside the
+      // body, released after it -- the stages still in flight cover the
+      // memory latency, and the registers stay below the spill point
+      constexpr bool kLate = LAMB;
+      [[maybe_unused]] float4 gv[4], ev[4];
       uint32_t owd[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t off = 1024u * i + 4u * p;
         owd[i] = valid[i] ? sow[(off >> 5) + wshift] : 0u;
-        if (valid[i]) {
-          if constexpr (BF16) {
-            const uint2 u = *reinterpret_cast<const uint2*>(st + off * 2);
-            gv[i] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-          } else {
-            gv[i] = *reinterpret_cast<const float4*>(st + off * 4);
-          }
-          ev[i] = *reinterpret_cast<const float4*>(st + S::kStageG + off * 4);
-        } else {
-          gv[i] = ev[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        if constexpr (!kLate) fetch(i, gv[i], ev[i]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers now
+      if constexpr (!kLate) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers now
+      }
 
       // UNI: the whole tile lies in one layer (sigma, rho scalar); else the
       // layers are walked element by element
@@ -282,24 +321,26 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint64_t k0 = tl.start + 1024u * i + 4u * p;
-          float4 xv;
+          float4 xv, g4, e4;
+          if constexpr (kLate) fetch(i, g4, e4);
+          else g4 = gv[i], e4 = ev[i];
           uint32_t nib = 0;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float x = 0.0f;
-            if (valid[i] && k0 + c < G.n) {
+            if (real(i, c, k0 + c)) {
               const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;  // scale*sign
-              const float et = __fsub_rn(f4get(ev[i], c), so);
-              const float mw = __fadd_rn(__fmul_rn(b1, f4get(mv[i], c)),
-                                         __fmul_rn(ob1, f4get(gv[i], c)));
-              if constexpr (LAMB) {
-                if constexpr (!UNI) {
-                  if (advance_layer(A.ws.layer_off, G.L, k0 + c, l, lend)) {
-                    s_l = __ldg(A.s + l);
-                    r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l))
-                                     : 1.0f;
-                  }
+              const float et = __fsub_rn(f4get(e4, c), so);
+              if constexpr (LAMB && !UNI) {
+                if (advance_layer(A.ws.layer_off, G.L, k0 + c, l, lend)) {
+                  s_l = __ldg(A.s + l);
+                  r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l))
+                                   : 1.0f;
                 }
+              }
+              const float mw =
+                  __fadd_rn(__fmul_rn(b1, f4get(mv[i], c)), __fmul_rn(ob1, f4get(g4, c)));
+              if constexpr (LAMB) {
                 x = __fadd_rn(__fmul_rn(s_l, mw), __fmul_rn(r_l, et));
               } else {
                 x = __fadd_rn(mw, et);
@@ -322,6 +363,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
         return acc;
       };
       float acc = uni ? body(std::true_type{}) : body(std::false_type{});
+      if constexpr (kLate) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage has been read
+      }
       acc = warp_butterfly_sum(acc);
       if (lane == 0) ws[w][warp] = acc;
     }
@@ -360,8 +405,12 @@ cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms
               : run_compress<false, false, false>(a, sms, s);
 }
 
-cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, int sms, cudaStream_t s) {
-  return bf16 ? run_compress<true, false, true>(a, sms, s)
+cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, bool lamb, int sms,
+                                  cudaStream_t s) {
+  if (bf16)
+    return lamb ? run_compress<true, true, true>(a, sms, s)
+                : run_compress<true, false, true>(a, sms, s);
+  return lamb ? run_compress<false, true, true>(a, sms, s)
               : run_compress<false, false, true>(a, sms, s);
 }
 

@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
                  run, &full[s]);
       // the previous server words of this tile (only this CTA rewrites
       // them, after this copy has landed; the rounding words read beyond
-      // the tile are not used)
-      bulk_g2s(st + kTile * 4 + (size_t)G.W * kRunWords * 4, A.sbits + w0, run, &full[s]);
+      // the tile are not used).  They come from sbits_old, which is sbits
+      // itself unless the caller double-buffers the server output.
+      bulk_g2s(st + kTile * 4 + (size_t)G.W * kRunWords * 4, A.sbits_old + w0, run, &full[s]);
     }
     if (!ok) s_abort = 1;
     for (uint32_t k = 0; k < kSStages && k < ti; ++k) {
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + tn.g);
       if (p == 0) s_tile[(ti + 1) & 1] = tn;
     }
-    const float osc = __ldcg(A.sscales + tl.g);
+    const float osc = __ldcg(A.sscales_old + tl.g);
     bool valid[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;

@@ -92,6 +92,11 @@ __device__ void lamb_ratio_all(const UpdateArgs& A) {
   }
 }
 
+// SIGNM: the momentum is held in sign form -- m_{t-1} = sscale_prev *
+// sign(sbit_prev)/sigma_l from the previous step's server output (double
+// buffered by the caller) instead of a dense buffer, and m_t is not written
+// (it is the current server output over sigma_l).
+template <bool SIGNM>
 __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
   __shared__ int s_last;
   const Geo& G = A.geo;
@@ -99,11 +104,13 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
     const Tile tl = decode_tile(G, T);
     const float osc = __ldcg(A.sscales + tl.g);
+    [[maybe_unused]] const float oscp = SIGNM ? __ldcg(A.sscales_prev + tl.g) : 0.0f;
     const uint32_t l_t = __ldg(A.ws.tile_layer + T);
     const uint64_t lend_t = __ldg(A.ws.layer_off + l_t + 1);
     const float s_t = __ldg(A.ls.s + l_t);
     // all loads of the tile first
     uint32_t wd[4];
+    [[maybe_unused]] uint32_t wdp[4];
     float4 mv[4], vt[4], vf[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -112,7 +119,11 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
       const bool live = off < tl.len && k0 < G.n;
       const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
       wd[i] = live ? __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7)) : 0u;
-      mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
+      if constexpr (SIGNM) {
+        wdp[i] = live ? __ldg(A.sbits_prev + (k0 >> 5)) >> (4 * (p & 7)) : 0u;
+      } else {
+        mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
+      }
       vt[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_fresh + k0)) : z4;
       vf[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0)) : z4;
     }
@@ -127,6 +138,7 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
       // M/sigma = +-(sscale/sigma) exactly (IEEE division is symmetric in
       // sign): one division per layer instead of one per element
       float q_l = __fdiv_rn(osc, s_t);
+      [[maybe_unused]] float qp_l = SIGNM ? __fdiv_rn(oscp, s_t) : 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
         for (int c = 0; c < 4; ++c) {
           const uint64_t k = k0 + c;
           if (1024u * i + 4u * p >= tl.len || k >= G.n) {
-            f4at(mv[i], c) = 0.0f;
+            if constexpr (!SIGNM) f4at(mv[i], c) = 0.0f;
             continue;
           }
           if constexpr (!UNI) {
@@ -142,15 +154,19 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
             if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
               if (rmax > 0.0f) atomicMax(A.ws.Rbits + l_old, __float_as_uint(rmax));
               rmax = 0.0f;
-              q_l = __fdiv_rn(osc, __ldg(A.ls.s + l));
+              const float sg = __ldg(A.ls.s + l);
+              q_l = __fdiv_rn(osc, sg);
+              if constexpr (SIGNM) qp_l = __fdiv_rn(oscp, sg);
             }
           }
           const float mt = ((wd[i] >> c) & 1u) ? q_l : -q_l;
-          const float gt =
-              __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, f4get(mv[i], c))), A.ob1);
+          float mprev;
+          if constexpr (SIGNM) mprev = ((wdp[i] >> c) & 1u) ? qp_l : -qp_l;
+          else mprev = f4get(mv[i], c);
+          const float gt = __fdiv_rn(__fsub_rn(mt, __fmul_rn(A.b1, mprev)), A.ob1);
           const float v = __fadd_rn(__fmul_rn(A.b2, f4get(vt[i], c)),
                                     __fmul_rn(A.ob2, __fmul_rn(gt, gt)));
-          f4at(mv[i], c) = mt;
+          if constexpr (!SIGNM) f4at(mv[i], c) = mt;
           f4at(vt[i], c) = v;
           const float ratio = __fdiv_rn(f4get(vf[i], c), v);
           if (ratio > rmax) rmax = ratio;  // NaN never wins
@@ -164,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
       const uint32_t off = 1024u * i + 4u * p;
       if (off >= tl.len) continue;
       const uint64_t k0 = tl.start + off;
-      __stcs(reinterpret_cast<float4*>(A.m + k0), mv[i]);
+      if constexpr (!SIGNM) __stcs(reinterpret_cast<float4*>(A.m + k0), mv[i]);
       if (k0 < G.n) __stcs(reinterpret_cast<float4*>(A.v_fresh + k0), vt[i]);
     }
     // Flush the running max: one atomic per warp when all its lanes ended
@@ -193,6 +209,9 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
   }
 }
 
+// SIGNM: m_t = sscale*sign(sbit)/sigma_l from the server output (the
+// momentum held in sign form) instead of a dense buffer.
+template <bool SIGNM>
 __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
   const Geo& G = A.geo;
   const int p = threadIdx.x;
@@ -202,6 +221,8 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
     const uint32_t l_t = __ldg(A.ws.tile_layer + T);
     const uint64_t lend_t = __ldg(A.ws.layer_off + l_t + 1);
     const float t1_t = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l_t));
+    [[maybe_unused]] const float osc = SIGNM ? __ldcg(A.sscales + tl.g) : 0.0f;
+    [[maybe_unused]] uint32_t wd[4];
     float4 mv[4], vf[4], pv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -209,7 +230,10 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
       const uint64_t k0 = tl.start + off;
       const bool live = off < tl.len && k0 < G.n;
       const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
+      if constexpr (SIGNM)
+        wd[i] = live ? __ldg(A.sbits + (k0 >> 5)) >> (4 * (p & 7)) : 0u;
+      else
+        mv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.m + k0)) : z4;
       vf[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.v_frozen + k0)) : z4;
       pv[i] = live ? __ldcs(reinterpret_cast<const float4*>(A.p + k0)) : z4;
     }
@@ -218,6 +242,8 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
       uint32_t l = l_t;
       uint64_t lend = lend_t;
       float t1 = t1_t;
+      // m_t = +-(sscale/sigma_l), the value pass A computed
+      [[maybe_unused]] float q_l = SIGNM ? __fdiv_rn(osc, __ldg(A.ls.s + l_t)) : 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;
@@ -226,11 +252,16 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
           const uint64_t k = k0 + c;
           if (1024u * i + 4u * p >= tl.len || k >= G.n) continue;
           if constexpr (!UNI) {
-            if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
+            if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) {
               t1 = __fmul_rn(A.lr, __ldcg(A.ls.c_t + l));
+              if constexpr (SIGNM) q_l = __fdiv_rn(osc, __ldg(A.ls.s + l));
+            }
           }
+          float mt;
+          if constexpr (SIGNM) mt = ((wd[i] >> c) & 1u) ? q_l : -q_l;
+          else mt = f4get(mv[i], c);
           const float d = __fadd_rn(__fsqrt_rn(f4get(vf[i], c)), A.eps);
-          const float u = __fdiv_rn(f4get(mv[i], c), d);
+          const float u = __fdiv_rn(mt, d);
           f4at(pv[i], c) = __fsub_rn(f4get(pv[i], c), __fmul_rn(t1, u));
         }
       }
@@ -333,12 +364,18 @@ cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s) {
 }
 
 cudaError_t launch_lamb_pass_a(const UpdateArgs& a, int sms, cudaStream_t s) {
-  k_lamb_pass_a<<<grid_for(k_lamb_pass_a, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  if (a.m)
+    k_lamb_pass_a<false><<<grid_for(k_lamb_pass_a<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  else
+    k_lamb_pass_a<true><<<grid_for(k_lamb_pass_a<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s) {
-  k_lamb_pass_b<<<grid_for(k_lamb_pass_b, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  if (a.m)
+    k_lamb_pass_b<false><<<grid_for(k_lamb_pass_b<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  else
+    k_lamb_pass_b<true><<<grid_for(k_lamb_pass_b<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -429,16 +429,29 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, flo
                   "compress: chunk scales");
 }
 
-ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scales, float* err_s,
-                           uint32_t* sbits, float* sscales, const ob_layer_state* ls,
-                           ob_stream_t stream) {
+// Two device ranges [a, a+na) and [b, b+nb) share a byte.
+static bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+static ob_status server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scales,
+                               float* err_s, const uint32_t* sbits_old, const float* sscales_old,
+                               uint32_t* sbits, float* sscales, const ob_layer_state* ls,
+                               ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
   OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
   OB_CHECK_PTR(ctx, err_s, 16, "err_s");
+  OB_CHECK_PTR(ctx, sbits_old, 16, "sbits_old");
+  OB_CHECK_PTR(ctx, sscales_old, 4, "sscales_old");
   OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
+  const size_t wb = (size_t)ctx->geo.words * sizeof(uint32_t), cb = (size_t)ctx->geo.nc * 4;
+  if ((sbits_old != sbits && overlap(sbits_old, wb, sbits, wb)) ||
+      (sscales_old != sscales && overlap(sscales_old, cb, sscales, cb)))
+    return fail(ctx, OB_ERR_INVALID, "old and new server buffers overlap without being equal");
   if (ls && (st = check_ls(ctx, ls, false))) return st;
   ob::ServerArgs a{};
   a.geo = ctx->geo;
@@ -448,6 +461,8 @@ ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scale
   a.e_s = err_s;
   a.sbits = sbits;
   a.sscales = sscales;
+  a.sbits_old = sbits_old;
+  a.sscales_old = sscales_old;
   if (ls) {
     a.c_prev = ls->c_prev;
     a.c_prev2 = ls->c_prev2;
@@ -458,6 +473,20 @@ ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scale
     return st;
   return launched(ctx, ob::launch_finalize_scales(ctx->geo, ctx->ws.spart, 1, sscales, ctx->sms, s),
                   "server_reduce: chunk scales");
+}
+
+ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scales, float* err_s,
+                           uint32_t* sbits, float* sscales, const ob_layer_state* ls,
+                           ob_stream_t stream) {
+  return server_reduce(ctx, bits, scales, err_s, sbits, sscales, sbits, sscales, ls, stream);
+}
+
+ob_status ob_server_reduce_db(ob_ctx* ctx, const uint32_t* bits, const float* scales,
+                              float* err_s, const uint32_t* sbits_old, const float* sscales_old,
+                              uint32_t* sbits, float* sscales, const ob_layer_state* ls,
+                              ob_stream_t stream) {
+  return server_reduce(ctx, bits, scales, err_s, sbits_old, sscales_old, sbits, sscales, ls,
+                       stream);
 }
 
 static void fill_update(const ob_ctx* ctx, ob::UpdateArgs& a) {
@@ -520,22 +549,35 @@ ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                   "adam_step");
 }
 
-ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
-                       const float* v_frozen, float* v_fresh, float* m, float* p,
-                       const ob_layer_state* ls, ob_stream_t stream) {
+// m != NULL: dense momentum (read as m_{t-1}, written as m_t); m == NULL:
+// m_{t-1} from (sbits_prev, sscales_prev) and m_t not written.
+static ob_status lamb_step(ob_ctx* ctx, const uint32_t* sbits_prev, const float* sscales_prev,
+                           const uint32_t* sbits, const float* sscales, const float* v_frozen,
+                           float* v_fresh, float* m, float* p, const ob_layer_state* ls,
+                           ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
   OB_CHECK_PTR(ctx, sbits, 16, "sbits");
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, v_frozen, 16, "v_frozen");
   OB_CHECK_PTR(ctx, v_fresh, 16, "v_fresh");
-  OB_CHECK_PTR(ctx, m, 16, "m");
+  if (m) {
+    OB_CHECK_PTR(ctx, m, 16, "m");
+  } else {
+    OB_CHECK_PTR(ctx, sbits_prev, 16, "sbits_prev");
+    OB_CHECK_PTR(ctx, sscales_prev, 4, "sscales_prev");
+    if (overlap(sbits_prev, (size_t)ctx->geo.words * 4, sbits, (size_t)ctx->geo.words * 4) ||
+        overlap(sscales_prev, (size_t)ctx->geo.nc * 4, sscales, (size_t)ctx->geo.nc * 4))
+      return fail(ctx, OB_ERR_INVALID, "the previous and current server buffers must be disjoint");
+  }
   OB_CHECK_PTR(ctx, p, 16, "p");
   if ((st = check_ls(ctx, ls, false))) return st;
   ob::UpdateArgs a{};
   fill_update(ctx, a);
   a.sbits = sbits;
   a.sscales = sscales;
+  a.sbits_prev = sbits_prev;
+  a.sscales_prev = sscales_prev;
   a.v_frozen = v_frozen;
   a.v_fresh = v_fresh;
   a.m = m;
@@ -546,9 +588,26 @@ ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
   return launched(ctx, ob::launch_lamb_pass_b(a, ctx->sms, s), "lamb_step pass B");
 }
 
-ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
-                            const float* sscales, float* const* err, uint32_t* bits,
-                            float* scales, ob_stream_t stream) {
+ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
+                       const float* v_frozen, float* v_fresh, float* m, float* p,
+                       const ob_layer_state* ls, ob_stream_t stream) {
+  ob_status st = ready(ctx);
+  if (st) return st;
+  OB_CHECK_PTR(ctx, m, 16, "m");
+  return lamb_step(ctx, nullptr, nullptr, sbits, sscales, v_frozen, v_fresh, m, p, ls, stream);
+}
+
+ob_status ob_lamb_step_signm(ob_ctx* ctx, const uint32_t* sbits_prev, const float* sscales_prev,
+                             const uint32_t* sbits, const float* sscales, const float* v_frozen,
+                             float* v_fresh, float* p, const ob_layer_state* ls,
+                             ob_stream_t stream) {
+  return lamb_step(ctx, sbits_prev, sscales_prev, sbits, sscales, v_frozen, v_fresh, nullptr, p,
+                   ls, stream);
+}
+
+ob_status ob_compress_signm_ls(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
+                               const float* sscales, float* const* err, uint32_t* bits,
+                               float* scales, const ob_layer_state* ls, ob_stream_t stream) {
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_grads(ctx, grads)) || (st = check_errs(ctx, err))) return st;
@@ -556,6 +615,7 @@ ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_
   OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   OB_CHECK_PTR(ctx, bits, 16, "bits");
   OB_CHECK_PTR(ctx, scales, 4, "scales");
+  if (ls && (st = check_ls(ctx, ls, false))) return st;
   ob::CompressArgs a{};
   a.geo = ctx->geo;
   a.ws = ctx->ws;
@@ -567,19 +627,31 @@ ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_
   a.msscales = sscales;
   a.bits = bits;
   a.scales = scales;
-  a.ratio_ef = 1;
+  if (ls) {
+    a.s = ls->s;
+    a.c_prev = ls->c_prev;
+    a.c_prev2 = ls->c_prev2;
+  }
+  a.ratio_ef = (ctx->cfg.flags & OB_FLAG_NO_RATIO_EF) ? 0 : 1;
   a.b1 = ctx->cfg.b1;
   a.ob1 = 1.0f - ctx->cfg.b1;
   a.clip = ctx->cfg.clip_value;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launched(ctx,
-                     ob::launch_compress_signm(a, ctx->cfg.grad_dtype == OB_GRAD_BF16, ctx->sms, s),
+                     ob::launch_compress_signm(a, ctx->cfg.grad_dtype == OB_GRAD_BF16,
+                                               ls != nullptr, ctx->sms, s),
                      "compress_signm")))
     return st;
   return launched(ctx,
                   ob::launch_finalize_scales(ctx->geo, ctx->ws.wpart, ctx->geo.W, scales,
                                              ctx->sms, s),
                   "compress_signm: chunk scales");
+}
+
+ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
+                            const float* sscales, float* const* err, uint32_t* bits,
+                            float* scales, ob_stream_t stream) {
+  return ob_compress_signm_ls(ctx, grads, sbits, sscales, err, bits, scales, nullptr, stream);
 }
 
 ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m, float* const* err,
@@ -599,6 +671,23 @@ ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m, float* const*
   if ((st = ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls, stream))) return st;
   if (!ls) return ob_adam_step(ctx, sbits, sscales, v_frozen, m, p, stream);
   return ob_lamb_step(ctx, sbits, sscales, v_frozen, v_fresh, m, p, ls, stream);
+}
+
+ob_status ob_step_db(ob_ctx* ctx, const void* const* grads, float* const* err, uint32_t* bits,
+                     float* scales, float* err_s, const uint32_t* sbits_prev,
+                     const float* sscales_prev, uint32_t* sbits, float* sscales,
+                     const float* v_frozen, float* v_fresh, float* p, const ob_layer_state* ls,
+                     ob_stream_t stream) {
+  ob_status st;
+  if ((st = ob_compress_signm_ls(ctx, grads, sbits_prev, sscales_prev, err, bits, scales, ls,
+                                 stream)))
+    return st;
+  if ((st = ob_server_reduce_db(ctx, bits, scales, err_s, sbits_prev, sscales_prev, sbits,
+                                sscales, ls, stream)))
+    return st;
+  if (!ls) return ob_adam_step(ctx, sbits, sscales, v_frozen, nullptr, p, stream);
+  return ob_lamb_step_signm(ctx, sbits_prev, sscales_prev, sbits, sscales, v_frozen, v_fresh, p,
+                            ls, stream);
 }
 
 ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,

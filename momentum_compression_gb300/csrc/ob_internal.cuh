@@ -238,6 +238,8 @@ struct ServerArgs {
   float* e_s;
   uint32_t* sbits;
   float* sscales;
+  const uint32_t* sbits_old;  // the previous server words and scales (the
+  const float* sscales_old;   // deferred error's); == sbits/sscales unless double-buffered
   const float* c_prev;
   const float* c_prev2;
   int ratio_ef;
@@ -250,7 +252,9 @@ struct UpdateArgs {
   const float* sscales;
   const float* v_frozen;
   float* v_fresh;
-  float* m;
+  float* m;              // null: the momentum is held in sign form
+  const uint32_t* sbits_prev;  // LAMB, sign form: the previous step's server words
+  const float* sscales_prev;   // and scales (m_{t-1} = sscale*sign/sigma)
   float* p;
   float* out;            // decompress
   ob_layer_state ls;     // LAMB arrays (device pointers)
@@ -373,7 +377,8 @@ inline int grid_for(K kernel, int sms, uint64_t items, int threads = kThreads,
 
 cudaError_t launch_compress(const CompressArgs& a, bool bf16, bool lamb, int sms,
                             cudaStream_t s);
-cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, int sms, cudaStream_t s);
+cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, bool lamb, int sms,
+                                  cudaStream_t s);
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s);
 cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
                                    float* scales, int sms, cudaStream_t s);

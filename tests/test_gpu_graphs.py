@@ -1,6 +1,8 @@
 """CUDA graphs and streams.  A compressed step captured in a CUDA graph and
 replayed gives the same bits as the same steps called eagerly (1-bit Adam
-with the momentum in sign form, and 1-bit LAMB): the library's calls
+with the momentum in sign form, 1-bit LAMB with a dense momentum and with
+the momentum in sign form, whose two server buffers alternate between two
+graphs): the library's calls
 allocate nothing and take every per-step quantity from device memory, so a
 replay is the step itself.  Two contexts stepped concurrently on two
 streams are independent."""
@@ -24,13 +26,13 @@ def _cuda():
     _build.build()
 
 
-def _make(lamb, seed):
+def _make(lamb, seed, sm=None):
     n, W = 300_001, 4
     off = [0, 1000, 70_000, 250_000, n] if lamb else None
     hp = dict(HP, **(dict(r_thr=0.1, r_min=0.5, r_max=4.0, c_min=0.01, c_max=10.0)
                      if lamb else {}))
     opt = ob.OneBitOptimizer(n, W, 1 << 16, 4096, "f32", off, lamb=lamb,
-                             sign_momentum=not lamb, **hp)
+                             sign_momentum=(not lamb) if sm is None else sm, **hp)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     opt.p[:n] = torch.randn(n, generator=gen, device="cuda") * 0.02
@@ -48,10 +50,10 @@ def _grads(n_pad, n, W, step):
     return out
 
 
-@pytest.mark.parametrize("lamb", [False, True])
-def test_graph_replay_matches_eager_steps(lamb):
-    a, n, W = _make(lamb, 1)
-    b, _, _ = _make(lamb, 1)
+@pytest.mark.parametrize("lamb,sm", [(False, True), (True, False), (True, True)])
+def test_graph_replay_matches_eager_steps(lamb, sm):
+    a, n, W = _make(lamb, 1, sm)
+    b, _, _ = _make(lamb, 1, sm)
     for opt in (a, b):
         for t in range(3):
             opt.warmup_step(_grads(opt.n_pad, n, W, t))
@@ -68,6 +70,7 @@ def test_graph_replay_matches_eager_steps(lamb):
         torch.cuda.synchronize()
         assert_bits_equal(host(b.p), host(a.p), f"p after step {t}")
         assert_bits_equal(host(b.sbits), host(a.sbits), f"sbits after step {t}")
+        assert_bits_equal(host(b.sscales), host(a.sscales), f"sscales after step {t}")
         assert_bits_equal(host(b.err_s), host(a.err_s), f"e_s after step {t}")
         if lamb:
             assert_bits_equal(host(b.ls.c_t), host(a.ls.c_t), f"c_t after step {t}")

@@ -299,22 +299,28 @@ LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=
                c_min=0.01, c_max=10.0)
 
 
-@pytest.mark.parametrize("flags,W,dt", [
-    (0, 4, "f32"), (ob.OB_FLAG_NO_RATIO_EF, 4, "f32"), (ob.OB_FLAG_FROZEN_C, 4, "f32"),
-    (0, 8, "bf16"),   # the W = 8 server specialisation, bf16 worker kernel
-    (0, 3, "f32"),    # generic W
-    (0, 12, "bf16"),  # workers beyond the 8-worker sign table
+@pytest.mark.parametrize("flags,W,dt,sm", [
+    (0, 4, "f32", False), (ob.OB_FLAG_NO_RATIO_EF, 4, "f32", False),
+    (ob.OB_FLAG_FROZEN_C, 4, "f32", False),
+    (0, 8, "bf16", False),   # the W = 8 server specialisation, bf16 worker kernel
+    (0, 3, "f32", False),    # generic W
+    (0, 12, "bf16", False),  # workers beyond the 8-worker sign table
+    # the momentum in sign form, server output double-buffered
+    (0, 4, "f32", True), (ob.OB_FLAG_NO_RATIO_EF, 3, "f32", True),
+    (ob.OB_FLAG_FROZEN_C, 8, "bf16", True), (0, 12, "bf16", True),
 ])
-def test_lamb_small_layers(flags, W, dt):
+def test_lamb_small_layers(flags, W, dt, sm):
     """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
     chunk 2048, 3 warmup + 6 compressed steps with the gradient std falling
     3x per step, so that r_t moves and the step-ratio error feedback
-    differs from 1."""
+    differs from 1.  sm: the momentum held as sscale*sign/sigma_l of the
+    server output (ob_step_db from the second compressed step on), which
+    must give the dense path's results bit for bit."""
     sizes = [7, 1, 2, 4095, 4097, 33, 1000, 20000, 3, 30000]
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.uint64)
     n, A, C = int(off[-1]), 32, 2048
     opt = ob.OneBitOptimizer(n, W, C, A, dt, [int(x) for x in off], lamb=True, flags=flags,
-                             **LAMB_HP)
+                             sign_momentum=sm, **LAMB_HP)
     lay = O.Layout(n, W, A, C)
     layers = O.Layers(off)
     st = O.State(lay, layers, lamb=True)
@@ -358,11 +364,17 @@ def test_lamb_small_layers(flags, W, dt):
     frozen = bool(flags & ob.OB_FLAG_FROZEN_C)
     for t in range(warm, warm + steps):
         gh, gd = grads(t)
+        prev = (st.sbits.copy(), st.sscales.copy())
         opt.compressed_step(gd)
         O.compressed_step(st, gh, hp, lamb=True, ratio_ef=ratio_ef, frozen=frozen)
         torch.cuda.synchronize()
         assert_bits_equal(host(opt.sbits)[: lay.words], st.sbits, f"sbits at step {t}")
+        assert_bits_equal(host(opt.sscales), st.sscales, f"sscales at step {t}")
         assert_bits_equal(host(opt.ls.c_t), st.c, f"c_t at step {t}")
+        if sm and t > warm:  # the previous output is left intact in the other buffer
+            assert opt.m_in_signs
+            assert_bits_equal(host(opt.sbits_alt)[: lay.words], prev[0], f"old sbits at {t}")
+            assert_bits_equal(host(opt.sscales_alt), prev[1], f"old sscales at {t}")
     for k in ("r_prev", "c_prev", "c_prev2"):
         assert_bits_equal(host(getattr(opt.ls, k)), st.ls[k], f"end: {k}")
     if not frozen:
