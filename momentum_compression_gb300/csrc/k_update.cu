@@ -17,9 +17,32 @@
 #include <type_traits>
 
 #include "ob_internal.cuh"
+#include "ptx.cuh"
 
 namespace ob {
 namespace {
+
+// Thread 0 asks the copy engine to bring tile Tn's rows of the given fp32
+// arrays and the runs of the given sign-word arrays covering it into L2,
+// while the CTA works on the current tile: the next grid-stride tile's
+// loads then hit L2.  Tiles start on multiples of 32 elements and hold a
+// multiple of 32, so the rows are 128-byte aligned; the word runs are
+// widened to 16-byte boundaries, which stay inside the rows (padded to 16
+// bytes).  Null arrays are skipped.
+__device__ __forceinline__ void prefetch_tile(const Geo& G, uint32_t Tn, const float* a0,
+                                              const float* a1, const float* a2,
+                                              const uint32_t* w0, const uint32_t* w1) {
+  if (threadIdx.x != 0 || Tn >= G.n_tiles) return;
+  const Tile t = decode_tile(G, Tn);
+  const uint32_t bytes = t.len * 4u;
+  if (a0) bulk_prefetch_l2(a0 + t.start, bytes);
+  if (a1) bulk_prefetch_l2(a1 + t.start, bytes);
+  if (a2) bulk_prefetch_l2(a2 + t.start, bytes);
+  const uint64_t wb = (t.start >> 5) & ~3ull;
+  const uint64_t we = (((t.start + t.len + 31) >> 5) + 3) & ~3ull;
+  if (w0) bulk_prefetch_l2(w0 + wb, (uint32_t)(we - wb) * 4u);
+  if (w1) bulk_prefetch_l2(w1 + wb, (uint32_t)(we - wb) * 4u);
+}
 
 __global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
   const Geo& G = A.geo;
@@ -28,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
   float* __restrict__ pp = A.p;
   float* __restrict__ mm = A.m;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    prefetch_tile(G, T + gridDim.x, vf, pp, nullptr, A.sbits, nullptr);
     const Tile tl = decode_tile(G, T);
     const float osc = __ldcg(A.sscales + tl.g);
     // all loads of the tile first (4 sign words, 4 x 2 128-bit rows), then
@@ -139,6 +163,9 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_a(const UpdateArgs A) {
       // sign): one division per layer instead of one per element
       float q_l = __fdiv_rn(osc, s_t);
       [[maybe_unused]] float qp_l = SIGNM ? __fdiv_rn(oscp, s_t) : 0.0f;
+      // (With the momentum in sign form g takes only +-g_same and +-g_diff
+      // per layer, but precomputing them measured slower: the per-element
+      // division keeps the tile's loads overlapped with more work.)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint64_t k0 = tl.start + 1024u * i + 4u * p;
@@ -216,6 +243,8 @@ __global__ void __launch_bounds__(kThreads) k_lamb_pass_b(const UpdateArgs A) {
   const Geo& G = A.geo;
   const int p = threadIdx.x;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+    prefetch_tile(G, T + gridDim.x, A.v_frozen, A.p, SIGNM ? nullptr : A.m,
+                  SIGNM ? A.sbits : nullptr, nullptr);
     const Tile tl = decode_tile(G, T);
     if (tl.start >= G.n) continue;
     const uint32_t l_t = __ldg(A.ws.tile_layer + T);

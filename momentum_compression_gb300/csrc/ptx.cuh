@@ -90,6 +90,13 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       : "memory");
 }
 
+// Asks the copy engine to bring `bytes` (multiple of 16; address 16-byte
+// aligned) of global memory into L2.  A hint: nothing is returned to the
+// SM and nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
