@@ -45,7 +45,7 @@ struct ServerSmem {
     return kTile * 4 + (size_t)(W + 1) * kRunWords * 4;
   }
   __host__ __device__ static size_t bytes(uint32_t W) {
-    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 2 * OB_MAX_WORKERS * 4 +
+    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 3 * OB_MAX_WORKERS * 4 +
            2 * 256 * 4;
   }
 };
@@ -69,10 +69,17 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSStages * stage_bytes);
   uint64_t* empty = full + kSStages;
   float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(empty + kSStages);
-  float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 2);
-  __shared__ float ws[8];
+  float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 3);
+  __shared__ float ws[2][8];
   __shared__ volatile int s_abort;
   __shared__ Tile s_tile[2];  // the current and the next tile, decoded by thread 0
+  // per-tile scalars of the current and the next tile, loaded by thread 0 a
+  // tile ahead so that no consumer waits on them: the previous server
+  // scale of the tile's chunk and (1-bit LAMB) the tile's first layer, its
+  // end and its step-ratio factor rho
+  __shared__ float s_osc[2], s_r[2];
+  __shared__ uint32_t s_l[2];
+  __shared__ uint64_t s_lend[2];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned* err = A.ws.err;
@@ -130,10 +137,31 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   const uint32_t Wc = WT ? WT : G.W;
   // scales of the first tile
   const uint32_t W8 = Wc < 8 ? Wc : 8;
+  // the layer factor rho = c_prev2/c_prev of layer l (1 without the
+  // step-ratio error feedback)
+  auto rho = [&](uint32_t l) {
+    return A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
+  };
+  // One barrier per tile: the worker scales are loaded two tiles ahead
+  // (ring of 3), so that the z table of tile t+1 can be built during tile
+  // t from scales published by the barrier ending tile t-1; the tile
+  // totals are double-buffered.
+  if (blockIdx.x + gridDim.x < G.n_tiles && (uint32_t)p < Wc)
+    s_sc[1][p] =
+        __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x + gridDim.x).g);
   if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc) {
     const Tile tl = decode_tile(G, blockIdx.x);
     s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
-    if (p == 0) s_tile[0] = tl;
+    if (p == 0) {
+      s_tile[0] = tl;
+      s_osc[0] = __ldcg(A.sscales_old + tl.g);
+      if constexpr (LAMB) {
+        const uint32_t l = __ldg(A.ws.tile_layer + blockIdx.x);
+        s_l[0] = l;
+        s_lend[0] = __ldg(A.ws.layer_off + l + 1);
+        s_r[0] = rho(l);
+      }
+    }
   }
   named_sync(1, kSConsumers);
   if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, p);
@@ -142,16 +170,20 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
     const Tile tl = s_tile[ti & 1];
     const uint32_t s = ti % kSStages;
-    // prefetch the next tile's worker scales (thread 0 also keeps the
-    // decoded tile for everyone)
-    float next_sc = 0.0f;
-    const uint32_t Tn = T + gridDim.x;
-    if (Tn < G.n_tiles && (uint32_t)p < Wc) {
+    // loads for later tiles: the worker scales of the tile after next;
+    // thread 0 decodes the next tile for everyone and loads its scalars
+    float next_sc = 0.0f, next_osc = 0.0f;
+    [[maybe_unused]] uint32_t next_l = 0;
+    const uint32_t Tn = T + gridDim.x, Tnn = Tn + gridDim.x;
+    if (Tnn < G.n_tiles && (uint32_t)p < Wc)
+      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tnn).g);
+    if (Tn < G.n_tiles && p == 0) {
       const Tile tn = decode_tile(G, Tn);
-      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + tn.g);
-      if (p == 0) s_tile[(ti + 1) & 1] = tn;
+      s_tile[(ti + 1) & 1] = tn;
+      next_osc = __ldcg(A.sscales_old + tn.g);
+      if constexpr (LAMB) next_l = __ldg(A.ws.tile_layer + Tn);
     }
-    const float osc = __ldcg(A.sscales_old + tl.g);
+    const float osc = s_osc[ti & 1];
     bool valid[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
@@ -161,7 +193,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
     const uint32_t* sow = sbw + Wc * kRunWords;  // the server's previous words
     const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
-    const float* sc = s_sc[ti & 1];
+    const float* sc = s_sc[ti % 3];
 
     const float* z8 = s_z8[ti & 1];
 
@@ -169,9 +201,9 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     uint64_t lend_t = 0;
     float r_t = 1.0f;
     if constexpr (LAMB) {
-      l_t = __ldg(A.ws.tile_layer + T);
-      lend_t = __ldg(A.ws.layer_off + l_t + 1);
-      r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
+      l_t = s_l[ti & 1];
+      lend_t = s_lend[ti & 1];
+      r_t = s_r[ti & 1];
     }
     // FULL: all 4096 elements of the tile are real (no length or padding
     // checks per element).  UNI: the whole tile lies in one layer (rho
@@ -239,8 +271,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
             const float et = __fsub_rn(f4get(ev[i], c), so);
             if constexpr (LAMB) {
               if constexpr (!UNI) {
-                if (advance_layer(A.ws.layer_off, G.L, k, l, lend))
-                  r_l = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
+                if (advance_layer(A.ws.layer_off, G.L, k, l, lend)) r_l = rho(l);
               }
               y = __fadd_rn(__fmul_rn(r_l, et), zc);
             } else {
@@ -270,13 +301,23 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       else acc = work(std::false_type{}, std::false_type{});
     }
     acc = warp_butterfly_sum(acc);
-    if (lane == 0) ws[warp] = acc;
-    if (Tn < G.n_tiles && (uint32_t)p < Wc) s_sc[(ti + 1) & 1][p] = next_sc;
-    named_sync(1, kSConsumers);
-    if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws);
-    if (Tn < G.n_tiles && (uint32_t)p < (1u << W8))
-      s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) & 1], Wc, p);
-    if (named_sync_or(1, kSConsumers, s_abort != 0)) break;
+    if (lane == 0) ws[ti & 1][warp] = acc;
+    if (Tnn < G.n_tiles && (uint32_t)p < Wc) s_sc[(ti + 2) % 3][p] = next_sc;
+    if (Tn < G.n_tiles) {
+      if ((uint32_t)p < (1u << W8)) s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, p);
+      if (p == 0) {
+        s_osc[(ti + 1) & 1] = next_osc;
+        if constexpr (LAMB) {
+          // issued a whole tile after next_l, so its latency is hidden
+          s_l[(ti + 1) & 1] = next_l;
+          s_lend[(ti + 1) & 1] = __ldg(A.ws.layer_off + next_l + 1);
+          s_r[(ti + 1) & 1] = rho(next_l);
+        }
+      }
+    }
+    const bool stop = named_sync_or(1, kSConsumers, s_abort != 0);
+    if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws[ti & 1]);
+    if (stop) break;
   }
 }
 
