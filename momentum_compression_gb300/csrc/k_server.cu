@@ -51,11 +51,13 @@ struct ServerSmem {
 };
 
 // Table entry b for the first W8 = min(W, 8) workers (see the file header).
-__device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, uint32_t b) {
+// The division by W (W <= 8) is the exact multiply by 1/W when W is a
+// power of two (inv_w != 0).
+__device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, float inv_w, uint32_t b) {
   const uint32_t W8 = W < 8 ? W : 8;
   float z = 0.0f;
   for (uint32_t w = 0; w < W8; ++w) z = __fadd_rn(z, ((b >> w) & 1u) ? sc[w] : -sc[w]);
-  return W <= 8 ? __fdiv_rn(z, (float)W) : z;
+  return W <= 8 ? div_by_workers(z, (float)W, inv_w) : z;
 }
 
 // WT: the worker count when it is a compile-time 4, 8 or 16 (the tables'
@@ -149,6 +151,11 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   if (blockIdx.x + gridDim.x < G.n_tiles && (uint32_t)p < Wc)
     s_sc[1][p] =
         __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x + gridDim.x).g);
+  // 1-bit LAMB, thread 0: the layer of the next tile, loaded a tile
+  // before the loads that depend on it
+  [[maybe_unused]] uint32_t l_next = 0;
+  if (LAMB && p == 0 && blockIdx.x + gridDim.x < G.n_tiles)
+    l_next = __ldg(A.ws.tile_layer + blockIdx.x + gridDim.x);
   if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc) {
     const Tile tl = decode_tile(G, blockIdx.x);
     s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     }
   }
   named_sync(1, kSConsumers);
-  if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, p);
+  if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, inv_w, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
@@ -174,6 +181,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     // thread 0 decodes the next tile for everyone and loads its scalars
     float next_sc = 0.0f, next_osc = 0.0f;
     [[maybe_unused]] uint32_t next_l = 0;
+    [[maybe_unused]] uint64_t next_lend = 0;
+    [[maybe_unused]] float next_c2 = 1.0f, next_c1 = 1.0f;
     const uint32_t Tn = T + gridDim.x, Tnn = Tn + gridDim.x;
     if (Tnn < G.n_tiles && (uint32_t)p < Wc)
       next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tnn).g);
@@ -181,7 +190,17 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       const Tile tn = decode_tile(G, Tn);
       s_tile[(ti + 1) & 1] = tn;
       next_osc = __ldcg(A.sscales_old + tn.g);
-      if constexpr (LAMB) next_l = __ldg(A.ws.tile_layer + Tn);
+      if constexpr (LAMB) {
+        // the next tile's layer end and rho operands (its layer arrived a
+        // tile ago), and the layer of the tile after it
+        next_l = l_next;
+        next_lend = __ldg(A.ws.layer_off + next_l + 1);
+        if (A.ratio_ef) {
+          next_c2 = __ldg(A.c_prev2 + next_l);
+          next_c1 = __ldg(A.c_prev + next_l);
+        }
+        l_next = Tnn < G.n_tiles ? __ldg(A.ws.tile_layer + Tnn) : 0u;
+      }
     }
     const float osc = s_osc[ti & 1];
     bool valid[4];
@@ -304,14 +323,14 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     if (lane == 0) ws[ti & 1][warp] = acc;
     if (Tnn < G.n_tiles && (uint32_t)p < Wc) s_sc[(ti + 2) % 3][p] = next_sc;
     if (Tn < G.n_tiles) {
-      if ((uint32_t)p < (1u << W8)) s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, p);
+      if ((uint32_t)p < (1u << W8))
+        s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, inv_w, p);
       if (p == 0) {
         s_osc[(ti + 1) & 1] = next_osc;
         if constexpr (LAMB) {
-          // issued a whole tile after next_l, so its latency is hidden
           s_l[(ti + 1) & 1] = next_l;
-          s_lend[(ti + 1) & 1] = __ldg(A.ws.layer_off + next_l + 1);
-          s_r[(ti + 1) & 1] = rho(next_l);
+          s_lend[(ti + 1) & 1] = next_lend;
+          s_r[(ti + 1) & 1] = A.ratio_ef ? __fdiv_rn(next_c2, next_c1) : 1.0f;
         }
       }
     }

@@ -274,6 +274,22 @@ def test_int8_full_size_sampled():
 # 1-bit LAMB on the BERT-large list
 # ---------------------------------------------------------------------------
 
+def _fill_lamb_state(opt, wl, seed):
+    """_fill_state plus per-layer LAMB state: sigma_l = 10^U(-1,1),
+    c_avg = 10^U(-0.5,0.5), r_prev = 1, c_prev = c_prev2 = c_avg."""
+    _fill_state(opt, wl, seed)
+    L = wl.n_layers
+    rng = np.random.default_rng(seed)
+    ls0 = {"s": (10.0 ** rng.uniform(-1, 1, L)).astype(f32),
+           "c_avg": (10.0 ** rng.uniform(-0.5, 0.5, L)).astype(f32)}
+    ls0["r_prev"] = np.ones(L, f32)
+    ls0["c_prev"] = ls0["c_avg"].copy()
+    ls0["c_prev2"] = ls0["c_avg"].copy()
+    for k, v in ls0.items():
+        getattr(opt.ls, k).copy_(torch.from_numpy(v))
+    return ls0
+
+
 def _layer_slices(off, s, r):
     """Layers intersecting [s, s+r), as local offsets and global ids."""
     l0 = int(np.searchsorted(off, s, side="right") - 1)
@@ -299,15 +315,7 @@ def test_bert_large_lamb_full_size():
     L = wl.n_layers
     hp = wl.hp
     std = _std_vector(wl, opt.n_pad)
-    _fill_state(opt, wl, seed=7)
-    rng = np.random.default_rng(7)
-    ls0 = {"s": (10.0 ** rng.uniform(-1, 1, L)).astype(f32),
-           "c_avg": (10.0 ** rng.uniform(-0.5, 0.5, L)).astype(f32)}
-    ls0["r_prev"] = np.ones(L, f32)
-    ls0["c_prev"] = ls0["c_avg"].copy()
-    ls0["c_prev2"] = ls0["c_avg"].copy()
-    for k, v in ls0.items():
-        getattr(opt.ls, k).copy_(torch.from_numpy(v))
+    ls0 = _fill_lamb_state(opt, wl, seed=7)
     lay = opt.layout
     P, C, cpp = lay["P"], lay["chunk"], lay["chunks_per_partition"]
     chunks = _chunks(lay, wl.n)
@@ -384,3 +392,42 @@ def test_bert_large_lamb_full_size():
     for g, co in cos.items():
         _compare_chunk_errors_and_p(opt, co, f"chunk {g}", p_exact=False)
     opt.close()
+
+
+def test_bert_large_lamb_sign_form_equals_dense_full_size():
+    """The property the sign-form momentum rests on, at full size: 1-bit
+    LAMB on the BERT-large list for 4 compressed steps with the momentum
+    held as the server's sign words (double-buffered, from the second step
+    on) gives bit for bit the results of the dense momentum -- parameters,
+    server words and scales, fresh variance, every layer's r and c, and m
+    itself (rebuilt from the signs).  The dense path is the one checked
+    against the oracle on sampled chunks above."""
+    wl = synth.workload("bert-large")
+    if _free_bytes() < 80e9:
+        pytest.skip("needs 80 GB")
+    off = [int(x) for x in wl.layer_offsets]
+    out = []
+    for sm in (False, True):
+        opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype, off, lamb=True,
+                                 sign_momentum=sm, **wl.hp)
+        std = _std_vector(wl, opt.n_pad)
+        _fill_lamb_state(opt, wl, seed=11)
+        for t in range(4):
+            grads = _grads(opt, wl, 300 + t, std)
+            opt.compressed_step(grads)
+            del grads
+        torch.cuda.synchronize()
+        assert ob.ob_device_error(opt.ctx) == 0
+        assert opt.m_in_signs == sm
+        opt.materialize_m()
+        torch.cuda.synchronize()
+        out.append({"p": host(opt.p), "m": host(opt.m), "v_fresh": host(opt.v_fresh),
+                    "sbits": host(opt.sbits), "sscales": host(opt.sscales),
+                    "e_s": host(opt.err_s), "e0": host(opt.err[0]),
+                    "c_t": host(opt.ls.c_t), "r_prev": host(opt.ls.r_prev),
+                    "c_prev2": host(opt.ls.c_prev2)})
+        del std
+        opt.close()
+        torch.cuda.empty_cache()
+    for k in out[0]:
+        assert_bits_equal(out[1][k], out[0][k], f"{k}: sign form vs dense")
