@@ -247,12 +247,26 @@ def recorded_traffic(workload, sign_m):
 # CPU baseline: the oracle, single-threaded, on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample_step_time(wl, sample, steps):
+def oracle_sample_step_time(wl, sample, steps, budget_s=None):
+    """Per-step times of the oracle's compressed step (1-bit Adam, or 1-bit
+    LAMB for a LAMB workload) on the first `sample` elements of the
+    workload: `steps` steps, or with budget_s, steps until budget_s seconds
+    have passed (at least 2, at most `steps`)."""
     import oracle as O
+    lamb = wl.mode == "lamb"
     lay = O.Layout(sample, wl.W, wl.align, wl.chunk)
-    st = O.State(lay)
+    layers = None
+    if lamb:  # the workload's layers cut at the sample's end
+        offs = [int(o) for o in (wl.layer_offsets if wl.layer_offsets is not None else [0])
+                if int(o) < sample] + [sample]
+        layers = O.Layers(np.array(offs, np.uint64))
+    st = O.State(lay, layers, lamb=lamb)
     st.v[:sample] = synth.state_slice(wl, "v", 0, sample)
     st.m[:sample] = synth.state_slice(wl, "m", 0, sample)
+    if lamb:  # compressed-phase LAMB state drawn directly: sigma = c = r = 1
+        st.v_fresh[:] = st.v
+        L = layers.count()
+        st.ls = {k: np.ones(L, np.float32) for k in ("s", "c_avg", "r_prev", "c_prev", "c_prev2")}
     grads = []
     for w in range(wl.W):
         a = np.zeros(lay.n_pad, np.float32)
@@ -263,8 +277,10 @@ def oracle_sample_step_time(wl, sample, steps):
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        O.compressed_step(st, grads, wl.hp)
+        O.compressed_step(st, grads, wl.hp, lamb=lamb)
         times.append(time.perf_counter() - t0)
+        if budget_s is not None and len(times) >= 2 and sum(times) >= budget_s:
+            break
     return times
 
 
@@ -630,12 +646,14 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1:
-        sample, steps = min(1 << 24, n), 4
-        times = oracle_sample_step_time(wl, sample, steps)
+        sample = min(1 << 24, n)
+        times = oracle_sample_step_time(wl, sample, 16, budget_s=12.0)
+        steps = len(times)
         cpu = {"value": sample * steps / sum(times), "unit": "elements/s", "cores": 1,
                "kind": "oracle",
                "sample": f"first {sample} elements of {wl.name}, W={wl.W}, {steps} compressed "
-                         f"steps ({sum(times):.1f} s)", "cpu": cpu_model()}
+                         f"{'1-bit LAMB' if wl.mode == 'lamb' else '1-bit Adam'} steps "
+                         f"({sum(times):.1f} s)", "cpu": cpu_model()}
 
     if rank != 0:
         return
