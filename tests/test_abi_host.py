@@ -77,6 +77,11 @@ def test_calls_need_a_workspace():
         lambda: ob.ob_server_reduce(ctx, 16, 16, 16, 16, 16, stream=0),
         lambda: ob.ob_adam_step(ctx, 16, 16, 16, 16, 16, stream=0),
         lambda: ob.ob_warmup_step(ctx, [16, 16], 16, 16, 16, stream=0),
+        lambda: ob.ob_compress_signm_ls(ctx, [16, 16], 16, 16, [16, 16], 16, 16, stream=0),
+        lambda: ob.ob_server_reduce_db(ctx, 16, 16, 16, 16, 16, 32, 32, stream=0),
+        lambda: ob.ob_lamb_step_signm(ctx, 16, 16, 32, 32, 16, 16, 16, None, stream=0),
+        lambda: ob.ob_step_db(ctx, [16, 16], [16, 16], 16, 16, 16, 16, 16, 32, 32, 16, 16, 16,
+                              stream=0),
     ):
         with pytest.raises(ob.OBError) as ei:
             call()

@@ -461,6 +461,36 @@ def test_misaligned_pointers_rejected_before_launch():
     c.close()
 
 
+def test_double_buffer_arguments_rejected_before_launch():
+    """The double-buffered calls refuse server buffers that overlap without
+    being equal, and a sign-form LAMB update whose previous and current
+    buffers coincide, on the host, before any launch."""
+    sizes = [1000, 3000]
+    opt = ob.OneBitOptimizer(sum(sizes), 2, 2048, 32, "f32", [0, 1000, 4000], lamb=True,
+                             sign_momentum=True, **LAMB_HP)
+    words = opt.layout["words_per_worker"]
+    big = torch.zeros(2 * words + 64, dtype=torch.int32, device="cuda")
+    shifted = big[4:4 + words]  # overlaps big[:words], 16 bytes further on
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_server_reduce_db(opt.ctx, opt.bits, opt.scales, opt.err_s, big, opt.sscales,
+                               shifted, opt.sscales_alt, opt.ls)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_lamb_step_signm(opt.ctx, opt.sbits, opt.sscales, opt.sbits, opt.sscales_alt,
+                              opt.v, opt.v_fresh, opt.p, opt.ls)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_lamb_step_signm(opt.ctx, None, opt.sscales, opt.sbits_alt, opt.sscales_alt,
+                              opt.v, opt.v_fresh, opt.p, opt.ls)
+    assert ei.value.status == ob.OB_ERR_INVALID
+    # equal pairs are the in-place server
+    ob.ob_server_reduce_db(opt.ctx, opt.bits, opt.scales, opt.err_s, opt.sbits, opt.sscales,
+                           opt.sbits, opt.sscales, opt.ls)
+    torch.cuda.synchronize()
+    assert ob.ob_device_error(opt.ctx) == 0
+    opt.close()
+
+
 @pytest.mark.parametrize("n", [1, 255, 256, 1000, 4097, (1 << 20) + 5])
 def test_int8_error_feedback_parity(n):
     """INT8 with error feedback and the per-block error monitor, three calls
