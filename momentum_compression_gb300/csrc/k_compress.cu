@@ -85,6 +85,24 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   // the workers' chunk scales of the current and the next tile
   float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(ws + OB_MAX_WORKERS);
   __shared__ volatile int s_abort;
+  // 1-bit LAMB per-tile scalars (first layer, its end, sigma, rho) of the
+  // current and the next work item, made by thread 0 an item ahead: the
+  // layer of the item after next and the loads that depend on the next
+  // item's layer go out by cp.async, so no register and no consumer waits
+  // on them (the chain tile -> layer -> sigma, rho used to stall every
+  // consumer at each item start).
+  struct LMeta {
+    uint64_t lend;
+    uint32_t l;
+    float s, r;
+  };
+  struct LRaw {
+    uint64_t lend;
+    uint32_t l, l_next;
+    float s, c2, c1;
+  };
+  __shared__ LMeta s_lm[2];
+  __shared__ LRaw s_lr;
 
   const Geo& G = A.geo;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -173,6 +191,23 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       mw_next[i] = off < tn.len ? __ldg(A.msbits + ((tn.start + off) >> 5)) : 0u;
     }
   };
+  // tile of work item V
+  auto tile_of = [&](uint32_t V) { return kGrouped ? V % G.n_tiles : V; };
+  if constexpr (LAMB) {
+    if (p == 0 && blockIdx.x < n_vt) {
+      const uint32_t T0 = tile_of(blockIdx.x);
+      const uint32_t l = __ldg(A.ws.tile_layer + T0);
+      s_lm[0].l = l;
+      s_lm[0].lend = __ldg(A.ws.layer_off + l + 1);
+      s_lm[0].s = __ldg(A.s + l);
+      s_lm[0].r = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l), __ldg(A.c_prev + l)) : 1.0f;
+      if (blockIdx.x + gridDim.x < n_vt) {
+        cp_async_4(&s_lr.l_next, A.ws.tile_layer + tile_of(blockIdx.x + gridDim.x));
+        cp_async_commit();
+        cp_async_wait_all();
+      }
+    }
+  }
   if (blockIdx.x < n_vt) {
     const uint32_t gi = kGrouped ? blockIdx.x / G.n_tiles : 0u, T0 = blockIdx.x - gi * G.n_tiles;
     if constexpr (MSIGN) load_msign(T0);
@@ -205,10 +240,26 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     uint64_t lend_t = 0;
     float s_t = 1.0f, r_t = 1.0f;
     if constexpr (LAMB) {
-      l_t = __ldg(A.ws.tile_layer + T);
-      lend_t = __ldg(A.ws.layer_off + l_t + 1);
-      s_t = __ldg(A.s + l_t);
-      r_t = A.ratio_ef ? __fdiv_rn(__ldg(A.c_prev2 + l_t), __ldg(A.c_prev + l_t)) : 1.0f;
+      const LMeta& lm = s_lm[ti & 1];
+      l_t = lm.l;
+      lend_t = lm.lend;
+      s_t = lm.s;
+      r_t = lm.r;
+      if (p == 0 && VTn < n_vt) {
+        // the next item's scalars, from its layer loaded an item ago; then
+        // the layer of the item after it
+        const uint32_t ln = s_lr.l_next;
+        s_lr.l = ln;
+        cp_async_8(&s_lr.lend, A.ws.layer_off + ln + 1);
+        cp_async_4(&s_lr.s, A.s + ln);
+        if (A.ratio_ef) {
+          cp_async_4(&s_lr.c2, A.c_prev2 + ln);
+          cp_async_4(&s_lr.c1, A.c_prev + ln);
+        }
+        if (VTn + gridDim.x < n_vt)
+          cp_async_4(&s_lr.l_next, A.ws.tile_layer + tile_of(VTn + gridDim.x));
+        cp_async_commit();
+      }
     }
     const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
     // the tile's m in registers, shared by its workers
@@ -375,6 +426,16 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     }
 
     if ((uint32_t)p < nwn) s_sc[(ti + 1) & 1][p] = sc_next;
+    if constexpr (LAMB) {
+      if (p == 0 && VTn < n_vt) {
+        cp_async_wait_all();
+        LMeta& nx = s_lm[(ti + 1) & 1];
+        nx.l = s_lr.l;
+        nx.lend = s_lr.lend;
+        nx.s = s_lr.s;
+        nx.r = A.ratio_ef ? __fdiv_rn(s_lr.c2, s_lr.c1) : 1.0f;
+      }
+    }
     named_sync(1, kConsumers);
     if ((uint32_t)p < wend - wbeg)
       A.ws.wpart[((uint64_t)(wbeg + p) * G.nc + tl.g) * G.tpc + tl.t] = tree8(ws[wbeg + p]);
