@@ -540,10 +540,12 @@ def run_ours(args, wl):
     per = {k: [ev[t][i].elapsed_time(ev[t][i + 1]) for t in range(K)]
            for i, k in enumerate(("compress", "server", "update"))}
     graph_info = None
-    if args.graph:
-        # The same steps replayed from CUDA graphs (one per gradient set):
-        # one launch per step instead of five or six.  Per-kernel times come
-        # from the eager loop above; the step time from the replays.
+    clocks = clk.summary()
+    if not args.eager:
+        # The same steps replayed from CUDA graphs (one per gradient set,
+        # OneBitOptimizer.capture_step): one launch per step instead of five
+        # or six.  Per-kernel times come from the eager loop above; the step
+        # time, and the clocks reported with it, from the replays.
         graphs = [opt.capture_step(gsets[i]) for i in range(2)]
         for t in range(2):
             graphs[t % 2].replay()
@@ -563,7 +565,8 @@ def run_ours(args, wl):
         eager_ms = max_over_ranks(total_ms, pg, device) / K
         total_ms = ga.elapsed_time(gb)
         graph_info = {"eager_ms_per_step": eager_ms, "graph_launches_per_step": 1,
-                      "clocks": gclk.summary()}
+                      "eager_clocks": clocks}
+        clocks = gclk.summary()
         del graphs
     # compress + scale finalisation, server + scale finalisation, update
     # (LAMB: pass A and pass B); the kernels inside a replayed graph count too
@@ -657,7 +660,6 @@ def run_ours(args, wl):
 
     if rank != 0:
         return
-    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -1000,8 +1002,11 @@ def main():
                     help="gradient type (flat workload only)")
     ap.add_argument("--mode", choices=("adam", "lamb"), default="adam",
                     help="1-bit Adam or 1-bit LAMB (flat workload only; one layer)")
+    ap.add_argument("--eager", action="store_true",
+                    help="1-bit workloads: time the eager launches only (by default the step "
+                         "is also captured in CUDA graphs and the replays are timed)")
     ap.add_argument("--graph", action="store_true",
-                    help="time the step as CUDA graph replays (1-bit workloads)")
+                    help="kept for old command lines: graph replay is the default")
     ap.add_argument("--dense-m", action="store_true",
                     help="keep the momentum as a dense fp32 buffer (default: its exact sign form)")
     ap.add_argument("--ef", action="store_true", help="int8 workload: with error feedback")
