@@ -511,14 +511,16 @@ class OneBitOptimizer:
 
     def capture_step(self, grads):
         """Captures one compressed step on the gradient buffers `grads` into
-        a CUDA graph and returns it (torch.cuda.CUDAGraph); each replay()
-        runs that step with whatever the buffers hold -- one launch instead
-        of five or six, for sizes where launches dominate.  The step reads
-        every per-step quantity (scales, sign words, LAMB state) from device
-        memory, so replays are the same steps as eager calls.  Host-side
-        schedules are not replayed: capture after the first compressed step
-        when the momentum is held in sign form, and without reset_interval.
-        The library allocates nothing, so capture needs no memory pool."""
+        a CUDA graph and returns an object whose replay() runs that step
+        with whatever the buffers hold -- one launch instead of five or six,
+        for sizes where launches dominate.  The step reads every per-step
+        quantity (scales, sign words, LAMB state) from device memory, so
+        replays are the same steps as eager calls.  Host-side schedules are
+        not replayed: capture after the first compressed step when the
+        momentum is held in sign form, and without reset_interval; replay()
+        refuses to run once the momentum's form has changed since the
+        capture (materialize_m / materialize_errors).  The library
+        allocates nothing, so capture needs no memory pool."""
         import torch
         if self.reset_interval:
             raise ValueError("capture_step: reset_interval is a host-side schedule")
@@ -532,7 +534,7 @@ class OneBitOptimizer:
             ob_step(self.ctx, grads, m, self.err, self.bits, self.scales, self.err_s,
                     self.sbits, self.sscales, self.v, self.v_fresh, self.p,
                     self.ls if self.lamb else None)
-        return graph
+        return _StepGraph(self, graph)
 
     def materialize_m(self, stream=None):
         """Writes the dense momentum (it is exact: sscale*sign)."""
@@ -547,7 +549,24 @@ class OneBitOptimizer:
                               self.sbits, self.sscales, stream)
 
 
-class _AlternatingGraphs:
+class _StepGraph:
+    """A captured compressed step: replay() runs it if the optimizer still
+    holds its momentum in the form the capture recorded."""
+
+    def __init__(self, opt, graph):
+        self.opt, self.graph, self.m_in_signs = opt, graph, opt.m_in_signs
+
+    def _check(self):
+        if self.opt.m_in_signs != self.m_in_signs:
+            raise RuntimeError("replay: the momentum's form changed since the capture; "
+                               "capture the step again")
+
+    def replay(self):
+        self._check()
+        self.graph.replay()
+
+
+class _AlternatingGraphs(_StepGraph):
     """Two CUDA graphs of one double-buffered sign-form step, one for each
     orientation of the two server buffers; replay() runs the one that
     matches the optimizer's current buffers and swaps them, so replays are
@@ -555,7 +574,7 @@ class _AlternatingGraphs:
 
     def __init__(self, opt, grads):
         import torch
-        self.opt = opt
+        super().__init__(opt, None)
         self.graphs = {}
         for _ in range(2):
             g = torch.cuda.CUDAGraph()
@@ -567,6 +586,7 @@ class _AlternatingGraphs:
             opt._swap()  # capture only records; the other orientation next
 
     def replay(self):
+        self._check()
         self.graphs[self.opt.sbits.data_ptr()].replay()
         self.opt._swap()
 

@@ -78,6 +78,24 @@ def test_graph_replay_matches_eager_steps(lamb, sm):
     b.close()
 
 
+def test_replay_refuses_a_changed_momentum_form():
+    """A graph captured with the momentum in sign form does not replay once
+    materialize_m has made it dense again."""
+    opt, n, W = _make(True, 3, sm=True)
+    for t in range(2):
+        opt.warmup_step(_grads(opt.n_pad, n, W, t))
+    opt.begin_compression()
+    opt.compressed_step(_grads(opt.n_pad, n, W, 2))
+    bufs = _grads(opt.n_pad, n, W, 3)  # the graph reads these buffers
+    graph = opt.capture_step(bufs)
+    graph.replay()
+    opt.materialize_m()
+    with pytest.raises(RuntimeError):
+        graph.replay()
+    torch.cuda.synchronize()
+    opt.close()
+
+
 def test_capture_refuses_host_schedules():
     opt, n, W = _make(False, 2)
     opt.begin_compression()
