@@ -281,7 +281,7 @@ ob_status ob_lamb_step_signm(ob_ctx* ctx, const uint32_t* sbits_prev, const floa
 /* compress + server_reduce + adam_step (ls == NULL) or lamb_step, in one
  * call, in that order.  With m == NULL (1-bit Adam only) the momentum is
  * held in its sign form: ob_compress_signm + server + ob_adam_step without
- * m. */
+ * m.  1-bit LAMB in sign form needs the double-buffered ob_step_db. */
 ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m,
                   float* const* err, uint32_t* bits, float* scales,
                   float* err_s, uint32_t* sbits, float* sscales,
