@@ -458,6 +458,53 @@ def test_lamb_lossless_reconstructs_gradient():
     _eq(vt, 0.5 * 1.0 + 0.5 * g * g)   # v_t = b2 v + (1-b2) g^2 with g recovered
 
 
+@pytest.mark.parametrize("lamb", [False, True])
+def test_stored_momentum_is_the_scaled_signs(lamb):
+    """After every compressed step the stored momentum is exactly the
+    server's chunk scale times its sign ([LAMB] 1-2: m_t = M/sigma_l for
+    LAMB, sscale*sign for Adam), element by element -- recomputed here in
+    NumPy from the server output, with one IEEE division per element.  This
+    is what lets the momentum be held in sign form between steps.  Odd
+    layer sizes, W = 3, padding, 4 steps with a falling gradient scale."""
+    sizes = [7, 1, 4095, 33, 3000]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.uint64)
+    n, W = int(off[-1]), 3
+    lay = O.Layout(n, W, 32, 1024)
+    layers = O.Layers(off) if lamb else O.Layers()
+    st = O.State(lay, layers, lamb=lamb)
+    rng = np.random.default_rng(5)
+    st.v[:n] = np.abs(rng.standard_normal(n)).astype(f32) * f32(1e-6) + f32(1e-12)
+    st.m[:n] = rng.standard_normal(n).astype(f32) * f32(1e-3)
+    st.p[:n] = rng.standard_normal(n).astype(f32) * f32(0.02)
+    hp = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=4.0,
+              c_min=0.01, c_max=10.0)
+    L = len(sizes)
+    if lamb:
+        st.v_fresh[:] = st.v
+        st.ls = {"s": (10.0 ** rng.uniform(-1, 1, L)).astype(f32),
+                 "c_avg": np.ones(L, f32), "r_prev": np.ones(L, f32),
+                 "c_prev": np.ones(L, f32), "c_prev2": np.ones(L, f32)}
+    # per element: its chunk's index and (LAMB) its layer's sigma
+    chunk_of = np.zeros(lay.n_pad, np.int64)
+    for g in range(lay.nc):
+        s0, ln, _ = lay.chunk_range(g)
+        chunk_of[s0:s0 + ln] = g
+    sigma = (np.repeat(st.ls["s"], sizes) if lamb else np.ones(n, f32)).astype(f32)
+    for t in range(4):
+        grads = []
+        for w in range(W):
+            a = np.zeros(lay.n_pad, f32)
+            a[:n] = rng.standard_normal(n).astype(f32) * f32(1e-3 * 3.0 ** -t)
+            grads.append(a)
+        O.compressed_step(st, grads, hp, lamb=lamb)
+        k = np.arange(n)
+        bit = (st.sbits[k >> 5] >> (k & 31).astype(np.uint32)) & 1
+        M = st.sscales[chunk_of[:n]] * np.where(bit == 1, f32(1), f32(-1))
+        want = (M / sigma).astype(f32) if lamb else M.astype(f32)
+        _eq(st.m[:n], want)
+        assert not st.m[n:].any()
+
+
 # ---------------------------------------------------------------------------
 # Warmup (uncompressed) steps
 # ---------------------------------------------------------------------------
