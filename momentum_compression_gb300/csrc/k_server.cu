@@ -136,6 +136,11 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 
   // ------------------------------------------------------------ consumers
   const int p = tid;
+  // the byte of a sign word holding this lane's nibble (selector for
+  // byte_perm: that byte of the first and of the second operand) and the
+  // nibble's offset in it
+  const uint32_t bsel = ((p & 7) >> 1) | ((4 + ((p & 7) >> 1)) << 4);
+  const uint32_t hs = 4 * (p & 1);
   const uint32_t Wc = WT ? WT : G.W;
   // scales of the first tile
   const uint32_t W8 = Wc < 8 ? Wc : 8;
@@ -245,15 +250,24 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         if (vi) {
           const uint32_t widx = (off >> 5) + wshift;
           const int sh = 4 * (p & 7);
-          // byte c of idx = the first W8 workers' bits of element c
-          uint32_t idx = 0;
+          // byte c of idx = the first W8 workers' bits of element c: an
+          // 8 x 4 bit transpose.  Gather the byte holding this lane's nibble
+          // from each word (workers 0-3 in xa, 4-7 in xb, absent workers
+          // 0), keep the nibbles (idx byte w: worker w's 4 bits low, worker
+          // w+4's high), then two delta swaps transpose the two 4 x 4 bit
+          // blocks (the 2 x 2 sub-blocks, then the bits inside them).
+          uint32_t wv[8];
 #pragma unroll
-          for (uint32_t w = 0; w < 8; ++w) {
-            if (w < W8) {
-              const uint32_t nib = (sbw[w * kRunWords + widx] >> sh) & 0xFu;
-              idx |= (nib * (0x00204081u << w)) & (0x01010101u << w);
-            }
-          }
+          for (uint32_t w = 0; w < 8; ++w) wv[w] = w < W8 ? sbw[w * kRunWords + widx] : 0u;
+          const uint32_t xa = __byte_perm(__byte_perm(wv[0], wv[1], bsel),
+                                          __byte_perm(wv[2], wv[3], bsel), 0x5410);
+          const uint32_t xb = __byte_perm(__byte_perm(wv[4], wv[5], bsel),
+                                          __byte_perm(wv[6], wv[7], bsel), 0x5410);
+          uint32_t idx = ((xa >> hs) & 0x0F0F0F0Fu) | ((xb << (4 - hs)) & 0xF0F0F0F0u);
+          uint32_t tsw = ((idx >> 14) ^ idx) & 0x0000CCCCu;
+          idx ^= tsw ^ (tsw << 14);
+          tsw = ((idx >> 7) ^ idx) & 0x00AA00AAu;
+          idx ^= tsw ^ (tsw << 7);
 #pragma unroll
           for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
           if (WT == 0 || WT > 8) {
