@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           tsw = ((idx >> 7) ^ idx) & 0x00AA00AAu;
           idx ^= tsw ^ (tsw << 7);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) z[i][c] = z8[(idx >> (8 * c)) & 0xFFu];
+          for (int c = 0; c < 4; ++c) z[i][c] = z8[__byte_perm(idx, 0u, 0x4440u | c)];
           if (WT == 0 || WT > 8) {
 #pragma unroll 8
             for (uint32_t w = 8; w < Wc; ++w) {
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           float y = 0.0f;
           if (FULL || (valid[i] && k < G.n)) {
             const float zc = Wc <= 8 ? z[i][c] : div_by_workers(z[i][c], fW, inv_w);
-            const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
+            const float so = signed_by_bit(osc, owd[i] >> (4 * (p & 7)), c);
             const float et = __fsub_rn(f4get(ev[i], c), so);
             if constexpr (LAMB) {
               if constexpr (!UNI) {

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) k_adam_update(const UpdateArgs A) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (k0 + c < G.n) {
-          const float mk = ((wd[i] >> c) & 1u) ? osc : -osc;
+          const float mk = signed_by_bit(osc, wd[i], c);
           const float d = __fadd_rn(__fsqrt_rn(f4get(vv[i], c)), A.eps);
           const float u = __fdiv_rn(mk, d);
           f4at(pv[i], c) = __fsub_rn(f4get(pv[i], c), __fmul_rn(A.lr, u));

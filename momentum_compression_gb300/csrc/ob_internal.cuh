@@ -153,6 +153,13 @@ __device__ __forceinline__ float ordered_sum(const float* part, uint32_t cnt, in
 // and z * (1/W) is the same correctly rounded number as z / W (both round
 // the same real value), so a multiply replaces the division; inv_w is
 // 1/W then and 0 otherwise.
+// +s if bit b of w is set, else -s: the sign bit of s flipped when the bit
+// is clear -- the same value as the select, for -0 and NaN too, in two
+// integer instructions.
+__device__ __forceinline__ float signed_by_bit(float s, uint32_t w, int b) {
+  return __uint_as_float(__float_as_uint(s) ^ (~(w << (31 - b)) & 0x80000000u));
+}
+
 __device__ __forceinline__ float div_by_workers(float z, float fW, float inv_w) {
   return inv_w != 0.0f ? __fmul_rn(z, inv_w) : __fdiv_rn(z, fW);
 }
