@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
           for (int c = 0; c < 4; ++c) {
             float x = 0.0f;
             if (real(i, c, k0 + c)) {
-              const float so = signed_by_bit(osc, owd[i] >> (4 * (p & 7)), c);  // scale*sign
+              // scale*sign (a test and select: fewer instructions here than
+              // flipping the sign bit)
+              const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
               const float et = __fsub_rn(f4get(e4, c), so);
               if constexpr (LAMB && !UNI) {
                 if (advance_layer(A.ws.layer_off, G.L, k0 + c, l, lend)) {
