@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       }
     }
     const bool uni = !LAMB || tl.start + tl.len <= lend_t || G.n <= lend_t;
+    // a separate full-tile body only where it fits the registers (bf16
+    // gradients with 1-bit Adam: the fp32 and LAMB variants spill with it)
+    constexpr bool kFullPath = BF16 && !LAMB;
+    const bool full_tile = kFullPath && tl.len == kTile && tl.start + kTile <= G.n;
     // the tile's m in registers, shared by its workers
     float4 mv[4];
     // row i (elements tl.start + 1024i + 4p + c) lies in the tile: padding
@@ -366,8 +370,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
 
       // UNI: the whole tile lies in one layer (sigma, rho scalar); else the
       // layers are walked element by element
-      auto body = [&](auto uni_tag) -> float {
+      // FULL: all 4096 elements of the tile are real (no per-element checks)
+      auto body = [&](auto uni_tag, auto full_tag) -> float {
         [[maybe_unused]] constexpr bool UNI = decltype(uni_tag)::value;
+        constexpr bool FULL = decltype(full_tag)::value;
         float acc = 0.0f;
         [[maybe_unused]] uint32_t l = l_t;
         [[maybe_unused]] uint64_t lend = lend_t;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float x = 0.0f;
-            if (real(i, c, k0 + c)) {
+            if (FULL || real(i, c, k0 + c)) {
               // scale*sign (a test and select: fewer instructions here than
               // flipping the sign bit)
               const float so = ((owd[i] >> (4 * (p & 7) + c)) & 1u) ? osc : -osc;
@@ -411,14 +417,21 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
             f4at(xv, c) = x;
           }
           const uint32_t word = pack_word(nib, lane);
-          if (valid[i]) {
+          if (FULL || valid[i]) {
             __stcs(reinterpret_cast<float4*>(e + k0), xv);
             if ((p & 7) == 0) bw[k0 >> 5] = word;
           }
         }
         return acc;
       };
-      float acc = uni ? body(std::true_type{}) : body(std::false_type{});
+      float acc;
+      if constexpr (kFullPath) {
+        acc = full_tile ? body(std::true_type{}, std::true_type{})
+                        : body(std::true_type{}, std::false_type{});
+      } else {
+        acc = uni ? body(std::true_type{}, std::false_type{})
+                  : body(std::false_type{}, std::false_type{});
+      }
       if constexpr (kLate) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage has been read
