@@ -39,11 +39,28 @@ constexpr int kSConsumers = kThreads;
 constexpr int kServerThreads = kThreads + 32;
 constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
 
+// Per-tile scalars, written by the producer into each stage next to the
+// copies (plain shared stores made visible by its release-arrive on the
+// stage's mbarrier): the decoded tile, the previous server scale of its
+// chunk and, for 1-bit LAMB, the tile's first layer, that layer's end and
+// its rho.  The consumers take them from the stage and wait on nothing
+// else at a tile start.
+struct TileHdr {
+  Tile tl;
+  float osc, r;
+  uint32_t l, pad;
+  uint64_t lend;
+};
+constexpr size_t kHdrBytes = 64;
+static_assert(sizeof(TileHdr) <= kHdrBytes && kHdrBytes % 16 == 0, "stage header");
+
 struct ServerSmem {
-  // the e_s tile, the W workers' word runs and the server's previous words
-  __host__ __device__ static size_t stage_bytes(uint32_t W) {
+  // the e_s tile, the W workers' word runs, the server's previous words
+  // and the tile header
+  __host__ __device__ static size_t hdr_offset(uint32_t W) {
     return kTile * 4 + (size_t)(W + 1) * kRunWords * 4;
   }
+  __host__ __device__ static size_t stage_bytes(uint32_t W) { return hdr_offset(W) + kHdrBytes; }
   __host__ __device__ static size_t bytes(uint32_t W) {
     return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 3 * OB_MAX_WORKERS * 4 +
            2 * 256 * 4;
@@ -74,14 +91,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 3);
   __shared__ float ws[2][8];
   __shared__ volatile int s_abort;
-  __shared__ Tile s_tile[2];  // the current and the next tile, decoded by thread 0
-  // per-tile scalars of the current and the next tile, loaded by thread 0 a
-  // tile ahead so that no consumer waits on them: the previous server
-  // scale of the tile's chunk and (1-bit LAMB) the tile's first layer, its
-  // end and its step-ratio factor rho
-  __shared__ float s_osc[2], s_r[2];
-  __shared__ uint32_t s_l[2];
-  __shared__ uint64_t s_lend[2];
+  const size_t hdr_off = ServerSmem::hdr_offset(G.W);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned* err = A.ws.err;
@@ -103,8 +113,26 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     const uint64_t pol = policy_evict_first();
     uint32_t ti = 0;
     bool ok = true;
+    // 1-bit LAMB: the layer of the tile, loaded a tile before the loads
+    // that depend on it
+    [[maybe_unused]] uint32_t l_cur =
+        LAMB && blockIdx.x < G.n_tiles ? __ldg(A.ws.tile_layer + blockIdx.x) : 0u;
     for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
       const Tile tl = decode_tile(G, T);
+      // the header's loads go out before the wait for a free stage
+      const float osc = __ldcg(A.sscales_old + tl.g);
+      [[maybe_unused]] uint32_t l = 0;
+      [[maybe_unused]] uint64_t lend = 0;
+      [[maybe_unused]] float c2 = 1.0f, c1 = 1.0f;
+      if constexpr (LAMB) {
+        l = l_cur;
+        lend = __ldg(A.ws.layer_off + l + 1);
+        if (A.ratio_ef) {
+          c2 = __ldg(A.c_prev2 + l);
+          c1 = __ldg(A.c_prev + l);
+        }
+        if (T + gridDim.x < G.n_tiles) l_cur = __ldg(A.ws.tile_layer + T + gridDim.x);
+      }
       const uint32_t s = ti % kSStages, r = ti / kSStages;
       if (r >= 1) ok = mbar_wait(&empty[s], (r - 1) & 1, err, kErrWaitEmpty);
       if (!ok || s_abort) {
@@ -115,6 +143,14 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
       const uint64_t w1 = ((tl.start + tl.len) / 32 + 3) & ~uint64_t(3);
       const uint32_t run = (uint32_t)(w1 - w0) * 4;
       unsigned char* st = stage0 + s * stage_bytes;
+      TileHdr* hd = reinterpret_cast<TileHdr*>(st + hdr_off);
+      hd->tl = tl;
+      hd->osc = osc;
+      if constexpr (LAMB) {
+        hd->l = l;
+        hd->lend = lend;
+        hd->r = A.ratio_ef ? __fdiv_rn(c2, c1) : 1.0f;
+      }
       mbar_arrive_expect_tx(&full[s], tl.len * 4 + (G.W + 1) * run);
       bulk_g2s_stream(st, A.e_s + tl.start, tl.len * 4, &full[s], pol);
       for (uint32_t w = 0; w < G.W; ++w)
@@ -156,64 +192,31 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   if (blockIdx.x + gridDim.x < G.n_tiles && (uint32_t)p < Wc)
     s_sc[1][p] =
         __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x + gridDim.x).g);
-  // 1-bit LAMB, thread 0: the layer of the next tile, loaded a tile
-  // before the loads that depend on it
-  [[maybe_unused]] uint32_t l_next = 0;
-  if (LAMB && p == 0 && blockIdx.x + gridDim.x < G.n_tiles)
-    l_next = __ldg(A.ws.tile_layer + blockIdx.x + gridDim.x);
-  if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc) {
-    const Tile tl = decode_tile(G, blockIdx.x);
-    s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + tl.g);
-    if (p == 0) {
-      s_tile[0] = tl;
-      s_osc[0] = __ldcg(A.sscales_old + tl.g);
-      if constexpr (LAMB) {
-        const uint32_t l = __ldg(A.ws.tile_layer + blockIdx.x);
-        s_l[0] = l;
-        s_lend[0] = __ldg(A.ws.layer_off + l + 1);
-        s_r[0] = rho(l);
-      }
-    }
-  }
+  if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc)
+    s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x).g);
   named_sync(1, kSConsumers);
   if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, inv_w, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
-    const Tile tl = s_tile[ti & 1];
     const uint32_t s = ti % kSStages;
-    // loads for later tiles: the worker scales of the tile after next;
-    // thread 0 decodes the next tile for everyone and loads its scalars
-    float next_sc = 0.0f, next_osc = 0.0f;
-    [[maybe_unused]] uint32_t next_l = 0;
-    [[maybe_unused]] uint64_t next_lend = 0;
-    [[maybe_unused]] float next_c2 = 1.0f, next_c1 = 1.0f;
+    // the worker scales of the tile after next
+    float next_sc = 0.0f;
     const uint32_t Tn = T + gridDim.x, Tnn = Tn + gridDim.x;
     if (Tnn < G.n_tiles && (uint32_t)p < Wc)
       next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tnn).g);
-    if (Tn < G.n_tiles && p == 0) {
-      const Tile tn = decode_tile(G, Tn);
-      s_tile[(ti + 1) & 1] = tn;
-      next_osc = __ldcg(A.sscales_old + tn.g);
-      if constexpr (LAMB) {
-        // the next tile's layer end and rho operands (its layer arrived a
-        // tile ago), and the layer of the tile after it
-        next_l = l_next;
-        next_lend = __ldg(A.ws.layer_off + next_l + 1);
-        if (A.ratio_ef) {
-          next_c2 = __ldg(A.c_prev2 + next_l);
-          next_c1 = __ldg(A.c_prev + next_l);
-        }
-        l_next = Tnn < G.n_tiles ? __ldg(A.ws.tile_layer + Tnn) : 0u;
-      }
-    }
-    const float osc = s_osc[ti & 1];
-    bool valid[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
     bool ok = s_abort == 0 && mbar_wait(&full[s], (ti / kSStages) & 1, err, kErrWaitFull);
     if (!ok) s_abort = 1;
     const unsigned char* st = stage0 + s * stage_bytes;
+    // the tile's scalars from the stage header (after a failed wait the
+    // tile is decoded here, so that addresses stay valid; the values are
+    // discarded when the loop exits at the tile's end)
+    const TileHdr& hd = *reinterpret_cast<const TileHdr*>(st + hdr_off);
+    const Tile tl = ok ? hd.tl : decode_tile(G, T);
+    const float osc = hd.osc;
+    bool valid[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
     const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
     const uint32_t* sow = sbw + Wc * kRunWords;  // the server's previous words
     const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
@@ -225,9 +228,9 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     uint64_t lend_t = 0;
     float r_t = 1.0f;
     if constexpr (LAMB) {
-      l_t = s_l[ti & 1];
-      lend_t = s_lend[ti & 1];
-      r_t = s_r[ti & 1];
+      l_t = ok ? hd.l : 0u;
+      lend_t = ok ? hd.lend : 0u;
+      r_t = hd.r;
     }
     // FULL: all 4096 elements of the tile are real (no length or padding
     // checks per element).  UNI: the whole tile lies in one layer (rho
@@ -339,14 +342,6 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     if (Tn < G.n_tiles) {
       if ((uint32_t)p < (1u << W8))
         s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, inv_w, p);
-      if (p == 0) {
-        s_osc[(ti + 1) & 1] = next_osc;
-        if constexpr (LAMB) {
-          s_l[(ti + 1) & 1] = next_l;
-          s_lend[(ti + 1) & 1] = next_lend;
-          s_r[(ti + 1) & 1] = A.ratio_ef ? __fdiv_rn(next_c2, next_c1) : 1.0f;
-        }
-      }
     }
     const bool stop = named_sync_or(1, kSConsumers, s_abort != 0);
     if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws[ti & 1]);
