@@ -222,8 +222,8 @@ def _run_adam_fullsize(wl, steps=2, need_bytes=None, sign_momentum=False):
 def test_bert_base_full_size(sign_momentum):
     """109,482,240 parameters (199 tensors), W = 8, chunk 2^20, fp32: the
     workload bench.py times (with the momentum in sign form, as bench.py
-    runs it, and dense)."""
-    _run_adam_fullsize(synth.workload("bert-base"), steps=3, need_bytes=20e9,
+    runs it, and dense), 10 compressed steps."""
+    _run_adam_fullsize(synth.workload("bert-base"), steps=10, need_bytes=20e9,
                        sign_momentum=sign_momentum)
 
 
