@@ -228,14 +228,22 @@ def test_flat_1m_adam_5_warmup_10_compressed():
     opt.close()
 
 
-@pytest.mark.parametrize("workload,dt", [("flat-1m", "f32"), ("gpt-1.3b", "bf16")])
-def test_sign_momentum_matches_oracle(workload, dt):
+@pytest.mark.parametrize("workload,dt,W", [
+    ("flat-1m", "f32", None), ("gpt-1.3b", "bf16", None),
+    # the worker kernel takes workers in groups of 4 in sign form: a ragged
+    # last group (5 = 4 + 1), four full groups (16), and bf16 with 6
+    ("flat", "f32", 5), ("flat", "f32", 16), ("flat", "bf16", 6),
+])
+def test_sign_momentum_matches_oracle(workload, dt, W):
     """1-bit Adam with the momentum held as the server's sign words and
     chunk scales (ob_compress_signm, ob_adam_step without m): the same
     results as the dense momentum, bit for bit; the dense m, rebuilt by
     ob_decompress, equals the oracle's."""
-    wl = synth.workload(workload)
-    if dt == "bf16":
+    if workload == "flat":
+        wl = synth.workload("flat", n=150_001, W=W, chunk=1 << 13, grad_dtype=dt)
+    else:
+        wl = synth.workload(workload)
+    if workload == "gpt-1.3b":
         wl.tensors = None
         wl.n = 250_000
         wl.chunk = 1 << 13
@@ -308,6 +316,7 @@ LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=
     # the momentum in sign form, server output double-buffered
     (0, 4, "f32", True), (ob.OB_FLAG_NO_RATIO_EF, 3, "f32", True),
     (ob.OB_FLAG_FROZEN_C, 8, "bf16", True), (0, 12, "bf16", True),
+    (ob.OB_FLAG_NO_RATIO_EF, 16, "f32", True),  # the W = 16 server specialisation
 ])
 def test_lamb_small_layers(flags, W, dt, sm):
     """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
