@@ -233,6 +233,7 @@ def test_flat_1m_adam_5_warmup_10_compressed():
     # the worker kernel takes workers in groups of 4 in sign form: a ragged
     # last group (5 = 4 + 1), four full groups (16), and bf16 with 6
     ("flat", "f32", 5), ("flat", "f32", 16), ("flat", "bf16", 6),
+    ("flat", "f32", 64),  # the largest W: 16 groups, the generic server
 ])
 def test_sign_momentum_matches_oracle(workload, dt, W):
     """1-bit Adam with the momentum held as the server's sign words and
@@ -240,7 +241,8 @@ def test_sign_momentum_matches_oracle(workload, dt, W):
     results as the dense momentum, bit for bit; the dense m, rebuilt by
     ob_decompress, equals the oracle's."""
     if workload == "flat":
-        wl = synth.workload("flat", n=150_001, W=W, chunk=1 << 13, grad_dtype=dt)
+        wl = synth.workload("flat", n=150_001 if W < 64 else 40_003, W=W, chunk=1 << 13,
+                            grad_dtype=dt)
     else:
         wl = synth.workload(workload)
     if workload == "gpt-1.3b":
@@ -317,6 +319,7 @@ LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=
     (0, 4, "f32", True), (ob.OB_FLAG_NO_RATIO_EF, 3, "f32", True),
     (ob.OB_FLAG_FROZEN_C, 8, "bf16", True), (0, 12, "bf16", True),
     (ob.OB_FLAG_NO_RATIO_EF, 16, "f32", True),  # the W = 16 server specialisation
+    (0, 64, "f32", True),                       # the largest W, the generic server
 ])
 def test_lamb_small_layers(flags, W, dt, sm):
     """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
