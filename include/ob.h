@@ -19,7 +19,12 @@
  *  or ob_lamb_step      unpack + 1-bit LAMB update               ([LAMB] 1-2)
  * The worker-to-server "all-to-all" is the server kernel reading the
  * workers' packed words straight from HBM (bulk copies of each worker's
- * 16-byte aligned run of words for a tile).
+ * 16-byte aligned run of words for a tile).  After a compressed step the
+ * momentum is exactly the server's scaled signs, so it can be held in that
+ * form between steps: ob_compress_signm (1-bit Adam, server in place) and
+ * ob_compress_signm_ls + ob_server_reduce_db + ob_lamb_step_signm (1-bit
+ * LAMB, server output double-buffered), or ob_step / ob_step_db in one
+ * call.
  *
  * Device errors.  Pipelined kernels wait on shared-memory barriers for
  * their own bulk copies; every wait is bounded (about a second), and a
