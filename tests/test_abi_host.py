@@ -33,6 +33,25 @@ def test_every_declared_symbol_is_exported():
         assert hasattr(lib, name), name
 
 
+def test_c_programs_compile_against_the_header():
+    """The plain-C programs the GPU tests run (tests/cuda/*.c) compile with
+    a host C compiler against include/ob.h and the CUDA runtime header:
+    the header is valid C and its declarations match their use."""
+    import glob
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("no host C compiler or CUDA headers")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for src in sorted(glob.glob(os.path.join(root, "tests", "cuda", "*.c"))):
+        r = subprocess.run([cc, "-std=c11", "-fsyntax-only", "-Wall", "-Werror",
+                            "-I", os.path.join(root, "include"), "-I", cuda_inc, src],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, src + "\n" + r.stderr
+
+
 def test_layout_matches_definition():
     ctx = ob.ob_init(109_482_240, 8, 1 << 20)
     lay = ob.ob_get_layout(ctx)
