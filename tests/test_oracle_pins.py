@@ -137,6 +137,16 @@ def test_cr_tiles_summed_in_order():
     assert O.cr_sum(b) == f32(2 ** 24 + 2)
 
 
+def test_cr_warp_sums_paired_in_order():
+    """The 8 warp sums of a tile are added as ((w0+w1)+(w2+w3)) + ...: with
+    w0 = 2^24, w1 = 1, w2 = -2^24, w3 = 1 (one element per warp, at lane
+    32w) this gives 2^24 + (-2^24 + 1) = 1, where (w0+w2)+(w1+w3) would
+    give 2."""
+    a = np.zeros(4096, f32)
+    a[0], a[128], a[256], a[384] = 2.0 ** 24, 1.0, -(2.0 ** 24), 1.0
+    assert O.cr_sum(a) == f32(1.0)
+
+
 @pytest.mark.parametrize("count", [0, 1, 3, 4, 5, 1023, 1024, 4095, 4096, 4097,
                                    12289, 70000])
 def test_cr_integers_exact(count):
@@ -505,9 +515,95 @@ def test_stored_momentum_is_the_scaled_signs(lamb):
         assert not st.m[n:].any()
 
 
+def test_adam_update_hand_with_eps():
+    """[LAMB] ¶1 / [BLOG] §2.1 with eps > 0, by hand (dyadic values):
+    m = sscale*sign = [1.25, -1.25]; d = sqrt(v) + eps = [2 + 0.5, 0.5 + 0.5];
+    u = m/d = [0.5, -1.25]; p = 0 - lr*u with lr = 0.5."""
+    lay = O.Layout(2, 1, 1, 2)
+    sbits = np.array([0b01], np.uint32)
+    sscales = np.array([1.25], f32)
+    v = np.array([4.0, 0.25], f32)
+    m = np.zeros(2, f32)
+    p = np.zeros(2, f32)
+    O.adam_update(lay, sbits, sscales, v, 0.5, 0.5, m, p)
+    _eq(m, [1.25, -1.25])
+    _eq(p, [-0.25, 0.625])
+
+
+def test_compress_momentum_with_b1_not_half():
+    """[BLOG] §2.1, m_w = b1*m + (1-b1)*g, with b1 = 0.75 so that b1 and
+    1 - b1 differ (the worked examples use 0.5), by hand:
+    m_w = [0.75 + 0.5, -1.5 + 1] = [1.25, -0.5]; scale = 0.875; bits 0b01;
+    e' = x - scale*sign = [0.375, 0.375]."""
+    lay = O.Layout(2, 1, 1, 2)
+    e = np.zeros(2, f32)
+    b, s, x = O.compress_worker(lay, np.array([2.0, 4.0], f32), np.array([1.0, -2.0], f32),
+                                e, 0.75)
+    _eq(x, [1.25, -0.5])
+    _eq(s, [0.875])
+    assert int(b[0]) == 0b01
+    _eq(e, [0.375, 0.375])
+
+
+def test_rho_is_the_ratio_of_the_two_previous_coefficients():
+    """[LAMB] ¶3: the error is scaled by rho = c_{t-2}/c_{t-1}."""
+    _eq(O.rho_of({"c_prev2": np.array([3.0, 1.0], f32), "c_prev": np.array([2.0, 4.0], f32)}),
+        [1.5, 0.25])
+
+
+def test_lamb_pass_a_hand_with_b2_not_half():
+    """[LAMB] ¶1 pass A with b1 = 0.5 and b2 = 0.75 (b2 and 1 - b2 differ), by
+    hand: M = [1, -1] (sigma 1) = m_t; g = (m_t - 0.5*[0.5, 0.5])/0.5 =
+    [1.5, -2.5]; v_t = 0.75*[1, 4] + 0.25*g^2 = [1.3125, 4.5625];
+    R = max(v_Tw / v_t) with v_Tw = [2.625, 4.5625] = 2."""
+    lay = O.Layout(2, 1, 1, 2)
+    layers = O.Layers([0, 2])
+    m = np.array([0.5, 0.5], f32)
+    vt = np.array([1.0, 4.0], f32)
+    R = O.lamb_pass_a(lay, layers, np.array([1.0], f32), np.array([0b01], np.uint32),
+                      np.array([1.0], f32), np.array([2.625, 4.5625], f32), 0.5, 0.75, m, vt)
+    _eq(m, [1.0, -1.0])
+    _eq(vt, [1.3125, 4.5625])
+    _eq(R, [2.0])
+
+
+def test_lamb_ratio_shifts_the_coefficient_history():
+    """After a LAMB step c_{t-2} <- c_{t-1} <- c_t and r_prev <- r_t
+    ([LAMB] ¶1, ¶3): with c_prev = 5 and c_prev2 = 7, c_prev2 becomes 5.
+    R = 3 is clipped to (1 + r_thr)*r_prev; c = c_avg*r."""
+    hp = dict(r_thr=0.1, r_min=0.5, r_max=4.0, c_min=0.01, c_max=10.0)
+    ls = {"c_avg": np.array([2.0], f32), "r_prev": np.array([1.0], f32),
+          "c_prev": np.array([5.0], f32), "c_prev2": np.array([7.0], f32)}
+    c = O.lamb_ratio(np.array([3.0], f32), hp, ls)
+    r = f32(1.0) + f32(0.1)
+    _eq(ls["r_prev"], [r])
+    _eq(c, [f32(2.0) * r])
+    _eq(ls["c_prev"], c)
+    _eq(ls["c_prev2"], [5.0])
+
+
 # ---------------------------------------------------------------------------
 # Warmup (uncompressed) steps
 # ---------------------------------------------------------------------------
+
+def test_warmup_adam_hand_two_workers():
+    """[BLOG] §6 warmup with W = 2, by hand: g_bar = (g0 + g1)/2 = [4, 2];
+    b1 = 0.5, b2 = 0.75: m = [2, 1], v = 0.25*g_bar^2 = [4, 1];
+    u = m/(sqrt(v) + 0) = [1, 1]; p = -lr*u with lr = 0.25.  (u alone would
+    not show a missing average: Adam's step is scale-free; m and v do.)"""
+    lay = O.Layout(2, 2, 1, 1)
+    g0 = np.array([2.0, 4.0], f32)
+    g1 = np.array([6.0, 0.0], f32)
+    m = np.zeros(lay.n_pad, f32)
+    v = np.zeros(lay.n_pad, f32)
+    p = np.zeros(lay.n_pad, f32)
+    z = np.zeros(lay.n_pad - 2, f32)
+    O.warmup_step(lay, [np.concatenate([g0, z]), np.concatenate([g1, z])], 0,
+                  dict(b1=0.5, b2=0.75, eps=0.0, lr=0.25), m, v, p)
+    _eq(m[:2], [2.0, 1.0])
+    _eq(v[:2], [4.0, 1.0])
+    _eq(p[:2], [-0.25, -0.25])
+
 
 def test_warmup_adam_matches_torch_adam():
     """Warmup Adam has no bias correction.  torch.optim.Adam always corrects,
@@ -676,6 +772,41 @@ def test_int8_unbiased_over_seeds():
     scale = np.repeat(np.abs(g).reshape(2, 256).max(axis=1) / 127, 256)
     sd = 0.5 * scale / math.sqrt(N)   # the code is floor or floor+1
     assert np.all(np.abs(mean - g) < 4.5 * sd + 1e-12)
+
+
+def test_int8_tie_rounds_down():
+    """[TUT] "FP32 → INT8 量化" / GradientQuantizeINT8: q = floor(x) plus 1
+    when the uniform is below the fraction, strictly.  A value whose
+    fraction equals its own uniform exactly (scale 1: the block holds 127)
+    rounds down; a comparison u <= frac would round it up."""
+    seed, step = 77, 5
+    u1 = O.uniform(seed, step, 1)
+    q, sc = O.quant_int8(np.array([127.0, u1], f32), 256, seed=seed, step=step)
+    assert sc[0] == f32(1.0)
+    assert int(q[0]) == 127 and int(q[1]) == 0
+
+
+def test_int8_code_clamped_to_127():
+    """[TUT] GradientQuantizeINT8 clamps the code to +-127: the block's
+    maximum can land just above 127 after x = g / (max/127) is rounded
+    (max = 1.0000035 gives x = 127 + 2^-17), and when its uniform falls
+    below that fraction the rounded-up 128 must be clamped back to 127.
+    The element index is searched so that its uniform does fall below."""
+    mx = f32(1.0)
+    while True:  # the first float above 1 whose quotient exceeds 127
+        mx = np.nextafter(mx, f32(2.0))
+        x = mx / (mx / f32(127.0))
+        if x > f32(127.0):
+            break
+    frac = x - np.floor(x)
+    seed, step = 4321, 9
+    k = next(k for k in range(3_000_000) if O.uniform(seed, step, k) < frac)
+    k0 = k // 256 * 256
+    g = np.zeros(256, f32)
+    g[k - k0] = mx
+    q, sc = O.quant_int8(g, 256, seed=seed, step=step, k0=k0)
+    assert sc[0] == mx / f32(127.0)
+    assert int(q[k - k0]) == 127
 
 
 def test_int8_edges():
