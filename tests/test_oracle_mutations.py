@@ -95,6 +95,31 @@ MUTATIONS = [
      "float ca = c_sum[l] / (float)warmup_steps;", "float ca = c_sum[l];"),
     ("INT8 code clamped at 128",
      "if (qf > 127.0f) qf = 127.0f;", "if (qf > 128.0f) qf = 127.0f;"),
+    # mixed widths: the b-bit block codec and the FP16 codec
+    ("b-bit code range one too wide",
+     "const float qmax = (float)((1 << (bits - 1)) - 1);",
+     "const float qmax = (float)(1 << (bits - 1));"),
+    ("b-bit codes not sign-extended",
+     "return field >= (1 << (bits - 1)) ? field - (1 << bits) : field;", "return field;"),
+    ("b-bit fields MSB first",
+     "words[bit / 32] |= field << (bit % 32);", "words[bit / 32] |= field << (32 - bits - bit % 32);"),
+    ("b-bit workers share their uniforms",
+     "x.data(), seed, step, w * L->n_pad,", "x.data(), seed, step, 0,"),
+    ("b-bit server uses worker 0's uniforms",
+     "y.data(), seed, step, L->W * L->n_pad,", "y.data(), seed, step, 0,"),
+    ("b-bit server sum not divided by W",
+     "      z = z / fW;\n      y[i] = e_s[b0 + i] + z;", "      (void)fW;\n      y[i] = e_s[b0 + i] + z;"),
+    ("b-bit error sign flipped",
+     "e[i] = x[i] - (qf * scale);", "e[i] = x[i] + (qf * scale);"),
+    ("binary16 ties rounded away from zero",
+     "const double r = std::nearbyint(a / step);", "const double r = std::round(a / step);"),
+    ("binary16 overflow threshold at the largest half",
+     "if (a >= 65520.0) return", "if (a >= 65504.0) return"),
+    ("binary16 subnormal step halved",
+     "const double step = sub ? std::ldexp(1.0, -24) : std::ldexp(1.0, e - 10);",
+     "const double step = sub ? std::ldexp(1.0, -25) : std::ldexp(1.0, e - 10);"),
+    ("FP16 group drops the error on a step without exchange",
+     "      e[k] = x;\n", "      e[k] = 0.0f;\n"),
 ]
 
 
