@@ -199,38 +199,45 @@ def ob_init(n, W, chunk, align=4096, grad_dtype=OB_GRAD_F32, layer_offsets=None,
 
 
 def ob_destroy(ctx):
+    """Frees the host context (device buffers stay the caller's)."""
     lib().ob_destroy(ctx)
 
 
 def ob_last_error(ctx=None):
+    """The context's last error message (or the global one for ctx None)."""
     return lib().ob_last_error(ctx).decode(errors="replace")
 
 
 def ob_get_layout(ctx):
+    """The layout of the fused buffer as a dict (n_pad, P, chunk, n_chunks, words_per_worker, n_tiles, ...)."""
     lay = ob_layout()
     _check(lib().ob_get_layout(ctx, ct.byref(lay)), ctx)
     return {k: getattr(lay, k) for k, _ in ob_layout._fields_}
 
 
 def ob_workspace_bytes(ctx):
+    """Bytes of device scratch the context needs (tile partials, per-layer tables)."""
     b = ct.c_size_t()
     _check(lib().ob_workspace_bytes(ctx, ct.byref(b)), ctx)
     return b.value
 
 
 def ob_set_workspace(ctx, workspace, nbytes=None, stream=None):
+    """Hands the context its device scratch and enqueues its initialisation on `stream`."""
     if nbytes is None:
         nbytes = workspace.numel() * workspace.element_size()
     _check(lib().ob_set_workspace(ctx, _ptr(workspace), nbytes, _stream(stream)), ctx)
 
 
 def ob_warmup_step(ctx, grads, m, v, p, mode=OB_MODE_ADAM, ls=None, stream=None):
+    """One uncompressed warmup step of 1-bit Adam (mode ADAM) or 1-bit LAMB (mode LAMB, with ls)."""
     _check(lib().ob_warmup_step(ctx, _ptr_array(grads), _ptr(m), _ptr(v), _ptr(p), mode,
                                 _ls(ls), _stream(stream)), ctx)
 
 
 def ob_begin_compression(ctx, err, err_s, bits, scales, sbits, sscales, m=None, v=None,
                          v_fresh=None, ls=None, warmup_steps=0, stream=None):
+    """End of warmup: zeroes errors and sign buffers, freezes v; for LAMB sets sigma, c_avg and the coefficient history."""
     _check(lib().ob_begin_compression(ctx, _ptr_array(err), _ptr(err_s), _ptr(bits),
                                       _ptr(scales), _ptr(sbits), _ptr(sscales), _ptr(m),
                                       _ptr(v), _ptr(v_fresh), _ls(ls), warmup_steps,
@@ -238,6 +245,7 @@ def ob_begin_compression(ctx, err, err_s, bits, scales, sbits, sscales, m=None, 
 
 
 def ob_compress(ctx, grads, m, err, bits, scales, ls=None, stream=None):
+    """Worker compression of all W workers with the dense momentum m (LAMB if ls is given)."""
     _check(lib().ob_compress(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err), _ptr(bits),
                              _ptr(scales), _ls(ls), _stream(stream)), ctx)
 
@@ -293,27 +301,32 @@ def ob_step_db(ctx, grads, err, bits, scales, err_s, sbits_prev, sscales_prev, s
 
 
 def ob_server_reduce(ctx, bits, scales, err_s, sbits, sscales, ls=None, stream=None):
+    """Server average of the workers' chunks, plus its own error, compressed again (in place)."""
     _check(lib().ob_server_reduce(ctx, _ptr(bits), _ptr(scales), _ptr(err_s), _ptr(sbits),
                                   _ptr(sscales), _ls(ls), _stream(stream)), ctx)
 
 
 def ob_decompress(ctx, sbits, sscales, out, ls=None, stream=None):
+    """out = sscale*sign(sbit) (over sigma_l with ls); padding 0."""
     _check(lib().ob_decompress(ctx, _ptr(sbits), _ptr(sscales), _ls(ls), _ptr(out),
                                _stream(stream)), ctx)
 
 
 def ob_adam_step(ctx, sbits, sscales, v_frozen, m, p, stream=None):
+    """Unpack + frozen-variance Adam update; m None keeps the momentum in sign form."""
     _check(lib().ob_adam_step(ctx, _ptr(sbits), _ptr(sscales), _ptr(v_frozen), _ptr(m),
                               _ptr(p), _stream(stream)), ctx)
 
 
 def ob_lamb_step(ctx, sbits, sscales, v_frozen, v_fresh, m, p, ls, stream=None):
+    """Unpack + 1-bit LAMB update (passes A and B) with the dense momentum m."""
     _check(lib().ob_lamb_step(ctx, _ptr(sbits), _ptr(sscales), _ptr(v_frozen), _ptr(v_fresh),
                               _ptr(m), _ptr(p), _ls(ls), _stream(stream)), ctx)
 
 
 def ob_step(ctx, grads, m, err, bits, scales, err_s, sbits, sscales, v_frozen, v_fresh, p,
             ls=None, stream=None):
+    """compress + server_reduce + update in one call; m None (1-bit Adam) uses the sign-form momentum."""
     _check(lib().ob_step(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err), _ptr(bits),
                          _ptr(scales), _ptr(err_s), _ptr(sbits), _ptr(sscales),
                          _ptr(v_frozen), _ptr(v_fresh), _ptr(p), _ls(ls), _stream(stream)),
@@ -321,12 +334,14 @@ def ob_step(ctx, grads, m, err, bits, scales, err_s, sbits, sscales, v_frozen, v
 
 
 def ob_materialize_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=None):
+    """Writes the true errors e' into err and err_s and zeroes the scales (checkpoint form)."""
     _check(lib().ob_materialize_errors(ctx, _ptr_array(err), _ptr(bits), _ptr(scales),
                                        _ptr(err_s), _ptr(sbits), _ptr(sscales),
                                        _stream(stream)), ctx)
 
 
 def ob_reset_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=None):
+    """Periodic error reset: the next compression sees worker and server errors of 0."""
     _check(lib().ob_reset_errors(ctx, _ptr_array(err), _ptr(bits), _ptr(scales), _ptr(err_s),
                                  _ptr(sbits), _ptr(sscales), _stream(stream)), ctx)
 
@@ -339,6 +354,7 @@ def ob_device_error(ctx, stream=None):
 
 
 def ob_quant_int8(g, q, block_scales, seed, step, deq=None, n=None, stream=None):
+    """Block-256 INT8 stochastic-rounding quantizer of g (Philox4x32-10 uniforms)."""
     if n is None:
         n = g.numel()
     _check(lib().ob_quant_int8(_ptr(g), n, _ptr(q), _ptr(block_scales), seed, step, _ptr(deq),
@@ -347,6 +363,7 @@ def ob_quant_int8(g, q, block_scales, seed, step, deq=None, n=None, stream=None)
 
 def ob_quant_int8_ef(g, e, q, block_scales, seed, step, deq=None, block_err2=None, n=None,
                      stream=None):
+    """INT8 quantizer with error feedback (e updated) and the per-block error monitor."""
     if n is None:
         n = g.numel()
     _check(lib().ob_quant_int8_ef(_ptr(g), _ptr(e), n, _ptr(q), _ptr(block_scales), seed, step,
@@ -361,36 +378,43 @@ def ob_qb_sizes(ctx, bits):
 
 
 def ob_zero_errors(ctx, err, err_s, stream=None):
+    """Zeroes a codec group's worker and server errors (start of compression)."""
     _check(lib().ob_zero_errors(ctx, _ptr_array(err), _ptr(err_s), _stream(stream)), ctx)
 
 
 def ob_compress_qb(ctx, bits, grads, m, err, codes, bscales, seed, step, stream=None):
+    """Worker compression with the b-bit block codec (b = 2, 4, 8)."""
     _check(lib().ob_compress_qb(ctx, bits, _ptr_array(grads), _ptr(m), _ptr_array(err),
                                 _ptr(codes), _ptr(bscales), seed, step, _stream(stream)), ctx)
 
 
 def ob_server_reduce_qb(ctx, bits, codes, bscales, err_s, scodes, sbscales, seed, step,
                         stream=None):
+    """Server average and re-quantisation with the b-bit block codec."""
     _check(lib().ob_server_reduce_qb(ctx, bits, _ptr(codes), _ptr(bscales), _ptr(err_s),
                                      _ptr(scodes), _ptr(sbscales), seed, step, _stream(stream)),
            ctx)
 
 
 def ob_adam_step_qb(ctx, bits, scodes, sbscales, v_frozen, m, p, stream=None):
+    """Decode of the server's b-bit message + frozen-variance Adam."""
     _check(lib().ob_adam_step_qb(ctx, bits, _ptr(scodes), _ptr(sbscales), _ptr(v_frozen), _ptr(m),
                                  _ptr(p), _stream(stream)), ctx)
 
 
 def ob_compress_f16(ctx, send, grads, m, err, h, stream=None):
+    """Worker step of the FP16 codec (sent only when `send`)."""
     _check(lib().ob_compress_f16(ctx, int(bool(send)), _ptr_array(grads), _ptr(m),
                                  _ptr_array(err), _ptr(h), _stream(stream)), ctx)
 
 
 def ob_server_reduce_f16(ctx, h, err_s, hs, stream=None):
+    """Server average of the FP16 messages, rounded to FP16 with error feedback."""
     _check(lib().ob_server_reduce_f16(ctx, _ptr(h), _ptr(err_s), _ptr(hs), _stream(stream)), ctx)
 
 
 def ob_adam_step_f16(ctx, send, hs, v_frozen, m, p, stream=None):
+    """Adam update from the FP16 server message (m = 0, p unchanged when not sent)."""
     _check(lib().ob_adam_step_f16(ctx, int(bool(send)), _ptr(hs), _ptr(v_frozen), _ptr(m),
                                   _ptr(p), _stream(stream)), ctx)
 
