@@ -43,6 +43,14 @@ def lib():
                                                f32p, u32p, f32p, vp]
         L.orc_server_reduce.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p,
                                         u32p, f32p, vp]
+        L.orc_compress_worker_range.argtypes = [lay, vp, u64, vp, vp, f32, f32, f32p, f32p,
+                                                f32p, u32p, f32p, vp, u64, u64]
+        L.orc_server_reduce_range.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p, u32p, f32p,
+                                              vp, u64, u64]
+        L.orc_lamb_pass_a_range.argtypes = [lay, vp, u64, f32p, u32p, f32p, f32p, f32, f32,
+                                            f32p, f32p, f32p, u64, u64]
+        L.orc_lamb_pass_b_range.argtypes = [lay, vp, u64, f32p, f32p, f32p, f32, f32, f32p,
+                                            u64, u64]
         L.orc_decompress.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p]
         L.orc_adam_update.argtypes = [lay, u32p, f32p, f32p, f32, f32, f32p, f32p]
         L.orc_lamb_pass_a.argtypes = [lay, vp, u64, f32p, u32p, f32p, f32p, f32,
@@ -130,14 +138,16 @@ def cr_sum(a):
     return np.float32(lib().orc_cr_sum(a, a.size))
 
 
-def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None, clip=0.0):
+def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None, clip=0.0,
+                    want_x=True):
     """One worker's compression.  e (n_pad,) is updated in place.  clip > 0
     limits the compensated value to [-clip, clip].
-    Returns (bits[words] u32, scales[nc] f32, x[n_pad] f32)."""
+    Returns (bits[words] u32, scales[nc] f32, x[n_pad] f32); x is None when
+    want_x is False (saves an n_pad array on whole-model sizes)."""
     layers = layers or Layers()
     bits = np.zeros(lay.words, np.uint32)
     scales = np.zeros(lay.nc, np.float32)
-    x = np.zeros(lay.n_pad, np.float32)
+    x = np.zeros(lay.n_pad, np.float32) if want_x else None
     sg = None if sigma is None else _f32(sigma)
     rh = None if rho is None else _f32(rho)
     lib().orc_compress_worker_clip(lay._s, _ptr(layers.off), layers.nl, _ptr(sg),
@@ -146,20 +156,62 @@ def compress_worker(lay, g, m, e, b1, layers=None, sigma=None, rho=None, clip=0.
     return bits, scales, x
 
 
-def server_reduce(lay, bits, scales, e_s, layers=None, rho=None):
+def server_reduce(lay, bits, scales, e_s, layers=None, rho=None, want_y=True):
     """bits (W, words) u32, scales (W, nc) f32; e_s (n_pad,) updated in place.
-    Returns (sbits[words], sscales[nc], y[n_pad])."""
+    Returns (sbits[words], sscales[nc], y[n_pad]); y is None when want_y is
+    False."""
     layers = layers or Layers()
     bits = np.ascontiguousarray(bits, dtype=np.uint32)
     scales = _f32(scales)
     sbits = np.zeros(lay.words, np.uint32)
     sscales = np.zeros(lay.nc, np.float32)
-    y = np.zeros(lay.n_pad, np.float32)
+    y = np.zeros(lay.n_pad, np.float32) if want_y else None
     rh = None if rho is None else _f32(rho)
     lib().orc_server_reduce(lay._s, _ptr(layers.off), layers.nl, _ptr(rh),
                             bits.reshape(-1), scales.reshape(-1), e_s, sbits,
                             sscales, _ptr(y))
     return sbits, sscales, y
+
+
+# Chunk ranges: the same computations for chunks g0 <= g < g1 only, writing
+# into the caller's whole-buffer arrays.  Disjoint ranges whose boundaries
+# fall on multiples of 32 elements may run in concurrent threads (the C
+# calls release the GIL); pass A returns the range's R, merged by maximum.
+
+def compress_worker_range(lay, g0, g1, g, m, e, bits, scales, b1, layers=None, sigma=None,
+                          rho=None, clip=0.0):
+    """compress_worker over chunks [g0, g1): e, bits (words,) and scales
+    (nc,) are updated in place for those chunks' elements."""
+    layers = layers or Layers()
+    sg = None if sigma is None else _f32(sigma)
+    rh = None if rho is None else _f32(rho)
+    lib().orc_compress_worker_range(lay._s, _ptr(layers.off), layers.nl, _ptr(sg), _ptr(rh),
+                                    b1, clip, g, m, e, bits, scales, None, g0, g1)
+
+
+def server_reduce_range(lay, g0, g1, bits, scales, e_s, sbits, sscales, layers=None, rho=None):
+    """server_reduce over chunks [g0, g1): e_s, sbits and sscales updated in
+    place for those chunks."""
+    layers = layers or Layers()
+    rh = None if rho is None else _f32(rho)
+    lib().orc_server_reduce_range(lay._s, _ptr(layers.off), layers.nl, _ptr(rh),
+                                  np.ascontiguousarray(bits, dtype=np.uint32).reshape(-1),
+                                  _f32(scales).reshape(-1), e_s, sbits, sscales, None, g0, g1)
+
+
+def lamb_pass_a_range(lay, g0, g1, layers, sigma, sbits, sscales, v_frozen, b1, b2, m,
+                      v_fresh):
+    """lamb_pass_a over chunks [g0, g1); returns that range's R."""
+    R = np.zeros(layers.count(), np.float32)
+    lib().orc_lamb_pass_a_range(lay._s, _ptr(layers.off), layers.nl, _f32(sigma),
+                                np.ascontiguousarray(sbits, np.uint32), _f32(sscales),
+                                _f32(v_frozen), b1, b2, m, v_fresh, R, g0, g1)
+    return R
+
+
+def lamb_pass_b_range(lay, g0, g1, layers, c, m, v_frozen, eps, lr, p):
+    lib().orc_lamb_pass_b_range(lay._s, _ptr(layers.off), layers.nl, _f32(c), _f32(m),
+                                _f32(v_frozen), eps, lr, p, g0, g1)
 
 
 def decompress(lay, sbits, sscales, layers=None, sigma=None):

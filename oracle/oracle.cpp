@@ -191,52 +191,48 @@ static float sgn_of_bit(const uint32_t* words, uint64_t k) {
 // clip > 0: the compensated value is limited to [-clip, clip] before it is
 // compressed ([BLOG] §4.1 "梯度裁剪": compensated_grad.clamp_(-clip_value,
 // clip_value), §6 clip_value 2.0); a NaN stays NaN.
-void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
-                              uint64_t nl, const float* sigma, const float* rho,
-                              float b1, float clip, const float* g, const float* m,
-                              float* e, uint32_t* bits, float* scales, float* x_out);
-
-void orc_compress_worker(const orc_layout* L, const uint64_t* layer_off,
-                         uint64_t nl, const float* sigma, const float* rho,
-                         float b1, const float* g, const float* m, float* e,
-                         uint32_t* bits, float* scales, float* x_out) {
-  orc_compress_worker_clip(L, layer_off, nl, sigma, rho, b1, 0.0f, g, m, e, bits,
-                           scales, x_out);
-}
-
-void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
-                              uint64_t nl, const float* sigma, const float* rho,
-                              float b1, float clip, const float* g, const float* m,
-                              float* e, uint32_t* bits, float* scales, float* x_out) {
+// Chunk ranges.  Every output element of the compression, the server, the
+// decompression and the updates depends only on its own chunk's inputs
+// (LAMB's R is a running maximum), so the functions taking [g0, g1) do the
+// same computation for chunks g0 <= g < g1 only, and the whole-buffer
+// functions are these over [0, nc).  Disjoint ranges may run concurrently
+// (each with its own R for pass A, merged by maximum) as long as no 32-bit
+// word of bits/sbits holds elements of two of them, i.e. the range
+// boundaries fall on multiples of 32 elements.
+void orc_compress_worker_range(const orc_layout* L, const uint64_t* layer_off,
+                               uint64_t nl, const float* sigma, const float* rho,
+                               float b1, float clip, const float* g, const float* m,
+                               float* e, uint32_t* bits, float* scales, float* x_out,
+                               uint64_t g0, uint64_t g1) {
   const float ob1 = 1.0f - b1;
-  std::vector<float> x(L->n_pad, 0.0f);
-  for (uint64_t k = 0; k < L->n; ++k) {
-    uint64_t l = layer_of(layer_off, nl, k);
-    float s = sigma ? sigma[l] : 1.0f;
-    float r = rho ? rho[l] : 1.0f;
-    float mw = (b1 * m[k]) + (ob1 * g[k]);
-    float xv = (s * mw) + (r * e[k]);
-    if (clip > 0.0f) {
-      if (xv > clip) xv = clip;
-      if (xv < -clip) xv = -clip;
-    }
-    x[k] = xv;
-  }
-  for (uint64_t wd = 0; wd < L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0); ++wd)
-    bits[wd] = 0u;
-  std::vector<float> ax;
-  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+  std::vector<float> xs, ax;
+  for (uint64_t g_id = g0; g_id < g1 && g_id < L->nc; ++g_id) {
     uint64_t start, len, real;
     chunk_range(L, g_id, &start, &len, &real);
+    xs.assign(len, 0.0f);
+    for (uint64_t q = 0; q < real; ++q) {
+      uint64_t k = start + q;
+      uint64_t l = layer_of(layer_off, nl, k);
+      float s = sigma ? sigma[l] : 1.0f;
+      float r = rho ? rho[l] : 1.0f;
+      float mw = (b1 * m[k]) + (ob1 * g[k]);
+      float xv = (s * mw) + (r * e[k]);
+      if (clip > 0.0f) {
+        if (xv > clip) xv = clip;
+        if (xv < -clip) xv = -clip;
+      }
+      xs[q] = xv;
+    }
     ax.assign(real, 0.0f);
-    for (uint64_t q = 0; q < real; ++q) ax[q] = std::fabs(x[start + q]);
+    for (uint64_t q = 0; q < real; ++q) ax[q] = std::fabs(xs[q]);
     float sum = orc_cr_sum(ax.data(), real);
     float scale = real ? sum / (float)real : 0.0f;
     scales[g_id] = scale;
     for (uint64_t q = 0; q < len; ++q) {
       uint64_t k = start + q;
+      bits[k >> 5] &= ~(1u << (k & 31));
       if (q < real) {
-        float xv = x[k];
+        float xv = xs[q];
         bool b = (xv >= 0.0f);
         if (b) bits[k >> 5] |= (1u << (k & 31));
         float sg = b ? 1.0f : -1.0f;
@@ -244,10 +240,27 @@ void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
       } else {
         e[k] = 0.0f;
       }
+      if (x_out) x_out[k] = xs[q];
     }
   }
-  if (x_out)
-    for (uint64_t k = 0; k < L->n_pad; ++k) x_out[k] = x[k];
+}
+
+void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
+                              uint64_t nl, const float* sigma, const float* rho,
+                              float b1, float clip, const float* g, const float* m,
+                              float* e, uint32_t* bits, float* scales, float* x_out) {
+  for (uint64_t wd = 0; wd < L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0); ++wd)
+    bits[wd] = 0u;
+  orc_compress_worker_range(L, layer_off, nl, sigma, rho, b1, clip, g, m, e, bits, scales,
+                            x_out, 0, L->nc);
+}
+
+void orc_compress_worker(const orc_layout* L, const uint64_t* layer_off,
+                         uint64_t nl, const float* sigma, const float* rho,
+                         float b1, const float* g, const float* m, float* e,
+                         uint32_t* bits, float* scales, float* x_out) {
+  orc_compress_worker_clip(L, layer_off, nl, sigma, rho, b1, 0.0f, g, m, e, bits,
+                           scales, x_out);
 }
 
 // Server side, all partitions ([LAMB] ¶3-¶4: worker chunks travel to the
@@ -259,16 +272,17 @@ void orc_compress_worker_clip(const orc_layout* L, const uint64_t* layer_off,
 // bits: [W][n_pad/32] words; scales: [W][nc] (each worker's scale for every
 // chunk of its full buffer).  Reading: the server uses the same chunking as
 // the workers, and divides by W after the sum.
-void orc_server_reduce(const orc_layout* L, const uint64_t* layer_off,
-                       uint64_t nl, const float* rho, const uint32_t* bits,
-                       const float* scales, float* e_s, uint32_t* sbits,
-                       float* sscales, float* y_out) {
+void orc_server_reduce_range(const orc_layout* L, const uint64_t* layer_off,
+                             uint64_t nl, const float* rho, const uint32_t* bits,
+                             const float* scales, float* e_s, uint32_t* sbits,
+                             float* sscales, float* y_out, uint64_t g0, uint64_t g1) {
   const uint64_t words = L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0);
   const float fW = (float)L->W;
-  std::vector<float> y(L->n_pad, 0.0f);
-  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+  std::vector<float> ys, ay;
+  for (uint64_t g_id = g0; g_id < g1 && g_id < L->nc; ++g_id) {
     uint64_t start, len, real;
     chunk_range(L, g_id, &start, &len, &real);
+    ys.assign(len, 0.0f);
     for (uint64_t q = 0; q < real; ++q) {
       uint64_t k = start + q;
       float z = 0.0f;
@@ -277,32 +291,36 @@ void orc_server_reduce(const orc_layout* L, const uint64_t* layer_off,
       z = z / fW;
       uint64_t l = layer_of(layer_off, nl, k);
       float r = rho ? rho[l] : 1.0f;
-      y[k] = (r * e_s[k]) + z;
+      ys[q] = (r * e_s[k]) + z;
     }
-  }
-  for (uint64_t wd = 0; wd < words; ++wd) sbits[wd] = 0u;
-  std::vector<float> ay;
-  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
-    uint64_t start, len, real;
-    chunk_range(L, g_id, &start, &len, &real);
     ay.assign(real, 0.0f);
-    for (uint64_t q = 0; q < real; ++q) ay[q] = std::fabs(y[start + q]);
+    for (uint64_t q = 0; q < real; ++q) ay[q] = std::fabs(ys[q]);
     float sum = orc_cr_sum(ay.data(), real);
     float sscale = real ? sum / (float)real : 0.0f;
     sscales[g_id] = sscale;
     for (uint64_t q = 0; q < len; ++q) {
       uint64_t k = start + q;
+      sbits[k >> 5] &= ~(1u << (k & 31));
       if (q < real) {
-        bool b = (y[k] >= 0.0f);
+        bool b = (ys[q] >= 0.0f);
         if (b) sbits[k >> 5] |= (1u << (k & 31));
-        e_s[k] = y[k] - (sscale * (b ? 1.0f : -1.0f));
+        e_s[k] = ys[q] - (sscale * (b ? 1.0f : -1.0f));
       } else {
         e_s[k] = 0.0f;
       }
+      if (y_out) y_out[k] = ys[q];
     }
   }
-  if (y_out)
-    for (uint64_t k = 0; k < L->n_pad; ++k) y_out[k] = y[k];
+}
+
+void orc_server_reduce(const orc_layout* L, const uint64_t* layer_off,
+                       uint64_t nl, const float* rho, const uint32_t* bits,
+                       const float* scales, float* e_s, uint32_t* sbits,
+                       float* sscales, float* y_out) {
+  const uint64_t words = L->n_pad / 32 + ((L->n_pad % 32) ? 1 : 0);
+  for (uint64_t wd = 0; wd < words; ++wd) sbits[wd] = 0u;
+  orc_server_reduce_range(L, layer_off, nl, rho, bits, scales, e_s, sbits, sscales, y_out, 0,
+                          L->nc);
 }
 
 // Decompression of the server result ([LAMB] ¶2: the global compressed
@@ -368,12 +386,13 @@ void orc_adam_update(const orc_layout* L, const uint32_t* sbits,
 //   R_l = max(R_l, v_Tw / v_t)                  (infinity norm of the ratio;
 //         a NaN ratio (0/0) is skipped, +Inf is kept)
 // m and v_t are updated in place; R must hold 0 on entry.
-void orc_lamb_pass_a(const orc_layout* L, const uint64_t* layer_off,
-                     uint64_t nl, const float* sigma, const uint32_t* sbits,
-                     const float* sscales, const float* v_frozen, float b1,
-                     float b2, float* m, float* v_fresh, float* R) {
+void orc_lamb_pass_a_range(const orc_layout* L, const uint64_t* layer_off,
+                           uint64_t nl, const float* sigma, const uint32_t* sbits,
+                           const float* sscales, const float* v_frozen, float b1,
+                           float b2, float* m, float* v_fresh, float* R, uint64_t g0,
+                           uint64_t g1) {
   const float ob1 = 1.0f - b1, ob2 = 1.0f - b2;
-  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+  for (uint64_t g_id = g0; g_id < g1 && g_id < L->nc; ++g_id) {
     uint64_t start, len, real;
     chunk_range(L, g_id, &start, &len, &real);
     for (uint64_t q = 0; q < len; ++q) {
@@ -393,6 +412,14 @@ void orc_lamb_pass_a(const orc_layout* L, const uint64_t* layer_off,
       if (!std::isnan(ratio) && ratio > R[l]) R[l] = ratio;
     }
   }
+}
+
+void orc_lamb_pass_a(const orc_layout* L, const uint64_t* layer_off,
+                     uint64_t nl, const float* sigma, const uint32_t* sbits,
+                     const float* sscales, const float* v_frozen, float b1,
+                     float b2, float* m, float* v_fresh, float* R) {
+  orc_lamb_pass_a_range(L, layer_off, nl, sigma, sbits, sscales, v_frozen, b1, b2, m, v_fresh,
+                        R, 0, L->nc);
 }
 
 static float fmax_plain(float a, float b) { return a > b ? a : b; }
@@ -436,16 +463,28 @@ void orc_lamb_rho(uint64_t nl, const float* c_prev2, const float* c_prev,
 
 // Pass B ([LAMB] ¶1, frozen denominator sqrt(v_Tw)):
 //   p = p - (lr*c_l) * (m_t / (sqrt(v_Tw) + eps))
+void orc_lamb_pass_b_range(const orc_layout* L, const uint64_t* layer_off,
+                           uint64_t nl, const float* c, const float* m,
+                           const float* v_frozen, float eps, float lr, float* p,
+                           uint64_t g0, uint64_t g1) {
+  for (uint64_t g_id = g0; g_id < g1 && g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    for (uint64_t q = 0; q < real; ++q) {
+      uint64_t k = start + q;
+      uint64_t l = layer_of(layer_off, nl, k);
+      float t1 = lr * c[l];
+      float d = std::sqrt(v_frozen[k]) + eps;
+      float u = m[k] / d;
+      p[k] = p[k] - (t1 * u);
+    }
+  }
+}
+
 void orc_lamb_pass_b(const orc_layout* L, const uint64_t* layer_off,
                      uint64_t nl, const float* c, const float* m,
                      const float* v_frozen, float eps, float lr, float* p) {
-  for (uint64_t k = 0; k < L->n; ++k) {
-    uint64_t l = layer_of(layer_off, nl, k);
-    float t1 = lr * c[l];
-    float d = std::sqrt(v_frozen[k]) + eps;
-    float u = m[k] / d;
-    p[k] = p[k] - (t1 * u);
-  }
+  orc_lamb_pass_b_range(L, layer_off, nl, c, m, v_frozen, eps, lr, p, 0, L->nc);
 }
 
 // ---------------------------------------------------------------------------

@@ -37,10 +37,10 @@ MUTATIONS = [
     ("server sum not divided by W",
      "      z = z / fW;\n", "      (void)fW;\n"),
     ("server error not added",
-     "y[k] = (r * e_s[k]) + z;", "y[k] = z;"),
+     "ys[q] = (r * e_s[k]) + z;", "ys[q] = z;"),
     ("server error sign flipped",
-     "e_s[k] = y[k] - (sscale * (b ? 1.0f : -1.0f));",
-     "e_s[k] = y[k] + (sscale * (b ? 1.0f : -1.0f));"),
+     "e_s[k] = ys[q] - (sscale * (b ? 1.0f : -1.0f));",
+     "e_s[k] = ys[q] + (sscale * (b ? 1.0f : -1.0f));"),
     ("Adam step direction flipped",
      "p[k] = p[k] - t;", "p[k] = p[k] + t;"),
     ("eps inside the square root",
