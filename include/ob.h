@@ -337,17 +337,30 @@ ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream);
  * and no workspace is needed: the scratch (per-tile totals and an error
  * word) is a static device array of OB_NOALLOC_SCRATCH_BYTES that every
  * GPU loading the library holds until exit.  Allocates nothing.
- *   - Layouts whose W * n_chunks * tiles_per_chunk * 4 bytes (+ 512) exceed
- *     OB_NOALLOC_SCRATCH_BYTES are rejected with OB_ERR_UNSUPPORTED
- *     (e.g. up to about 2^28 elements at W = 8).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
- *   - All calls share the array: calls that overlap on the GPU race. */
+ *   - A layout is accepted exactly when
+ *       W * n_chunks * ceil(chunk / 4096) * 4  <=  OB_NOALLOC_SCRATCH_BYTES - 256
+ *     (n_chunks and chunk as ob_get_layout reports them; the last 256
+ *     bytes hold the error word); others get OB_ERR_UNSUPPORTED before
+ *     any launch (e.g. up to about 2^28 elements at W = 8).
+ *   - The first call on a device (of this function or of
+ *     ob_noalloc_device_error) looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and clears the error
+ *     word on `stream`; make that first call before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race.
+ *   - A bounded wait that gives up records its code (as for ob_device_error)
+ *     in the array's error word, which no call clears: read it with
+ *     ob_noalloc_device_error. */
 #define OB_NOALLOC_SCRATCH_BYTES (4u << 20)
 ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads, const float* m,
                               float* const* err, uint32_t* bits, float* scales,
                               ob_stream_t stream);
+
+/* No counterpart in the pages.  Reads and clears the error word of the
+ * current device's static scratch array used by ob_compress_noalloc (0 =
+ * none, else the first code any call recorded since the last read; codes
+ * as for ob_device_error).  Needs no ctx and allocates nothing.
+ * Synchronises `stream`. */
+ob_status ob_noalloc_device_error(unsigned* code, ob_stream_t stream);
 
 /* Block-wise INT8 stochastic rounding ([TUT] "FP32 → INT8 量化" and the
  * GradientQuantizeINT8 example), blocks of 256 elements (the last may be

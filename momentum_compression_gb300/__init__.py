@@ -24,6 +24,7 @@ OB_OK, OB_ERR_INVALID, OB_ERR_ALIGN, OB_ERR_UNSUPPORTED, OB_ERR_CUDA, OB_ERR_STA
 OB_GRAD_F32, OB_GRAD_BF16 = 0, 1
 OB_MODE_ADAM, OB_MODE_LAMB = 0, 1
 OB_MAX_WORKERS = 64
+OB_NOALLOC_SCRATCH_BYTES = 4 << 20  # the static scratch of ob_compress_noalloc
 OB_FLAG_NO_RATIO_EF = 1 << 0
 OB_FLAG_FROZEN_C = 1 << 1
 
@@ -37,6 +38,7 @@ EXPORTS = (
     "ob_qb_sizes", "ob_zero_errors", "ob_compress_qb", "ob_server_reduce_qb", "ob_adam_step_qb",
     "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
     "ob_compress_signm_ls", "ob_server_reduce_db", "ob_lamb_step_signm", "ob_step_db",
+    "ob_noalloc_device_error",
 )
 
 
@@ -100,6 +102,7 @@ def lib():
         L.ob_device_error.argtypes = [vp, ct.POINTER(ct.c_uint), vp]
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
         L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.ob_noalloc_device_error.argtypes = [ct.POINTER(ct.c_uint), vp]
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
         L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
@@ -255,6 +258,14 @@ def ob_compress_noalloc(ctx, grads, m, err, bits, scales, stream=None):
     a workspace: for callers that cannot allocate device memory."""
     _check(lib().ob_compress_noalloc(ctx, _ptr_array(grads), _ptr(m), _ptr_array(err),
                                      _ptr(bits), _ptr(scales), _stream(stream)), ctx)
+
+
+def ob_noalloc_device_error(stream=None):
+    """Reads and clears the error word of ob_compress_noalloc's static scratch
+    on the current device (0 = none)."""
+    v = ct.c_uint()
+    _check(lib().ob_noalloc_device_error(ct.byref(v), _stream(stream)))
+    return v.value
 
 
 def ob_compress_signm(ctx, grads, sbits, sscales, err, bits, scales, stream=None):
