@@ -2,20 +2,25 @@
 
 One step = worker compression of all W workers (ob_compress), the server
 average and re-compression (ob_server_reduce) and the unpack + frozen
-variance Adam update (ob_adam_step), on the BERT-base-shaped workload:
-109,482,240 fp32 parameters in 199 tensors fused into one buffer, W = 8
-simulated data-parallel workers, chunk 2^20.  Inputs are resident in HBM
-(13.9 GB touched per step, far above the 129 MB L2, so no flush is
-needed).
+variance update (ob_adam_step, or ob_lamb_step for 1-bit LAMB).  The
+headline workload is the largest single-GPU one: the GPT-1.3B-shaped list
+(1,315,723,264 parameters in 292 tensors fused into one buffer), bf16
+gradients, fp32 state, W = 4 simulated data-parallel workers, chunk 2^20.
+Inputs are resident in HBM (about 92 GB touched per step, far above the
+129 MB L2, so no flush is needed).
 
 Prints ONE JSON line (rank 0): elements/s of the whole job, GB/s and the
 roofline fraction of the dominant kernel, the oracle's CPU throughput on a
 bounded sample, an end-to-end number through host buffers, and the SM
-clocks seen during the timed region.
+clocks seen during the timed region.  With the default workload and one
+GPU the line also carries, under "configs", the same measurements of every
+other configuration: BERT-base 1-bit Adam, BERT-large 1-bit LAMB, the flat
+2^20 case, the INT8 quantizer at 2^30 and the largest flat sweep point that
+fits in memory.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload bert-base|flat-1m|gpt-1.3b|bert-large|int8|flat|
-                              resnet50-mixed]
+                  [--workload gpt-1.3b|bert-base|flat-1m|bert-large|int8|flat|
+                              resnet50-mixed] [--no-extras]
 
 N > 1 runs under torchrun as independent replicas (one per GPU, no
 collective on the data path); timing is the max over ranks.
@@ -198,9 +203,12 @@ def kernel_source_hash(files=("k_compress.cu", "ob_internal.cuh")):
 
 INT8_SOURCES = ("k_int8.cu", "philox.cuh", "ob_internal.cuh")
 
-# Issue rate of the GPU: 152 SMs x 4 schedulers x one warp instruction (32
-# thread instructions) per clock each.
-ISSUE_THREADS_PER_CLK = 152 * 4 * 32
+
+
+def issue_threads_per_clk(props):
+    """Issue rate of the GPU in thread instructions per clock: its SMs x 4
+    schedulers x one warp instruction (32 thread instructions) per clock."""
+    return props.multi_processor_count * 4 * 32
 
 
 def recorded_kv(name, source_files):
@@ -348,26 +356,27 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def run_int8(args):
+def run_int8(args, n=None, ef=None):
     """The block-256 INT8 stochastic-rounding quantizer on the sweep's
     largest size, n = 2^30 fp32 values (4 GB in, 1 GB of codes and 16 MB of
-    scales out per call; larger than L2).  --ef: with error feedback (the
-    residual is read and written, 13 B per element) and the per-block
-    error monitor."""
+    scales out per call; larger than L2).  ef (--ef): with error feedback
+    (the residual is read and written, 13 B per element) and the per-block
+    error monitor.  Returns the JSON line (rank 0) or None."""
     import torch
 
     import momentum_compression_gb300 as ob
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
-    n = args.n or (1 << 30)
+    n = n or args.n or (1 << 30)
+    ef = ef if ef is None else ef
     g = torch.randn(n, device="cuda") * 1e-3
     q = torch.empty(n, dtype=torch.int8, device="cuda")
     sc = torch.empty((n + 255) // 256, device="cuda")
-    e = torch.zeros(n, device="cuda") if args.ef else None
-    e2 = torch.empty((n + 255) // 256, device="cuda") if args.ef else None
+    e = torch.zeros(n, device="cuda") if ef else None
+    e2 = torch.empty((n + 255) // 256, device="cuda") if ef else None
 
     def call(t):
-        if args.ef:
+        if ef:
             ob.ob_quant_int8_ef(g, e, q, sc, 1234, t, None, e2)
         else:
             ob.ob_quant_int8(g, q, sc, 1234, t)
@@ -388,7 +397,7 @@ def run_int8(args):
         b.record(stream)
         torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    bpe = (4 + 4 + 4 + 1 + 8 / 256) if args.ef else (4 + 1 + 4 / 256)
+    bpe = (4 + 4 + 4 + 1 + 8 / 256) if ef else (4 + 1 + 4 / 256)
     peak, kind = measured_peak()
     gbs = bpe * n / (ms * 1e-3) / 1e9
     clocks = clk.summary()
@@ -396,15 +405,16 @@ def run_int8(args):
     # is the issue rate at the clock seen, against the thread instructions
     # per element that ncu counted for this kernel source (profiles/).
     kv = recorded_kv("int8_instructions.txt", INT8_SOURCES) or {}
-    ipe = kv.get("thread_instructions_per_element_ef" if args.ef else
+    ipe = kv.get("thread_instructions_per_element_ef" if ef else
                  "thread_instructions_per_element")
     mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070
-    issue_peak = ISSUE_THREADS_PER_CLK * mhz * 1e6 / 1e12
+    issue_peak = issue_threads_per_clk(props) * mhz * 1e6 / 1e12
     if ipe is not None:
         ach = float(ipe) * n / (ms * 1e-3) / 1e12
         roofline = {"bound": "alu", "kernel": "quant_int8", "achieved": ach,
                     "peak": issue_peak, "peak_kind": f"issue rate at the median SM clock "
-                    f"({mhz:.0f} MHz): 152 SMs x 4 schedulers x 32 lanes",
+                    f"({mhz:.0f} MHz): {props.multi_processor_count} SMs x 4 schedulers x 32 "
+                    "lanes",
                     "unit": "T thread-instructions/s", "frac": ach / issue_peak,
                     "instructions_per_element": float(ipe),
                     "hbm": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
@@ -415,18 +425,25 @@ def run_int8(args):
                     "bytes_per_element": bpe, "traffic": None,
                     "note": "no instruction count recorded for this kernel source"}
     if rank == 0:
-        what = "with error feedback and error monitor" if args.ef else ""
-        print(json.dumps({
+        what = "with error feedback and error monitor" if ef else ""
+        return {
             "metric": "INT8 block-256 stochastic-rounding quantizer elements/s", "value": n / (ms * 1e-3),
             "unit": "elements/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32 -> int8", "data": "synthetic",
             "config": {"workload": f"int8 quantizer {what}, n = {n}, block 256, Philox4x32-10",
                        "l2": "inputs larger than L2; no flush"},
-            "roofline": roofline, "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+            "roofline": roofline, "gpu_launches": args.steps, "clocks": clocks}
+    return None
 
 
-def run_ours(args, wl):
+def run_ours(args, wl, with_e2e=True, with_cpu=True, grad_sets=2):
+    """One 1-bit workload: warmup steps, then K timed compressed steps
+    (eager with per-kernel events, and CUDA-graph replays), the end-to-end
+    step through host buffers (with_e2e) and the oracle's CPU rate on a
+    bounded sample (with_cpu).  grad_sets: resident gradient sets the steps
+    alternate between (1 for the largest sweep point, whose memory it
+    saves).  Returns the JSON line (rank 0) or None."""
     import torch
 
     import momentum_compression_gb300 as ob
@@ -455,7 +472,9 @@ def run_ours(args, wl):
     p0[:n] = torch.randn(n, generator=gen, device=device) * 0.02
     opt.p.copy_(p0)
     del p0
-    gsets = [device_grads(torch, wl, n_pad, s, gdt, device) for s in range(2)]
+    gsets = [device_grads(torch, wl, n_pad, s, gdt, device) for s in range(grad_sets)]
+    if grad_sets == 1:
+        gsets = gsets * 2
     # prerequisite: a few uncompressed warmup steps freeze v (timed on their
     # own: the warmup step is a row of the path, not the metric)
     stream0 = torch.cuda.current_stream()
@@ -585,70 +604,72 @@ def run_ours(args, wl):
     achieved = dom_bytes / (kms[dom] * 1e-3) / 1e9
     traffic = recorded_traffic(wl, sign_m) if dom == "compress" else None
 
-    # End to end through host buffers, pipelined through the public calls.
-    # Every step copies all W gradients host -> device (pinned memory) and
-    # reads the updated parameters back.  A copy stream brings step t+1's
-    # gradients into the other device buffer set while the compute stream
-    # runs step t; a read-back stream copies step t's parameters to the
-    # host, and the update of step t+1 waits for that read-back (it
-    # rewrites p).  The host link (about 210 GB/s here) bounds it.
-    host_g = [torch.empty(n_pad, dtype=gdt, pin_memory=True) for _ in range(wl.W)]
-    for w in range(wl.W):
-        host_g[w].copy_(gsets[0][w])
-    host_p = torch.empty(n_pad, dtype=torch.float32, pin_memory=True)
-    s_h2d, s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    ev = lambda: torch.cuda.Event()
-    ev_h2d, ev_used = [ev(), ev()], [ev(), ev()]
-    ev_upd, ev_back = ev(), ev()
+    e2e = None
+    if with_e2e:
+        # End to end through host buffers, pipelined through the public calls.
+        # Every step copies all W gradients host -> device (pinned memory) and
+        # reads the updated parameters back.  A copy stream brings step t+1's
+        # gradients into the other device buffer set while the compute stream
+        # runs step t; a read-back stream copies step t's parameters to the
+        # host, and the update of step t+1 waits for that read-back (it
+        # rewrites p).  The host link (about 210 GB/s here) bounds it.
+        host_g = [torch.empty(n_pad, dtype=gdt, pin_memory=True) for _ in range(wl.W)]
+        for w in range(wl.W):
+            host_g[w].copy_(gsets[0][w])
+        host_p = torch.empty(n_pad, dtype=torch.float32, pin_memory=True)
+        s_h2d, s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        ev = lambda: torch.cuda.Event()
+        ev_h2d, ev_used = [ev(), ev()], [ev(), ev()]
+        ev_upd, ev_back = ev(), ev()
 
-    def issue_h2d(t):
-        b = t % 2
-        if t >= 2:
-            s_h2d.wait_event(ev_used[b])
-        with torch.cuda.stream(s_h2d):
-            for w in range(wl.W):
-                gsets[b][w].copy_(host_g[w], non_blocking=True)
-        ev_h2d[b].record(s_h2d)
+        def issue_h2d(t):
+            b = t % 2
+            if t >= 2:
+                s_h2d.wait_event(ev_used[b])
+            with torch.cuda.stream(s_h2d):
+                for w in range(wl.W):
+                    gsets[b][w].copy_(host_g[w], non_blocking=True)
+            ev_h2d[b].record(s_h2d)
 
-    def issue_step(t):
-        b = t % 2
-        stream.wait_event(ev_h2d[b])
-        compress(gsets[b])
-        server()
-        ev_used[b].record(stream)
-        if t >= 1:
-            stream.wait_event(ev_back)
-        update()
-        ev_upd.record(stream)
-        s_d2h.wait_event(ev_upd)
-        with torch.cuda.stream(s_d2h):
-            host_p.copy_(opt.p, non_blocking=True)
-        ev_back.record(s_d2h)
+        def issue_step(t):
+            b = t % 2
+            stream.wait_event(ev_h2d[b])
+            compress(gsets[b])
+            server()
+            ev_used[b].record(stream)
+            if t >= 1:
+                stream.wait_event(ev_back)
+            update()
+            ev_upd.record(stream)
+            s_d2h.wait_event(ev_upd)
+            with torch.cuda.stream(s_d2h):
+                host_p.copy_(opt.p, non_blocking=True)
+            ev_back.record(s_d2h)
 
-    def pipeline(steps):
-        issue_h2d(0)
-        for t in range(steps):
-            if t + 1 < steps:
-                issue_h2d(t + 1)
-            issue_step(t)
+        def pipeline(steps):
+            issue_h2d(0)
+            for t in range(steps):
+                if t + 1 < steps:
+                    issue_h2d(t + 1)
+                issue_step(t)
 
-    pipeline(2)
-    torch.cuda.synchronize()
-    K2 = max(3, min(K, 10))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_h2d)
-    pipeline(K2)
-    b.record(s_d2h)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, pg, device)
-    e2e = {"value": job_rate(n, world, e2e_ms), "unit": "elements/s",
-           "h2d_bytes_per_step": wl.W * n_pad * G, "d2h_bytes_per_step": n_pad * 4,
-           "ms_per_step": e2e_ms,
-           "pipelined": "H2D of step t+1 overlaps step t and its parameter read-back"}
-    del host_g, host_p
+        pipeline(2)
+        torch.cuda.synchronize()
+        K2 = max(3, min(K, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_h2d)
+        pipeline(K2)
+        b.record(s_d2h)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / K2, pg, device)
+        e2e = {"value": job_rate(n, world, e2e_ms), "unit": "elements/s",
+               "h2d_bytes_per_step": wl.W * n_pad * G, "d2h_bytes_per_step": n_pad * 4,
+               "ms_per_step": e2e_ms,
+               "pipelined": "H2D of step t+1 overlaps step t and its parameter read-back"}
+        del host_g, host_p
 
     cpu = None
-    if rank == 0 and world == 1:
+    if with_cpu and rank == 0 and world == 1:
         sample = min(1 << 24, n)
         times = oracle_sample_step_time(wl, sample, 16, budget_s=12.0)
         steps = len(times)
@@ -659,7 +680,8 @@ def run_ours(args, wl):
                          f"({sum(times):.1f} s)", "cpu": cpu_model()}
 
     if rank != 0:
-        return
+        opt.close()
+        return None
     line = {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -694,8 +716,8 @@ def run_ours(args, wl):
     if graph_info is not None:
         line["config"]["launch"] = "CUDA graph replay (one graph launch per step)"
         line["graph"] = graph_info
-    print(json.dumps(line), flush=True)
     opt.close()
+    return line
 
 
 def mixed_bytes(bits, W, G, send=True):
@@ -993,7 +1015,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--workload", default="bert-base")
+    ap.add_argument("--workload", default=None,
+                    help="default gpt-1.3b (the largest single-GPU configuration), with the "
+                         "other configurations measured under \"configs\"")
     ap.add_argument("--n", "--elements", dest="n", type=int,
                     help="elements (flat and int8 workloads); use --elements under torchrun")
     ap.add_argument("--W", type=int, help="workers (flat workload only)")
@@ -1014,13 +1038,20 @@ def main():
                     help="clamp of the compensated values (the write-up's stability variant)")
     ap.add_argument("--sweep", action="store_true",
                     help="the flat n x W x chunk bandwidth sweep, one JSON line per point")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload: leave out the other configurations")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.sweep:
         run_sweep(args)
         return
+    default = args.workload is None
+    if default:
+        args.workload = DEFAULT_WORKLOAD
     if args.impl == "ours" and args.workload == "int8":
-        run_int8(args)
+        line = run_int8(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
         return
     if args.workload == "resnet50-mixed":
         if args.impl == "reference":
@@ -1052,8 +1083,66 @@ def main():
         wl.hp["clip_value"] = args.clip_value
     if args.impl == "reference":
         run_reference(args, wl)
-    else:
-        run_ours(args, wl)
+        return
+    line = run_ours(args, wl)
+    world, rank, _ = dist_env()
+    if default and world == 1 and not args.no_extras:
+        line["configs"] = run_extras(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+DEFAULT_WORKLOAD = "gpt-1.3b"
+
+
+def config_entry(line):
+    """The measurements of one configuration as carried in the headline's
+    "configs": its own step time, per-kernel times and GB/s, the roofline
+    of its dominant kernel (bytes per element and kernel time, so the
+    fraction recomputes), and the clocks seen while it ran."""
+    keep = ("metric", "value", "unit", "ms_per_step", "steps", "dtype", "config", "gbs",
+            "worker_elements_per_s", "roofline", "step_roofline_frac", "warmup_step",
+            "kernels_ms", "kernels_gbs", "gpu_launches", "clocks", "graph")
+    return {k: line[k] for k in keep if k in line}
+
+
+def run_extras(args):
+    """Every other configuration, one after the other on this GPU (N = 1),
+    each with its buffers freed before the next: BERT-base 1-bit Adam,
+    BERT-large 1-bit LAMB, the flat 2^20 case (launch-bound and
+    L2-resident), the INT8 quantizer at 2^30, and the largest point of the
+    flat sweep (n = 2^30, W = 16, chunk 2^20, or the largest W that fits)."""
+    import gc
+
+    import torch
+    out = {}
+
+    def settle():
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    for name in ("bert-base", "bert-large", "flat-1m"):
+        settle()
+        wl = synth.workload(name)
+        log(f"[bench] extra configuration {name}")
+        out[name] = config_entry(run_ours(args, wl, with_e2e=False, with_cpu=False))
+    settle()
+    log("[bench] extra configuration int8")
+    out["int8-2^30"] = config_entry(run_int8(args, n=1 << 30, ef=False))
+    settle()
+    free, _ = torch.cuda.mem_get_info()
+    for W in (16, 8, 4):
+        n = 1 << 30
+        # W gradient and error buffers, m, v, p, e_s, sign words: 8W + 20 B/element
+        if n * (8 * W + 20) * 1.1 < free * 0.9:
+            wl = synth.workload("flat", n=n, W=W, chunk=1 << 20)
+            log(f"[bench] extra configuration flat 2^30 x {W}")
+            out[f"flat-2^30-W{W}"] = config_entry(
+                run_ours(args, wl, with_e2e=False, with_cpu=False, grad_sets=1))
+            break
+    settle()
+    return out
 
 
 if __name__ == "__main__":
