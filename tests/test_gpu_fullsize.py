@@ -1,27 +1,32 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py
 times (the same OneBitOptimizer calls, grids sized by the library).
 
-The whole buffers are too large for the oracle, but the 1-bit Adam step is
-chunk-local: every output element depends only on the inputs of its own
-chunk (the chunk's scale, its W workers' signs, the server's error).  So
-each test runs the full-size step on the GPU and the oracle on a few
-sampled chunks -- the first, one in the middle, the last real one (with
-the padding tail) and the short last chunk of a partition -- and compares
-them element by element.  For 1-bit LAMB the per-layer coefficient needs
-whole layers: it is checked exactly for layers that lie inside a sampled
-chunk, and through the clip bounds it must satisfy for every other layer.
+The 1-bit Adam step is chunk-local: every output element depends only on
+the inputs of its own chunk (the chunk's scale, its W workers' signs, the
+server's error), and Adam's warmup step is elementwise.  So the Adam tests
+run the full-size steps on the GPU and the oracle on a few sampled chunks
+-- the first, one in the middle, the last real one (with the padding tail)
+and the short last chunk of a partition -- as problems of their own, over
+the configurations' own step counts, and compare them element by element.
+1-bit LAMB's per-layer coefficient needs whole layers, so its multi-step
+test runs the oracle on the whole buffer, split over the partitions on a
+thread pool (tests/oracle_parallel.py).
 
 Inputs are drawn on the GPU by torch's seeded generator with the synth
 recipe's distributions (host generation of billions of values would take
-minutes); the sampled slices are copied to the host before the step and
-given to the oracle.
+minutes); the slices the oracle needs are copied to the host before each
+step.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
 
 import momentum_compression_gb300 as ob
 import oracle as O
+import oracle_parallel as OP
 import synth
 from helpers import assert_bits_equal, assert_close, host
 
@@ -227,9 +232,77 @@ def test_bert_base_full_size(sign_momentum):
                        sign_momentum=sign_momentum)
 
 
-def test_gpt_1p3b_bf16_full_size():
-    """1,315,723,264 parameters (292 tensors), W = 4, bf16 gradients."""
-    _run_adam_fullsize(synth.workload("gpt-1.3b"), steps=2, need_bytes=70e9)
+def _run_adam_from_warmup(wl, warmup, steps, need_bytes, sign_momentum=True):
+    """The configuration's own schedule at full size: p0 ~ N(0, 0.02), m =
+    v = 0, `warmup` uncompressed steps, the end of warmup, then `steps`
+    compressed steps (the momentum in sign form from the second one, as
+    bench.py runs it).  The oracle runs the sampled chunks as problems of
+    their own (Adam's warmup is elementwise and its compressed step
+    chunk-local), on a thread pool.  The sampled server words and scales are
+    compared after every compressed step, everything else at the end."""
+    if _free_bytes() < need_bytes:
+        pytest.skip(f"needs {need_bytes / 1e9:.0f} GB of free device memory")
+    opt = ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype,
+                             sign_momentum=sign_momentum, **wl.hp)
+    std = _std_vector(wl, opt.n_pad)
+    opt.p[: wl.n] = torch.randn(wl.n, generator=_gen(synth.SEED_BASE + 17), device="cuda") * 0.02
+    chunks = _chunks(opt.layout, wl.n)
+    st0 = _slices(opt, chunks)
+    cos = {g: ChunkOracle(wl.W, s, ln, r, st0[g]) for g, s, ln, r in chunks}
+    hp = wl.hp
+    with ThreadPoolExecutor(len(cos)) as pool:
+        for t in range(warmup):
+            grads = _grads(opt, wl, t, std)
+            gsl = _grad_slices(grads, chunks)
+            opt.warmup_step(grads)
+            list(pool.map(lambda g: O.warmup_step(cos[g].lay, cos[g].grads(gsl[g]), 0, hp,
+                                                  cos[g].state.m, cos[g].state.v,
+                                                  cos[g].state.p), cos))
+            del grads
+        opt.begin_compression()
+        for co in cos.values():
+            O.begin_compression(co.state, warmup)
+        torch.cuda.synchronize()
+        for g, co in cos.items():
+            S, a, r = co.state, co.s, co.r
+            assert_bits_equal(host(opt.v[a:a + r]), S.v[:r], f"chunk {g}: v after warmup")
+            assert_bits_equal(host(opt.p[a:a + r]), S.p[:r], f"chunk {g}: p after warmup")
+        for t in range(warmup, warmup + steps):
+            grads = _grads(opt, wl, t, std)
+            gsl = _grad_slices(grads, chunks)
+            opt.compressed_step(grads)
+            list(pool.map(lambda g: O.compressed_step(cos[g].state, cos[g].grads(gsl[g]), hp),
+                          cos))
+            del grads
+            torch.cuda.synchronize()
+            for g, co in cos.items():
+                words = co.ln // 32
+                assert_bits_equal(host(opt.sbits[co.s // 32: co.s // 32 + words]),
+                                  co.state.sbits[:words], f"chunk {g} sbits at step {t}")
+                assert_bits_equal(host(opt.sscales[g]), co.state.sscales[0],
+                                  f"chunk {g} sscale at step {t}")
+    assert ob.ob_device_error(opt.ctx) == 0
+    opt.materialize_m()
+    for g, co in cos.items():
+        _compare_chunk(opt, co, g, f"chunk {g}")
+    opt.materialize_errors()
+    torch.cuda.synchronize()
+    for g, co in cos.items():
+        _compare_chunk_errors_and_p(opt, co, f"chunk {g}")
+    opt.close()
+
+
+def test_gpt_1p3b_bf16_5_warmup_10_compressed():
+    """1,315,723,264 parameters (292 tensors), W = 4, bf16 gradients, chunk
+    2^20: 5 warmup steps then 10 compressed steps, the configuration's
+    counts, in the launch configuration bench.py times."""
+    _run_adam_from_warmup(synth.workload("gpt-1.3b"), 5, 10, need_bytes=80e9)
+
+
+def test_bert_base_100_warmup_50_compressed():
+    """109,482,240 parameters (199 tensors), W = 8, fp32, chunk 2^20: the
+    configuration's 100 warmup and 50 compressed steps."""
+    _run_adam_from_warmup(synth.workload("bert-base"), 100, 50, need_bytes=30e9)
 
 
 @pytest.mark.parametrize("n,W,chunk", [
@@ -431,3 +504,104 @@ def test_bert_large_lamb_sign_form_equals_dense_full_size():
         torch.cuda.empty_cache()
     for k in out[0]:
         assert_bits_equal(out[1][k], out[0][k], f"{k}: sign form vs dense")
+
+
+def _host_avail_bytes():
+    try:
+        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
+
+
+def test_bert_large_lamb_whole_buffer_3_warmup_10_compressed():
+    """1-bit LAMB on the whole BERT-large list (336,226,108 parameters, 302
+    tensors, W = 8, fp32): 3 warmup steps, the end of warmup, then 10
+    compressed steps with the gradient std falling 10x over them (v_t falls
+    100x, so r_t moves and its clip acts; rho = c_{t-2}/c_{t-1} differs
+    from 1 from the third compressed step on).  The oracle runs the whole
+    buffer -- every layer whole, so every layer's R, r and c is the
+    oracle's own -- with the compressed step split over the partitions on a
+    thread pool (tests/oracle_parallel.py, bit for bit the whole-buffer
+    step).  The GPU runs it twice, with the dense momentum and with the
+    momentum in sign form (server output double-buffered, as bench.py
+    runs it), and both are compared with the oracle after every step (c
+    of every layer, server words and scales) and, at the end, on every
+    element of every buffer."""
+    wl = synth.workload("bert-large")
+    if _free_bytes() < 60e9:
+        pytest.skip("needs 60 GB of free device memory")
+    if _host_avail_bytes() < 48e9:
+        pytest.skip("needs 48 GB of free host memory for the whole-buffer oracle")
+    hp = wl.hp
+    off = wl.layer_offsets.astype(np.uint64)
+    opts = {sm: ob.OneBitOptimizer(wl.n, wl.W, wl.chunk, wl.align, wl.grad_dtype,
+                                   [int(x) for x in off], lamb=True, sign_momentum=sm, **hp)
+            for sm in (False, True)}
+    n, n_pad = wl.n, opts[False].n_pad
+    lay = O.Layout(n, wl.W, wl.align, wl.chunk)
+    assert lay.n_pad == n_pad
+    layers = O.Layers(off)
+    st = O.State(lay, layers, lamb=True)
+    std = _std_vector(wl, n_pad)
+    p0 = torch.zeros(n_pad, device="cuda")
+    p0[:n] = torch.randn(n, generator=_gen(synth.SEED_BASE + 17), device="cuda") * 0.02
+    for o in opts.values():
+        o.p.copy_(p0)
+    st.p[:] = host(p0)
+    del p0
+    warm, steps = 3, 10
+    with ThreadPoolExecutor(os.cpu_count() or 8) as pool:
+        for t in range(warm):
+            grads = _grads(opts[False], wl, t, std)
+            for o in opts.values():
+                o.warmup_step(grads)
+            gh = [host(x) for x in grads]
+            del grads
+            c = O.warmup_step(lay, gh, 1, hp, st.m, st.v, st.p, layers, st.c_sum)
+            torch.cuda.synchronize()
+            for sm, o in opts.items():
+                assert_bits_equal(host(o.ls.c_t), c, f"warmup c at step {t} (sign form {sm})")
+            del gh
+        for o in opts.values():
+            o.begin_compression()
+        O.begin_compression(st, warm, lamb=True)
+        torch.cuda.synchronize()
+        for sm, o in opts.items():
+            for k in ("s", "c_avg", "r_prev", "c_prev", "c_prev2"):
+                assert_bits_equal(host(getattr(o.ls, k)), st.ls[k], f"begin: {k} (sign form {sm})")
+        for t in range(warm, warm + steps):
+            f = 10.0 ** (-(t - warm) / (steps - 1))
+            grads = _grads(opts[False], wl, t, std * f)
+            for o in opts.values():
+                o.compressed_step(grads)
+            gh = [host(x) for x in grads]
+            del grads
+            OP.compressed_step(st, gh, hp, pool, lamb=True)
+            del gh
+            torch.cuda.synchronize()
+            for sm, o in opts.items():
+                what = f"step {t} (sign form {sm})"
+                assert_bits_equal(host(o.ls.c_t), st.c, f"c of every layer, {what}")
+                assert_bits_equal(host(o.sscales), st.sscales, f"server scales, {what}")
+                assert_bits_equal(host(o.sbits)[: lay.words], st.sbits, f"server words, {what}")
+    assert np.any(st.ls["r_prev"] != 1.0), "the ratio never moved"
+    assert np.any(st.ls["c_prev"] != st.ls["c_prev2"]), "rho stayed 1"
+    for sm, o in opts.items():
+        assert ob.ob_device_error(o.ctx) == 0
+        what = f"(sign form {sm})"
+        for k in ("r_prev", "c_prev", "c_prev2"):
+            assert_bits_equal(host(getattr(o.ls, k)), st.ls[k], f"{k} {what}")
+        o.materialize_m()
+        assert_bits_equal(host(o.bits)[:, : lay.words], st.bits, f"worker words {what}")
+        assert_bits_equal(host(o.scales), st.scales, f"worker scales {what}")
+        o.materialize_errors()
+        torch.cuda.synchronize()
+        pairs = [("m", o.m, st.m), ("p", o.p, st.p), ("e_s", o.err_s, st.e_s),
+                 ("v_fresh", o.v_fresh, st.v_fresh)]
+        pairs += [(f"e[{w}]", o.err[w], st.e[w]) for w in range(wl.W)]
+        for name, gbuf, want in pairs:
+            got = host(gbuf)
+            assert_close(got, want, f"{name} {what}")
+            assert_bits_equal(got, want, f"{name} {what}")
+        o.close()
+    torch.cuda.empty_cache()

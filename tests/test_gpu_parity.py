@@ -309,25 +309,32 @@ LAMB_HP = dict(b1=0.9, b2=0.999, eps=1e-6, lr=1e-3, r_thr=0.1, r_min=0.5, r_max=
                c_min=0.01, c_max=10.0)
 
 
-@pytest.mark.parametrize("flags,W,dt,sm", [
-    (0, 4, "f32", False), (ob.OB_FLAG_NO_RATIO_EF, 4, "f32", False),
-    (ob.OB_FLAG_FROZEN_C, 4, "f32", False),
-    (0, 8, "bf16", False),   # the W = 8 server specialisation, bf16 worker kernel
-    (0, 3, "f32", False),    # generic W
-    (0, 12, "bf16", False),  # workers beyond the 8-worker sign table
+@pytest.mark.parametrize("flags,W,dt,sm,warm,steps", [
+    (0, 4, "f32", False, 3, 6), (ob.OB_FLAG_NO_RATIO_EF, 4, "f32", False, 3, 6),
+    (ob.OB_FLAG_FROZEN_C, 4, "f32", False, 3, 6),
+    (0, 8, "bf16", False, 3, 6),   # the W = 8 server specialisation, bf16 worker kernel
+    (0, 3, "f32", False, 3, 6),    # generic W
+    (0, 12, "bf16", False, 3, 6),  # workers beyond the 8-worker sign table
     # the momentum in sign form, server output double-buffered
-    (0, 4, "f32", True), (ob.OB_FLAG_NO_RATIO_EF, 3, "f32", True),
-    (ob.OB_FLAG_FROZEN_C, 8, "bf16", True), (0, 12, "bf16", True),
-    (ob.OB_FLAG_NO_RATIO_EF, 16, "f32", True),  # the W = 16 server specialisation
-    (0, 64, "f32", True),                       # the largest W, the generic server
+    (0, 4, "f32", True, 3, 6), (ob.OB_FLAG_NO_RATIO_EF, 3, "f32", True, 3, 6),
+    (ob.OB_FLAG_FROZEN_C, 8, "bf16", True, 3, 6), (0, 12, "bf16", True, 3, 6),
+    (ob.OB_FLAG_NO_RATIO_EF, 16, "f32", True, 3, 6),  # the W = 16 server specialisation
+    (0, 64, "f32", True, 3, 6),                       # the largest W, the generic server
+    # the BERT-large LAMB configuration's step counts (W = 8, fp32, 10
+    # warmup + 50 compressed steps, v falling 100x over the compressed
+    # steps) under each flag setting, sign form and dense
+    (0, 8, "f32", True, 10, 50), (ob.OB_FLAG_NO_RATIO_EF, 8, "f32", True, 10, 50),
+    (ob.OB_FLAG_FROZEN_C, 8, "f32", True, 10, 50), (0, 8, "f32", False, 10, 50),
 ])
-def test_lamb_small_layers(flags, W, dt, sm):
+def test_lamb_small_layers(flags, W, dt, sm, warm, steps):
     """Layers of odd sizes (1, 2, 7, 4095, 4097, ...) fused into one buffer,
-    chunk 2048, 3 warmup + 6 compressed steps with the gradient std falling
-    3x per step, so that r_t moves and the step-ratio error feedback
-    differs from 1.  sm: the momentum held as sscale*sign/sigma_l of the
-    server output (ob_step_db from the second compressed step on), which
-    must give the dense path's results bit for bit."""
+    chunk 2048, `warm` warmup + `steps` compressed steps with the gradient
+    std falling over the compressed steps (3x per step in the short runs,
+    10x over the 50 steps of the long ones), so that r_t moves and the
+    step-ratio error feedback differs from 1.  sm: the momentum held as
+    sscale*sign/sigma_l of the server output (ob_step_db from the second
+    compressed step on), which must give the dense path's results bit for
+    bit."""
     sizes = [7, 1, 2, 4095, 4097, 33, 1000, 20000, 3, 30000]
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.uint64)
     n, A, C = int(off[-1]), 32, 2048
@@ -342,10 +349,13 @@ def test_lamb_small_layers(flags, W, dt, sm):
     st.p[:] = p0
     opt.p.copy_(torch.from_numpy(p0))
     layer_std = np.repeat(10.0 ** rng.uniform(-4, -2, size=len(sizes)), sizes).astype(f32)
-    warm, steps = 3, 6
+
+    def decay(t):
+        k = max(0, t - warm)
+        return f32(3.0 ** -k) if steps <= 6 else f32(10.0 ** (-k / (steps - 1)))
 
     def grads(t):
-        f = f32(3.0 ** -max(0, t - warm))
+        f = decay(t)
         gh = []
         for w in range(W):
             a = np.zeros(lay.n_pad, f32)
