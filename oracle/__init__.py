@@ -43,6 +43,7 @@ def lib():
                                                f32p, u32p, f32p, vp]
         L.orc_server_reduce.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p,
                                         u32p, f32p, vp]
+        L.orc_error_norm.argtypes = [lay, f32p, f32p]
         L.orc_compress_worker_range.argtypes = [lay, vp, u64, vp, vp, f32, f32, f32p, f32p,
                                                 f32p, u32p, f32p, vp, u64, u64]
         L.orc_server_reduce_range.argtypes = [lay, vp, u64, vp, u32p, f32p, f32p, u32p, f32p,
@@ -212,6 +213,14 @@ def lamb_pass_a_range(lay, g0, g1, layers, sigma, sbits, sscales, v_frozen, b1, 
 def lamb_pass_b_range(lay, g0, g1, layers, c, m, v_frozen, eps, lr, p):
     lib().orc_lamb_pass_b_range(lay._s, _ptr(layers.off), layers.nl, _f32(c), _f32(m),
                                 _f32(v_frozen), eps, lr, p, g0, g1)
+
+
+def error_norm(lay, e):
+    """Per chunk, the sum of squares of the true errors e' (n_pad,) over the
+    chunk's real elements, in the fixed order: (nc,) f32."""
+    out = np.zeros(lay.nc, np.float32)
+    lib().orc_error_norm(lay._s, _f32(e), out)
+    return out
 
 
 def decompress(lay, sbits, sscales, layers=None, sigma=None):

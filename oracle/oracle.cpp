@@ -323,6 +323,25 @@ void orc_server_reduce(const orc_layout* L, const uint64_t* layer_off,
                           L->nc);
 }
 
+// Quantisation-error monitor ([TUT] "监控与诊断": watch the norm of the
+// quantisation error; [BLOG] §7: check that the error term stays bounded),
+// for the 1-bit compressor: per chunk g,
+//   out[g] = CR(e[k]^2 over the chunk's real elements)
+// the square of the error's 2-norm on that chunk, summed in the fixed order.
+// `e` holds true errors e' (worker or server).  Reading: the pages name the
+// monitored quantity only as the error's norm; the squared 2-norm per chunk
+// is the quantity that adds up over chunks and needs no square root.
+void orc_error_norm(const orc_layout* L, const float* e, float* out) {
+  std::vector<float> sq;
+  for (uint64_t g_id = 0; g_id < L->nc; ++g_id) {
+    uint64_t start, len, real;
+    chunk_range(L, g_id, &start, &len, &real);
+    sq.assign(real, 0.0f);
+    for (uint64_t q = 0; q < real; ++q) sq[q] = e[start + q] * e[start + q];
+    out[g_id] = orc_cr_sum(sq.data(), real);
+  }
+}
+
 // Decompression of the server result ([LAMB] ¶2: the global compressed
 // momentum is divided by the same fixed coefficient afterwards):
 //   out_k = sscale(chunk(k)) * sign(sbit_k) / sigma_l   (sigma = 1 if NULL)

@@ -95,6 +95,12 @@ MUTATIONS = [
      "float ca = c_sum[l] / (float)warmup_steps;", "float ca = c_sum[l];"),
     ("INT8 code clamped at 128",
      "if (qf > 127.0f) qf = 127.0f;", "if (qf > 128.0f) qf = 127.0f;"),
+    ("error monitor sums |e| instead of e^2",
+     "for (uint64_t q = 0; q < real; ++q) sq[q] = e[start + q] * e[start + q];",
+     "for (uint64_t q = 0; q < real; ++q) sq[q] = std::fabs(e[start + q]);"),
+    ("error monitor takes the mean instead of the sum",
+     "out[g_id] = orc_cr_sum(sq.data(), real);",
+     "out[g_id] = real ? orc_cr_sum(sq.data(), real) / (float)real : 0.0f;"),
     # mixed widths: the b-bit block codec and the FP16 codec
     ("b-bit code range one too wide",
      "const float qmax = (float)((1 << (bits - 1)) - 1);",

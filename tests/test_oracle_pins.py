@@ -63,6 +63,35 @@ def test_worked_example_adam():
     _eq(m, x["m"])
     _eq(p, x["p"])
     _eq(O.decompress(lay, sbits, sscales), x["m"])
+    # the error monitor on the same step, by hand: per chunk the sum of the
+    # squared errors, e_0 = [-0.5,-0.5 | 1.5,-1.5] -> [0.5, 4.5],
+    # e_1 = [0.5,-0.5 | 0,0] -> [0.5, 0], e_s = [0.75,-0.75 | 0,0] -> [1.125, 0]
+    _eq(O.error_norm(lay, e[0]), [0.5, 4.5])
+    _eq(O.error_norm(lay, e[1]), [0.5, 0.0])
+    _eq(O.error_norm(lay, e_s), [1.125, 0.0])
+
+
+def test_error_norm_against_fp64_and_padding():
+    """Random errors over a layout with ragged chunks and a padding tail:
+    each chunk's value is within the fp32 summation bound of the fp64 sum
+    of squares of its real elements, and whatever sits in the padding
+    changes nothing."""
+    rng = np.random.default_rng(41)
+    n, W, A, C = 30_001, 3, 4096, 3000
+    lay = O.Layout(n, W, A, C)
+    e = np.zeros(lay.n_pad, f32)
+    e[:n] = rng.standard_normal(n).astype(f32) * f32(1e-3)
+    got = O.error_norm(lay, e)
+    assert got.shape == (lay.nc,)
+    for g in range(lay.nc):
+        s, ln, real = lay.chunk_range(g)
+        want = float(np.sum(e[s:s + real].astype(np.float64) ** 2))
+        assert abs(float(got[g]) - want) <= (real + 2) * 2.0 ** -23 * want + 1e-45, g
+        if real == 0:
+            assert got[g] == 0.0
+    junk = e.copy()
+    junk[n:] = f32(1e30)
+    _eq(O.error_norm(lay, junk), got)
 
 
 def test_worked_example_lamb():
