@@ -796,10 +796,10 @@ def run_mixed(args):
                     ke = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                     g.t += 1
                     ob.ob_compress_qb(g.ctx, 2, gsets[t % 2][i], g.m, g.err, g.codes, g.bscales,
-                                      g.seed, g.t)
+                                      g.key, g.t)
                     ke[0].record(stream)
                     ob.ob_server_reduce_qb(g.ctx, 2, g.codes, g.bscales, g.err_s, g.scodes,
-                                           g.sbscales, g.seed, g.t)
+                                           g.sbscales, g.key, g.t)
                     ke[1].record(stream)
                     ob.ob_adam_step_qb(g.ctx, 2, g.scodes, g.sbscales, g.v, g.m, g.p)
                     ke[2].record(stream)

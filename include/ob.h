@@ -128,6 +128,18 @@ typedef struct ob_config {
   float clip_value;             /* > 0: workers' compensated values are
                                    limited to [-clip_value, clip_value]
                                    before compression ([BLOG] 4.1); 0 = off */
+  /* The method's schedules ([BLOG] 4.1, 3.2 table, 6 layerwise_bits); see
+   * ob_plan_step.  All zero: no reset, every step exchanged, key = bits. */
+  uint32_t reset_interval;      /* > 0: worker and server errors are reset
+                                   to 0 before every reset_interval-th
+                                   compressed step ([BLOG] 4.1: every 2000);
+                                   0 = never */
+  uint32_t send_period;         /* FP16 codec groups: exchanged on the
+                                   compressed steps t with t % send_period
+                                   == 0 ([BLOG] 3.2: every 10th); 0 or 1 =
+                                   every step */
+  uint64_t seed;                /* b-bit codec groups: the Philox key is
+                                   seed + bits, one stream per width */
 } ob_config;
 
 typedef struct ob_layout {
@@ -323,6 +335,21 @@ ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
                           const float* scales, float* err_s, const uint32_t* sbits,
                           const float* sscales, ob_stream_t stream);
 
+/* The quantisation-error monitor of [TUT] "监控与诊断" (watch the norm of
+ * the quantisation error) and [BLOG] 7 (check that the error term stays
+ * bounded), for the 1-bit compressor.  From the deferred buffers of the
+ * last step (the same ones ob_materialize_errors reads; nothing is
+ * written but `out` and the workspace's tile totals):
+ *   out[w*n_chunks + g] = sum over chunk g's real elements of e_w'^2,
+ *   out[W*n_chunks + g] = the same for the server error e_s',
+ * e' = x - scale*sign(x) decoded as the next compression would, each sum
+ * in the fixed order of the scales.  out: (W+1)*n_chunks floats, 4-byte
+ * aligned; the square root of a row's total is that error's 2-norm.  Uses
+ * the workspace like the other calls of the ctx. */
+ob_status ob_error_norm(ob_ctx* ctx, const float* const* err, const uint32_t* bits,
+                        const float* scales, const float* err_s, const uint32_t* sbits,
+                        const float* sscales, float* out, ob_stream_t stream);
+
 /* Reads and clears the device error word of the workspace (0 = none;
  * 1 = a consumer's wait for a copy ran out, 2 = the producer's wait for a
  * free stage ran out, 3 = copies still in flight at exit).  Synchronises
@@ -387,6 +414,25 @@ ob_status ob_quant_int8(const float* g, size_t n, int8_t* q,
 ob_status ob_quant_int8_ef(const float* g, float* e, size_t n, int8_t* q, float* block_scales,
                            uint64_t seed, uint64_t step, float* deq, float* block_err2,
                            ob_stream_t stream);
+
+/* The schedule of compressed step t (t = 1, 2, ... counts the compressed
+ * steps since ob_begin_compression or ob_zero_errors) for a group of width
+ * `bits` (1, 2, 4, 8 or 16), from the ctx's configuration -- host only, no
+ * CUDA call:
+ *   reset  1 iff reset_interval > 0, t > 1 and (t - 1) % reset_interval == 0:
+ *          the errors are reset before this step ([BLOG] 4.1), by
+ *          ob_reset_errors (width 1) or ob_zero_errors (the codecs)
+ *   send   width 16: 1 iff t % send_period == 0 ([BLOG] 3.2, "FP16, 每10步");
+ *          other widths: 1
+ *   key    width 2, 4, 8: seed + bits, the Philox key of ob_compress_qb and
+ *          ob_server_reduce_qb; other widths: 0
+ *   step   t, their Philox step counter
+ * ob_codec_step applies it; a caller of the width-1 calls reads `reset`. */
+typedef struct ob_plan {
+  int reset, send;
+  uint64_t key, step;
+} ob_plan;
+ob_status ob_plan_step(const ob_ctx* ctx, int bits, uint64_t t, ob_plan* out);
 
 /* ------------------------------------------------------------------------
  * Layerwise mixed bit widths ([BLOG] 3.2 table: a bit width and an update
@@ -467,6 +513,20 @@ ob_status ob_server_reduce_f16(ob_ctx* ctx, const uint16_t* h, float* err_s, uin
  * p is left as it is (hs, v_frozen, p may be NULL).  Padding: m = 0. */
 ob_status ob_adam_step_f16(ob_ctx* ctx, int send, const uint16_t* hs, const float* v_frozen,
                            float* m, float* p, ob_stream_t stream);
+
+/* One compressed step of a codec group of width `bits` (2, 4, 8 or 16) at
+ * compressed step t >= 1, following ob_plan_step(ctx, bits, t): the errors
+ * are zeroed first if `reset`; then, width 2/4/8: ob_compress_qb,
+ * ob_server_reduce_qb, ob_adam_step_qb with the plan's key and step, msg =
+ * codes [W][words_per_worker] u32, msg_scales = bscales, smsg = scodes,
+ * smsg_scales = sbscales; width 16: ob_compress_f16 with the plan's send,
+ * then (sending steps) ob_server_reduce_f16 and ob_adam_step_f16, msg = h
+ * [W][n_pad] u16, smsg = hs [n_pad] u16, the two scale pointers unused
+ * (may be NULL).  Arguments as for those calls. */
+ob_status ob_codec_step(ob_ctx* ctx, int bits, uint64_t t, const void* const* grads, float* m,
+                        float* const* err, void* msg, float* msg_scales, float* err_s,
+                        void* smsg, float* smsg_scales, const float* v_frozen, float* p,
+                        ob_stream_t stream);
 
 #ifdef __cplusplus
 }

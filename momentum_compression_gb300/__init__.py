@@ -38,7 +38,7 @@ EXPORTS = (
     "ob_qb_sizes", "ob_zero_errors", "ob_compress_qb", "ob_server_reduce_qb", "ob_adam_step_qb",
     "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
     "ob_compress_signm_ls", "ob_server_reduce_db", "ob_lamb_step_signm", "ob_step_db",
-    "ob_noalloc_device_error",
+    "ob_noalloc_device_error", "ob_error_norm", "ob_plan_step", "ob_codec_step",
 )
 
 
@@ -55,7 +55,9 @@ class ob_config(ct.Structure):
                 ("b1", ct.c_float), ("b2", ct.c_float), ("eps", ct.c_float),
                 ("lr", ct.c_float), ("r_thr", ct.c_float), ("r_min", ct.c_float),
                 ("r_max", ct.c_float), ("c_min", ct.c_float), ("c_max", ct.c_float),
-                ("flags", ct.c_uint32), ("clip_value", ct.c_float)]
+                ("flags", ct.c_uint32), ("clip_value", ct.c_float),
+                ("reset_interval", ct.c_uint32), ("send_period", ct.c_uint32),
+                ("seed", ct.c_uint64)]
 
 
 class ob_layout(ct.Structure):
@@ -63,6 +65,11 @@ class ob_layout(ct.Structure):
                 ("chunk", ct.c_size_t), ("chunks_per_partition", ct.c_size_t),
                 ("n_chunks", ct.c_size_t), ("words_per_worker", ct.c_size_t),
                 ("n_tiles", ct.c_size_t), ("W", ct.c_int), ("n_layers", ct.c_int)]
+
+
+class ob_plan(ct.Structure):
+    _fields_ = [("reset", ct.c_int), ("send", ct.c_int), ("key", ct.c_uint64),
+                ("step", ct.c_uint64)]
 
 
 class ob_layer_state(ct.Structure):
@@ -103,6 +110,9 @@ def lib():
         L.ob_quant_int8.argtypes = [vp, sz, vp, vp, u64, u64, vp, vp]
         L.ob_compress_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.ob_noalloc_device_error.argtypes = [ct.POINTER(ct.c_uint), vp]
+        L.ob_error_norm.argtypes = [vp] * 9
+        L.ob_plan_step.argtypes = [vp, i32, u64, ct.POINTER(ob_plan)]
+        L.ob_codec_step.argtypes = [vp, i32, u64] + [vp] * 11
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
         L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
@@ -185,12 +195,15 @@ def _ls(ls):
 
 def ob_init(n, W, chunk, align=4096, grad_dtype=OB_GRAD_F32, layer_offsets=None,
             b1=0.9, b2=0.999, eps=1e-8, lr=1e-4, r_thr=0.1, r_min=0.5, r_max=4.0,
-            c_min=0.01, c_max=10.0, flags=0, clip_value=0.0):
+            c_min=0.01, c_max=10.0, flags=0, clip_value=0.0, reset_interval=0, send_period=0,
+            seed=0):
     """Returns an opaque ctx handle (int).  layer_offsets: sequence of
-    n_layers+1 ints, or None for one layer."""
+    n_layers+1 ints, or None for one layer.  reset_interval, send_period and
+    seed configure the schedules of ob_plan_step."""
     cfg = ob_config(n=n, W=W, chunk=chunk, align=align, grad_dtype=grad_dtype,
                     b1=b1, b2=b2, eps=eps, lr=lr, r_thr=r_thr, r_min=r_min, r_max=r_max,
-                    c_min=c_min, c_max=c_max, flags=flags, clip_value=clip_value)
+                    c_min=c_min, c_max=c_max, flags=flags, clip_value=clip_value,
+                    reset_interval=reset_interval, send_period=send_period, seed=seed)
     keep = None
     if layer_offsets is not None:
         keep = (ct.c_size_t * len(layer_offsets))(*[int(x) for x in layer_offsets])
@@ -357,6 +370,31 @@ def ob_reset_errors(ctx, err, bits, scales, err_s, sbits, sscales, stream=None):
                                  _ptr(sbits), _ptr(sscales), _stream(stream)), ctx)
 
 
+def ob_error_norm(ctx, err, bits, scales, err_s, sbits, sscales, out, stream=None):
+    """Per chunk, the sums of squares of every worker's and the server's
+    true error (the 1-bit error monitor): out has (W+1)*n_chunks floats."""
+    _check(lib().ob_error_norm(ctx, _ptr_array(err), _ptr(bits), _ptr(scales), _ptr(err_s),
+                               _ptr(sbits), _ptr(sscales), _ptr(out), _stream(stream)), ctx)
+
+
+def ob_plan_step(ctx, bits, t):
+    """The schedule of compressed step t (from 1) for a group of width bits:
+    a dict with reset, send, key and step (host only)."""
+    pl = ob_plan()
+    _check(lib().ob_plan_step(ctx, bits, t, ct.byref(pl)), ctx)
+    return {"reset": bool(pl.reset), "send": bool(pl.send), "key": pl.key, "step": pl.step}
+
+
+def ob_codec_step(ctx, bits, t, grads, m, err, msg, msg_scales, err_s, smsg, smsg_scales,
+                  v_frozen, p, stream=None):
+    """One compressed step of a codec group (bits 2, 4, 8 or 16) at
+    compressed step t, with the schedule of ob_plan_step applied inside."""
+    _check(lib().ob_codec_step(ctx, bits, t, _ptr_array(grads), _ptr(m), _ptr_array(err),
+                               _ptr(msg), _ptr(msg_scales), _ptr(err_s), _ptr(smsg),
+                               _ptr(smsg_scales), _ptr(v_frozen), _ptr(p), _stream(stream)),
+           ctx)
+
+
 def ob_device_error(ctx, stream=None):
     """Reads and clears the device error word (0 = none)."""
     v = ct.c_uint()
@@ -462,7 +500,7 @@ class OneBitOptimizer:
         self.grad_dtype = grad_dtype
         self.ctx = ob_init(n, W, chunk, align,
                            OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32,
-                           layer_offsets, **hp)
+                           layer_offsets, reset_interval=reset_interval, **hp)
         lay = ob_get_layout(self.ctx)
         self.layout = lay
         self.n, self.W, self.n_pad = n, W, lay["n_pad"]
@@ -519,7 +557,7 @@ class OneBitOptimizer:
                         self.sscales, stream)
 
     def compressed_step(self, grads, stream=None):
-        if self.reset_interval and self.cstep and self.cstep % self.reset_interval == 0:
+        if self.reset_interval and ob_plan_step(self.ctx, 1, self.cstep + 1)["reset"]:
             self.reset_errors(stream)
         self.cstep += 1
         if self.double_buffered and self.m_in_signs:
@@ -570,6 +608,18 @@ class OneBitOptimizer:
                     self.sbits, self.sscales, self.v, self.v_fresh, self.p,
                     self.ls if self.lamb else None)
         return _StepGraph(self, graph)
+
+    def error_norm(self, out=None, stream=None):
+        """The 1-bit error monitor: a (W+1, n_chunks) float32 tensor whose
+        row w (and row W, the server's) holds, per chunk, the sum of the
+        squared true errors after the last step."""
+        import torch
+        if out is None:
+            out = torch.empty((self.W + 1, self.layout["n_chunks"]), dtype=torch.float32,
+                              device=self.m.device)
+        ob_error_norm(self.ctx, self.err, self.bits, self.scales, self.err_s, self.sbits,
+                      self.sscales, out, stream)
+        return out
 
     def materialize_m(self, stream=None):
         """Writes the dense momentum (it is exact: sscale*sign)."""
@@ -642,7 +692,8 @@ class CodecGroup:
         self.reset_interval = reset_interval
         self.grad_dtype = grad_dtype
         self.ctx = ob_init(n, W, align, align,
-                           OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32, None, **hp)
+                           OB_GRAD_BF16 if grad_dtype == "bf16" else OB_GRAD_F32, None,
+                           reset_interval=reset_interval, send_period=period, seed=seed, **hp)
         lay = ob_get_layout(self.ctx)
         self.layout = lay
         self.n, self.W, self.n_pad = n, W, lay["n_pad"]
@@ -688,23 +739,20 @@ class CodecGroup:
         ob_zero_errors(self.ctx, self.err, self.err_s, stream)
         self.t = 0
 
+    @property
+    def key(self):
+        """The Philox key the library uses for this group (seed + bits)."""
+        return ob_plan_step(self.ctx, self.bits, 1)["key"]
+
     def compressed_step(self, grads, stream=None):
-        if self.reset_interval and self.t and self.t % self.reset_interval == 0:
-            ob_zero_errors(self.ctx, self.err, self.err_s, stream)
         self.t += 1
         if self.bits == 16:
-            send = self.t % self.period == 0
-            ob_compress_f16(self.ctx, send, grads, self.m, self.err, self.h, stream)
-            if send:
-                ob_server_reduce_f16(self.ctx, self.h, self.err_s, self.hs, stream)
-            ob_adam_step_f16(self.ctx, send, self.hs, self.v, self.m, self.p, stream)
-            return
-        b = self.bits
-        ob_compress_qb(self.ctx, b, grads, self.m, self.err, self.codes, self.bscales,
-                       self.seed, self.t, stream)
-        ob_server_reduce_qb(self.ctx, b, self.codes, self.bscales, self.err_s, self.scodes,
-                            self.sbscales, self.seed, self.t, stream)
-        ob_adam_step_qb(self.ctx, b, self.scodes, self.sbscales, self.v, self.m, self.p, stream)
+            ob_codec_step(self.ctx, 16, self.t, grads, self.m, self.err, self.h, None,
+                          self.err_s, self.hs, None, self.v, self.p, stream)
+        else:
+            ob_codec_step(self.ctx, self.bits, self.t, grads, self.m, self.err, self.codes,
+                          self.bscales, self.err_s, self.scodes, self.sbscales, self.v, self.p,
+                          stream)
 
 
 class MixedOptimizer:
@@ -713,8 +761,9 @@ class MixedOptimizer:
     and dense layers, 2 for convolution weights, FP16 every 10th step for
     normalisation parameters).  `groups` is a list of (bits, n,
     layer_offsets); width 1 runs the scaled-sign 1-bit Adam
-    (OneBitOptimizer), the others a CodecGroup whose uniforms use the key
-    seed + bits.  Steps run the groups in list order."""
+    (OneBitOptimizer), the others a CodecGroup configured with `seed` (the
+    library keys each width's uniforms by seed + bits).  Steps run the
+    groups in list order."""
 
     def __init__(self, groups, W, chunk=1 << 20, align=4096, grad_dtype="f32", device="cuda",
                  period=10, seed=1234, sign_momentum=False, reset_interval=0, **hp):
@@ -725,7 +774,7 @@ class MixedOptimizer:
                                     sign_momentum=sign_momentum,
                                     reset_interval=reset_interval, **hp)
             else:
-                g = CodecGroup(n, W, bits, align, grad_dtype, device, period, seed + bits,
+                g = CodecGroup(n, W, bits, align, grad_dtype, device, period, seed,
                                reset_interval, **hp)
             self.groups.append((bits, g))
 

@@ -6,12 +6,14 @@
 // cross-CTA fences and counters.
 //
 // One warp per (row, chunk) sequence; rows are workers (compress) or the
-// single server row.
+// single server row.  The same ordered sum without the division finishes
+// the error monitor's per-chunk sums of squares (k_monitor.cu).
 #include "ob_internal.cuh"
 
 namespace ob {
 namespace {
 
+template <bool MEAN>
 __global__ void __launch_bounds__(kThreads)
     k_finalize_scales(const Geo G, const float* __restrict__ part, uint32_t rows,
                       float* __restrict__ scales) {
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t cstart = (uint64_t)j * G.P + (uint64_t)kc * G.C;
     const uint64_t real = G.n > cstart ? (G.n - cstart < clen ? G.n - cstart : clen) : 0;
     const float sum = ordered_sum(part + (uint64_t)q * G.tpc, ntc, lane);
-    if (lane == 0) scales[q] = mean_of(sum, real);
+    if (lane == 0) scales[q] = MEAN ? mean_of(sum, real) : sum;
   }
 }
 
@@ -37,8 +39,16 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
                                    float* scales, int sms, cudaStream_t s) {
   const uint64_t ctas = ((uint64_t)rows * G.nc + kThreads / 32 - 1) / (kThreads / 32);
-  k_finalize_scales<<<grid_for(k_finalize_scales, sms, ctas), kThreads, 0, s>>>(G, part, rows,
-                                                                               scales);
+  k_finalize_scales<true><<<grid_for(k_finalize_scales<true>, sms, ctas), kThreads, 0, s>>>(
+      G, part, rows, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_sums(const Geo& G, const float* part, uint32_t rows, float* sums,
+                                 int sms, cudaStream_t s) {
+  const uint64_t ctas = ((uint64_t)rows * G.nc + kThreads / 32 - 1) / (kThreads / 32);
+  k_finalize_scales<false><<<grid_for(k_finalize_scales<false>, sms, ctas), kThreads, 0, s>>>(
+      G, part, rows, sums);
   return cudaGetLastError();
 }
 

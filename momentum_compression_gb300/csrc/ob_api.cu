@@ -140,10 +140,12 @@ ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg) {
 extern "C" {
 
 const char* ob_last_error(const ob_ctx* ctx) {
+  OB_TRACE();
   return ctx ? ctx->err.c_str() : g_err.c_str();
 }
 
 ob_status ob_init(const ob_config* cfg, ob_ctx** out) {
+  OB_TRACE();
   if (!cfg || !out) return fail(nullptr, OB_ERR_INVALID, "cfg or out is NULL");
   *out = nullptr;
   const ob_config& c = *cfg;
@@ -254,23 +256,27 @@ ob_status ob_init(const ob_config* cfg, ob_ctx** out) {
 }
 
 ob_status ob_destroy(ob_ctx* ctx) {
+  OB_TRACE();
   delete ctx;
   return OB_OK;
 }
 
 ob_status ob_get_layout(const ob_ctx* ctx, ob_layout* out) {
+  OB_TRACE();
   if (!ctx || !out) return fail(nullptr, OB_ERR_INVALID, "ctx or out is NULL");
   *out = ctx->lay;
   return OB_OK;
 }
 
 ob_status ob_workspace_bytes(const ob_ctx* ctx, size_t* bytes) {
+  OB_TRACE();
   if (!ctx || !bytes) return fail(nullptr, OB_ERR_INVALID, "ctx or bytes is NULL");
   *bytes = regions_of(ctx->geo).total;
   return OB_OK;
 }
 
 ob_status ob_set_workspace(ob_ctx* ctx, void* workspace, size_t bytes, ob_stream_t stream) {
+  OB_TRACE();
   if (!ctx) return fail(nullptr, OB_ERR_INVALID, "ctx is NULL");
   const Regions r = regions_of(ctx->geo);
   if (!workspace) return fail(ctx, OB_ERR_INVALID, "workspace is NULL");
@@ -313,6 +319,7 @@ ob_status ob_set_workspace(ob_ctx* ctx, void* workspace, size_t bytes, ob_stream
 
 ob_status ob_warmup_step(ob_ctx* ctx, const void* const* grads, float* m, float* v, float* p,
                          int mode, const ob_layer_state* ls, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if (mode != OB_MODE_ADAM && mode != OB_MODE_LAMB)
@@ -351,6 +358,7 @@ ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s, uin
                                float* scales, uint32_t* sbits, float* sscales, const float* m,
                                const float* v, float* v_fresh, const ob_layer_state* ls,
                                int warmup_steps, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_errs(ctx, err))) return st;
@@ -391,6 +399,7 @@ ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s, uin
 ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, float* const* err,
                       uint32_t* bits, float* scales, const ob_layer_state* ls,
                       ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_grads(ctx, grads)) || (st = check_errs(ctx, err))) return st;
@@ -478,6 +487,7 @@ static ob_status server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* s
 ob_status ob_server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* scales, float* err_s,
                            uint32_t* sbits, float* sscales, const ob_layer_state* ls,
                            ob_stream_t stream) {
+  OB_TRACE();
   return server_reduce(ctx, bits, scales, err_s, sbits, sscales, sbits, sscales, ls, stream);
 }
 
@@ -485,6 +495,7 @@ ob_status ob_server_reduce_db(ob_ctx* ctx, const uint32_t* bits, const float* sc
                               float* err_s, const uint32_t* sbits_old, const float* sscales_old,
                               uint32_t* sbits, float* sscales, const ob_layer_state* ls,
                               ob_stream_t stream) {
+  OB_TRACE();
   return server_reduce(ctx, bits, scales, err_s, sbits_old, sscales_old, sbits, sscales, ls,
                        stream);
 }
@@ -510,6 +521,7 @@ static void fill_update(const ob_ctx* ctx, ob::UpdateArgs& a) {
 
 ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                         const ob_layer_state* ls, float* out, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   OB_CHECK_PTR(ctx, sbits, 16, "sbits");
@@ -530,6 +542,7 @@ ob_status ob_decompress(ob_ctx* ctx, const uint32_t* sbits, const float* sscales
 
 ob_status ob_adam_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                        const float* v_frozen, float* m, float* p, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   OB_CHECK_PTR(ctx, sbits, 16, "sbits");
@@ -591,6 +604,7 @@ static ob_status lamb_step(ob_ctx* ctx, const uint32_t* sbits_prev, const float*
 ob_status ob_lamb_step(ob_ctx* ctx, const uint32_t* sbits, const float* sscales,
                        const float* v_frozen, float* v_fresh, float* m, float* p,
                        const ob_layer_state* ls, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   OB_CHECK_PTR(ctx, m, 16, "m");
@@ -601,6 +615,7 @@ ob_status ob_lamb_step_signm(ob_ctx* ctx, const uint32_t* sbits_prev, const floa
                              const uint32_t* sbits, const float* sscales, const float* v_frozen,
                              float* v_fresh, float* p, const ob_layer_state* ls,
                              ob_stream_t stream) {
+  OB_TRACE();
   return lamb_step(ctx, sbits_prev, sscales_prev, sbits, sscales, v_frozen, v_fresh, nullptr, p,
                    ls, stream);
 }
@@ -608,6 +623,7 @@ ob_status ob_lamb_step_signm(ob_ctx* ctx, const uint32_t* sbits_prev, const floa
 ob_status ob_compress_signm_ls(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
                                const float* sscales, float* const* err, uint32_t* bits,
                                float* scales, const ob_layer_state* ls, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_grads(ctx, grads)) || (st = check_errs(ctx, err))) return st;
@@ -651,6 +667,7 @@ ob_status ob_compress_signm_ls(ob_ctx* ctx, const void* const* grads, const uint
 ob_status ob_compress_signm(ob_ctx* ctx, const void* const* grads, const uint32_t* sbits,
                             const float* sscales, float* const* err, uint32_t* bits,
                             float* scales, ob_stream_t stream) {
+  OB_TRACE();
   return ob_compress_signm_ls(ctx, grads, sbits, sscales, err, bits, scales, nullptr, stream);
 }
 
@@ -658,6 +675,7 @@ ob_status ob_step(ob_ctx* ctx, const void* const* grads, float* m, float* const*
                   uint32_t* bits, float* scales, float* err_s, uint32_t* sbits, float* sscales,
                   const float* v_frozen, float* v_fresh, float* p, const ob_layer_state* ls,
                   ob_stream_t stream) {
+  OB_TRACE();
   ob_status st;
   if (!m && !ls) {
     // 1-bit Adam with the momentum held in its sign form
@@ -678,6 +696,7 @@ ob_status ob_step_db(ob_ctx* ctx, const void* const* grads, float* const* err, u
                      const float* sscales_prev, uint32_t* sbits, float* sscales,
                      const float* v_frozen, float* v_fresh, float* p, const ob_layer_state* ls,
                      ob_stream_t stream) {
+  OB_TRACE();
   ob_status st;
   if ((st = ob_compress_signm_ls(ctx, grads, sbits_prev, sscales_prev, err, bits, scales, ls,
                                  stream)))
@@ -693,6 +712,7 @@ ob_status ob_step_db(ob_ctx* ctx, const void* const* grads, float* const* err, u
 ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
                                 float* scales, float* err_s, const uint32_t* sbits,
                                 float* sscales, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_errs(ctx, err))) return st;
@@ -720,6 +740,7 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* 
 ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
                           const float* scales, float* err_s, const uint32_t* sbits,
                           const float* sscales, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if ((st = check_errs(ctx, err))) return st;
@@ -742,7 +763,42 @@ ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
                   "reset_errors");
 }
 
+ob_status ob_error_norm(ob_ctx* ctx, const float* const* err, const uint32_t* bits,
+                        const float* scales, const float* err_s, const uint32_t* sbits,
+                        const float* sscales, float* out, ob_stream_t stream) {
+  OB_TRACE();
+  ob_status st = ready(ctx);
+  if (st) return st;
+  if ((st = check_errs(ctx, const_cast<float* const*>(err)))) return st;
+  OB_CHECK_PTR(ctx, bits, 16, "bits");
+  OB_CHECK_PTR(ctx, scales, 4, "scales");
+  OB_CHECK_PTR(ctx, err_s, 16, "err_s");
+  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
+  OB_CHECK_PTR(ctx, sscales, 4, "sscales");
+  OB_CHECK_PTR(ctx, out, 4, "out");
+  const Geo& G = ctx->geo;
+  ob::MaterializeArgs a{};
+  a.geo = G;
+  for (uint32_t w = 0; w < G.W; ++w) a.e[w] = const_cast<float*>(err[w]);
+  a.bits = bits;
+  a.scales = scales;
+  a.e_s = const_cast<float*>(err_s);
+  a.sbits = sbits;
+  a.sscales = sscales;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launched(ctx, ob::launch_error_norm(a, ctx->ws, ctx->sms, s), "error_norm")))
+    return st;
+  if ((st = launched(ctx, ob::launch_finalize_sums(G, ctx->ws.wpart, G.W, out, ctx->sms, s),
+                     "error_norm: worker sums")))
+    return st;
+  return launched(ctx,
+                  ob::launch_finalize_sums(G, ctx->ws.spart, 1, out + (size_t)G.W * G.nc,
+                                           ctx->sms, s),
+                  "error_norm: server sums");
+}
+
 ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
   if (!code) return fail(ctx, OB_ERR_INVALID, "code is NULL");
@@ -758,6 +814,7 @@ ob_status ob_device_error(ob_ctx* ctx, unsigned* code, ob_stream_t stream) {
 
 ob_status ob_quant_int8(const float* g, size_t n, int8_t* q, float* block_scales, uint64_t seed,
                         uint64_t step, float* deq, ob_stream_t stream) {
+  OB_TRACE();
   if (n < 1 || n >= (1ull << 34))
     return fail(nullptr, OB_ERR_INVALID, "n = %zu must be in [1, 2^34)", n);
   OB_CHECK_PTR(nullptr, g, 16, "g");
@@ -777,6 +834,7 @@ ob_status ob_quant_int8(const float* g, size_t n, int8_t* q, float* block_scales
 ob_status ob_quant_int8_ef(const float* g, float* e, size_t n, int8_t* q, float* block_scales,
                            uint64_t seed, uint64_t step, float* deq, float* block_err2,
                            ob_stream_t stream) {
+  OB_TRACE();
   if (n < 1 || n >= (1ull << 34))
     return fail(nullptr, OB_ERR_INVALID, "n = %zu must be in [1, 2^34)", n);
   OB_CHECK_PTR(nullptr, g, 16, "g");

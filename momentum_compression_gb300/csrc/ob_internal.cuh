@@ -9,6 +9,7 @@
 #include <cstdint>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "ob.h"
 
@@ -346,6 +347,18 @@ struct F16Args {
 // the cudaError_t of its launch.
 // ---------------------------------------------------------------------------
 
+// One NVTX range, named after the C entry point, for the duration of each
+// ob_* call, so that the library's calls show up by name on a profiler's
+// timeline next to the caller's own work.  Without a tool attached an NVTX
+// call costs one indirect call.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+#define OB_TRACE() ::ob::TraceRange ob_trace_range_(__func__)
+
 // Views of a ctx (defined with the C entry points).
 const Geo* ctx_geo(const ob_ctx* ctx);
 const ob_config* ctx_config(const ob_ctx* ctx);
@@ -389,6 +402,10 @@ cudaError_t launch_compress_signm(const CompressArgs& a, bool bf16, bool lamb, i
 cudaError_t launch_server(const ServerArgs& a, bool lamb, int sms, cudaStream_t s);
 cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t rows,
                                    float* scales, int sms, cudaStream_t s);
+cudaError_t launch_finalize_sums(const Geo& G, const float* part, uint32_t rows, float* sums,
+                                 int sms, cudaStream_t s);
+cudaError_t launch_error_norm(const MaterializeArgs& a, const Workspace& ws, int sms,
+                              cudaStream_t s);
 cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_lamb_pass_a(const UpdateArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_lamb_pass_b(const UpdateArgs& a, int sms, cudaStream_t s);

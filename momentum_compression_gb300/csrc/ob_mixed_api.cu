@@ -71,6 +71,7 @@ extern "C" {
 
 ob_status ob_qb_sizes(const ob_ctx* ctx, int bits, size_t* words_per_worker,
                       size_t* n_blocks) {
+  OB_TRACE();
   ob_status st = check_ctx(const_cast<ob_ctx*>(ctx), bits);
   if (st) return st;
   if (bits == 0) return failf(const_cast<ob_ctx*>(ctx), OB_ERR_INVALID, "bits = 0");
@@ -81,6 +82,7 @@ ob_status ob_qb_sizes(const ob_ctx* ctx, int bits, size_t* words_per_worker,
 }
 
 ob_status ob_zero_errors(ob_ctx* ctx, float* const* err, float* err_s, ob_stream_t stream) {
+  OB_TRACE();
   if (!ctx) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "ctx is NULL");
   const ob::Geo& G = *ob::ctx_geo(ctx);
   if (!err) return failf(ctx, OB_ERR_INVALID, "err is NULL");
@@ -97,6 +99,7 @@ ob_status ob_zero_errors(ob_ctx* ctx, float* const* err, float* err_s, ob_stream
 ob_status ob_compress_qb(ob_ctx* ctx, int bits, const void* const* grads, const float* m,
                          float* const* err, uint32_t* codes, float* bscales, uint64_t seed,
                          uint64_t step, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, bits);
   if (st) return st;
   if (bits == 0) return failf(ctx, OB_ERR_INVALID, "bits = 0");
@@ -134,6 +137,7 @@ ob_status ob_server_reduce_qb(ob_ctx* ctx, int bits, const uint32_t* codes,
                               const float* bscales, float* err_s, uint32_t* scodes,
                               float* sbscales, uint64_t seed, uint64_t step,
                               ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, bits);
   if (st) return st;
   if (bits == 0) return failf(ctx, OB_ERR_INVALID, "bits = 0");
@@ -164,6 +168,7 @@ ob_status ob_server_reduce_qb(ob_ctx* ctx, int bits, const uint32_t* codes,
 
 ob_status ob_adam_step_qb(ob_ctx* ctx, int bits, const uint32_t* scodes, const float* sbscales,
                           const float* v_frozen, float* m, float* p, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, bits);
   if (st) return st;
   if (bits == 0) return failf(ctx, OB_ERR_INVALID, "bits = 0");
@@ -192,6 +197,7 @@ ob_status ob_adam_step_qb(ob_ctx* ctx, int bits, const uint32_t* scodes, const f
 
 ob_status ob_compress_f16(ob_ctx* ctx, int send, const void* const* grads, const float* m,
                           float* const* err, uint16_t* h, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, 0);
   if (st) return st;
   if ((st = check_workers(ctx, grads, err))) return st;
@@ -222,6 +228,7 @@ ob_status ob_compress_f16(ob_ctx* ctx, int send, const void* const* grads, const
 
 ob_status ob_server_reduce_f16(ob_ctx* ctx, const uint16_t* h, float* err_s, uint16_t* hs,
                                ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, 0);
   if (st) return st;
   OB_MIX_PTR(ctx, h, 16, "h");
@@ -244,6 +251,7 @@ ob_status ob_server_reduce_f16(ob_ctx* ctx, const uint16_t* h, float* err_s, uin
 
 ob_status ob_adam_step_f16(ob_ctx* ctx, int send, const uint16_t* hs, const float* v_frozen,
                            float* m, float* p, ob_stream_t stream) {
+  OB_TRACE();
   ob_status st = check_ctx(ctx, 0);
   if (st) return st;
   OB_MIX_PTR(ctx, m, 16, "m");
@@ -269,6 +277,56 @@ ob_status ob_adam_step_f16(ob_ctx* ctx, int send, const uint16_t* hs, const floa
   a.eps = c.eps;
   return launched(ctx, ob::launch_f16_adam(a, sms, reinterpret_cast<cudaStream_t>(stream)),
                   "adam_step_f16");
+}
+
+ob_status ob_plan_step(const ob_ctx* ctx, int bits, uint64_t t, ob_plan* out) {
+  OB_TRACE();
+  if (!ctx || !out) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "ctx or out is NULL");
+  ob_ctx* c = const_cast<ob_ctx*>(ctx);
+  if (bits != 1 && bits != 2 && bits != 4 && bits != 8 && bits != 16)
+    return failf(c, OB_ERR_INVALID, "bits = %d must be 1, 2, 4, 8 or 16", bits);
+  if (t < 1) return failf(c, OB_ERR_INVALID, "t = 0: compressed steps count from 1");
+  const ob_config& cfg = *ob::ctx_config(ctx);
+  ob_plan pl{};
+  // the periodic reset of the "1bit Adam" write-up, section 4.1
+  pl.reset = cfg.reset_interval > 0 && t > 1 && (t - 1) % cfg.reset_interval == 0;
+  // the FP16 group is exchanged every send_period-th step (section 3.2 table)
+  const uint64_t period = cfg.send_period > 1 ? cfg.send_period : 1;
+  pl.send = bits == 16 ? (t % period == 0) : 1;
+  // one Philox stream per width (section 6, layerwise_bits)
+  pl.key = (bits == 2 || bits == 4 || bits == 8) ? cfg.seed + (uint64_t)bits : 0;
+  pl.step = t;
+  *out = pl;
+  return OB_OK;
+}
+
+ob_status ob_codec_step(ob_ctx* ctx, int bits, uint64_t t, const void* const* grads, float* m,
+                        float* const* err, void* msg, float* msg_scales, float* err_s,
+                        void* smsg, float* smsg_scales, const float* v_frozen, float* p,
+                        ob_stream_t stream) {
+  OB_TRACE();
+  if (!ctx) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "ctx is NULL");
+  if (bits == 1) return failf(ctx, OB_ERR_INVALID, "bits = 1: use the 1-bit calls");
+  ob_plan pl;
+  ob_status st = ob_plan_step(ctx, bits, t, &pl);
+  if (st) return st;
+  if (pl.reset && (st = ob_zero_errors(ctx, err, err_s, stream))) return st;
+  if (bits == 16) {
+    uint16_t* h = static_cast<uint16_t*>(msg);
+    uint16_t* hs = static_cast<uint16_t*>(smsg);
+    if ((st = ob_compress_f16(ctx, pl.send, grads, m, err, h, stream))) return st;
+    if (pl.send && (st = ob_server_reduce_f16(ctx, h, err_s, hs, stream))) return st;
+    return ob_adam_step_f16(ctx, pl.send, hs, v_frozen, m, p, stream);
+  }
+  uint32_t* codes = static_cast<uint32_t*>(msg);
+  uint32_t* scodes = static_cast<uint32_t*>(smsg);
+  if ((st = ob_compress_qb(ctx, bits, grads, m, err, codes, msg_scales, pl.key, pl.step,
+                           stream)))
+    return st;
+  if ((st = ob_server_reduce_qb(ctx, bits, codes, msg_scales, err_s, scodes, smsg_scales,
+                                pl.key, pl.step, stream)))
+    return st;
+  return ob_adam_step_qb(ctx, bits, scodes, smsg_scales, v_frozen, m, p, stream);
 }
 
 }  // extern "C"

@@ -71,6 +71,7 @@ cudaError_t scratch_base(void** base, cudaStream_t s) {
 extern "C" ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads,
                                          const float* m, float* const* err, uint32_t* bits,
                                          float* scales, ob_stream_t stream) {
+  OB_TRACE();
   if (!ctx) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "ctx is NULL");
   const ob::Geo& G = *ob::ctx_geo(ctx);
   const ob_config& cfg = *ob::ctx_config(ctx);
@@ -127,6 +128,7 @@ extern "C" ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads,
 }
 
 extern "C" ob_status ob_noalloc_device_error(unsigned* code, ob_stream_t stream) {
+  OB_TRACE();
   if (!code) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "noalloc_device_error: code is NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* base = nullptr;

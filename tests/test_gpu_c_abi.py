@@ -4,7 +4,9 @@ functions bit for bit after every step.  c_abi_step.c: 2 warmup and 3
 compressed 1-bit Adam steps.  c_abi_lamb_signm.c: 2 warmup and 4
 compressed 1-bit LAMB steps over three layers, the last 3 with the
 momentum in sign form and the server output double-buffered
-(ob_step_db)."""
+(ob_step_db).  c_abi_mixed.c: a 1-bit, a 2-bit and an FP16 group over 7
+compressed steps, with the periodic reset, the FP16 send period and the
+per-width key taken from the library (ob_plan_step, ob_codec_step)."""
 import os
 import subprocess
 
@@ -16,7 +18,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.mark.parametrize("prog,ok", [("c_abi_step", "c abi ok"),
-                                     ("c_abi_lamb_signm", "c abi lamb ok")])
+                                     ("c_abi_lamb_signm", "c abi lamb ok"),
+                                     ("c_abi_mixed", "c abi mixed ok")])
 def test_c_program_drives_the_abi(tmp_path, prog, ok):
     from momentum_compression_gb300 import _build
     import oracle.build as obuild

@@ -73,7 +73,7 @@ class Group:
     def step(self, t, scale=1e-3):
         gh, gd = self.grads(scale)
         self.opt.compressed_step(gd)
-        O.codec_step(self.st, gh, self.hp, self.bits, t, self.seed, period=3)
+        O.codec_step(self.st, gh, self.hp, self.bits, t, self.seed + self.bits, period=3)
         torch.cuda.synchronize()
 
     def check(self, what):
@@ -148,7 +148,7 @@ def test_qb_nan_codes_zero_and_matches():
     gh[0][100] = np.nan
     gd[0][100] = float("nan")
     g.opt.compressed_step(gd)
-    O.codec_step(g.st, gh, g.hp, 2, 1, g.seed, period=3)
+    O.codec_step(g.st, gh, g.hp, 2, 1, g.seed + 2, period=3)
     torch.cuda.synchronize()
     codes = host(g.opt.codes).view(np.uint32)
     assert_bits_equal(codes, g.st.codes, "codes")
@@ -285,14 +285,14 @@ def test_resnet50_mixed_full_size():
         codes, scs = [], []
         for w in range(W):
             c, sc = O.qb_compress_worker(lay2, 2, d["g"][w], d["m"], d["e"][w], hp["b1"], w,
-                                         g2.seed, 1, k0=k0, length=256)
+                                         g2.key, 1, k0=k0, length=256)
             codes.append(c)
             scs.append(sc)
             assert_bits_equal(host(g2.codes[w, 16 * b: 16 * b + 16]).view(np.uint32), c,
                               f"block {b} codes of worker {w}")
             assert_bits_equal(host(g2.bscales[w, b: b + 1]), sc, f"block {b} scale {w}")
             assert_bits_equal(host(g2.err[w][s]), d["e"][w], f"block {b} e[{w}]")
-        sc_, ss_ = O.qb_server(lay2, 2, np.stack(codes), np.stack(scs), d["e_s"], g2.seed, 1,
+        sc_, ss_ = O.qb_server(lay2, 2, np.stack(codes), np.stack(scs), d["e_s"], g2.key, 1,
                                k0=k0, length=256)
         assert_bits_equal(host(g2.scodes[16 * b: 16 * b + 16]).view(np.uint32), sc_,
                           f"block {b} server codes")
@@ -303,7 +303,7 @@ def test_resnet50_mixed_full_size():
         assert_bits_equal(host(g2.m[s]), m, f"block {b} m")
         assert_bits_equal(host(g2.p[s]), p, f"block {b} p")
 
-    O.codec_step(st16, g16h, hp, 16, 10, g16.seed, period=synth.NORM_PERIOD)
+    O.codec_step(st16, g16h, hp, 16, 10, g16.key, period=synth.NORM_PERIOD)
     assert_bits_equal(host(g16.p), st16.p, "FP16 group p")
     assert_bits_equal(host(g16.m), st16.m, "FP16 group m")
     assert_bits_equal(host(g16.err_s), st16.e_s, "FP16 group e_s")

@@ -13,7 +13,8 @@ import torch
 import momentum_compression_gb300 as ob
 import oracle as O
 import synth
-from helpers import (assert_bits_equal, assert_close, bf16_tensor, dev, host)
+from helpers import (Guarded, assert_bits_equal, assert_close, assert_guards, bf16_tensor, dev,
+                     host)
 
 pytestmark = pytest.mark.gpu
 
@@ -88,17 +89,25 @@ def _materialize(c, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t):
 
 @pytest.mark.parametrize("case", CASES, ids=_ids)
 def test_compress_server_update_single_kernels(case):
+    """Each kernel of the step on the same inputs as the oracle, bit for
+    bit, with every buffer a call writes (and m, which it must not) in a
+    guarded allocation whose poisoned margins are checked after each call;
+    then the error monitor on the same deferred state."""
     c = Case(*case)
     lay = c.lay
     g_host, g_dev = c.grads()
     m = c.vec(1e-3)
     e = [c.vec(1e-4) for _ in range(c.W)]
     # --- worker compression
-    err_t = [dev(x) for x in e]  # deferred form with zero scales = true errors
-    bits_t = torch.zeros((c.W, c.words), dtype=torch.int32, device="cuda")
-    scales_t = torch.zeros((c.W, lay.nc), dtype=torch.float32, device="cuda")
-    m_t = dev(m)
+    err_g = [Guarded(lay.n_pad, torch.float32, x) for x in e]  # deferred form, zero scales
+    err_t = [x.t for x in err_g]
+    bits_g = Guarded((c.W, c.words), torch.int32, np.zeros((c.W, c.words), np.int32))
+    scales_g = Guarded((c.W, lay.nc), torch.float32, np.zeros((c.W, lay.nc), f32))
+    m_g = Guarded(lay.n_pad, torch.float32, m)
+    bits_t, scales_t, m_t = bits_g.t, scales_g.t, m_g.t
     ob.ob_compress(c.ctx, g_dev, m_t, err_t, bits_t, scales_t)
+    torch.cuda.synchronize()
+    assert_guards("compress", bits_g, scales_g, m_g, *err_g)
     bits_o = np.zeros((c.W, lay.words), np.uint32)
     scales_o = np.zeros((c.W, lay.nc), f32)
     e_o = [x.copy() for x in e]
@@ -112,32 +121,52 @@ def test_compress_server_update_single_kernels(case):
     assert_bits_equal(host(m_t), m, "m is read only")
     # --- server
     es = c.vec(1e-4)
-    es_t = dev(es)
-    sbits_t = torch.zeros(c.words, dtype=torch.int32, device="cuda")
-    sscales_t = torch.zeros(lay.nc, dtype=torch.float32, device="cuda")
+    es_g = Guarded(lay.n_pad, torch.float32, es)
+    sbits_g = Guarded(c.words, torch.int32, np.zeros(c.words, np.int32))
+    sscales_g = Guarded(lay.nc, torch.float32, np.zeros(lay.nc, f32))
+    es_t, sbits_t, sscales_t = es_g.t, sbits_g.t, sscales_g.t
     ob.ob_server_reduce(c.ctx, bits_t, scales_t, es_t, sbits_t, sscales_t)
+    torch.cuda.synchronize()
+    assert_guards("server", es_g, sbits_g, sscales_g, bits_g, scales_g)
     es_o = es.copy()
     sbits_o, sscales_o, y_o = O.server_reduce(lay, bits_o, scales_o, es_o)
     assert ob.ob_device_error(c.ctx) == 0
     assert_bits_equal(host(es_t), y_o, "server y")
     assert_bits_equal(host(sbits_t)[: lay.words], sbits_o, "server sign words")
     assert_bits_equal(host(sscales_t), sscales_o, "server scales")
+    # --- the error monitor on the deferred state: per chunk, the sums of
+    # the squared true errors of every worker and of the server
+    norm_g = Guarded((c.W + 1, lay.nc), torch.float32, np.full((c.W + 1, lay.nc), 5.0, f32))
+    ob.ob_error_norm(c.ctx, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t, norm_g.t)
+    torch.cuda.synchronize()
+    assert_guards("error_norm", norm_g)
+    got = host(norm_g.t)
+    for w in range(c.W):
+        assert_bits_equal(got[w], O.error_norm(lay, e_o[w]), f"error norm of worker {w}")
+    assert_bits_equal(got[c.W], O.error_norm(lay, es_o), "error norm of the server")
     # --- decompression and the Adam update
-    out_t = torch.full((lay.n_pad,), 7.0, device="cuda")
-    ob.ob_decompress(c.ctx, sbits_t, sscales_t, out_t)
-    assert_bits_equal(host(out_t), O.decompress(lay, sbits_o, sscales_o), "decompress")
+    out_g = Guarded(lay.n_pad, torch.float32, np.full(lay.n_pad, 7.0, f32))
+    ob.ob_decompress(c.ctx, sbits_t, sscales_t, out_g.t)
+    torch.cuda.synchronize()
+    assert_guards("decompress", out_g)
+    assert_bits_equal(host(out_g.t), O.decompress(lay, sbits_o, sscales_o), "decompress")
     v = np.abs(c.vec(1e-6)) + f32(1e-12)
     p = c.vec(0.02)
-    v_t, p_t = dev(v), dev(p)
-    m2_t = torch.full((lay.n_pad,), 3.0, device="cuda")
-    ob.ob_adam_step(c.ctx, sbits_t, sscales_t, v_t, m2_t, p_t)
+    v_t = dev(v)
+    p_g = Guarded(lay.n_pad, torch.float32, p)
+    m2_g = Guarded(lay.n_pad, torch.float32, np.full(lay.n_pad, 3.0, f32))
+    ob.ob_adam_step(c.ctx, sbits_t, sscales_t, v_t, m2_g.t, p_g.t)
+    torch.cuda.synchronize()
+    assert_guards("adam_step", p_g, m2_g)
     m_o = np.full(lay.n_pad, 3.0, f32)
     p_o = p.copy()
     O.adam_update(lay, sbits_o, sscales_o, v, 1e-8, 1e-4, m_o, p_o)
-    assert_bits_equal(host(m2_t), m_o, "m after update")
-    assert_bits_equal(host(p_t), p_o, "p after update")
+    assert_bits_equal(host(m2_g.t), m_o, "m after update")
+    assert_bits_equal(host(p_g.t), p_o, "p after update")
     # --- deferred errors made explicit
     _materialize(c, err_t, bits_t, scales_t, es_t, sbits_t, sscales_t)
+    torch.cuda.synchronize()
+    assert_guards("materialize", es_g, scales_g, sscales_g, *err_g)
     for w in range(c.W):
         assert_bits_equal(host(err_t[w]), e_o[w], f"e' of worker {w}")
     assert_bits_equal(host(es_t), es_o, "server e'")
@@ -202,6 +231,10 @@ def _run_adam(wl, warm, steps, check_every=False, sign_momentum=False, reset_int
 
 def _compare_state(opt, st, lay, exact=True):
     assert ob.ob_device_error(opt.ctx) == 0
+    norms = host(opt.error_norm())  # from the deferred state, before it is made explicit
+    for w in range(lay.W):
+        assert_bits_equal(norms[w], O.error_norm(lay, st.e[w]), f"error norm of worker {w}")
+    assert_bits_equal(norms[lay.W], O.error_norm(lay, st.e_s), "error norm of the server")
     opt.materialize_m()
     assert_bits_equal(host(opt.sbits)[: lay.words], st.sbits, "server sign words")
     assert_bits_equal(host(opt.sscales), st.sscales, "server scales")
@@ -417,17 +450,18 @@ def test_int8_parity(n):
         g[256:512] = 0.0  # an all-zero block
         g[700] = np.float32(5.0)  # a block dominated by one value
     nb = (n + 255) // 256
-    g_t = dev(g)
-    q_t = torch.zeros(n + 16, dtype=torch.int8, device="cuda")
-    s_t = torch.zeros(nb, dtype=torch.float32, device="cuda")
-    d_t = torch.zeros(n + 4, dtype=torch.float32, device="cuda")
+    g_g = Guarded(n, torch.float32, g)
+    q_g = Guarded(n, torch.int8, np.zeros(n, np.int8))
+    s_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
+    d_g = Guarded(n, torch.float32, np.zeros(n, f32))
     for step in (0, 1, 2 ** 33 + 5):
-        ob.ob_quant_int8(g_t, q_t, s_t, 1234, step, d_t, n=n)
+        ob.ob_quant_int8(g_g.t, q_g.t, s_g.t, 1234, step, d_g.t, n=n)
+        torch.cuda.synchronize()
+        assert_guards(f"quant_int8, step {step}", g_g, q_g, s_g, d_g)
         q_o, s_o, d_o = O.quant_int8(g, 256, 1234, step, deq=True)
-        assert np.array_equal(host(q_t)[:n], q_o), f"codes, step {step}"
-        assert_bits_equal(host(s_t), s_o, "block scales")
-        assert_bits_equal(host(d_t)[:n], d_o, "dequantised")
-    assert not host(q_t)[n:].any()
+        assert np.array_equal(host(q_g.t), q_o), f"codes, step {step}"
+        assert_bits_equal(host(s_g.t), s_o, "block scales")
+        assert_bits_equal(host(d_g.t), d_o, "dequantised")
 
 
 def test_int8_large_seed_and_no_deq():
@@ -519,21 +553,23 @@ def test_int8_error_feedback_parity(n):
     in a row (the residual carries over), against the oracle bit for bit."""
     rng = np.random.default_rng(n + 17)
     e_o = (rng.standard_normal(n) * 1e-5).astype(f32)
-    e_t = dev(e_o)
     nb = (n + 255) // 256
-    q_t = torch.zeros(n + 16, dtype=torch.int8, device="cuda")
-    s_t = torch.zeros(nb, device="cuda")
-    d_t = torch.zeros(n + 4, device="cuda")
-    e2_t = torch.zeros(nb, device="cuda")
+    e_g = Guarded(n, torch.float32, e_o)
+    q_g = Guarded(n, torch.int8, np.zeros(n, np.int8))
+    s_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
+    d_g = Guarded(n, torch.float32, np.zeros(n, f32))
+    e2_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
     for step in range(3):
         g = (rng.standard_normal(n) * 1e-3).astype(f32)
-        ob.ob_quant_int8_ef(dev(g), e_t, q_t, s_t, 77, step, d_t, e2_t, n=n)
+        ob.ob_quant_int8_ef(dev(g), e_g.t, q_g.t, s_g.t, 77, step, d_g.t, e2_g.t, n=n)
+        torch.cuda.synchronize()
+        assert_guards(f"quant_int8_ef, call {step}", e_g, q_g, s_g, d_g, e2_g)
         q_o, s_o, d_o, e2_o = O.quant_int8_ef(g, e_o, 77, step, deq=True, err2=True)
-        assert np.array_equal(host(q_t)[:n], q_o), f"codes, call {step}"
-        assert_bits_equal(host(s_t), s_o, "scales")
-        assert_bits_equal(host(d_t)[:n], d_o, "dequantised")
-        assert_bits_equal(host(e_t), e_o, "residual")
-        assert_bits_equal(host(e2_t), e2_o, "error monitor")
+        assert np.array_equal(host(q_g.t), q_o), f"codes, call {step}"
+        assert_bits_equal(host(s_g.t), s_o, "scales")
+        assert_bits_equal(host(d_g.t), d_o, "dequantised")
+        assert_bits_equal(host(e_g.t), e_o, "residual")
+        assert_bits_equal(host(e2_g.t), e2_o, "error monitor")
 
 
 # ---------------------------------------------------------------------------
