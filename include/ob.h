@@ -192,7 +192,8 @@ ob_status ob_warmup_step(ob_ctx* ctx, const void* const* grads, float* m,
                          const ob_layer_state* ls, ob_stream_t stream);
 
 /* End of warmup.  Zeroes err (W host-array pointers), err_s, bits, scales,
- * sbits, sscales (the deferred form of e = 0).  v becomes the frozen
+ * sbits, sscales (the deferred form of e = 0); all six may be NULL together
+ * (a rank of a multi-process job clears its own slices).  v becomes the frozen
  * variance v_Tw.  LAMB (ls != NULL): v_fresh = v; per layer
  *   rms_l = ||m_l||/sqrt(n_l); s_l = mean(rms)/rms_l (1 if rms_l = 0)
  *   c_avg = c_sum/warmup_steps; r_prev = 1; c_prev = c_prev2 = c_avg
@@ -433,6 +434,57 @@ typedef struct ob_plan {
   uint64_t key, step;
 } ob_plan;
 ob_status ob_plan_step(const ob_ctx* ctx, int bits, uint64_t t, ob_plan* out);
+
+/* ------------------------------------------------------------------------
+ * One rank of a multi-process job: one worker and one server per process
+ * ([LAMB] 2 and 4: the 3-phase compressed exchange -- local compression,
+ * an all-to-all of the compressed chunks, each server's average and
+ * re-compression, an all-gather of the result).  The collectives are the
+ * caller's (e.g. NCCL all-to-all and all-gather of the blocks below); these
+ * calls do the compute of rank j, on the same kernels as the resident
+ * path, with the same layout (ctx for n, W = the number of ranks, ...).
+ *
+ * Per step on rank j:
+ *   ob_compress_worker      own gradient -> bits_row [words_per_worker],
+ *                           scales_row [n_chunks]; partition i's block is
+ *                           words [i*P/32, (i+1)*P/32) and scales
+ *                           [i*cpp, (i+1)*cpp)
+ *   all-to-all              block i to rank i: recv_bits [W][P/32] and
+ *                           recv_scales [W][cpp], row w from rank w
+ *   ob_server_reduce_part   partition j -> sbits_part [P/32],
+ *                           sscales_part [cpp] (err_s_part [P] kept)
+ *   all-gather              in rank order: sbits [n_pad/32] and sscales
+ *                           [n_chunks], the whole server output
+ *   ob_adam_step / ob_lamb_step on the whole (replicated) m, v, p
+ * The rank's own bits_row/scales_row and sbits_part/sscales_part must be
+ * kept from one step to the next (the deferred errors decode with them),
+ * and are zeroed with err and err_s_part at the start of compression; for
+ * 1-bit LAMB, ob_begin_compression with all six error and sign buffers
+ * NULL does the rest.  The warmup steps average all W gradients
+ * (ob_warmup_step on a gathered set).  P must be a multiple of 128 (A a
+ * multiple of 128) for ob_server_reduce_part. */
+
+/* Rank compression of one worker: ob_compress for worker `rank`'s own
+ * buffers only.  grad, err: n_pad elements; bits_row: words_per_worker
+ * words; scales_row: n_chunks floats (both from the previous step on entry,
+ * for the deferred error).  The momentum is dense (m, msbits = msscales =
+ * NULL) or in its sign form (m = NULL, msbits/msscales the last step's
+ * gathered server output, as ob_compress_signm_ls).  ls: 1-bit LAMB. */
+ob_status ob_compress_worker(ob_ctx* ctx, const void* grad, const float* m,
+                             const uint32_t* msbits, const float* msscales, float* err,
+                             uint32_t* bits_row, float* scales_row, const ob_layer_state* ls,
+                             ob_stream_t stream);
+
+/* Rank server of partition j, from the W received blocks: recv_bits
+ * [W][P/32] words (row w from worker w), recv_scales [W][cpp];
+ * err_s_part [P] (deferred form), sbits_part [P/32] and sscales_part [cpp]
+ * are read as the previous step's output and overwritten with this
+ * step's.  The same arithmetic as ob_server_reduce on partition j.
+ * OB_ERR_UNSUPPORTED if P % 128 != 0. */
+ob_status ob_server_reduce_part(ob_ctx* ctx, int j, const uint32_t* recv_bits,
+                                const float* recv_scales, float* err_s_part,
+                                uint32_t* sbits_part, float* sscales_part,
+                                const ob_layer_state* ls, ob_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Layerwise mixed bit widths ([BLOG] 3.2 table: a bit width and an update

@@ -39,6 +39,7 @@ EXPORTS = (
     "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
     "ob_compress_signm_ls", "ob_server_reduce_db", "ob_lamb_step_signm", "ob_step_db",
     "ob_noalloc_device_error", "ob_error_norm", "ob_plan_step", "ob_codec_step",
+    "ob_compress_worker", "ob_server_reduce_part",
 )
 
 
@@ -113,6 +114,8 @@ def lib():
         L.ob_error_norm.argtypes = [vp] * 9
         L.ob_plan_step.argtypes = [vp, i32, u64, ct.POINTER(ob_plan)]
         L.ob_codec_step.argtypes = [vp, i32, u64] + [vp] * 11
+        L.ob_compress_worker.argtypes = [vp] * 10
+        L.ob_server_reduce_part.argtypes = [vp, i32] + [vp] * 7
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
         L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
@@ -254,7 +257,8 @@ def ob_warmup_step(ctx, grads, m, v, p, mode=OB_MODE_ADAM, ls=None, stream=None)
 def ob_begin_compression(ctx, err, err_s, bits, scales, sbits, sscales, m=None, v=None,
                          v_fresh=None, ls=None, warmup_steps=0, stream=None):
     """End of warmup: zeroes errors and sign buffers, freezes v; for LAMB sets sigma, c_avg and the coefficient history."""
-    _check(lib().ob_begin_compression(ctx, _ptr_array(err), _ptr(err_s), _ptr(bits),
+    _check(lib().ob_begin_compression(ctx, None if err is None else _ptr_array(err),
+                                      _ptr(err_s), _ptr(bits),
                                       _ptr(scales), _ptr(sbits), _ptr(sscales), _ptr(m),
                                       _ptr(v), _ptr(v_fresh), _ls(ls), warmup_steps,
                                       _stream(stream)), ctx)
@@ -393,6 +397,23 @@ def ob_codec_step(ctx, bits, t, grads, m, err, msg, msg_scales, err_s, smsg, sms
                                _ptr(msg), _ptr(msg_scales), _ptr(err_s), _ptr(smsg),
                                _ptr(smsg_scales), _ptr(v_frozen), _ptr(p), _stream(stream)),
            ctx)
+
+
+def ob_compress_worker(ctx, grad, err, bits_row, scales_row, m=None, msbits=None,
+                       msscales=None, ls=None, stream=None):
+    """One rank's compression of its own worker (dense m, or the momentum
+    in sign form from the gathered server output)."""
+    _check(lib().ob_compress_worker(ctx, _ptr(grad), _ptr(m), _ptr(msbits), _ptr(msscales),
+                                    _ptr(err), _ptr(bits_row), _ptr(scales_row), _ls(ls),
+                                    _stream(stream)), ctx)
+
+
+def ob_server_reduce_part(ctx, j, recv_bits, recv_scales, err_s_part, sbits_part,
+                          sscales_part, ls=None, stream=None):
+    """One rank's server: partition j from the W received blocks."""
+    _check(lib().ob_server_reduce_part(ctx, j, _ptr(recv_bits), _ptr(recv_scales),
+                                       _ptr(err_s_part), _ptr(sbits_part), _ptr(sscales_part),
+                                       _ls(ls), _stream(stream)), ctx)
 
 
 def ob_device_error(ctx, stream=None):

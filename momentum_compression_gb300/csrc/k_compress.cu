@@ -125,8 +125,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   // once measured faster there); a dense m would be re-read per group, and
   // 1-bit LAMB's per-tile layer setup measured slower repeated per group
   constexpr bool kGrouped = MSIGN && !LAMB;
-  const uint32_t gsz = kGrouped ? kGroup : G.W;
-  const uint32_t n_groups = kGrouped ? (G.W + kGroup - 1) / kGroup : 1u;
+  // NW workers are compressed: all W of the layout, or one (a rank's own)
+  const uint32_t NW = A.nw;
+  const uint32_t gsz = kGrouped ? kGroup : NW;
+  const uint32_t n_groups = kGrouped ? (NW + kGroup - 1) / kGroup : 1u;
   const uint32_t n_vt = G.n_tiles * n_groups;
 
   // ------------------------------------------------------------ producer
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     bool ok = true;
     for (uint32_t VT = blockIdx.x; ok && VT < n_vt; VT += gridDim.x, ++ti) {
       const uint32_t gi = kGrouped ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
-      const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < G.W ? wbeg + gsz : G.W;
+      const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < NW ? wbeg + gsz : NW;
       const Tile tl = decode_tile(G, T);
       if constexpr (!MSIGN) {
         if (ti >= 1) ok = mbar_wait(mempty, (ti - 1) & 1, err, kErrWaitEmpty);
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   if (blockIdx.x < n_vt) {
     const uint32_t gi = kGrouped ? blockIdx.x / G.n_tiles : 0u, T0 = blockIdx.x - gi * G.n_tiles;
     if constexpr (MSIGN) load_msign(T0);
-    const uint32_t wb = gi * gsz, nw = (wb + gsz < G.W ? wb + gsz : G.W) - wb;
+    const uint32_t wb = gi * gsz, nw = (wb + gsz < NW ? wb + gsz : NW) - wb;
     if ((uint32_t)p < nw)
       s_sc[0][p] = __ldcg(A.scales + (uint64_t)(wb + p) * G.nc + decode_tile(G, T0).g);
   }
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   uint32_t item = 0, ti = 0;
   for (uint32_t VT = blockIdx.x; VT < n_vt; VT += gridDim.x, ++ti) {
     const uint32_t gi = kGrouped ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
-    const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < G.W ? wbeg + gsz : G.W;
+    const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < NW ? wbeg + gsz : NW;
     const Tile tl = decode_tile(G, T);
     bool ok = true;
     // the next item group's worker scales, stored after this one's last barrier
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       const uint32_t gin = kGrouped ? VTn / G.n_tiles : 0u;
       Tn = VTn - gin * G.n_tiles;
       const uint32_t wbn = gin * gsz;
-      nwn = (wbn + gsz < G.W ? wbn + gsz : G.W) - wbn;
+      nwn = (wbn + gsz < NW ? wbn + gsz : NW) - wbn;
       if ((uint32_t)p < nwn)
         sc_next = __ldcg(A.scales + (uint64_t)(wbn + p) * G.nc + decode_tile(G, Tn).g);
     }

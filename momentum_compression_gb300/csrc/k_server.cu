@@ -116,11 +116,12 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     // 1-bit LAMB: the layer of the tile, loaded a tile before the loads
     // that depend on it
     [[maybe_unused]] uint32_t l_cur =
-        LAMB && blockIdx.x < G.n_tiles ? __ldg(A.ws.tile_layer + blockIdx.x) : 0u;
-    for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
+        LAMB && A.T0 + blockIdx.x < A.T1 ? __ldg(A.ws.tile_layer + A.T0 + blockIdx.x) : 0u;
+    for (uint32_t T = A.T0 + blockIdx.x; T < A.T1; T += gridDim.x, ++ti) {
       const Tile tl = decode_tile(G, T);
+      const uint64_t lstart = tl.start - A.base;  // the tile's index in this call's buffers
       // the header's loads go out before the wait for a free stage
-      const float osc = __ldcg(A.sscales_old + tl.g);
+      const float osc = __ldcg(A.sscales_old + (tl.g - A.g0));
       [[maybe_unused]] uint32_t l = 0;
       [[maybe_unused]] uint64_t lend = 0;
       [[maybe_unused]] float c2 = 1.0f, c1 = 1.0f;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           c2 = __ldg(A.c_prev2 + l);
           c1 = __ldg(A.c_prev + l);
         }
-        if (T + gridDim.x < G.n_tiles) l_cur = __ldg(A.ws.tile_layer + T + gridDim.x);
+        if (T + gridDim.x < A.T1) l_cur = __ldg(A.ws.tile_layer + T + gridDim.x);
       }
       const uint32_t s = ti % kSStages, r = ti / kSStages;
       if (r >= 1) ok = mbar_wait(&empty[s], (r - 1) & 1, err, kErrWaitEmpty);
@@ -139,8 +140,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         ok = false;
         break;
       }
-      const uint64_t w0 = (tl.start >> 5) & ~uint64_t(3);
-      const uint64_t w1 = ((tl.start + tl.len) / 32 + 3) & ~uint64_t(3);
+      const uint64_t w0 = (lstart >> 5) & ~uint64_t(3);
+      const uint64_t w1 = ((lstart + tl.len) / 32 + 3) & ~uint64_t(3);
       const uint32_t run = (uint32_t)(w1 - w0) * 4;
       unsigned char* st = stage0 + s * stage_bytes;
       TileHdr* hd = reinterpret_cast<TileHdr*>(st + hdr_off);
@@ -152,9 +153,9 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         hd->r = A.ratio_ef ? __fdiv_rn(c2, c1) : 1.0f;
       }
       mbar_arrive_expect_tx(&full[s], tl.len * 4 + (G.W + 1) * run);
-      bulk_g2s_stream(st, A.e_s + tl.start, tl.len * 4, &full[s], pol);
+      bulk_g2s_stream(st, A.e_s + lstart, tl.len * 4, &full[s], pol);
       for (uint32_t w = 0; w < G.W; ++w)
-        bulk_g2s(st + kTile * 4 + (size_t)w * kRunWords * 4, A.bits + (uint64_t)w * G.words + w0,
+        bulk_g2s(st + kTile * 4 + (size_t)w * kRunWords * 4, A.bits + w * A.bits_stride + w0,
                  run, &full[s]);
       // the previous server words of this tile (only this CTA rewrites
       // them, after this copy has landed; the rounding words read beyond
@@ -189,22 +190,24 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   // (ring of 3), so that the z table of tile t+1 can be built during tile
   // t from scales published by the barrier ending tile t-1; the tile
   // totals are double-buffered.
-  if (blockIdx.x + gridDim.x < G.n_tiles && (uint32_t)p < Wc)
-    s_sc[1][p] =
-        __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x + gridDim.x).g);
-  if (blockIdx.x < G.n_tiles && (uint32_t)p < Wc)
-    s_sc[0][p] = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, blockIdx.x).g);
+  // worker w's scale of chunk g
+  auto wscale = [&](uint32_t w, uint32_t g) {
+    return __ldcg(A.scales + (uint64_t)w * A.sc_stride + (g - A.g0));
+  };
+  if (A.T0 + blockIdx.x + gridDim.x < A.T1 && (uint32_t)p < Wc)
+    s_sc[1][p] = wscale(p, decode_tile(G, A.T0 + blockIdx.x + gridDim.x).g);
+  if (A.T0 + blockIdx.x < A.T1 && (uint32_t)p < Wc)
+    s_sc[0][p] = wscale(p, decode_tile(G, A.T0 + blockIdx.x).g);
   named_sync(1, kSConsumers);
   if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, inv_w, p);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
-  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x, ++ti) {
+  for (uint32_t T = A.T0 + blockIdx.x; T < A.T1; T += gridDim.x, ++ti) {
     const uint32_t s = ti % kSStages;
     // the worker scales of the tile after next
     float next_sc = 0.0f;
     const uint32_t Tn = T + gridDim.x, Tnn = Tn + gridDim.x;
-    if (Tnn < G.n_tiles && (uint32_t)p < Wc)
-      next_sc = __ldcg(A.scales + (uint64_t)p * G.nc + decode_tile(G, Tnn).g);
+    if (Tnn < A.T1 && (uint32_t)p < Wc) next_sc = wscale(p, decode_tile(G, Tnn).g);
     bool ok = s_abort == 0 && mbar_wait(&full[s], (ti / kSStages) & 1, err, kErrWaitFull);
     if (!ok) s_abort = 1;
     const unsigned char* st = stage0 + s * stage_bytes;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     for (int i = 0; i < 4; ++i) valid[i] = 1024u * i + 4u * p < tl.len;
     const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
     const uint32_t* sow = sbw + Wc * kRunWords;  // the server's previous words
-    const uint32_t wshift = (uint32_t)((tl.start >> 5) & 3);  // rounding of the runs
+    const uint32_t wshift = (uint32_t)(((tl.start - A.base) >> 5) & 3);  // rounding of the runs
     const float* sc = s_sc[ti % 3];
 
     const float* z8 = s_z8[ti & 1];
@@ -320,8 +323,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         }
         const uint32_t word = pack_word(nib, lane);
         if (FULL || valid[i]) {
-          __stcs(reinterpret_cast<float4*>(A.e_s + k0), yv);
-          if ((p & 7) == 0) A.sbits[k0 >> 5] = word;
+          __stcs(reinterpret_cast<float4*>(A.e_s + (k0 - A.base)), yv);
+          if ((p & 7) == 0) A.sbits[(k0 - A.base) >> 5] = word;
         }
       }
       return acc;
@@ -338,8 +341,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     }
     acc = warp_butterfly_sum(acc);
     if (lane == 0) ws[ti & 1][warp] = acc;
-    if (Tnn < G.n_tiles && (uint32_t)p < Wc) s_sc[(ti + 2) % 3][p] = next_sc;
-    if (Tn < G.n_tiles) {
+    if (Tnn < A.T1 && (uint32_t)p < Wc) s_sc[(ti + 2) % 3][p] = next_sc;
+    if (Tn < A.T1) {
       if ((uint32_t)p < (1u << W8))
         s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, inv_w, p);
     }
@@ -358,7 +361,7 @@ cudaError_t run_server(const ServerArgs& a, int sms, cudaStream_t s) {
                                 (int)ServerSmem::bytes(OB_MAX_WORKERS));
   });
   if (attr != cudaSuccess) return attr;
-  const int grid = grid_for(k_server<LAMB, WT>, sms, a.geo.n_tiles, kServerThreads, bytes);
+  const int grid = grid_for(k_server<LAMB, WT>, sms, a.T1 - a.T0, kServerThreads, bytes);
   k_server<LAMB, WT><<<grid, kServerThreads, bytes, s>>>(a);
   return cudaGetLastError();
 }

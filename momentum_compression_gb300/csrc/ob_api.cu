@@ -130,6 +130,8 @@ namespace ob {
 // Read-only views of a ctx and its error slot, for the other translation
 // units of the library.
 const Geo* ctx_geo(const ob_ctx* ctx) { return &ctx->geo; }
+const Workspace* ctx_ws(const ob_ctx* ctx) { return ctx->ws_base ? &ctx->ws : nullptr; }
+int ctx_sms(const ob_ctx* ctx) { return ctx->sms; }
 const ob_config* ctx_config(const ob_ctx* ctx) { return &ctx->cfg; }
 ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg) {
   return fail(ctx, st, "%s", msg);
@@ -361,23 +363,28 @@ ob_status ob_begin_compression(ob_ctx* ctx, float* const* err, float* err_s, uin
   OB_TRACE();
   ob_status st = ready(ctx);
   if (st) return st;
-  if ((st = check_errs(ctx, err))) return st;
-  OB_CHECK_PTR(ctx, err_s, 16, "err_s");
-  OB_CHECK_PTR(ctx, bits, 16, "bits");
-  OB_CHECK_PTR(ctx, scales, 4, "scales");
-  OB_CHECK_PTR(ctx, sbits, 16, "sbits");
-  OB_CHECK_PTR(ctx, sscales, 4, "sscales");
   const Geo& G = ctx->geo;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  for (uint32_t w = 0; w < G.W && e == cudaSuccess; ++w)
-    e = cudaMemsetAsync(err[w], 0, G.n_pad * sizeof(float), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(err_s, 0, G.n_pad * sizeof(float), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(bits, 0, (size_t)G.W * G.words * sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(scales, 0, (size_t)G.W * G.nc * sizeof(float), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(sbits, 0, (size_t)G.words * sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(sscales, 0, (size_t)G.nc * sizeof(float), s);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "begin_compression: clearing the errors");
+  // All six error and sign buffers NULL: a rank of a multi-process job
+  // clears its own slices; only the LAMB part below runs.
+  const bool none = !err && !err_s && !bits && !scales && !sbits && !sscales;
+  if (!none) {
+    if ((st = check_errs(ctx, err))) return st;
+    OB_CHECK_PTR(ctx, err_s, 16, "err_s");
+    OB_CHECK_PTR(ctx, bits, 16, "bits");
+    OB_CHECK_PTR(ctx, scales, 4, "scales");
+    OB_CHECK_PTR(ctx, sbits, 16, "sbits");
+    OB_CHECK_PTR(ctx, sscales, 4, "sscales");
+    for (uint32_t w = 0; w < G.W && e == cudaSuccess; ++w)
+      e = cudaMemsetAsync(err[w], 0, G.n_pad * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err_s, 0, G.n_pad * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(bits, 0, (size_t)G.W * G.words * sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scales, 0, (size_t)G.W * G.nc * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(sbits, 0, (size_t)G.words * sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(sscales, 0, (size_t)G.nc * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "begin_compression: clearing the errors");
+  }
   if (!ls) return OB_OK;
   if ((st = check_ls(ctx, ls, true))) return st;
   OB_CHECK_PTR(ctx, m, 16, "m");
@@ -410,6 +417,7 @@ ob_status ob_compress(ob_ctx* ctx, const void* const* grads, const float* m, flo
   ob::CompressArgs a{};
   a.geo = ctx->geo;
   a.ws = ctx->ws;
+  a.nw = ctx->geo.W;
   for (int w = 0; w < ctx->cfg.W; ++w) {
     a.g[w] = grads[w];
     a.e[w] = err[w];
@@ -465,6 +473,10 @@ static ob_status server_reduce(ob_ctx* ctx, const uint32_t* bits, const float* s
   ob::ServerArgs a{};
   a.geo = ctx->geo;
   a.ws = ctx->ws;
+  a.T0 = 0;
+  a.T1 = ctx->geo.n_tiles;
+  a.bits_stride = ctx->geo.words;
+  a.sc_stride = ctx->geo.nc;
   a.bits = bits;
   a.scales = scales;
   a.e_s = err_s;
@@ -635,6 +647,7 @@ ob_status ob_compress_signm_ls(ob_ctx* ctx, const void* const* grads, const uint
   ob::CompressArgs a{};
   a.geo = ctx->geo;
   a.ws = ctx->ws;
+  a.nw = ctx->geo.W;
   for (int w = 0; w < ctx->cfg.W; ++w) {
     a.g[w] = grads[w];
     a.e[w] = err[w];

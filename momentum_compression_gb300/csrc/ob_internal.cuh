@@ -223,6 +223,8 @@ __device__ __forceinline__ bool advance_layer(const uint64_t* off, uint32_t L,
 struct CompressArgs {
   Geo geo;
   Workspace ws;
+  uint32_t nw;             // workers compressed by this call: geo.W, or 1 for one
+                           // rank's own worker (its buffers are g[0], e[0], row 0)
   const void* g[OB_MAX_WORKERS];
   float* e[OB_MAX_WORKERS];
   const float* m;          // dense momentum, or null: then m = msscale*sign(msbits)
@@ -241,6 +243,14 @@ struct CompressArgs {
 struct ServerArgs {
   Geo geo;
   Workspace ws;
+  // The tiles [T0, T1) this call reduces: every tile, or one partition's
+  // (one rank's server).  Index 0 of e_s, sbits and sbits_old is element
+  // `base`, index 0 of sscales and sscales_old is chunk g0; the workers'
+  // rows of bits are bits_stride words apart, those of scales sc_stride
+  // floats apart.  The whole buffer: T0 = 0, T1 = n_tiles, base = g0 = 0,
+  // strides words and nc.
+  uint32_t T0, T1, g0, sc_stride;
+  uint64_t base, bits_stride;
   const uint32_t* bits;
   const float* scales;
   float* e_s;
@@ -361,6 +371,8 @@ struct TraceRange {
 
 // Views of a ctx (defined with the C entry points).
 const Geo* ctx_geo(const ob_ctx* ctx);
+const Workspace* ctx_ws(const ob_ctx* ctx);  // null before ob_set_workspace
+int ctx_sms(const ob_ctx* ctx);
 const ob_config* ctx_config(const ob_ctx* ctx);
 ob_status ctx_fail(ob_ctx* ctx, ob_status st, const char* msg);
 
@@ -404,6 +416,10 @@ cudaError_t launch_finalize_scales(const Geo& G, const float* part, uint32_t row
                                    float* scales, int sms, cudaStream_t s);
 cudaError_t launch_finalize_sums(const Geo& G, const float* part, uint32_t rows, float* sums,
                                  int sms, cudaStream_t s);
+// The scales of chunks [g0, g0 + count) of `rows` rows into scales[row][count].
+cudaError_t launch_finalize_scales_range(const Geo& G, const float* part, uint32_t rows,
+                                         uint32_t g0, uint32_t count, float* scales, int sms,
+                                         cudaStream_t s);
 cudaError_t launch_error_norm(const MaterializeArgs& a, const Workspace& ws, int sms,
                               cudaStream_t s);
 cudaError_t launch_adam_update(const UpdateArgs& a, int sms, cudaStream_t s);

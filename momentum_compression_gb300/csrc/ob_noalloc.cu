@@ -108,6 +108,7 @@ extern "C" ob_status ob_compress_noalloc(ob_ctx* ctx, const void* const* grads,
 
   ob::CompressArgs a{};
   a.geo = G;
+  a.nw = G.W;
   a.ws.wpart = static_cast<float*>(base);
   a.ws.err = reinterpret_cast<unsigned*>(static_cast<char*>(base) + kErrOffset);
   for (uint32_t w = 0; w < G.W; ++w) {
