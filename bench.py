@@ -201,7 +201,7 @@ def kernel_source_hash(files=("k_compress.cu", "ob_internal.cuh")):
     return h.hexdigest()[:16]
 
 
-INT8_SOURCES = ("k_int8.cu", "philox.cuh", "ob_internal.cuh")
+INT8_SOURCES = ("k_int8.cu", "sround.cuh", "philox.cuh", "ob_internal.cuh")
 
 
 
@@ -368,7 +368,7 @@ def run_int8(args, n=None, ef=None):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     n = n or args.n or (1 << 30)
-    ef = ef if ef is None else ef
+    ef = args.ef if ef is None else ef
     g = torch.randn(n, device="cuda") * 1e-3
     q = torch.empty(n, dtype=torch.int8, device="cuda")
     sc = torch.empty((n + 255) // 256, device="cuda")

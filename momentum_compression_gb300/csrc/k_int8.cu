@@ -12,34 +12,48 @@
 // Philox4x32-10 is in philox.cuh.
 #include "ob_internal.cuh"
 #include "philox.cuh"
+#include "sround.cuh"
 
 namespace ob {
 namespace {
 
 // Quantizes the 4 values x of group `grp` (elements 4*grp .. 4*grp+3);
-// dq receives q*scale.
-__device__ __forceinline__ uint32_t quant4(const float4& xv, float scale, uint64_t grp,
-                                           uint64_t step, const PhiloxKeys& K, int nvalid,
+// dq receives q*scale.  rcp: code_rcp(scale) (sround.cuh): the codes come
+// from code_fast where certain, else from code_exact.  Every lane
+// of the warp calls it (the fallback is taken by vote); values beyond the
+// tensor are 0 and code as 0.
+__device__ __forceinline__ uint32_t quant4(const float4& xv, float scale, float rcp,
+                                           uint64_t grp, uint64_t step, const PhiloxKeys& K,
                                            float4& dq) {
   const uint4 ctr = make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
                                (uint32_t)(step >> 32));
   const uint4 rnd = philox4x32_10(ctr, K);
+  float qf[4], u[4];
+  bool unsure = false;
+  if (rcp != 0.0f) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      u[c] = uniform_of(word_of(rnd, c));
+      bool certain;
+      qf[c] = code_fast<127>(f4get(xv, c), rcp, u[c], &certain);
+      unsure |= !certain;
+    }
+    // the definition where code_fast is not certain
+    if (__any_sync(kFull, unsure) && unsure) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) qf[c] = code_exact<127>(f4get(xv, c), scale, u[c]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      qf[c] = scale != 0.0f ? code_exact<127>(f4get(xv, c), scale, uniform_of(word_of(rnd, c)))
+                            : 0.0f;
+  }
   uint32_t packed = 0;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    float qf = 0.0f;
-    if (c < nvalid && scale != 0.0f) {
-      const float x = __fdiv_rn(f4get(xv, c), scale);
-      const float f = floorf(x);
-      const float fr = __fsub_rn(x, f);
-      const float u = __fmul_rn((float)(word_of(rnd, c) >> 8), 5.9604644775390625e-08f);
-      qf = __fadd_rn(f, (u < fr) ? 1.0f : 0.0f);
-      qf = qf > 127.0f ? 127.0f : qf;
-      qf = qf < -127.0f ? -127.0f : qf;
-      if (qf != qf) qf = 0.0f;
-    }
-    f4at(dq, c) = __fmul_rn(qf, scale);
-    packed |= ((uint32_t)(int32_t)qf & 0xffu) << (8 * c);
+    f4at(dq, c) = __fmul_rn(qf[c], scale);
+    packed |= ((uint32_t)(int32_t)qf[c] & 0xffu) << (8 * c);
   }
   return packed;
 }
@@ -119,14 +133,18 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, 127.0f);
+    // 1/scale for the division-free codes (quant4); a scale below the
+    // normal range takes the definition for every value
+    const float rcp = code_rcp(scale);
     if (lane == 0) scales[b] = scale;
     float acc2 = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
       float4 dq = make_float4(0.f, 0.f, 0.f, 0.f);
+      // every lane quantises (values beyond the tensor are 0 and code as 0)
+      const uint32_t packed = quant4(xv[h], scale, rcp, k >> 2, step, K, dq);
       if (nv[h] > 0) {
-        const uint32_t packed = quant4(xv[h], scale, k >> 2, step, K, nv[h], dq);
         if (nv[h] == 4) {
           *reinterpret_cast<uint32_t*>(q + k) = packed;
         } else {

@@ -464,6 +464,69 @@ def test_int8_parity(n):
         assert_bits_equal(host(d_g.t), d_o, "dequantised")
 
 
+def _int8_adversarial(seed, step, nblk=96):
+    """Blocks whose values put the quotient g/scale at, just above or just
+    below (0 to a few times 2^-15 away) an integer plus the value's own
+    uniform -- where the rounding decision flips -- and near integers, at
+    +-127, inside (-1, 0); some blocks with zeros, a NaN, or a scale below
+    the normal range.  The uniforms are the oracle's."""
+    rng = np.random.default_rng(seed)
+    n = 256 * nblk
+    k = np.arange(n)
+    u = np.array([O.uniform(seed, step, int(i)) for i in k], np.float64)
+    deltas = np.array([0.0, 2.0 ** -24, -2.0 ** -24, 2.0 ** -20, -2.0 ** -20, 2.0 ** -17,
+                       -2.0 ** -17, 5 * 2.0 ** -18, -5 * 2.0 ** -18, 2.0 ** -15, -2.0 ** -15,
+                       1.5 * 2.0 ** -15, -1.5 * 2.0 ** -15, 2.0 ** -12, -2.0 ** -12])
+    g = np.zeros(n, np.float32)
+    for b in range(nblk):
+        sl = slice(256 * b, 256 * b + 256)
+        kind = b % 6
+        mx = np.float32(10.0 ** rng.uniform(-6, 2)) if kind != 5 else np.float32(1e-37)
+        s = np.float64(np.float32(mx / np.float32(127.0)))
+        j = rng.integers(-127, 127, 256).astype(np.float64)
+        if kind == 1:
+            j[:] = -1.0  # quotients in (-1, 0)
+        d = deltas[rng.integers(0, len(deltas), 256)]
+        frac = u[sl] + d if kind != 2 else d  # kind 2: near integers
+        v = np.clip(s * (j + frac), -float(mx), float(mx)).astype(np.float32)
+        v[0] = mx if b % 2 else -mx
+        if kind == 3:
+            v[1::3] = 0.0
+        if kind == 4:
+            v[7] = np.nan
+        g[sl] = v
+    return g
+
+
+@pytest.mark.parametrize("variant", ["plain", "deq", "ef"])
+def test_int8_decision_adversarial(variant):
+    """The codes next to every rounding decision's boundary, bit for bit with
+    the oracle's (the division-free codes are taken only where provably
+    equal to the division's; the rest go through the division)."""
+    seed, step = 4321, 9
+    g = _int8_adversarial(seed, step)
+    n = g.size
+    nb = n // 256
+    q_g = Guarded(n, torch.int8, np.zeros(n, np.int8))
+    s_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
+    d_g = Guarded(n, torch.float32, np.zeros(n, f32))
+    if variant == "ef":
+        e0 = (np.random.default_rng(2).standard_normal(n) * 1e-9).astype(f32)
+        e_g = Guarded(n, torch.float32, e0)
+        ob.ob_quant_int8_ef(dev(g), e_g.t, q_g.t, s_g.t, seed, step, d_g.t, None, n=n)
+        q_o, s_o, d_o, _ = O.quant_int8_ef(g, e0.copy(), seed, step, deq=True, err2=True)
+    else:
+        ob.ob_quant_int8(dev(g), q_g.t, s_g.t, seed, step, d_g.t if variant == "deq" else None,
+                         n=n)
+        q_o, s_o, d_o = O.quant_int8(g, 256, seed, step, deq=True)
+    torch.cuda.synchronize()
+    assert_guards(f"int8 {variant}", q_g, s_g, d_g)
+    assert np.array_equal(host(q_g.t), q_o), f"{(host(q_g.t) != q_o).sum()} codes differ"
+    assert_bits_equal(host(s_g.t), s_o, "block scales")
+    if variant != "plain":
+        assert_bits_equal(host(d_g.t), d_o, "dequantised")
+
+
 def test_int8_large_seed_and_no_deq():
     n = 3 * 256 + 17
     g = (np.random.default_rng(1).standard_normal(n) * 10).astype(f32)
