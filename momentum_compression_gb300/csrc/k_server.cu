@@ -24,8 +24,13 @@
 // -s_w)) for all 2^min(W,8) patterns b -- the same additions in the same
 // order as element by element, hence the same bits -- divided by W when
 // W <= 8.  An element then gathers its first 8 workers' bits into a byte
-// (a 4-bit nibble per worker is spread to 4 bytes with one multiply) and
-// reads its z from the table; workers 8.. are added after it in order.
+// (an 8 x 4 bit transpose of the lane's nibbles) and reads its z from the
+// table; workers 8.. are added after it in order: for W = 16 one select and
+// addition per element and worker, for any other W two elements at a time
+// -- per tile, a table holds for each such worker w the four pairs
+// (+-s_w, +-s_w) a lane's two sign bits select, and one paired addition
+// (add.rn.f32x2, each half rounded as on its own) adds worker w's terms to
+// two elements' sums.
 #include <type_traits>
 
 #include "ob_internal.cuh"
@@ -34,7 +39,6 @@
 namespace ob {
 namespace {
 
-constexpr int kSStages = 3;
 constexpr int kSConsumers = kThreads;
 constexpr int kServerThreads = kThreads + 32;
 constexpr uint32_t kRunWords = kTile / 32 + 8;  // one tile's words + rounding slack
@@ -54,6 +58,14 @@ struct TileHdr {
 constexpr size_t kHdrBytes = 64;
 static_assert(sizeof(TileHdr) <= kHdrBytes && kHdrBytes % 16 == 0, "stage header");
 
+// Stages in the ring: 3 up to 8 workers (3 CTAs per SM); beyond that a
+// stage holds more word runs and the per-element sums are longer, and 2
+// stages keep 3 CTAs per SM where 3 would allow only 2.
+template <uint32_t WT>
+__host__ __device__ constexpr int server_stages() {
+  return WT != 0 && WT <= 8 ? 3 : 2;
+}
+
 struct ServerSmem {
   // the e_s tile, the W workers' word runs, the server's previous words
   // and the tile header
@@ -61,9 +73,13 @@ struct ServerSmem {
     return kTile * 4 + (size_t)(W + 1) * kRunWords * 4;
   }
   __host__ __device__ static size_t stage_bytes(uint32_t W) { return hdr_offset(W) + kHdrBytes; }
-  __host__ __device__ static size_t bytes(uint32_t W) {
-    return kSStages * stage_bytes(W) + (2 * kSStages) * 8 + 3 * OB_MAX_WORKERS * 4 +
-           2 * 256 * 4;
+  // the pair table of workers 8.. (two tiles' worth)
+  __host__ __device__ static size_t pairs_bytes(uint32_t W) {
+    return W > 8 && W != 16 ? 2 * (size_t)(W - 8) * 4 * 8 : 0;
+  }
+  __host__ __device__ static size_t bytes(uint32_t W, int stages) {
+    return stages * stage_bytes(W) + (2 * stages) * 8 + 3 * OB_MAX_WORKERS * 4 + 2 * 256 * 4 +
+           pairs_bytes(W);
   }
 };
 
@@ -81,6 +97,7 @@ __device__ __forceinline__ float z8_entry(const float* sc, uint32_t W, float inv
 // and loops' bounds are then constants), 0 for any other W.
 template <bool LAMB, uint32_t WT>
 __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A) {
+  constexpr int kSStages = server_stages<WT>();
   extern __shared__ __align__(128) unsigned char smem[];
   const Geo& G = A.geo;
   const size_t stage_bytes = ServerSmem::stage_bytes(G.W);
@@ -89,6 +106,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   uint64_t* empty = full + kSStages;
   float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(empty + kSStages);
   float(*s_z8)[256] = reinterpret_cast<float(*)[256]>(s_sc + 3);
+  // [2][W - 8][4] pairs (see the file header); 8-byte aligned after s_z8
+  unsigned long long* s_pairs = reinterpret_cast<unsigned long long*>(s_z8 + 2);
   __shared__ float ws[2][8];
   __shared__ volatile int s_abort;
   const size_t hdr_off = ServerSmem::hdr_offset(G.W);
@@ -200,6 +219,14 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     s_sc[0][p] = wscale(p, decode_tile(G, A.T0 + blockIdx.x).g);
   named_sync(1, kSConsumers);
   if ((uint32_t)p < (1u << W8)) s_z8[0][p] = z8_entry(s_sc[0], Wc, inv_w, p);
+  // entry b of worker w's pairs: (bit 0 of b ? s_w : -s_w, bit 1 of b ? s_w : -s_w)
+  auto pairs_entry = [&](const float* sc, int q) {
+    const uint32_t w = 8 + (uint32_t)q / 4, b = (uint32_t)q & 3u;
+    const float sw = sc[w];
+    return f2_make((b & 1u) ? sw : -sw, (b & 2u) ? sw : -sw);
+  };
+  const int n_pairs = WT == 0 && Wc > 8 ? (int)(Wc - 8) * 4 : 0;
+  for (int q = p; q < n_pairs; q += kSConsumers) s_pairs[q] = pairs_entry(s_sc[0], q);
   named_sync(1, kSConsumers);
   uint32_t ti = 0;
   for (uint32_t T = A.T0 + blockIdx.x; T < A.T1; T += gridDim.x, ++ti) {
@@ -223,9 +250,10 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     const uint32_t* sbw = reinterpret_cast<const uint32_t*>(st + kTile * 4);
     const uint32_t* sow = sbw + Wc * kRunWords;  // the server's previous words
     const uint32_t wshift = (uint32_t)(((tl.start - A.base) >> 5) & 3);  // rounding of the runs
-    const float* sc = s_sc[ti % 3];
 
     const float* z8 = s_z8[ti & 1];
+    [[maybe_unused]] const float* sc = s_sc[ti % 3];
+    const unsigned long long* pairs = s_pairs + (ti & 1) * n_pairs;
 
     uint32_t l_t = 0;
     uint64_t lend_t = 0;
@@ -276,8 +304,11 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
           idx ^= tsw ^ (tsw << 7);
 #pragma unroll
           for (int c = 0; c < 4; ++c) z[i][c] = z8[__byte_perm(idx, 0u, 0x4440u | c)];
-          if (WT == 0 || WT > 8) {
-#pragma unroll 8
+          if (WT > 8) {
+            // a compile-time 16: the worker loop unrolled, one select and
+            // one addition per element and worker (on the integer and FP
+            // pipes; the pair table's loads measured slower here)
+#pragma unroll
             for (uint32_t w = 8; w < Wc; ++w) {
               const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
               const float scw = sc[w];
@@ -285,6 +316,18 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
               for (int c = 0; c < 4; ++c)
                 z[i][c] = __fadd_rn(z[i][c], ((wd >> c) & 1u) ? scw : -scw);
             }
+          } else if (WT == 0) {
+            unsigned long long z01 = f2_make(z[i][0], z[i][1]);
+            unsigned long long z23 = f2_make(z[i][2], z[i][3]);
+#pragma unroll 8
+            for (uint32_t w = 8; w < Wc; ++w) {
+              const uint32_t wd = sbw[w * kRunWords + widx] >> sh;
+              const unsigned long long* pw = pairs + (w - 8) * 4;
+              z01 = f2_add(z01, pw[wd & 3u]);
+              z23 = f2_add(z23, pw[(wd >> 2) & 3u]);
+            }
+            f2_split(z01, z[i][0], z[i][1]);
+            f2_split(z23, z[i][2], z[i][3]);
           }
         }
       }
@@ -345,6 +388,8 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
     if (Tn < A.T1) {
       if ((uint32_t)p < (1u << W8))
         s_z8[(ti + 1) & 1][p] = z8_entry(s_sc[(ti + 1) % 3], Wc, inv_w, p);
+      for (int q = p; q < n_pairs; q += kSConsumers)
+        s_pairs[((ti + 1) & 1) * n_pairs + q] = pairs_entry(s_sc[(ti + 1) % 3], q);
     }
     const bool stop = named_sync_or(1, kSConsumers, s_abort != 0);
     if (p == 0) A.ws.spart[(uint64_t)tl.g * G.tpc + tl.t] = tree8(ws[ti & 1]);
@@ -354,11 +399,12 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
 
 template <bool LAMB, uint32_t WT>
 cudaError_t run_server(const ServerArgs& a, int sms, cudaStream_t s) {
-  const size_t bytes = ServerSmem::bytes(a.geo.W);
+  constexpr int kSt = server_stages<WT>();
+  const size_t bytes = ServerSmem::bytes(a.geo.W, kSt);
   static PerDeviceOnce once;
   const cudaError_t attr = once.run([] {
     return cudaFuncSetAttribute(k_server<LAMB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)ServerSmem::bytes(OB_MAX_WORKERS));
+                                (int)ServerSmem::bytes(WT ? WT : OB_MAX_WORKERS, kSt));
   });
   if (attr != cudaSuccess) return attr;
   const int grid = grid_for(k_server<LAMB, WT>, sms, a.T1 - a.T0, kServerThreads, bytes);

@@ -173,6 +173,24 @@ __device__ __forceinline__ float mean_of(float sum, uint64_t count) {
   return count ? __fdiv_rn(sum, __ull2float_rn(count)) : 0.0f;
 }
 
+// Two fp32 values in one 64-bit register pair, and the paired IEEE addition
+// of sm_100-class GPUs (PTX add.rn.f32x2): each half is rounded on its own,
+// to nearest even, with subnormals kept -- the result of __fadd_rn on that
+// half -- in one instruction for both.
+__device__ __forceinline__ unsigned long long f2_make(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(unsigned long long a, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ float fmax_plain(float a, float b) { return a > b ? a : b; }
 __device__ __forceinline__ float fmin_plain(float a, float b) { return a < b ? a : b; }
 
