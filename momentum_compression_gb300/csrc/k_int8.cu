@@ -67,7 +67,7 @@ __device__ __forceinline__ void load_block(const float* __restrict__ g, uint64_t
     const uint64_t k = b * 256 + 128 * h + 4 * lane;
     nv[h] = k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
     if (nv[h] == 4) {
-      gv[h] = __ldcs(reinterpret_cast<const float4*>(g + k));
+      gv[h] = *reinterpret_cast<const float4*>(g + k);
     } else {
       gv[h] = make_float4(nv[h] > 0 ? g[k] : 0.f, nv[h] > 1 ? g[k + 1] : 0.f,
                           nv[h] > 2 ? g[k + 2] : 0.f, 0.f);
@@ -78,7 +78,7 @@ __device__ __forceinline__ void load_block(const float* __restrict__ g, uint64_t
 __device__ __forceinline__ void store4(float* __restrict__ dst, uint64_t k, int nv,
                                        const float4& v) {
   if (nv == 4) {
-    __stcs(reinterpret_cast<float4*>(dst + k), v);
+    *reinterpret_cast<float4*>(dst + k) = v;
   } else {
 #pragma unroll
     for (int c = 0; c < 3; ++c)

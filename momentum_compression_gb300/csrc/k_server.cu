@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
   // ------------------------------------------------------------ producer
   if (warp == kSConsumers / 32) {
     if (lane != 0) return;
-    const uint64_t pol = policy_evict_first();
     uint32_t ti = 0;
     bool ok = true;
     // 1-bit LAMB: the layer of the tile, loaded a tile before the loads
@@ -172,7 +171,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         hd->r = A.ratio_ef ? __fdiv_rn(c2, c1) : 1.0f;
       }
       mbar_arrive_expect_tx(&full[s], tl.len * 4 + (G.W + 1) * run);
-      bulk_g2s_stream(st, A.e_s + lstart, tl.len * 4, &full[s], pol);
+      bulk_g2s(st, A.e_s + lstart, tl.len * 4, &full[s]);
       for (uint32_t w = 0; w < G.W; ++w)
         bulk_g2s(st + kTile * 4 + (size_t)w * kRunWords * 4, A.bits + w * A.bits_stride + w0,
                  run, &full[s]);
@@ -366,7 +365,7 @@ __global__ void __launch_bounds__(kServerThreads, 3) k_server(const ServerArgs A
         }
         const uint32_t word = pack_word(nib, lane);
         if (FULL || valid[i]) {
-          __stcs(reinterpret_cast<float4*>(A.e_s + (k0 - A.base)), yv);
+          *reinterpret_cast<float4*>(A.e_s + (k0 - A.base)) = yv;
           if ((p & 7) == 0) A.sbits[(k0 - A.base) >> 5] = word;
         }
       }

@@ -80,16 +80,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Same, with an L2 evict-first policy (data streamed once).
-__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes,
-                                                uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // Asks the copy engine to bring `bytes` (multiple of 16; address 16-byte
 // aligned) of global memory into L2.  A hint: nothing is returned to the
 // SM and nothing waits for it.
@@ -113,12 +103,6 @@ __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
 
 // Named barrier among the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_sync(int id, int threads) {
