@@ -58,7 +58,8 @@ def log(*a):
 
 def bytes_per_element(W, G, lamb=False, sign_m=False):
     """compress: m read 4 (sign form: the server's word, 1/8, once per group
-    of up to 4 workers for Adam, once per tile for LAMB) + per worker
+    of up to 4 workers for Adam -- 2 with bf16 gradients -- once per tile for
+    LAMB) + per worker
     g read G, e read 4 + write 4, old sign word read 1/8 + new word write
     1/8; server: W/8 word reads, e_s read 4 + write 4, sign word 1/8 + 1/8;
     Adam: sign word 1/8, v 4, p 4 + 4, m write 4 (none in sign form).  LAMB
@@ -66,7 +67,8 @@ def bytes_per_element(W, G, lamb=False, sign_m=False):
     p 4+4.  LAMB in sign form: pass A reads the previous and the current
     sign word (1/8 + 1/8) instead of m, pass B the current word instead of
     m, and m is not written."""
-    comp = (0.125 * (1 if lamb else (W + 3) // 4) if sign_m else 4) + W * (G + 8 + 0.25)
+    grp = 2 if G == 2 else 4
+    comp = (0.125 * (1 if lamb else (W + grp - 1) // grp) if sign_m else 4) + W * (G + 8 + 0.25)
     serv = W / 8 + 8 + 0.25
     if lamb:
         upd = (0.25 + 12 + 0.125 + 12) if sign_m else (0.125 + 20 + 16)

@@ -40,10 +40,13 @@ constexpr int kCompressThreads = kThreads + 32;  // + 1 producer warp
 // With the momentum in sign form (re-reading it costs 1/8 byte per element)
 // a tile's workers are taken in groups of at most kGroup, group-major over
 // the buffer: fewer workers' arrays are streamed at once, which measured
-// faster (compress at W = 3-4 ran at ~98% of the copy peak, at W = 8 ~90%;
-// grouped, W = 8 and 16 run at ~97%).  With a dense m the groups measured
-// slower (m is re-read per group and its single buffer serialises them).
-constexpr uint32_t kGroup = 4;
+// faster (fp32 gradients: compress at W = 3-4 ran at ~98% of the copy peak,
+// at W = 8 ~90%; in groups of 4, W = 8 and 16 run at ~97%; groups of 2
+// were 14% slower there).  With bf16 gradients groups of 2 measured best
+// (GPT-1.3B, W = 4: 3.3% faster than one group of 4, W = 8: 4.5%; groups of
+// 1 slower).  With a dense m the groups measured slower (m is re-read per
+// group and its single buffer serialises them).
+constexpr uint32_t kGroupF32 = 4, kGroupBF16 = 2;
 
 // A stage holds one (tile, worker) item: the gradient tile, the error tile
 // and the worker's previous sign words of the tile (a 16-byte aligned run),
@@ -126,6 +129,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   // once measured faster there); a dense m would be re-read per group, and
   // 1-bit LAMB's per-tile layer setup measured slower repeated per group
   constexpr bool kGrouped = MSIGN && !LAMB;
+  constexpr uint32_t kGroup = BF16 ? kGroupBF16 : kGroupF32;
   // NW workers are compressed: all W of the layout, or one (a rank's own)
   const uint32_t NW = A.nw;
   const uint32_t gsz = kGrouped ? kGroup : NW;

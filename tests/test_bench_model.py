@@ -13,7 +13,9 @@ WORD = 1 / 8  # bytes of packed sign per element
 
 def touched(W, G, lamb, sign_m):
     """Buffers per kernel: (bytes per element, times) for every read and write."""
-    groups = 1 if lamb else math.ceil(W / 4)  # sign-form m words, read per worker group
+    # sign-form m words, read per worker group (groups of 4 workers, 2 with
+    # bf16 gradients; one read per tile for LAMB)
+    groups = 1 if lamb else math.ceil(W / (2 if G == 2 else 4))
     compress = [(WORD, groups) if sign_m else (4, 1)]        # m
     compress += [(G, W), (4, W), (4, W), (WORD, W), (WORD, W)]  # g; e read, write; old, new word
     server = [(WORD, W), (4, 1), (4, 1), (WORD, 1), (WORD, 1)]  # worker words; e_s r/w; old, new
