@@ -90,14 +90,15 @@ __device__ __forceinline__ void store4(float* __restrict__ dst, uint64_t k, int 
 // e := x - q*scale.  ERR2: per-block sum of the squared residual (lane j
 // adds its 8 squares in element order, then a warp butterfly).
 template <bool DEQ, bool EF, bool ERR2>
-__global__ void __launch_bounds__(kThreads)
-    k_quant_int8(const float* __restrict__ g, float* __restrict__ e, uint64_t n,
-                 int8_t* __restrict__ q, float* __restrict__ scales, uint64_t seed,
-                 uint64_t step, float* __restrict__ deq, float* __restrict__ err2) {
+__device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
+                                                float* __restrict__ e, uint64_t n,
+                                                int8_t* __restrict__ q,
+                                                float* __restrict__ scales, const PhiloxKeys& K,
+                                                uint64_t step, float* __restrict__ deq,
+                                                float* __restrict__ err2) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
-  const PhiloxKeys K = philox_keys((uint32_t)seed, (uint32_t)(seed >> 32));
   uint64_t b = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   float4 gv[2], ev[2];
   int nv[2];
@@ -179,14 +180,40 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Without error feedback the kernel fits 5 CTAs per SM without spills (40
+// warps instead of 32: 2.4% faster at 2^30; with the dequantized output, 4);
+// the error-feedback forms spill there and keep the compiler's choice.
+template <bool DEQ>
+__global__ void __launch_bounds__(kThreads, DEQ ? 4 : 5)
+    k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
+                 float* __restrict__ scales, const PhiloxKeys K, uint64_t step,
+                 float* __restrict__ deq) {
+  quant_int8_body<DEQ, false, false>(g, nullptr, n, q, scales, K, step, deq, nullptr);
+}
+
+template <bool DEQ, bool ERR2>
+__global__ void __launch_bounds__(kThreads)
+    k_quant_int8_ef(const float* __restrict__ g, float* __restrict__ e, uint64_t n,
+                    int8_t* __restrict__ q, float* __restrict__ scales, const PhiloxKeys K,
+                    uint64_t step, float* __restrict__ deq, float* __restrict__ err2) {
+  quant_int8_body<DEQ, true, ERR2>(g, e, n, q, scales, K, step, deq, err2);
+}
+
 template <bool DEQ, bool EF, bool ERR2>
 cudaError_t run_int8(const float* g, float* e, uint64_t n, int8_t* q, float* scales,
                      uint64_t seed, uint64_t step, float* deq, float* err2, int sms,
                      cudaStream_t s) {
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t ctas = (nblk + kThreads / 32 - 1) / (kThreads / 32);
-  k_quant_int8<DEQ, EF, ERR2><<<grid_for(k_quant_int8<DEQ, EF, ERR2>, sms, ctas), kThreads, 0,
-                                s>>>(g, e, n, q, scales, seed, step, deq, err2);
+  // the round keys go in as a kernel parameter (see philox.cuh)
+  const PhiloxKeys K = philox_keys((uint32_t)seed, (uint32_t)(seed >> 32));
+  if constexpr (EF) {
+    k_quant_int8_ef<DEQ, ERR2><<<grid_for(k_quant_int8_ef<DEQ, ERR2>, sms, ctas), kThreads, 0,
+                                 s>>>(g, e, n, q, scales, K, step, deq, err2);
+  } else {
+    k_quant_int8<DEQ><<<grid_for(k_quant_int8<DEQ>, sms, ctas), kThreads, 0, s>>>(
+        g, n, q, scales, K, step, deq);
+  }
   return cudaGetLastError();
 }
 

@@ -12,12 +12,14 @@
 namespace ob {
 
 // Round keys of Philox4x32-10: key k advanced by (0x9E3779B9, 0xBB67AE85)
-// before every round but the first; computed once per thread.
+// before every round but the first; computed once per thread, or once on
+// the host and passed to a kernel as a parameter (its rounds then read the
+// keys from the constant bank instead of holding 20 registers).
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
 
-__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+__host__ __device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
   PhiloxKeys K;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
