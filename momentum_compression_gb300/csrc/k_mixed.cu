@@ -65,20 +65,15 @@ __device__ __forceinline__ float code_val(uint32_t v, int c) {
 // Quantises the lane's 8 values of one block (x, nv real values per half)
 // with error feedback; writes the code words (whole words, by the lanes
 // that own them), the block scale and the residual e' (padding 0).
-// Round keys of the quantizer's Philox: held in registers (hoisted, 20 of
-// them) or formed round by round from the seed.
-struct KeysHoisted {
-  PhiloxKeys K;
-  __device__ explicit KeysHoisted(uint64_t seed)
-      : K(philox_keys((uint32_t)seed, (uint32_t)(seed >> 32))) {}
+// Round keys of the quantizer's Philox, computed once on the host and
+// passed as a kernel parameter: the rounds read them from the constant bank.
+// (Held in registers they took 20 of them, which the 3-CTA bound of the
+// worker kernel could not spare; formed round by round, as the server did,
+// they cost 20 additions per call.  Both forms measured about 4% slower.)
+struct KeysParam {
+  const PhiloxKeys& K;
+  __device__ explicit KeysParam(const PhiloxKeys& k) : K(k) {}
   __device__ uint4 operator()(uint4 c) const { return philox4x32_10(c, K); }
-};
-
-struct KeysRolling {
-  uint32_t k0, k1;
-  __device__ explicit KeysRolling(uint64_t seed)
-      : k0((uint32_t)seed), k1((uint32_t)(seed >> 32)) {}
-  __device__ uint4 operator()(uint4 c) const { return philox4x32_10_rk(c, k0, k1); }
 };
 
 template <int BITS, class Keys>
@@ -137,12 +132,13 @@ __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (
 // ---------------------------------------------------------------------------
 
 template <bool BF16, int BITS>
-__global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArgs A) {
+__global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArgs A,
+                                                              const PhiloxKeys K) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
   const float ob1 = __fsub_rn(1.0f, A.b1);
-  const KeysHoisted keys(A.seed);
+  const KeysParam keys(K);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 mv[2], gv[2], ev[2];
@@ -197,15 +193,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArg
 }
 
 // 3 CTAs per SM (80 registers, no spill; unbounded it took 127 and ran 2):
-// the 2-bit server 0.141 -> 0.129 ms on ResNet-50's group.
-template <int BITS, class Keys>
-__global__ void __launch_bounds__(kThreads, 3) k_qb_server(const QbServerArgs A) {
+// the 2-bit server 0.141 -> 0.129 ms on ResNet-50's group (0.123 ms with the round
+// keys as a kernel parameter).
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 3) k_qb_server(const QbServerArgs A,
+                                                           const PhiloxKeys K) {
   using S = CodeSlot<BITS>;
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
   const float fW = (float)A.W, inv_w = inv_workers(A.W);
-  const Keys keys(A.seed);
+  const KeysParam keys(K);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 es[2], z[2];
@@ -431,8 +429,9 @@ uint64_t warp_ctas(uint64_t n_pad) {
 cudaError_t launch_qb_compress(const QbCompressArgs& a, int bits, bool bf16, int sms,
                                cudaStream_t s) {
   const uint64_t ctas = warp_ctas(a.n_pad);
+  const PhiloxKeys K = philox_keys((uint32_t)a.seed, (uint32_t)(a.seed >> 32));
 #define OB_QB_COMPRESS(BF, B)                                                         \
-  k_qb_compress<BF, B><<<grid_for(k_qb_compress<BF, B>, sms, ctas), kThreads, 0, s>>>(a)
+  k_qb_compress<BF, B><<<grid_for(k_qb_compress<BF, B>, sms, ctas), kThreads, 0, s>>>(a, K)
   if (bf16) {
     if (bits == 2) OB_QB_COMPRESS(true, 2);
     else if (bits == 4) OB_QB_COMPRESS(true, 4);
@@ -446,14 +445,10 @@ cudaError_t launch_qb_compress(const QbCompressArgs& a, int bits, bool bf16, int
   return cudaGetLastError();
 }
 
-// The server forms its Philox round keys round by round: with 80 registers
-// it keeps 3 CTAs per SM, where hoisted keys (100 registers) allow 2 and
-// measured 15% slower.  The worker kernel keeps them hoisted: there the
-// extra additions cost more than the occupancy gains.
 template <int B>
 void run_qb_server(const QbServerArgs& a, int sms, uint64_t ctas, cudaStream_t s) {
-  k_qb_server<B, KeysRolling>
-      <<<grid_for(k_qb_server<B, KeysRolling>, sms, ctas), kThreads, 0, s>>>(a);
+  const PhiloxKeys K = philox_keys((uint32_t)a.seed, (uint32_t)(a.seed >> 32));
+  k_qb_server<B><<<grid_for(k_qb_server<B>, sms, ctas), kThreads, 0, s>>>(a, K);
 }
 
 cudaError_t launch_qb_server(const QbServerArgs& a, int bits, int sms, cudaStream_t s) {

@@ -40,21 +40,6 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& K) {
   return c;
 }
 
-// The same generator with the round keys formed as it goes (two additions
-// per round instead of 20 registers held across a kernel's loop).
-__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
-    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
-                   (uint32_t)p0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-  return c;
-}
-
 // Word c of a Philox output.
 __device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
   return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
