@@ -17,6 +17,64 @@
 namespace ob {
 namespace {
 
+// Quantizes the lane's 8 values xv[h] (h = 0, 1; elements 4*grp[h] ..
+// 4*grp[h]+3), one Philox output per group, both drawn side by side; dq[h]
+// receives q*scale and packed[h] the four codes.  rcp: code_rcp(scale)
+// (sround.cuh): the codes come from code_fast where certain, else from
+// code_exact (for all 8 values of a lane that has an uncertain one; the
+// two agree wherever code_fast is certain).  Every lane of the warp calls
+// it (the fallback is taken by vote); values beyond the tensor are 0 and
+// code as 0.
+__device__ __forceinline__ void quant8(const float4 (&xv)[2], float scale, float rcp,
+                                       const uint64_t (&grp)[2], uint64_t step,
+                                       const PhiloxKeys& K, float4 (&dq)[2],
+                                       uint32_t (&packed)[2]) {
+  uint4 rnd[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    rnd[h] = make_uint4((uint32_t)grp[h], (uint32_t)(grp[h] >> 32), (uint32_t)step,
+                        (uint32_t)(step >> 32));
+  philox4x32_10_x2(rnd[0], rnd[1], K);
+  float qf[2][4], u[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[h][c] = uniform_of(word_of(rnd[h], c));
+  if (rcp != 0.0f) {
+    bool unsure = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        bool certain;
+        qf[h][c] = code_fast<127>(f4get(xv[h], c), rcp, u[h][c], &certain);
+        unsure |= !certain;
+      }
+    // the definition where code_fast is not certain
+    if (__any_sync(kFull, unsure) && unsure) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) qf[h][c] = code_exact<127>(f4get(xv[h], c), scale, u[h][c]);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        qf[h][c] = scale != 0.0f ? code_exact<127>(f4get(xv[h], c), scale, u[h][c]) : 0.0f;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    packed[h] = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      f4at(dq[h], c) = __fmul_rn(qf[h][c], scale);
+      packed[h] |= ((uint32_t)(int32_t)qf[h][c] & 0xffu) << (8 * c);
+    }
+  }
+}
+
 // Quantizes the 4 values x of group `grp` (elements 4*grp .. 4*grp+3);
 // dq receives q*scale.  rcp: code_rcp(scale) (sround.cuh): the codes come
 // from code_fast where certain, else from code_exact.  Every lane
@@ -139,12 +197,25 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
     const float rcp = code_rcp(scale);
     if (lane == 0) scales[b] = scale;
     float acc2 = 0.0f;
+    // every lane quantises (values beyond the tensor are 0 and code as 0).
+    // Without error feedback both halves' Philox outputs are drawn side by
+    // side (quant8: 5.7% faster at 4 CTAs per SM); with it the registers
+    // that takes cost a CTA per SM and the halves go one at a time (quant4).
+    float4 dqv[2];
+    uint32_t pk[2];
+    if constexpr (!EF) {
+      const uint64_t grp[2] = {(b * 256 + 4 * lane) >> 2, (b * 256 + 128 + 4 * lane) >> 2};
+      quant8(xv, scale, rcp, grp, step, K, dqv, pk);
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
-      float4 dq = make_float4(0.f, 0.f, 0.f, 0.f);
-      // every lane quantises (values beyond the tensor are 0 and code as 0)
-      const uint32_t packed = quant4(xv[h], scale, rcp, k >> 2, step, K, dq);
+      if constexpr (EF) {
+        dqv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        pk[h] = quant4(xv[h], scale, rcp, k >> 2, step, K, dqv[h]);
+      }
+      const float4 dq = dqv[h];
+      const uint32_t packed = pk[h];
       if (nv[h] > 0) {
         if (nv[h] == 4) {
           *reinterpret_cast<uint32_t*>(q + k) = packed;
@@ -180,11 +251,11 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
   }
 }
 
-// Without error feedback the kernel fits 5 CTAs per SM without spills (40
-// warps instead of 32: 2.4% faster at 2^30; with the dequantized output, 4);
-// the error-feedback forms spill there and keep the compiler's choice.
+// Without error feedback the kernel runs at 4 CTAs per SM (56 registers,
+// no spill; with one Philox output at a time 5 CTAs fitted and measured
+// 5.7% slower); the error-feedback forms keep the compiler's choice.
 template <bool DEQ>
-__global__ void __launch_bounds__(kThreads, DEQ ? 4 : 5)
+__global__ void __launch_bounds__(kThreads, 4)
     k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
                  float* __restrict__ scales, const PhiloxKeys K, uint64_t step,
                  float* __restrict__ deq) {

@@ -65,21 +65,19 @@ __device__ __forceinline__ float code_val(uint32_t v, int c) {
 // Quantises the lane's 8 values of one block (x, nv real values per half)
 // with error feedback; writes the code words (whole words, by the lanes
 // that own them), the block scale and the residual e' (padding 0).
-// Round keys of the quantizer's Philox, computed once on the host and
-// passed as a kernel parameter: the rounds read them from the constant bank.
-// (Held in registers they took 20 of them, which the 3-CTA bound of the
-// worker kernel could not spare; formed round by round, as the server did,
-// they cost 20 additions per call.  Both forms measured about 4% slower.)
-struct KeysParam {
-  const PhiloxKeys& K;
-  __device__ explicit KeysParam(const PhiloxKeys& k) : K(k) {}
-  __device__ uint4 operator()(uint4 c) const { return philox4x32_10(c, K); }
-};
-
-template <int BITS, class Keys>
+// The quantizer's Philox round keys are computed once on the host and
+// passed to the kernels as a parameter: the rounds read them from the
+// constant bank.  (Held in registers they took 20 of them, which the 3-CTA
+// bound of the worker kernel could not spare; formed round by round, as the
+// server did, they cost 20 additions per call.  Both forms measured about
+// 4% slower.)
+// PAIR: both halves' Philox outputs are drawn side by side (two independent
+// chains; the server, 2% faster) or one at a time (the worker kernel, where
+// the pair's registers spill at its 3-CTA bound: 23% slower).
+template <int BITS, bool PAIR>
 __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (&nv)[2],
                                                uint64_t u_index0, uint64_t step,
-                                               const Keys& keys, int lane,
+                                               const PhiloxKeys& K, int lane,
                                                uint32_t* __restrict__ codes, float* scale_out,
                                                float4 (&e_out)[2]) {
   constexpr float qmax = (float)((1 << (BITS - 1)) - 1);
@@ -95,14 +93,24 @@ __device__ __forceinline__ void quantize_block(const float4 (&x)[2], const int (
   for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
   const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, qmax);
   if (lane == 0) *scale_out = scale;
+  // the halves' Philox counters (u_index0 + 128h + 4 lane is a multiple
+  // of 4); the outputs are used only where a value is real and the scale
+  // is not 0
+  uint4 rnds[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint64_t ui = u_index0 + 128 * h + 4 * lane;  // a multiple of 4
+    const uint64_t grp = (u_index0 + 128 * h + 4 * lane) >> 2;
+    rnds[h] = make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
+                         (uint32_t)(step >> 32));
+  }
+  if constexpr (PAIR) philox4x32_10_x2(rnds[0], rnds[1], K);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
     uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-    if (nv[h] > 0 && scale != 0.0f) {
-      const uint64_t grp = ui >> 2;
-      rnd = keys(make_uint4((uint32_t)grp, (uint32_t)(grp >> 32), (uint32_t)step,
-                            (uint32_t)(step >> 32)));
+    if constexpr (PAIR) {
+      rnd = rnds[h];
+    } else if (nv[h] > 0 && scale != 0.0f) {
+      rnd = philox4x32_10(rnds[h], K);
     }
     uint32_t piece = 0;
 #pragma unroll
@@ -138,7 +146,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArg
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
   const float ob1 = __fsub_rn(1.0f, A.b1);
-  const KeysParam keys(K);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 mv[2], gv[2], ev[2];
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_compress(const QbCompressArg
           f4at(x[h], c) = c < nv[h] ? xv : 0.0f;
         }
       float4 r[2];
-      quantize_block<BITS>(x, nv, (uint64_t)w * A.n_pad + b * 256, A.step, keys, lane,
+      quantize_block<BITS, false>(x, nv, (uint64_t)w * A.n_pad + b * 256, A.step, K, lane,
                            A.codes + (uint64_t)w * A.row_words + b * CodeSlot<BITS>::kBlockWords,
                            A.scales + (uint64_t)w * nblk + b, r);
 #pragma unroll
@@ -203,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_server(const QbServerArgs A,
   const uint64_t nblk = A.n_pad / 256;
   const uint64_t warps = (uint64_t)gridDim.x * kWarps;
   const float fW = (float)A.W, inv_w = inv_workers(A.W);
-  const KeysParam keys(K);
   for (uint64_t b = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); b < nblk; b += warps) {
     int nv[2];
     float4 es[2], z[2];
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_qb_server(const QbServerArgs A,
             c < nv[h] ? __fadd_rn(f4get(es[h], c), div_by_workers(f4get(z[h], c), fW, inv_w))
                       : 0.0f;
     float4 r[2];
-    quantize_block<BITS>(y, nv, (uint64_t)A.W * A.n_pad + b * 256, A.step, keys, lane,
+    quantize_block<BITS, true>(y, nv, (uint64_t)A.W * A.n_pad + b * 256, A.step, K, lane,
                          A.scodes + b * S::kBlockWords, A.sscales + b, r);
 #pragma unroll
     for (int h = 0; h < 2; ++h)

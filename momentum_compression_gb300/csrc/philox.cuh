@@ -40,6 +40,23 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& K) {
   return c;
 }
 
+// The same generator on two counters at once, round by round: two
+// independent chains side by side in program order, so that one lane's
+// dependent multiply-xor chains overlap.
+__device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, const PhiloxKeys& K) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t a0 = (uint64_t)0xD2511F53u * a.x;
+    const uint64_t a1 = (uint64_t)0xCD9E8D57u * a.z;
+    const uint64_t b0 = (uint64_t)0xD2511F53u * b.x;
+    const uint64_t b1 = (uint64_t)0xCD9E8D57u * b.z;
+    a = make_uint4((uint32_t)(a1 >> 32) ^ a.y ^ K.k0[r], (uint32_t)a1,
+                   (uint32_t)(a0 >> 32) ^ a.w ^ K.k1[r], (uint32_t)a0);
+    b = make_uint4((uint32_t)(b1 >> 32) ^ b.y ^ K.k0[r], (uint32_t)b1,
+                   (uint32_t)(b0 >> 32) ^ b.w ^ K.k1[r], (uint32_t)b0);
+  }
+}
+
 // Word c of a Philox output.
 __device__ __forceinline__ uint32_t word_of(const uint4& u, int c) {
   return c == 0 ? u.x : c == 1 ? u.y : c == 2 ? u.z : u.w;
