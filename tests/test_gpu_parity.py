@@ -610,9 +610,11 @@ def test_double_buffer_arguments_rejected_before_launch():
     opt.close()
 
 
+@pytest.mark.parametrize("deq,err2", [(True, True), (False, True), (False, False)])
 @pytest.mark.parametrize("n", [1, 255, 256, 1000, 4097, (1 << 20) + 5])
-def test_int8_error_feedback_parity(n):
-    """INT8 with error feedback and the per-block error monitor, three calls
+def test_int8_error_feedback_parity(n, deq, err2):
+    """INT8 with error feedback (with and without the dequantised output and
+    the per-block error monitor: each pair is its own kernel), three calls
     in a row (the residual carries over), against the oracle bit for bit."""
     rng = np.random.default_rng(n + 17)
     e_o = (rng.standard_normal(n) * 1e-5).astype(f32)
@@ -620,19 +622,24 @@ def test_int8_error_feedback_parity(n):
     e_g = Guarded(n, torch.float32, e_o)
     q_g = Guarded(n, torch.int8, np.zeros(n, np.int8))
     s_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
-    d_g = Guarded(n, torch.float32, np.zeros(n, f32))
-    e2_g = Guarded(nb, torch.float32, np.zeros(nb, f32))
+    d_g = Guarded(n, torch.float32, np.zeros(n, f32)) if deq else None
+    e2_g = Guarded(nb, torch.float32, np.zeros(nb, f32)) if err2 else None
+    outs = [x for x in (d_g, e2_g) if x is not None]
     for step in range(3):
         g = (rng.standard_normal(n) * 1e-3).astype(f32)
-        ob.ob_quant_int8_ef(dev(g), e_g.t, q_g.t, s_g.t, 77, step, d_g.t, e2_g.t, n=n)
+        ob.ob_quant_int8_ef(dev(g), e_g.t, q_g.t, s_g.t, 77, step, d_g.t if deq else None,
+                            e2_g.t if err2 else None, n=n)
         torch.cuda.synchronize()
-        assert_guards(f"quant_int8_ef, call {step}", e_g, q_g, s_g, d_g, e2_g)
-        q_o, s_o, d_o, e2_o = O.quant_int8_ef(g, e_o, 77, step, deq=True, err2=True)
+        assert_guards(f"quant_int8_ef, call {step}", e_g, q_g, s_g, *outs)
+        ref = O.quant_int8_ef(g, e_o, 77, step, deq=deq, err2=err2)
+        q_o, s_o = ref[0], ref[1]
         assert np.array_equal(host(q_g.t), q_o), f"codes, call {step}"
         assert_bits_equal(host(s_g.t), s_o, "scales")
-        assert_bits_equal(host(d_g.t), d_o, "dequantised")
+        if deq:
+            assert_bits_equal(host(d_g.t), ref[2], "dequantised")
         assert_bits_equal(host(e_g.t), e_o, "residual")
-        assert_bits_equal(host(e2_g.t), e2_o, "error monitor")
+        if err2:
+            assert_bits_equal(host(e2_g.t), ref[-1], "error monitor")
 
 
 # ---------------------------------------------------------------------------
