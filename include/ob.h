@@ -94,7 +94,7 @@ typedef int ob_status;
 #define OB_OK 0
 #define OB_ERR_INVALID 1     /* bad argument or size */
 #define OB_ERR_ALIGN 2       /* misaligned pointer */
-#define OB_ERR_UNSUPPORTED 3 /* a configuration this build does not run */
+#define OB_ERR_UNSUPPORTED 3 /* a configuration the library does not support */
 #define OB_ERR_CUDA 4        /* a CUDA call or launch failed */
 #define OB_ERR_STATE 5       /* call out of order (e.g. no workspace) */
 
