@@ -3,11 +3,11 @@
 // rounding; and its GradientQuantizeINT8 example: floor plus a Bernoulli
 // draw on the fractional part, clamp to ±127).
 //
-// One warp per block of 256 elements: lane j holds elements 4j..4j+3 and
-// 128+4j..128+4j+3 (two 128-bit loads, the next block's issued before this
-// one is quantised), the block max is a warp max, and each group of four
-// elements draws one Philox4x32-10 output (four 32-bit words) from counter
-// (k>>2, step).
+// Each group of four elements draws one Philox4x32-10 output (four 32-bit
+// words) from counter (k>>2, step), whichever lane quantises it.  Without
+// error feedback half a warp takes a block of 256 elements (16 per lane);
+// with it a warp does (8 per lane, in the order of the per-block error
+// monitor's sums).  The block max is a (half-)warp max.
 //
 // Philox4x32-10 is in philox.cuh.
 #include "ob_internal.cuh"
@@ -147,13 +147,19 @@ __device__ __forceinline__ void store4(float* __restrict__ dst, uint64_t k, int 
 // DEQ: write q*scale.  EF: error feedback -- x = g + e is quantised and
 // e := x - q*scale.  ERR2: per-block sum of the squared residual (lane j
 // adds its 8 squares in element order, then a warp butterfly).
-template <bool DEQ, bool EF, bool ERR2>
-__device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
-                                                float* __restrict__ e, uint64_t n,
-                                                int8_t* __restrict__ q,
-                                                float* __restrict__ scales, const PhiloxKeys& K,
-                                                uint64_t step, float* __restrict__ deq,
-                                                float* __restrict__ err2) {
+// With error feedback: one warp per block, lane j holding elements 4j ..
+// 4j+3 and 128+4j .. 128+4j+3 (the next block's loads in flight while this
+// one is quantised); x = g + e is quantised and e := x - q*scale.  The two
+// halves' Philox outputs are drawn one at a time (quant4): side by side
+// (quant8) their registers cost a CTA per SM and measured 6.4% slower.
+template <bool DEQ, bool ERR2>
+__device__ __forceinline__ void quant_int8_ef_body(const float* __restrict__ g,
+                                                   float* __restrict__ e, uint64_t n,
+                                                   int8_t* __restrict__ q,
+                                                   float* __restrict__ scales,
+                                                   const PhiloxKeys& K, uint64_t step,
+                                                   float* __restrict__ deq,
+                                                   float* __restrict__ err2) {
   const int lane = threadIdx.x & 31;
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
@@ -162,26 +168,20 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
   int nv[2];
   if (b < nblk) {
     load_block(g, n, b, lane, gv, nv);
-    if constexpr (EF) load_block(e, n, b, lane, ev, nv);
+    load_block(e, n, b, lane, ev, nv);
   }
   for (; b < nblk; b += warps) {
-    // the next block's loads are in flight while this block is quantised
     float4 gn[2], en[2];
     int nn[2] = {0, 0};
     if (b + warps < nblk) {
       load_block(g, n, b + warps, lane, gn, nn);
-      if constexpr (EF) load_block(e, n, b + warps, lane, en, nn);
+      load_block(e, n, b + warps, lane, en, nn);
     }
     float4 xv[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if constexpr (EF) {
-        xv[h] = make_float4(__fadd_rn(gv[h].x, ev[h].x), __fadd_rn(gv[h].y, ev[h].y),
-                            __fadd_rn(gv[h].z, ev[h].z), __fadd_rn(gv[h].w, ev[h].w));
-      } else {
-        xv[h] = gv[h];
-      }
-    }
+    for (int h = 0; h < 2; ++h)
+      xv[h] = make_float4(__fadd_rn(gv[h].x, ev[h].x), __fadd_rn(gv[h].y, ev[h].y),
+                          __fadd_rn(gv[h].z, ev[h].z), __fadd_rn(gv[h].w, ev[h].w));
     // fmaxf returns the other operand when one is NaN: a NaN never wins
     float mx = 0.0f;
 #pragma unroll
@@ -197,25 +197,12 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
     const float rcp = code_rcp(scale);
     if (lane == 0) scales[b] = scale;
     float acc2 = 0.0f;
-    // every lane quantises (values beyond the tensor are 0 and code as 0).
-    // Without error feedback both halves' Philox outputs are drawn side by
-    // side (quant8: 5.7% faster at 4 CTAs per SM); with it the registers
-    // that takes cost a CTA per SM and the halves go one at a time (quant4).
-    float4 dqv[2];
-    uint32_t pk[2];
-    if constexpr (!EF) {
-      const uint64_t grp[2] = {(b * 256 + 4 * lane) >> 2, (b * 256 + 128 + 4 * lane) >> 2};
-      quant8(xv, scale, rcp, grp, step, K, dqv, pk);
-    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint64_t k = b * 256 + 128 * h + 4 * lane;
-      if constexpr (EF) {
-        dqv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-        pk[h] = quant4(xv[h], scale, rcp, k >> 2, step, K, dqv[h]);
-      }
-      const float4 dq = dqv[h];
-      const uint32_t packed = pk[h];
+      // every lane quantises (values beyond the tensor are 0 and code as 0)
+      float4 dq = make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t packed = quant4(xv[h], scale, rcp, k >> 2, step, K, dq);
       if (nv[h] > 0) {
         if (nv[h] == 4) {
           *reinterpret_cast<uint32_t*>(q + k) = packed;
@@ -226,15 +213,13 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
         }
         if constexpr (DEQ) store4(deq, k, nv[h], dq);
       }
-      if constexpr (EF) {
-        float4 r;
+      float4 r;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          f4at(r, c) = __fsub_rn(f4get(xv[h], c), f4get(dq, c));
-          if (ERR2 && c < nv[h]) acc2 = __fadd_rn(acc2, __fmul_rn(f4get(r, c), f4get(r, c)));
-        }
-        if (nv[h] > 0) store4(e, k, nv[h], r);
+      for (int c = 0; c < 4; ++c) {
+        f4at(r, c) = __fsub_rn(f4get(xv[h], c), f4get(dq, c));
+        if (ERR2 && c < nv[h]) acc2 = __fadd_rn(acc2, __fmul_rn(f4get(r, c), f4get(r, c)));
       }
+      if (nv[h] > 0) store4(e, k, nv[h], r);
     }
     if constexpr (ERR2) {
       acc2 = warp_butterfly_sum(acc2);
@@ -242,24 +227,85 @@ __device__ __forceinline__ void quant_int8_body(const float* __restrict__ g,
     }
     gv[0] = gn[0];
     gv[1] = gn[1];
-    if constexpr (EF) {
-      ev[0] = en[0];
-      ev[1] = en[1];
-    }
+    ev[0] = en[0];
+    ev[1] = en[1];
     nv[0] = nn[0];
     nv[1] = nn[1];
   }
 }
 
-// Without error feedback the kernel runs at 4 CTAs per SM (56 registers,
-// no spill; with one Philox output at a time 5 CTAs fitted and measured
-// 5.7% slower); the error-feedback forms keep the compiler's choice.
+// Without error feedback: half a warp per block.  Lanes 16h .. 16h+15 take
+// block 2*pair + h, and lane j = lane % 16 holds elements 64r + 4j ..
+// 64r + 4j + 3 (r = 0..3) of it -- four 128-bit loads, 256 contiguous bytes
+// per half-warp and row -- so the block max, the scale and its reciprocal
+// are paid once per 16 values, and the four Philox outputs are drawn in two
+// side-by-side pairs.  (The error-feedback forms keep a warp per block: the
+// per-block error monitor's order is lane j's 8 values, then the warp.)
 template <bool DEQ>
 __global__ void __launch_bounds__(kThreads, 4)
     k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
                  float* __restrict__ scales, const PhiloxKeys K, uint64_t step,
                  float* __restrict__ deq) {
-  quant_int8_body<DEQ, false, false>(g, nullptr, n, q, scales, K, step, deq, nullptr);
+  const int lane = threadIdx.x & 31, j = lane & 15, half = lane >> 4;
+  const uint64_t nblk = (n + 255) / 256;
+  const uint64_t npair = (nblk + 1) / 2;
+  const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
+  for (uint64_t pr = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); pr < npair;
+       pr += warps) {
+    // b == nblk for the missing second block of an odd count: every value
+    // lies beyond n there, codes as 0 and is not stored
+    const uint64_t b = 2 * pr + half;
+    float4 xv[4];
+    int nv[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint64_t k = b * 256 + 64 * r + 4 * j;
+      nv[r] = k >= n ? 0 : (n - k >= 4 ? 4 : (int)(n - k));
+      if (nv[r] == 4) {
+        xv[r] = *reinterpret_cast<const float4*>(g + k);
+      } else {
+        xv[r] = make_float4(nv[r] > 0 ? g[k] : 0.f, nv[r] > 1 ? g[k + 1] : 0.f,
+                            nv[r] > 2 ? g[k + 2] : 0.f, 0.f);
+      }
+    }
+    // fmaxf returns the other operand when one is NaN: a NaN never wins
+    float mx = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < nv[r]) mx = fmaxf(mx, fabsf(f4get(xv[r], c)));
+    // the half-warp's max (xor offsets below 16 stay inside the half)
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    const float scale = mx == 0.0f ? 0.0f : __fdiv_rn(mx, 127.0f);
+    const float rcp = code_rcp(scale);
+    if (j == 0 && b < nblk) scales[b] = scale;
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp) {
+      const float4 xp[2] = {xv[2 * rp], xv[2 * rp + 1]};
+      const uint64_t k0 = b * 256 + 128 * rp + 4 * j;
+      const uint64_t grp[2] = {k0 >> 2, (k0 + 64) >> 2};
+      float4 dqv[2];
+      uint32_t pk[2];
+      quant8(xp, scale, rcp, grp, step, K, dqv, pk);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = 2 * rp + h;
+        const uint64_t k = k0 + 64 * h;
+        if (nv[r] > 0) {
+          if (nv[r] == 4) {
+            *reinterpret_cast<uint32_t*>(q + k) = pk[h];
+          } else {
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+              if (c < nv[r]) q[k + c] = (int8_t)((pk[h] >> (8 * c)) & 0xffu);
+          }
+          if constexpr (DEQ) store4(deq, k, nv[r], dqv[h]);
+        }
+      }
+    }
+  }
 }
 
 template <bool DEQ, bool ERR2>
@@ -267,7 +313,7 @@ __global__ void __launch_bounds__(kThreads)
     k_quant_int8_ef(const float* __restrict__ g, float* __restrict__ e, uint64_t n,
                     int8_t* __restrict__ q, float* __restrict__ scales, const PhiloxKeys K,
                     uint64_t step, float* __restrict__ deq, float* __restrict__ err2) {
-  quant_int8_body<DEQ, true, ERR2>(g, e, n, q, scales, K, step, deq, err2);
+  quant_int8_ef_body<DEQ, ERR2>(g, e, n, q, scales, K, step, deq, err2);
 }
 
 template <bool DEQ, bool EF, bool ERR2>
@@ -282,7 +328,8 @@ cudaError_t run_int8(const float* g, float* e, uint64_t n, int8_t* q, float* sca
     k_quant_int8_ef<DEQ, ERR2><<<grid_for(k_quant_int8_ef<DEQ, ERR2>, sms, ctas), kThreads, 0,
                                  s>>>(g, e, n, q, scales, K, step, deq, err2);
   } else {
-    k_quant_int8<DEQ><<<grid_for(k_quant_int8<DEQ>, sms, ctas), kThreads, 0, s>>>(
+    const uint64_t pctas = ((nblk + 1) / 2 + kThreads / 32 - 1) / (kThreads / 32);
+    k_quant_int8<DEQ><<<grid_for(k_quant_int8<DEQ>, sms, pctas), kThreads, 0, s>>>(
         g, n, q, scales, K, step, deq);
   }
   return cudaGetLastError();
