@@ -54,18 +54,19 @@ class RankOptimizer:
     its row of compressed words and scales, the received blocks, its
     partition's server error and output, and the replicated m, v, p (and
     v_fresh, LAMB state) that every rank updates identically from the
-    gathered server output.  1-bit Adam may hold the momentum in its sign
-    form (the gathered output) after the first compressed step; 1-bit LAMB
-    keeps it dense here."""
+    gathered server output.  With sign_momentum the momentum is held in its
+    sign form (the gathered output) after the first compressed step; for
+    1-bit LAMB the gathered output is then double-buffered, since the update
+    reads the previous step's words too (server_targets names the pair this
+    step's all-gather fills)."""
 
     def __init__(self, n, world, rank, chunk, align=4096, grad_dtype="f32",
                  layer_offsets=None, lamb=False, sign_momentum=False, group=None,
                  device="cuda", **hp):
         import torch
-        if sign_momentum and lamb:
-            raise ValueError("the rank path keeps 1-bit LAMB's momentum dense")
         self.rank, self.world, self.group, self.lamb = rank, world, group, lamb
         self.sign_momentum, self.m_in_signs = sign_momentum, False
+        self.double_buffered = bool(sign_momentum and lamb)
         self.ctx = ob.ob_init(n, world, chunk, align,
                               ob.OB_GRAD_BF16 if grad_dtype == "bf16" else ob.OB_GRAD_F32,
                               layer_offsets, **hp)
@@ -86,6 +87,8 @@ class RankOptimizer:
         self.sscales_part = z(cpp)
         self.sbits = z(lay["words_per_worker"], dt=torch.int32)
         self.sscales = z(lay["n_chunks"])
+        self.sbits_alt = z(lay["words_per_worker"], dt=torch.int32) if self.double_buffered else None
+        self.sscales_alt = z(lay["n_chunks"]) if self.double_buffered else None
         nbytes = ob.ob_workspace_bytes(self.ctx)
         self.workspace = z((nbytes + 255) // 256 * 64)
         ob.ob_set_workspace(self.ctx, self.workspace, nbytes)
@@ -105,8 +108,9 @@ class RankOptimizer:
 
     def begin_compression(self):
         for t in (self.err, self.bits_row, self.scales_row, self.err_s_part, self.sbits_part,
-                  self.sscales_part, self.sbits, self.sscales):
-            t.zero_()
+                  self.sscales_part, self.sbits, self.sscales, self.sbits_alt, self.sscales_alt):
+            if t is not None:
+                t.zero_()
         if self.lamb:
             ob.ob_begin_compression(self.ctx, None, None, None, None, None, None, self.m,
                                     self.v, self.v_fresh, self.ls, max(self.warmup_steps, 1))
@@ -114,20 +118,37 @@ class RankOptimizer:
 
     def compress(self, grad):
         if self.m_in_signs:
+            # m_{t-1} = sscale*sign (over sigma_l for LAMB) from the last gathered output
             ob.ob_compress_worker(self.ctx, grad, self.err, self.bits_row, self.scales_row,
-                                  msbits=self.sbits, msscales=self.sscales)
+                                  msbits=self.sbits, msscales=self.sscales, ls=self.ls)
         else:
             ob.ob_compress_worker(self.ctx, grad, self.err, self.bits_row, self.scales_row,
                                   m=self.m, ls=self.ls)
 
     def server(self):
+        # in place: each tile's previous words and scale are read before it
+        # is rewritten, and only the gathered copies feed the update
         ob.ob_server_reduce_part(self.ctx, self.rank, self.recv_bits, self.recv_scales,
                                  self.err_s_part, self.sbits_part, self.sscales_part, self.ls)
 
+    def server_targets(self):
+        """The whole-output buffers this step's all-gather fills: the current
+        pair, or -- 1-bit LAMB in sign form after its first compressed step --
+        the other pair, so that the update still sees the previous words."""
+        if self.double_buffered and self.m_in_signs:
+            return self.sbits_alt, self.sscales_alt
+        return self.sbits, self.sscales
+
     def update(self):
-        if self.lamb:
+        if self.double_buffered and self.m_in_signs:
+            ob.ob_lamb_step_signm(self.ctx, self.sbits, self.sscales, self.sbits_alt,
+                                  self.sscales_alt, self.v, self.v_fresh, self.p, self.ls)
+            self.sbits, self.sbits_alt = self.sbits_alt, self.sbits
+            self.sscales, self.sscales_alt = self.sscales_alt, self.sscales
+        elif self.lamb:
             ob.ob_lamb_step(self.ctx, self.sbits, self.sscales, self.v, self.v_fresh, self.m,
                             self.p, self.ls)
+            self.m_in_signs = self.sign_momentum
         else:
             ob.ob_adam_step(self.ctx, self.sbits, self.sscales, self.v,
                             None if self.sign_momentum else self.m, self.p)
@@ -140,6 +161,7 @@ class RankOptimizer:
         exchange_worker_blocks(self.bits_row, self.scales_row, self.layout, self.recv_bits,
                                self.recv_scales, self.group)
         self.server()
-        gather_server(self.sbits_part, self.sscales_part, self.layout, self.sbits, self.sscales,
+        sbits, sscales = self.server_targets()
+        gather_server(self.sbits_part, self.sscales_part, self.layout, sbits, sscales,
                       self.group)
         self.update()

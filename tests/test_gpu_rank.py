@@ -6,7 +6,9 @@ blocks exchange.py hands to the collectives.  After every compressed step
 each rank's parameters, its row of words and scales, its error and its
 partition of the server output equal the resident path's (all W workers in
 one ctx) bit for bit, and the gathered server words and scales equal the
-oracle's."""
+oracle's.  With the momentum in sign form (1-bit Adam in place, 1-bit LAMB
+with the gathered output double-buffered) the ranks match the resident
+path's sign form and the dense oracle all the same."""
 import numpy as np
 import pytest
 import torch
@@ -44,13 +46,15 @@ def _exchange(ranks, lay):
 
 
 def _gather(ranks, lay):
+    """The all-gather, into the buffers each rank names for this step."""
     wp, _ = X.block_sizes(lay)
     W = len(ranks)
     full_b = torch.cat([r.sbits_part for r in ranks])
     full_s = torch.cat([r.sscales_part for r in ranks])
     for r in ranks:
-        r.sbits[: W * wp].copy_(full_b)
-        r.sscales.copy_(full_s)
+        sbits, sscales = r.server_targets()
+        sbits[: W * wp].copy_(full_b)
+        sscales.copy_(full_s)
 
 
 @pytest.mark.parametrize("n,W,A,C,lamb,sign_m,dt", [
@@ -59,6 +63,8 @@ def _gather(ranks, lay):
     (50_000, 3, 128, 2048, False, True, "f32"),
     (70_001, 8, 128, 4096, True, False, "f32"),
     (40_000, 16, 128, 1024, True, False, "bf16"),
+    (70_001, 8, 128, 4096, True, True, "f32"),
+    (40_000, 4, 128, 1024, True, True, "bf16"),
 ])
 def test_ranks_match_resident_path_and_oracle(n, W, A, C, lamb, sign_m, dt):
     hp = LAMB_HP if lamb else ADAM_HP
