@@ -486,6 +486,19 @@ ob_status ob_server_reduce_part(ob_ctx* ctx, int j, const uint32_t* recv_bits,
                                 uint32_t* sbits_part, float* sscales_part,
                                 const ob_layer_state* ls, ob_stream_t stream);
 
+/* Rank form of ob_reset_errors ([BLOG] 4.1, the periodic reset): rank j's
+ * own worker error (err [n_pad], decoded with bits_row and scales_row) and
+ * its server partition's error (err_s_part [P], with sbits_part [P/32] and
+ * sscales_part [cpp]) become exactly 0 for the next compression, in the
+ * deferred form (err := scale*sign, err_s_part := sscale*sign), so the
+ * words and scales -- and a momentum held in sign form -- are untouched.
+ * Every rank calls it before the same steps (ob_plan_step's `reset`).
+ * Needs no workspace. */
+ob_status ob_reset_errors_rank(ob_ctx* ctx, int j, float* err, const uint32_t* bits_row,
+                               const float* scales_row, float* err_s_part,
+                               const uint32_t* sbits_part, const float* sscales_part,
+                               ob_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Layerwise mixed bit widths ([BLOG] 3.2 table: a bit width and an update
  * period per parameter type -- embeddings and transformer FFN 1 bit, CNN

@@ -39,7 +39,7 @@ EXPORTS = (
     "ob_compress_f16", "ob_server_reduce_f16", "ob_adam_step_f16",
     "ob_compress_signm_ls", "ob_server_reduce_db", "ob_lamb_step_signm", "ob_step_db",
     "ob_noalloc_device_error", "ob_error_norm", "ob_plan_step", "ob_codec_step",
-    "ob_compress_worker", "ob_server_reduce_part",
+    "ob_compress_worker", "ob_server_reduce_part", "ob_reset_errors_rank",
 )
 
 
@@ -116,6 +116,7 @@ def lib():
         L.ob_codec_step.argtypes = [vp, i32, u64] + [vp] * 11
         L.ob_compress_worker.argtypes = [vp] * 10
         L.ob_server_reduce_part.argtypes = [vp, i32] + [vp] * 7
+        L.ob_reset_errors_rank.argtypes = [vp, i32] + [vp] * 7
         L.ob_compress_signm.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.ob_reset_errors.argtypes = [vp] * 8
         L.ob_quant_int8_ef.argtypes = [vp, vp, sz, vp, vp, u64, u64, vp, vp, vp]
@@ -414,6 +415,15 @@ def ob_server_reduce_part(ctx, j, recv_bits, recv_scales, err_s_part, sbits_part
     _check(lib().ob_server_reduce_part(ctx, j, _ptr(recv_bits), _ptr(recv_scales),
                                        _ptr(err_s_part), _ptr(sbits_part), _ptr(sscales_part),
                                        _ls(ls), _stream(stream)), ctx)
+
+
+def ob_reset_errors_rank(ctx, j, err, bits_row, scales_row, err_s_part, sbits_part,
+                         sscales_part, stream=None):
+    """One rank's periodic error reset: its own worker error and its server
+    partition's error become 0 (deferred form; words and scales untouched)."""
+    _check(lib().ob_reset_errors_rank(ctx, j, _ptr(err), _ptr(bits_row), _ptr(scales_row),
+                                      _ptr(err_s_part), _ptr(sbits_part), _ptr(sscales_part),
+                                      _stream(stream)), ctx)
 
 
 def ob_device_error(ctx, stream=None):

@@ -373,30 +373,34 @@ template <bool RESET>
 __global__ void __launch_bounds__(kThreads) k_materialize(const MaterializeArgs A) {
   const Geo& G = A.geo;
   const int p = threadIdx.x;
-  for (uint32_t T = blockIdx.x; T < G.n_tiles; T += gridDim.x) {
+  const uint32_t NW = A.nw;
+  for (uint32_t T = A.T0 + blockIdx.x; T < A.T1; T += gridDim.x) {
     const Tile tl = decode_tile(G, T);
     if (tl.start >= G.n) continue;
-    for (uint32_t w = 0; w <= G.W; ++w) {
-      // w < W: worker errors; w == W: the server error
-      float* e = w < G.W ? A.e[w] : A.e_s;
-      const uint32_t* bw = w < G.W ? A.bits + (uint64_t)w * G.words : A.sbits;
-      const float sc = w < G.W ? __ldcg(A.scales + (uint64_t)w * G.nc + tl.g)
-                               : __ldcg(A.sscales + tl.g);
+    for (uint32_t w = 0; w <= NW; ++w) {
+      // w < nw: worker errors; w == nw: the server error (if given)
+      if (w == NW && !A.e_s) break;
+      const uint64_t base = w < NW ? 0 : A.base;
+      float* e = w < NW ? A.e[w] : A.e_s;
+      const uint32_t* bw = w < NW ? A.bits + (uint64_t)w * G.words : A.sbits;
+      const float sc = w < NW ? __ldcg(A.scales + (uint64_t)w * G.nc + tl.g)
+                              : __ldcg(A.sscales + (tl.g - A.g0));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t off = 1024u * i + 4u * p;
         if (off >= tl.len) continue;
         const uint64_t k0 = tl.start + off;
         if (k0 >= G.n) continue;
-        const uint32_t wd = bw[k0 >> 5] >> (4 * (p & 7));
-        float4 ev = *reinterpret_cast<const float4*>(e + k0);
+        const uint64_t kl = k0 - base;  // base is a multiple of 32: same bit in the word
+        const uint32_t wd = bw[kl >> 5] >> (4 * (p & 7));
+        float4 ev = *reinterpret_cast<const float4*>(e + kl);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (k0 + c >= G.n) continue;
           const float so = ((wd >> c) & 1u) ? sc : -sc;
           f4at(ev, c) = RESET ? so : __fsub_rn(f4at(ev, c), so);
         }
-        *reinterpret_cast<float4*>(e + k0) = ev;
+        *reinterpret_cast<float4*>(e + kl) = ev;
       }
     }
   }
@@ -435,12 +439,12 @@ cudaError_t launch_decompress(const UpdateArgs& a, bool layered, int sms,
 }
 
 cudaError_t launch_materialize(const MaterializeArgs& a, int sms, cudaStream_t s) {
-  k_materialize<false><<<grid_for(k_materialize<false>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  k_materialize<false><<<grid_for(k_materialize<false>, sms, a.T1 - a.T0), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_reset_errors(const MaterializeArgs& a, int sms, cudaStream_t s) {
-  k_materialize<true><<<grid_for(k_materialize<true>, sms, a.geo.n_tiles), kThreads, 0, s>>>(a);
+  k_materialize<true><<<grid_for(k_materialize<true>, sms, a.T1 - a.T0), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

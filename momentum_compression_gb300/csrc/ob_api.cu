@@ -737,6 +737,8 @@ ob_status ob_materialize_errors(ob_ctx* ctx, float* const* err, const uint32_t* 
   const Geo& G = ctx->geo;
   ob::MaterializeArgs a{};
   a.geo = G;
+  a.nw = G.W;
+  a.T1 = G.n_tiles;
   for (uint32_t w = 0; w < G.W; ++w) a.e[w] = err[w];
   a.bits = bits;
   a.scales = scales;
@@ -765,6 +767,8 @@ ob_status ob_reset_errors(ob_ctx* ctx, float* const* err, const uint32_t* bits,
   const Geo& G = ctx->geo;
   ob::MaterializeArgs a{};
   a.geo = G;
+  a.nw = G.W;
+  a.T1 = G.n_tiles;
   for (uint32_t w = 0; w < G.W; ++w) a.e[w] = err[w];
   a.bits = bits;
   a.scales = scales;
@@ -792,6 +796,8 @@ ob_status ob_error_norm(ob_ctx* ctx, const float* const* err, const uint32_t* bi
   const Geo& G = ctx->geo;
   ob::MaterializeArgs a{};
   a.geo = G;
+  a.nw = G.W;
+  a.T1 = G.n_tiles;
   for (uint32_t w = 0; w < G.W; ++w) a.e[w] = const_cast<float*>(err[w]);
   a.bits = bits;
   a.scales = scales;

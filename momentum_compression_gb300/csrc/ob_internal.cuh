@@ -306,6 +306,12 @@ struct MaterializeArgs {
   float* e_s;
   const uint32_t* sbits;
   const float* sscales;
+  // k_materialize: workers 0..nw-1 (rows of bits and scales) and, if e_s is
+  // set, the server, over the tiles [T0, T1); the server's element k is at
+  // index k - base of e_s and sbits, its chunk g at g - g0 of sscales.  The
+  // whole buffer: nw = W, T0 = 0, T1 = n_tiles, base = g0 = 0.
+  uint32_t nw, T0, T1, g0;
+  uint64_t base;
 };
 
 struct WarmupArgs {

@@ -162,4 +162,45 @@ ob_status ob_server_reduce_part(ob_ctx* ctx, int j, const uint32_t* recv_bits,
                   "server_reduce_part: chunk scales");
 }
 
+ob_status ob_reset_errors_rank(ob_ctx* ctx, int j, float* err, const uint32_t* bits_row,
+                               const float* scales_row, float* err_s_part,
+                               const uint32_t* sbits_part, const float* sscales_part,
+                               ob_stream_t stream) {
+  OB_TRACE();
+  if (!ctx) return ob::ctx_fail(nullptr, OB_ERR_INVALID, "ctx is NULL");
+  const ob::Geo& G = *ob::ctx_geo(ctx);
+  if (j < 0 || (uint32_t)j >= G.W)
+    return failf(ctx, OB_ERR_INVALID, "partition %d is not in [0, W = %u)", j, G.W);
+  OB_RANK_PTR(ctx, err, 16, "err");
+  OB_RANK_PTR(ctx, bits_row, 16, "bits_row");
+  OB_RANK_PTR(ctx, scales_row, 4, "scales_row");
+  OB_RANK_PTR(ctx, err_s_part, 16, "err_s_part");
+  OB_RANK_PTR(ctx, sbits_part, 16, "sbits_part");
+  OB_RANK_PTR(ctx, sscales_part, 4, "sscales_part");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = ob::ctx_sms(ctx);
+  ob::MaterializeArgs a{};
+  a.geo = G;
+  // the rank's own worker row, every tile
+  a.nw = 1;
+  a.T1 = G.n_tiles;
+  a.e[0] = err;
+  a.bits = bits_row;
+  a.scales = scales_row;
+  ob_status st = launched(ctx, ob::launch_reset_errors(a, sms, s), "reset_errors_rank: worker");
+  if (st) return st;
+  // its server partition: partition j's tiles, indexed from the partition
+  ob::MaterializeArgs b{};
+  b.geo = G;
+  b.nw = 0;
+  b.T0 = (uint32_t)j * G.tpp;
+  b.T1 = b.T0 + G.tpp;
+  b.g0 = (uint32_t)j * G.cpp;
+  b.base = (uint64_t)j * G.P;
+  b.e_s = err_s_part;
+  b.sbits = sbits_part;
+  b.sscales = sscales_part;
+  return launched(ctx, ob::launch_reset_errors(b, sms, s), "reset_errors_rank: server");
+}
+
 }  // extern "C"

@@ -62,14 +62,17 @@ class RankOptimizer:
 
     def __init__(self, n, world, rank, chunk, align=4096, grad_dtype="f32",
                  layer_offsets=None, lamb=False, sign_momentum=False, group=None,
-                 device="cuda", **hp):
+                 device="cuda", reset_interval=0, **hp):
+        """reset_interval > 0: the periodic error reset, before the steps the
+        library's plan names (ob_plan_step), as in OneBitOptimizer."""
         import torch
         self.rank, self.world, self.group, self.lamb = rank, world, group, lamb
         self.sign_momentum, self.m_in_signs = sign_momentum, False
         self.double_buffered = bool(sign_momentum and lamb)
+        self.reset_interval, self.cstep = reset_interval, 0
         self.ctx = ob.ob_init(n, world, chunk, align,
                               ob.OB_GRAD_BF16 if grad_dtype == "bf16" else ob.OB_GRAD_F32,
-                              layer_offsets, **hp)
+                              layer_offsets, reset_interval=reset_interval, **hp)
         lay = ob.ob_get_layout(self.ctx)
         self.layout = lay
         wp, cpp = block_sizes(lay)
@@ -111,10 +114,20 @@ class RankOptimizer:
                   self.sscales_part, self.sbits, self.sscales, self.sbits_alt, self.sscales_alt):
             if t is not None:
                 t.zero_()
+        self.cstep = 0
         if self.lamb:
             ob.ob_begin_compression(self.ctx, None, None, None, None, None, None, self.m,
                                     self.v, self.v_fresh, self.ls, max(self.warmup_steps, 1))
         self.m_in_signs = False
+
+    def begin_step(self):
+        """Counts the compressed step and, when the plan says so, resets this
+        rank's worker error and its server partition's error first."""
+        self.cstep += 1
+        if self.reset_interval and ob.ob_plan_step(self.ctx, 1, self.cstep)["reset"]:
+            ob.ob_reset_errors_rank(self.ctx, self.rank, self.err, self.bits_row,
+                                    self.scales_row, self.err_s_part, self.sbits_part,
+                                    self.sscales_part)
 
     def compress(self, grad):
         if self.m_in_signs:
@@ -157,6 +170,7 @@ class RankOptimizer:
     def compressed_step(self, grad):
         """One compressed step of this rank; every rank of the group calls it
         together."""
+        self.begin_step()
         self.compress(grad)
         exchange_worker_blocks(self.bits_row, self.scales_row, self.layout, self.recv_bits,
                                self.recv_scales, self.group)

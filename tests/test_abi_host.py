@@ -181,3 +181,30 @@ def test_codec_calls_check_before_cuda():
         ob.ob_adam_step_f16(ctx, 0, None, None, 16, None, stream=0)
     assert ei.value.status == ob.OB_ERR_UNSUPPORTED
     ob.ob_destroy(ctx)
+
+
+def test_rank_reset_checks_before_cuda():
+    """ob_reset_errors_rank rejects a partition outside [0, W) and missing or
+    misaligned buffers before any launch (it needs no workspace)."""
+    ctx = ob.ob_init(1 << 16, 2, 4096)
+    ok = dict(err=0x1000, bits_row=0x2000, scales_row=0x3000, err_s_part=0x4000,
+              sbits_part=0x5000, sscales_part=0x6000)
+    cases = [
+        (dict(j=2), ob.OB_ERR_INVALID, "partition"),
+        (dict(j=-1), ob.OB_ERR_INVALID, "partition"),
+        (dict(err=None), ob.OB_ERR_INVALID, "err is NULL"),
+        (dict(err=0x1004), ob.OB_ERR_ALIGN, "err"),
+        (dict(sbits_part=0x5008), ob.OB_ERR_ALIGN, "sbits_part"),
+        (dict(sscales_part=0x6001), ob.OB_ERR_ALIGN, "sscales_part"),
+    ]
+    for over, status, msg in cases:
+        kw = dict(ok, j=0)
+        kw.update(over)
+        with pytest.raises(ob.OBError) as ei:
+            ob.ob_reset_errors_rank(ctx, kw.pop("j"), stream=0, **kw)
+        assert ei.value.status == status, over
+        assert msg in ob.ob_last_error(ctx), (over, ob.ob_last_error(ctx))
+    ob.ob_destroy(ctx)
+    with pytest.raises(ob.OBError) as ei:
+        ob.ob_reset_errors_rank(None, 0, **ok, stream=0)
+    assert ei.value.status == ob.OB_ERR_INVALID

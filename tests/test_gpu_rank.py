@@ -57,24 +57,29 @@ def _gather(ranks, lay):
         sscales.copy_(full_s)
 
 
-@pytest.mark.parametrize("n,W,A,C,lamb,sign_m,dt", [
-    (100_003, 2, 4096, 8192, False, False, "f32"),
-    (300_001, 4, 4096, 1 << 16, False, True, "bf16"),
-    (50_000, 3, 128, 2048, False, True, "f32"),
-    (70_001, 8, 128, 4096, True, False, "f32"),
-    (40_000, 16, 128, 1024, True, False, "bf16"),
-    (70_001, 8, 128, 4096, True, True, "f32"),
-    (40_000, 4, 128, 1024, True, True, "bf16"),
+@pytest.mark.parametrize("n,W,A,C,lamb,sign_m,dt,reset", [
+    (100_003, 2, 4096, 8192, False, False, "f32", 0),
+    (300_001, 4, 4096, 1 << 16, False, True, "bf16", 0),
+    (50_000, 3, 128, 2048, False, True, "f32", 0),
+    (70_001, 8, 128, 4096, True, False, "f32", 0),
+    (40_000, 16, 128, 1024, True, False, "bf16", 0),
+    (70_001, 8, 128, 4096, True, True, "f32", 0),
+    (40_000, 4, 128, 1024, True, True, "bf16", 0),
+    # the periodic error reset before compressed steps 3 and 5
+    (100_003, 4, 128, 8192, False, True, "f32", 2),
+    (70_001, 3, 128, 4096, True, True, "f32", 2),
 ])
-def test_ranks_match_resident_path_and_oracle(n, W, A, C, lamb, sign_m, dt):
+def test_ranks_match_resident_path_and_oracle(n, W, A, C, lamb, sign_m, dt, reset):
     hp = LAMB_HP if lamb else ADAM_HP
     sizes = [7, 1, 4095, 4097, 33] if lamb else None
     off = None
     if lamb:
         off = [0] + list(np.cumsum(sizes))
         off.append(n)
-    res = ob.OneBitOptimizer(n, W, C, A, dt, off, lamb=lamb, sign_momentum=sign_m, **hp)
-    ranks = [X.RankOptimizer(n, W, r, C, A, dt, off, lamb=lamb, sign_momentum=sign_m, **hp)
+    res = ob.OneBitOptimizer(n, W, C, A, dt, off, lamb=lamb, sign_momentum=sign_m,
+                             reset_interval=reset, **hp)
+    ranks = [X.RankOptimizer(n, W, r, C, A, dt, off, lamb=lamb, sign_momentum=sign_m,
+                             reset_interval=reset, **hp)
              for r in range(W)]
     lay = res.layout
     wp, cpp = X.block_sizes(lay)
@@ -119,6 +124,7 @@ def test_ranks_match_resident_path_and_oracle(n, W, A, C, lamb, sign_m, dt):
         gh, gd = grads(t)
         res.compressed_step(gd)
         for r in ranks:
+            r.begin_step()
             r.compress(gd[r.rank])
         _exchange(ranks, lay)
         for r in ranks:
@@ -126,6 +132,9 @@ def test_ranks_match_resident_path_and_oracle(n, W, A, C, lamb, sign_m, dt):
         _gather(ranks, lay)
         for r in ranks:
             r.update()
+        c = t - warm
+        if reset and c and c % reset == 0:
+            O.reset_errors(st)
         O.compressed_step(st, gh, hp, lamb=lamb)
         torch.cuda.synchronize()
         what = f"step {t}"

@@ -30,7 +30,9 @@ for call in (lambda: ob.ob_compress(ctx, [None] * 4, None, [None] * 4, None, Non
                                       stream=0),
              lambda: ob.ob_quant_int8(None, None, None, 1, 0, n=0, stream=0),
              lambda: ob.ob_compress_noalloc(ctx, [None] * 4, None, [None] * 4, None, None,
-                                            stream=0)):
+                                            stream=0),
+             lambda: ob.ob_reset_errors_rank(ctx, 9, None, None, None, None, None, None,
+                                             stream=0)):
     try:
         call()
     except ob.OBError:
@@ -61,7 +63,7 @@ def test_every_call_opens_and_closes_a_named_range(tmp_path):
     pushes = [e.split(" ", 1)[1] for e in events if e.startswith("push ")]
     # the binding reads ob_last_error after every rejected call
     failing = ["ob_compress", "ob_server_reduce", "ob_adam_step", "ob_error_norm",
-               "ob_quant_int8", "ob_compress_noalloc"]
+               "ob_quant_int8", "ob_compress_noalloc", "ob_reset_errors_rank"]
     want = ["ob_init", "ob_get_layout", "ob_workspace_bytes"]
     for name in failing:
         want += [name, "ob_last_error"]
@@ -72,3 +74,18 @@ def test_every_call_opens_and_closes_a_named_range(tmp_path):
         depth += 1 if e.startswith("push ") else -1
         assert depth in (0, 1), "ranges must not be left open or nested here"
     assert depth == 0
+
+
+def test_every_entry_point_opens_its_range_first():
+    """Source check for the calls the child above cannot reach without a
+    GPU: the body of every exported ob_* function starts with OB_TRACE()."""
+    import re
+    import momentum_compression_gb300 as ob
+    csrc = os.path.join(ROOT, "momentum_compression_gb300", "csrc")
+    src = "".join(open(os.path.join(csrc, f)).read() for f in sorted(os.listdir(csrc))
+                  if f.endswith(".cu"))
+    for name in ob.EXPORTS:
+        m = re.search(r"\b" + name + r"\s*\([^;{]*\)\s*\{", src)
+        assert m, f"{name}: no definition under csrc/"
+        first = src[m.end():].lstrip().split("\n", 1)[0].strip()
+        assert first == "OB_TRACE();", f"{name} starts with {first!r}"
