@@ -17,7 +17,7 @@
 namespace ob {
 namespace {
 
-// Quantizes the lane's 8 values xv[h] (h = 0, 1; elements 4*grp[h] ..
+// Quantizes two groups of 4 values, xv[h] (h = 0, 1; elements 4*grp[h] ..
 // 4*grp[h]+3), one Philox output per group, both drawn side by side; dq[h]
 // receives q*scale and packed[h] the four codes.  rcp: code_rcp(scale)
 // (sround.cuh): the codes come from code_fast where certain, else from
