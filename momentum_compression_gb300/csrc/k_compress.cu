@@ -66,7 +66,7 @@ struct CompressSmem {
   static constexpr size_t kStage = kStageG + kStageE + kStageB;
   static constexpr size_t kM = MSIGN ? 0 : kTile * 4;
   static constexpr size_t kBars = (2 * kStages + 2) * 8;
-  static constexpr size_t kWs = OB_MAX_WORKERS * 8 * 4;
+  static constexpr size_t kWs = 2 * OB_MAX_WORKERS * 8 * 4;  // warp totals, by tile parity
   static constexpr size_t kSc = 2 * OB_MAX_WORKERS * 4;
   static constexpr size_t kBytes = kM + kStages * kStage + kBars + kWs + kSc;
 };
@@ -85,9 +85,12 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   uint64_t* empty = bars + kStages;
   uint64_t* mfull = bars + 2 * kStages;
   uint64_t* mempty = bars + 2 * kStages + 1;
-  float(*ws)[8] = reinterpret_cast<float(*)[8]>(bars + 2 * kStages + 2);
+  // warp totals [2][OB_MAX_WORKERS][8], double-buffered by tile parity so
+  // that one barrier per tile suffices
+  float(*ws2)[8] = reinterpret_cast<float(*)[8]>(bars + 2 * kStages + 2);
   // the workers' chunk scales of the current and the next tile
-  float(*s_sc)[OB_MAX_WORKERS] = reinterpret_cast<float(*)[OB_MAX_WORKERS]>(ws + OB_MAX_WORKERS);
+  float(*s_sc)[OB_MAX_WORKERS] =
+      reinterpret_cast<float(*)[OB_MAX_WORKERS]>(ws2 + 2 * OB_MAX_WORKERS);
   __shared__ volatile int s_abort;
   // 1-bit LAMB per-tile scalars (first layer, its end, sigma, rho) of the
   // current and the next work item, made by thread 0 an item ahead: the
@@ -188,8 +191,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   // loaded one tile ahead, so their latency hides behind the current tile
   uint32_t mw_next[4] = {0u, 0u, 0u, 0u};
   float mss_next = 0.0f;
-  auto load_msign = [&](uint32_t Tn) {
-    const Tile tn = decode_tile(G, Tn);
+  auto load_msign = [&](const Tile& tn) {
     mss_next = __ldcg(A.msscales + tn.g);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -216,10 +218,10 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
   }
   if (blockIdx.x < n_vt) {
     const uint32_t gi = kGrouped ? blockIdx.x / G.n_tiles : 0u, T0 = blockIdx.x - gi * G.n_tiles;
-    if constexpr (MSIGN) load_msign(T0);
+    const Tile t0 = decode_tile(G, T0);
+    if constexpr (MSIGN) load_msign(t0);
     const uint32_t wb = gi * gsz, nw = (wb + gsz < NW ? wb + gsz : NW) - wb;
-    if ((uint32_t)p < nw)
-      s_sc[0][p] = __ldcg(A.scales + (uint64_t)(wb + p) * G.nc + decode_tile(G, T0).g);
+    if ((uint32_t)p < nw) s_sc[0][p] = __ldcg(A.scales + (uint64_t)(wb + p) * G.nc + t0.g);
   }
   named_sync(1, kConsumers);
   uint32_t item = 0, ti = 0;
@@ -227,18 +229,31 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
     const uint32_t gi = kGrouped ? VT / G.n_tiles : 0u, T = VT - gi * G.n_tiles;
     const uint32_t wbeg = gi * gsz, wend = wbeg + gsz < NW ? wbeg + gsz : NW;
     const Tile tl = decode_tile(G, T);
+    float(*ws)[8] = ws2 + (ti & 1) * OB_MAX_WORKERS;
     bool ok = true;
-    // the next item group's worker scales, stored after this one's last barrier
+    // MSIGN: this tile's momentum words and scale, taken before the next
+    // tile's are loaded over them
+    [[maybe_unused]] uint32_t mnib[4];
+    [[maybe_unused]] float mss = 0.0f;
+    if constexpr (MSIGN) {
+      mss = mss_next;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mnib[i] = mw_next[i] >> (4 * (p & 7));
+    }
+    // the next item group: its tile decoded once (two integer divisions;
+    // with one worker per tile a second decode of it was a noticeable share
+    // of the work) for its worker scales, stored before this group's
+    // barrier, and its momentum words
     float sc_next = 0.0f;
     const uint32_t VTn = VT + gridDim.x;
-    uint32_t Tn = 0, nwn = 0;
+    uint32_t nwn = 0;
     if (VTn < n_vt) {
       const uint32_t gin = kGrouped ? VTn / G.n_tiles : 0u;
-      Tn = VTn - gin * G.n_tiles;
+      const Tile tn = decode_tile(G, VTn - gin * G.n_tiles);
       const uint32_t wbn = gin * gsz;
       nwn = (wbn + gsz < NW ? wbn + gsz : NW) - wbn;
-      if ((uint32_t)p < nwn)
-        sc_next = __ldcg(A.scales + (uint64_t)(wbn + p) * G.nc + decode_tile(G, Tn).g);
+      if ((uint32_t)p < nwn) sc_next = __ldcg(A.scales + (uint64_t)(wbn + p) * G.nc + tn.g);
+      if constexpr (MSIGN) load_msign(tn);
     }
     // 1-bit LAMB: the layer of the tile's first element; every worker pass
     // walks the layers forward from it (layers change rarely inside a tile)
@@ -293,11 +308,6 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
       // m = sscale*sign (1-bit Adam) or sscale*sign/sigma_l (1-bit LAMB);
       // +-sscale/sigma = (+-sscale)/sigma exactly (IEEE division is
       // symmetric in sign): one division per layer
-      const float mss = mss_next;
-      uint32_t mnib[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mnib[i] = mw_next[i] >> (4 * (p & 7));
-      if (VTn < n_vt) load_msign(Tn);
       [[maybe_unused]] uint32_t lq = l_t;
       [[maybe_unused]] uint64_t lqend = lend_t;
       float q = LAMB ? __fdiv_rn(mss, s_t) : mss;
@@ -457,10 +467,12 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
         nx.r = A.ratio_ef ? __fdiv_rn(s_lr.c2, s_lr.c1) : 1.0f;
       }
     }
-    named_sync(1, kConsumers);
+    // one barrier per tile: the warp totals are double-buffered by parity
+    // (the next tile writes the other half), and it also agrees on stopping
+    const bool stop = named_sync_or(1, kConsumers, s_abort != 0);
     if ((uint32_t)p < wend - wbeg)
       A.ws.wpart[((uint64_t)(wbeg + p) * G.nc + tl.g) * G.tpc + tl.t] = tree8(ws[wbeg + p]);
-    if (named_sync_or(1, kConsumers, s_abort != 0)) break;
+    if (stop) break;
   }
 }
 
