@@ -239,10 +239,12 @@ __device__ __forceinline__ void quant_int8_ef_body(const float* __restrict__ g,
 // 64r + 4j + 3 (r = 0..3) of it -- four 128-bit loads, 256 contiguous bytes
 // per half-warp and row -- so the block max, the scale and its reciprocal
 // are paid once per 16 values, and the four Philox outputs are drawn in two
-// side-by-side pairs.  (The error-feedback forms keep a warp per block: the
-// per-block error monitor's order is lane j's 8 values, then the warp.)
+// side-by-side pairs.  The next pair's loads are in flight while this one is
+// quantised (3 CTAs per SM, 79 registers: 2.3% faster than without them at
+// 4).  (The error-feedback forms keep a warp per block: the per-block error
+// monitor's order is lane j's 8 values, then the warp.)
 template <bool DEQ>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
     k_quant_int8(const float* __restrict__ g, uint64_t n, int8_t* __restrict__ q,
                  float* __restrict__ scales, const PhiloxKeys K, uint64_t step,
                  float* __restrict__ deq) {
@@ -250,13 +252,10 @@ __global__ void __launch_bounds__(kThreads, 4)
   const uint64_t nblk = (n + 255) / 256;
   const uint64_t npair = (nblk + 1) / 2;
   const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
-  for (uint64_t pr = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); pr < npair;
-       pr += warps) {
-    // b == nblk for the missing second block of an odd count: every value
-    // lies beyond n there, codes as 0 and is not stored
-    const uint64_t b = 2 * pr + half;
-    float4 xv[4];
-    int nv[4];
+  // lane j's 16 values of block b (b == nblk for the missing second block
+  // of an odd count: every value lies beyond n there, codes as 0 and is not
+  // stored)
+  auto load_block16 = [&](uint64_t b, float4 (&xv)[4], int (&nv)[4]) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const uint64_t k = b * 256 + 64 * r + 4 * j;
@@ -268,6 +267,21 @@ __global__ void __launch_bounds__(kThreads, 4)
                             nv[r] > 2 ? g[k + 2] : 0.f, 0.f);
       }
     }
+  };
+  uint64_t pr = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  float4 xn[4];
+  int nn[4] = {0, 0, 0, 0};
+  if (pr < npair) load_block16(2 * pr + half, xn, nn);
+  for (; pr < npair; pr += warps) {
+    const uint64_t b = 2 * pr + half;
+    float4 xv[4];
+    int nv[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      xv[r] = xn[r];
+      nv[r] = nn[r];
+    }
+    if (pr + warps < npair) load_block16(2 * (pr + warps) + half, xn, nn);
     // fmaxf returns the other operand when one is NaN: a NaN never wins
     float mx = 0.0f;
 #pragma unroll
