@@ -240,10 +240,8 @@ __global__ void __launch_bounds__(kCompressThreads, 2) k_compress(const Compress
 #pragma unroll
       for (int i = 0; i < 4; ++i) mnib[i] = mw_next[i] >> (4 * (p & 7));
     }
-    // the next item group: its tile decoded once (two integer divisions;
-    // with one worker per tile a second decode of it was a noticeable share
-    // of the work) for its worker scales, stored before this group's
-    // barrier, and its momentum words
+    // the next item group: its tile, decoded once, for its worker scales
+    // (stored before this group's barrier) and its momentum words
     float sc_next = 0.0f;
     const uint32_t VTn = VT + gridDim.x;
     uint32_t nwn = 0;
