@@ -462,7 +462,12 @@ ob_status ob_plan_step(const ob_ctx* ctx, int bits, uint64_t t, ob_plan* out);
  * 1-bit LAMB, ob_begin_compression with all six error and sign buffers
  * NULL does the rest.  The warmup steps average all W gradients
  * (ob_warmup_step on a gathered set).  P must be a multiple of 128 (A a
- * multiple of 128) for ob_server_reduce_part. */
+ * multiple of 128) for ob_server_reduce_part.  With the momentum in sign
+ * form (after the first compressed step) ob_compress_worker reads it from
+ * the last gathered output; for 1-bit LAMB the gathered output is then
+ * double-buffered, since ob_lamb_step_signm reads the previous one too,
+ * while sbits_part/sscales_part are rewritten in place.  The periodic reset
+ * is ob_reset_errors_rank on every rank before the same steps. */
 
 /* Rank compression of one worker: ob_compress for worker `rank`'s own
  * buffers only.  grad, err: n_pad elements; bits_row: words_per_worker
